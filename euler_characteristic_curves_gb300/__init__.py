@@ -1,0 +1,16 @@
+"""Euler characteristic curves of dense 2-D/3-D grids on one GB300 (sm_103a).
+
+The compute runs in the CUDA library built from ``csrc/`` behind the C ABI in
+``include/ecc.h``; this package only marshals arguments (``ecc`` module). The native library is
+loaded on first use and a missing library raises immediately: there is no CPU fallback.
+"""
+__all__ = ["ecc_hard", "ecc_soft_fwd", "ecc_soft_bwd", "soft_workspace_bytes", "SoftECC",
+           "soft_ecc"]
+
+
+def __getattr__(name):
+    if name in __all__:
+        from . import ecc
+
+        return getattr(ecc, name)
+    raise AttributeError(name)
