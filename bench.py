@@ -1,0 +1,537 @@
+"""Benchmark of the ECC hot path on GB300 (prints one JSON line on rank 0).
+
+A step is one pass of the whole hot path over one batch of synthetic input, inputs resident in
+HBM: the hard ECC of the 2-D 8192^2 float32 image (nbins 1024) and of the 3-D 1024^3 float32
+volume (nbins 256) -- the two grids the headline metric is quoted on -- plus the soft ECC
+forward and backward on 64 images of 256^2 (K = 128, lambda = 50). ``value`` is hard-ECC
+Gvoxels per second of the whole step; the per-part device times, the roofline fraction of the
+dominant kernel and the soft fwd+bwd milliseconds are reported beside it.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload headline|2d8192|3d1024|2d1024x16|2d128u8|3d512u8|soft]
+
+Under torchrun every rank runs the same workload on its own GPU (independent problems, no
+collective on the data path; weak scaling); the timed region is bracketed by barriers and the
+slowest rank's time is reported. ``--impl reference`` times the CPU oracle (the plain C
+definition) on a bounded sample of the same workload on this host's cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = ("Gvoxels/s hard ECC (2D 8192^2, 3D 1024^3) as % HBM roofline; "
+          "soft-ECC fwd+bwd ms")
+
+# ------------------------------------------------------------------------------------ workloads
+
+WORKLOADS = {
+    # name: list of parts; a part is ("hard", shape, batch, dtype, nbins, vmin, vmax, seed) or
+    # ("soft", shape, batch, K, lam, seed_img, seed_u, seed_g)
+    "2d128u8": [("hard", (128, 128), 1, "u8blur", 256, 0.0, 255.0, 1)],
+    "2d1024x16": [("hard", (1024, 1024), 16, "f32", 256, 0.0, 1.0, 2)],
+    "2d8192": [("hard", (8192, 8192), 1, "f32", 1024, 0.0, 1.0, 3)],
+    "3d1024": [("hard", (1024, 1024, 1024), 1, "f32", 256, 0.0, 1.0, 4)],
+    "3d512u8": [("hard", (512, 512, 512), 1, "u8grf", 256, 0.0, 255.0, 5)],
+    "soft": [("soft", (256, 256), 64, 128, 50.0, 6, 7, 8)],
+}
+WORKLOADS["headline"] = WORKLOADS["2d8192"] + WORKLOADS["3d1024"] + WORKLOADS["soft"]
+
+DESCRIPTION = {
+    "headline": "hard ECC 2D 8192^2 f32 nbins 1024 + 3D 1024^3 f32 nbins 256; "
+                "soft ECC fwd+bwd 64x256^2 f32 K 128 lambda 50",
+}
+
+
+def part_name(p):
+    if p[0] == "hard":
+        dims = "x".join(str(s) for s in p[1])
+        return f"hard_{len(p[1])}d_{p[2]}x{dims}_{p[3]}_H{p[4]}"
+    return f"soft_fwd_bwd_{p[2]}x{p[1][0]}x{p[1][1]}_K{p[3]}"
+
+
+def part_voxels(p):
+    n = p[2]
+    for s in p[1]:
+        n *= s
+    return n
+
+
+# ------------------------------------------------------------------------------------ helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "euler_characteristic_curves_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current source."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as fh:
+        d = json.load(fh)
+    ent = d.get(kernel_key)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "samples": len(sm), "power_w_max": max(power) if power else None,
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------------------------ our arm
+
+def make_inputs(parts, device):
+    import numpy as np
+    import torch
+
+    from euler_characteristic_curves_gb300 import synthetic
+
+    inputs = []
+    for p in parts:
+        if p[0] == "hard":
+            _, shape, batch, kind, nbins, vmin, vmax, seed = p
+            if kind == "u8blur":
+                img = torch.from_numpy(synthetic.blurred_noise_u8(shape, seed)).to(device)
+            elif kind == "u8grf":
+                img = synthetic.quantise_u8(synthetic.grf(shape, seed, device=device))
+            else:
+                img = synthetic.grf(shape, seed, device=device,
+                                    batch=batch if batch > 1 else None)
+            if batch == 1:
+                img = img.unsqueeze(0)
+            inputs.append({"img": img.contiguous(), "ndim": len(shape)})
+        else:
+            _, shape, batch, K, lam, s_img, s_u, s_g = p
+            img = synthetic.grf(shape, s_img, device=device, batch=batch)
+            tau = torch.from_numpy(synthetic.uniform_thresholds(K)).to(device)
+            u = torch.from_numpy(synthetic.soft_direction(len(shape), s_u)).to(device)
+            g = torch.from_numpy(synthetic.upstream_grad((batch, K), s_g)).to(device)
+            alpha = torch.ones(1, dtype=torch.float32, device=device)
+            inputs.append({"img": img.contiguous(), "tau": tau, "u": u, "g": g, "alpha": alpha,
+                           "lam": lam})
+    torch.cuda.synchronize()
+    return inputs
+
+
+class OurStep:
+    """One pass of the hot path through the library's public binding (device-resident)."""
+
+    def __init__(self, parts, inputs, device):
+        import torch
+
+        from euler_characteristic_curves_gb300 import ecc
+
+        self.ecc = ecc
+        self.parts, self.inputs = parts, inputs
+        self.outs = []
+        for p, x in zip(parts, inputs):
+            if p[0] == "hard":
+                self.outs.append(torch.empty((x["img"].shape[0], p[4]), dtype=torch.int64,
+                                             device=device))
+            else:
+                K = p[3]
+                nb = x["img"].shape[0]
+                ws = torch.empty(ecc.soft_workspace_bytes(p[1], nb, K), dtype=torch.uint8,
+                                 device=device)
+                s = torch.empty((nb, K), dtype=torch.float32, device=device)
+                self.outs.append({"ws": ws, "s": s})
+        self.launches_per_step = sum(2 if p[0] == "hard" else 6 for p in parts)
+
+    def run_part(self, i):
+        p, x, o = self.parts[i], self.inputs[i], self.outs[i]
+        if p[0] == "hard":
+            self.ecc.ecc_hard(x["img"], p[4], p[5], p[6], ndim=x["ndim"], out=o)
+        else:
+            self.ecc.ecc_soft_fwd(x["img"], x["tau"], x["lam"], x["alpha"], x["u"], ws=o["ws"],
+                                  out=o["s"])
+            o["grads"] = self.ecc.ecc_soft_bwd(x["img"], x["tau"], x["lam"], x["alpha"], x["u"],
+                                               x["g"], o["ws"])
+
+    def results(self):
+        res = []
+        for p, o in zip(self.parts, self.outs):
+            if p[0] == "hard":
+                res.append(o)
+            else:
+                res.append(o["s"])
+                res.extend(o["grads"].values())
+        return res
+
+
+def time_ours(args, parts, rank, world, device):
+    import torch
+
+    inputs = make_inputs(parts, device)
+    step = OurStep(parts, inputs, device)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        for i in range(len(parts)):
+            step.run_part(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in parts] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    start.record(stream)
+    for s in range(args.steps):
+        for i in range(len(parts)):
+            ev[s][i][0].record(stream)
+            step.run_part(i)
+            ev[s][i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    total_ms = start.elapsed_time(end)
+    part_ms = [statistics.mean(ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(args.steps))
+               for i in range(len(parts))]
+    total_ms = max_over_ranks(total_ms, world)
+    e2e = time_e2e(args, parts, inputs, step, device, world)
+    return total_ms, part_ms, clocks, step.launches_per_step * args.steps, e2e
+
+
+def time_e2e(args, parts, inputs, step, device, world):
+    """Same step through the public binding with HOST inputs: every step copies its inputs from
+    pinned host memory to the device and reads the results back."""
+    import torch
+
+    host = []
+    h2d = 0
+    for x in inputs:
+        hx = {}
+        for k, v in x.items():
+            if isinstance(v, torch.Tensor):
+                hv = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+                hv.copy_(v)
+                hx[k] = hv
+                h2d += v.numel() * v.element_size()
+        host.append(hx)
+    res_dev = step.results()
+    d2h = sum(t.numel() * t.element_size() for t in res_dev)
+    res_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in res_dev]
+    steps = max(1, min(args.steps, 5))
+    stream = torch.cuda.current_stream()
+
+    def one():
+        for hx, x in zip(host, inputs):
+            for k, hv in hx.items():
+                x[k].copy_(hv, non_blocking=True)
+        for i in range(len(parts)):
+            step.run_part(i)
+        for hr, t in zip(res_host, step.results()):
+            hr.copy_(t, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    barrier(world)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        one()
+    end.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(start.elapsed_time(end) / steps, world)
+    hard_vox = sum(part_voxels(p) for p in parts if p[0] == "hard") or \
+        sum(part_voxels(p) for p in parts)
+    return {"value": round(hard_vox * world / (ms * 1e-3) / 1e9, 3), "unit": "Gvoxels/s",
+            "ms_per_step": round(ms, 3), "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": steps}
+
+
+# ------------------------------------------------------------------------------------ oracle arm
+
+def oracle_sample_step(parts, cache):
+    """The oracle on a bounded sample of every part of the workload; returns voxels processed.
+
+    Samples: 2-D images are cropped to at most 1024 x 1024 (one image of a batch), 3-D volumes
+    to 96 x 256 x 256 voxels, the soft part to one image with all K thresholds (fwd + bwd)."""
+    import numpy as np
+
+    import oracle
+    from euler_characteristic_curves_gb300 import synthetic
+
+    vox = 0
+    for p in parts:
+        key = part_name(p)
+        if key not in cache:
+            if p[0] == "hard":
+                _, shape, batch, kind, nbins, vmin, vmax, seed = p
+                if len(shape) == 2:
+                    sh = (min(shape[0], 1024), min(shape[1], 1024))
+                else:
+                    sh = (min(shape[0], 96), min(shape[1], 256), min(shape[2], 256))
+                if kind == "u8blur":
+                    img = synthetic.blurred_noise_u8(sh, seed)
+                elif kind == "u8grf":
+                    img = synthetic.quantise_u8(synthetic.grf(sh, seed))
+                else:
+                    img = synthetic.grf(sh, seed)
+                cache[key] = img
+            else:
+                _, shape, batch, K, lam, s_img, s_u, s_g = p
+                cache[key] = (synthetic.grf(shape, s_img), synthetic.uniform_thresholds(K),
+                              synthetic.soft_direction(len(shape), s_u),
+                              synthetic.upstream_grad((1, K), s_g))
+        x = cache[key]
+        if p[0] == "hard":
+            oracle.ecc_hard(x, p[4], p[5], p[6])
+            vox += x.size
+        else:
+            img, tau, u, g = x
+            oracle.ecc_soft_fwd(img, tau, p[4], 1.0, u)
+            oracle.ecc_soft_bwd(img, tau, p[4], 1.0, u, g, want_img=False)
+            vox += img.size
+    return vox
+
+
+def time_oracle(steps, warmup, parts):
+    cache = {}
+    for _ in range(warmup):
+        oracle_sample_step(parts, cache)
+    t0 = time.perf_counter()
+    vox = 0
+    for _ in range(steps):
+        vox += oracle_sample_step(parts, cache)
+    dt = time.perf_counter() - t0
+    return vox, dt
+
+
+# ------------------------------------------------------------------------------------ dist
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world, backend):
+    if world > 1:
+        import torch.distributed as dist
+
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Slowest rank's value (timings are maxima over ranks)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------------ main
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="headline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank, world, local = dist_env()
+    parts = WORKLOADS[args.workload]
+    hard_vox = sum(part_voxels(p) for p in parts if p[0] == "hard")
+    unit_vox = hard_vox if hard_vox else sum(part_voxels(p) for p in parts)
+    config = {"workload": DESCRIPTION.get(args.workload, args.workload),
+              "parts": [part_name(p) for p in parts],
+              "l2": "inputs larger than L2 (the 268 MB image and the 4 GiB volume evict L2 "
+                    "between passes)" if args.workload == "headline" else "not flushed",
+              "parallelism": f"independent replicas x{world}"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        vox, dt = time_oracle(args.steps, args.warmup, parts)
+        value = vox / dt / 1e9
+        line = {"impl": "reference", "metric": METRIC, "value": round(value, 6),
+                "unit": "Gvoxels/s", "n_gpus": args.gpus, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f64 oracle on f32/u8 inputs", "data": "synthetic (seeded GRF)",
+                "config": config,
+                "cpu_baseline": {"value": round(value, 6), "unit": "Gvoxels/s", "cores": 1,
+                                 "kind": "oracle",
+                                 "sample": "per step: each 2-D part cropped to <= 1024^2 "
+                                           "(one image), each 3-D part to 96x256x256, soft "
+                                           "part one 256^2 image fwd+bwd"},
+                "e2e": {"value": round(value, 6), "unit": "Gvoxels/s",
+                        "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
+
+    import torch
+
+    init_dist(world, "nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    from euler_characteristic_curves_gb300 import build as libbuild
+
+    libbuild.build()
+    total_ms, part_ms, clocks, launches, e2e = time_ours(args, parts, rank, world, device)
+    ms_step = total_ms / args.steps
+    value = unit_vox * world / (ms_step * 1e-3) / 1e9
+
+    peak, peak_kind = load_peaks()
+    # dominant kernel: the part with the largest device time
+    dom = max(range(len(parts)), key=lambda i: part_ms[i])
+    breakdown = {}
+    for i, p in enumerate(parts):
+        ms = part_ms[i]
+        ent = {"ms": round(ms, 4), "gvoxels_s": round(part_voxels(p) / (ms * 1e-3) / 1e9, 3)}
+        if p[0] == "hard":
+            elem = 1 if p[3].startswith("u8") else 4
+            alg = part_voxels(p) * elem + 8 * p[2] * p[4]
+            ent["hbm_gbs"] = round(alg / (ms * 1e-3) / 1e9, 1)
+            ent["hbm_frac"] = round(alg / (ms * 1e-3) / 1e9 / peak, 4)
+        breakdown[part_name(p)] = ent
+    roofline = None
+    pd = parts[dom]
+    if pd[0] == "hard":
+        elem = 1 if pd[3].startswith("u8") else 4
+        alg = part_voxels(pd) * elem + 8 * pd[2] * pd[4]
+        achieved = alg / (part_ms[dom] * 1e-3) / 1e9
+        key = "ecc_hard3d_kernel" if len(pd[1]) == 3 else "ecc_hard2d_kernel"
+        roofline = {"bound": "hbm", "kernel": key, "achieved": round(achieved, 1),
+                    "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                    "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                    "traffic": recorded_traffic(f"{key}:{part_name(pd)}"),
+                    "algorithmic_bytes": int(alg),
+                    "timing": "CUDA events around the library call (memset + kernel + scan)"}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu_steps = 1
+        vox, dt = time_oracle(cpu_steps, 0, parts)
+        cpu = {"value": round(vox / dt / 1e9, 6), "unit": "Gvoxels/s", "cores": 1,
+               "kind": "oracle", "seconds": round(dt, 2),
+               "sample": "one pass: each 2-D part cropped to <= 1024^2 (one image), each 3-D "
+                         "part to 96x256x256, soft part one 256^2 image fwd+bwd"}
+    soft_ms = [part_ms[i] for i, p in enumerate(parts) if p[0] == "soft"]
+    line = {"metric": METRIC, "value": round(value, 3), "unit": "Gvoxels/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32 compare / int32+int64 histogram (hard); f32 + fp64 reductions (soft)",
+            "data": "synthetic (seeded Gaussian random fields, k^-3 spectrum)",
+            "config": config, "parts": breakdown,
+            "soft_fwd_bwd_ms": round(soft_ms[0], 4) if soft_ms else None,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches, "clocks": clocks,
+            "kernel_source": kernel_source_hash()}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,188 @@
+// ecc_api.cu -- the extern "C" entry points declared in include/ecc.h: argument validation, the
+// exact fp32 threshold tables and the dispatch to the hard / soft kernels.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "ecc.h"
+#include "ecc_internal.cuh"
+
+namespace ecc {
+
+// Thresholds of the hard ECC in fp64: t_0 = vmin, t_{H-1} = vmax, interior
+// vmin + ((vmax - vmin) * k) / (H - 1); a single threshold at vmax when H == 1.
+static double threshold(int k, int H, double vmin, double vmax)
+{
+    if (H == 1 || k == H - 1) return vmax;
+    if (k == 0) return vmin;
+    return vmin + ((vmax - vmin) * (double)k) / (double)(H - 1);
+}
+
+// Largest float <= x.
+static float round_down_f32(double x)
+{
+    float f = (float)x;
+    if ((double)f > x) f = nextafterf(f, -INFINITY);
+    return f;
+}
+
+static bool mul_ok(int64_t a, int64_t b, int64_t &r)
+{
+    if (a < 0 || b < 0) return false;
+    if (a != 0 && b > INT64_MAX / a) return false;
+    r = a * b;
+    return true;
+}
+
+}  // namespace ecc
+
+using namespace ecc;
+
+extern "C" {
+
+const char *ecc_status_str(int status)
+{
+    switch (status) {
+    case ECC_OK: return "ECC_OK";
+    case ECC_EINVAL: return "ECC_EINVAL: invalid argument";
+    case ECC_EDTYPE: return "ECC_EDTYPE: unsupported dtype";
+    case ECC_EDIM: return "ECC_EDIM: unsupported ndim or extent";
+    case ECC_EWS: return "ECC_EWS: workspace missing or too small";
+    case ECC_ECUDA: return "ECC_ECUDA: CUDA error";
+    case ECC_ERANGE: return "ECC_ERANGE: size above the library maximum";
+    default: return "ECC: unknown status";
+    }
+}
+
+int ecc_version(void) { return 10000; }
+
+int ecc_hard(const void *img, int dtype, int ndim, const int64_t *dims, int64_t batch, int nbins,
+             double vmin, double vmax, int64_t *out, ecc_stream_t stream)
+{
+    if (!img || !out || !dims) return ECC_EINVAL;
+    if (dtype != ECC_U8 && dtype != ECC_F32) return ECC_EDTYPE;
+    if (ndim != 2 && ndim != 3) return ECC_EDIM;
+    for (int d = 0; d < ndim; ++d)
+        if (dims[d] < 1) return ECC_EDIM;
+    if (batch < 1) return ECC_EINVAL;
+    if (nbins < 1) return ECC_EINVAL;
+    if (nbins > ECC_MAX_NBINS) return ECC_ERANGE;
+    if (!isfinite(vmin) || !isfinite(vmax) || !(vmin <= vmax) || !isfinite(vmax - vmin))
+        return ECC_EINVAL;
+    const int64_t D = ndim == 3 ? dims[0] : 1;
+    const int64_t Hy = dims[ndim - 2], W = dims[ndim - 1];
+    int64_t plane, elems, total, outn;
+    if (!mul_ok(Hy, W, plane) || !mul_ok(plane, D, elems) || !mul_ok(elems, batch, total) ||
+        total > ((int64_t)1 << 50) || !mul_ok(batch, nbins, outn) || batch > 65535)
+        return ECC_ERANGE;
+
+    HardPlan pl;
+    pl.ndim = ndim;
+    pl.dtype = dtype;
+    pl.D = D;
+    pl.Hy = Hy;
+    pl.W = W;
+    pl.batch = batch;
+    pl.H = nbins;
+    pl.img = img;
+    pl.out = out;
+    float table[ECC_MAX_NBINS + 2];
+    const int H = nbins;
+    if (dtype == ECC_U8) {
+        // key of every byte value: first k with b <= t_k (H if none)
+        for (int v = 0; v < 256; ++v) {
+            int lo = 0, hi = H;
+            while (lo < hi) {
+                const int mid = (lo + hi) / 2;
+                if ((double)v <= threshold(mid, H, vmin, vmax))
+                    hi = mid;
+                else
+                    lo = mid + 1;
+            }
+            table[v] = (float)lo;
+        }
+        pl.key_mode = kKeyLut;
+        pl.scale = pl.offset = 0.0f;
+        pl.vec_ok = ((uintptr_t)img % 4 == 0) && (W % 4 == 0);
+    } else {
+        for (int k = 0; k < H; ++k) table[k] = round_down_f32(threshold(k, H, vmin, vmax));
+        table[H] = table[H + 1] = INFINITY;
+        // Estimator t = v * scale + offset; its error in bins (fp64 threshold rounding plus fp32
+        // evaluation) must stay below 1/4 for the two-comparison correction to be exact.
+        pl.key_mode = kKeySearch;
+        pl.scale = pl.offset = 0.0f;
+        if (H >= 2 && vmax > vmin) {
+            const double s = (double)(H - 1) / (vmax - vmin);
+            const double M = fmax(fabs(vmin), fabs(vmax));
+            const double err = ldexp(1.0, -22) * (M * s + (double)H + 2.0);
+            if (isfinite(s) && s < 1e30 && err <= 0.25) {
+                pl.key_mode = kKeyEstimate;
+                pl.scale = (float)s;
+                pl.offset = (float)(-vmin * s);
+            }
+        }
+        pl.vec_ok = ((uintptr_t)img % 16 == 0) && (W % 4 == 0);
+    }
+    pl.table = table;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(out, 0, sizeof(int64_t) * (size_t)outn, s) != cudaSuccess)
+        return ECC_ECUDA;
+    if (hard_run(pl, s) != cudaSuccess) return ECC_ECUDA;
+    return ECC_OK;
+}
+
+size_t ecc_soft_workspace_bytes(int ndim, const int64_t *dims, int64_t batch, int K)
+{
+    SoftLayout L;
+    if (!soft_layout(ndim, dims, batch, K, L)) return 0;
+    return L.total;
+}
+
+static int soft_check(const float *img, int ndim, const int64_t *dims, int64_t batch,
+                      const float *tau, int K, float lambda, const float *alpha, const float *u,
+                      void *ws, size_t ws_bytes, SoftLayout &L)
+{
+    if (!img || !dims || !tau || !alpha || !u) return ECC_EINVAL;
+    if (ndim != 2) return ECC_EDIM;
+    for (int d = 0; d < ndim; ++d)
+        if (dims[d] < 1) return ECC_EDIM;
+    if (batch < 1 || K < 1) return ECC_EINVAL;
+    if (K > ECC_MAX_K || batch > 65535) return ECC_ERANGE;
+    if (!(lambda > 0.0f) || !isfinite(lambda)) return ECC_EINVAL;
+    if (!soft_layout(ndim, dims, batch, K, L)) return ECC_ERANGE;
+    if (L.tiles > 2147483647) return ECC_ERANGE;
+    if (!ws || ws_bytes < L.total || ((uintptr_t)ws % 256) != 0) return ECC_EWS;
+    return ECC_OK;
+}
+
+int ecc_soft_fwd(const float *img, int ndim, const int64_t *dims, int64_t batch, const float *tau,
+                 int K, float lambda, const float *alpha, const float *u, float *out, void *ws,
+                 size_t ws_bytes, ecc_stream_t stream)
+{
+    SoftLayout L;
+    const int rc = soft_check(img, ndim, dims, batch, tau, K, lambda, alpha, u, ws, ws_bytes, L);
+    if (rc != ECC_OK) return rc;
+    if (!out) return ECC_EINVAL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (soft_run_fwd(L, img, tau, lambda, alpha, u, out, ws, s) != cudaSuccess) return ECC_ECUDA;
+    return ECC_OK;
+}
+
+int ecc_soft_bwd(const float *img, int ndim, const int64_t *dims, int64_t batch, const float *tau,
+                 int K, float lambda, const float *alpha, const float *u, const float *grad_out,
+                 float *grad_tau, float *grad_alpha, float *grad_u, float *grad_img, void *ws,
+                 size_t ws_bytes, ecc_stream_t stream)
+{
+    SoftLayout L;
+    const int rc = soft_check(img, ndim, dims, batch, tau, K, lambda, alpha, u, ws, ws_bytes, L);
+    if (rc != ECC_OK) return rc;
+    if (!grad_out || !grad_tau || !grad_alpha || !grad_u) return ECC_EINVAL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (soft_run_bwd(L, img, tau, lambda, alpha, grad_out, grad_tau, grad_alpha, grad_u, grad_img,
+                     ws, s) != cudaSuccess)
+        return ECC_ECUDA;
+    return ECC_OK;
+}
+
+}  // extern "C"

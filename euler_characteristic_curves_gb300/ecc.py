@@ -1,0 +1,242 @@
+"""Thin Python binding of the C ABI in include/ecc.h (argument marshalling only).
+
+Every computation runs in the CUDA library libecc_gb300.so; this module checks shapes, passes
+device pointers, sizes and the current CUDA stream, and turns negative status codes into
+exceptions. There is no CPU path: CPU tensors are rejected, and a missing library raises.
+
+Names follow the C entry points: ``ecc_hard``, ``ecc_soft_fwd``, ``ecc_soft_bwd``,
+``soft_workspace_bytes``; ``SoftECC`` / ``soft_ecc`` wrap the soft pair as a differentiable
+PyTorch layer ("Key designs -- differentiable ECC layer (sigmoid relaxation)" in the paper notes
+"Scalable GPU-Accelerated Euler Characteristic Curves").
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+ECC_U8, ECC_F32 = 0, 1
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library():
+    """Load libecc_gb300.so (built in-tree by ``build.build()``); raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"ECC CUDA library not found at {path}; build it first with "
+                "`python -m euler_characteristic_curves_gb300.build` (there is no CPU fallback)")
+        lib = ctypes.CDLL(path)
+        p, i, i64, d, f, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double,
+                               ctypes.c_float, ctypes.c_size_t)
+        lib.ecc_hard.argtypes = [p, i, i, p, i64, i, d, d, p, p]
+        lib.ecc_hard.restype = i
+        lib.ecc_soft_workspace_bytes.argtypes = [i, p, i64, i]
+        lib.ecc_soft_workspace_bytes.restype = sz
+        lib.ecc_soft_fwd.argtypes = [p, i, p, i64, p, i, f, p, p, p, p, sz, p]
+        lib.ecc_soft_fwd.restype = i
+        lib.ecc_soft_bwd.argtypes = [p, i, p, i64, p, i, f, p, p, p, p, p, p, p, p, sz, p]
+        lib.ecc_soft_bwd.restype = i
+        lib.ecc_status_str.argtypes = [i]
+        lib.ecc_status_str.restype = ctypes.c_char_p
+        lib.ecc_version.argtypes = []
+        lib.ecc_version.restype = i
+        _lib = lib
+        return lib
+
+
+class ECCError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        msg = load_library().ecc_status_str(status).decode()
+        super().__init__(f"{where}: {msg} (status {status})")
+        self.status = status
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        raise ECCError(rc, where)
+
+
+def _dims_array(dims):
+    arr = (ctypes.c_int64 * len(dims))(*[int(x) for x in dims])
+    return arr
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need_cuda(t: torch.Tensor, name: str):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor (the ECC library has no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _split(img: torch.Tensor, ndim):
+    if ndim is None:
+        if img.dim() == 2:
+            ndim = 2
+        elif img.dim() == 4:
+            ndim = 3
+        else:
+            raise ValueError("pass ndim=2 (batch of images) or ndim=3 (one volume) for a 3-D "
+                             "tensor")
+    if img.dim() == ndim:
+        return ndim, 1, tuple(img.shape), False
+    if img.dim() == ndim + 1:
+        return ndim, img.shape[0], tuple(img.shape[1:]), True
+    raise ValueError(f"tensor of shape {tuple(img.shape)} is not a {ndim}-D image or a batch")
+
+
+def ecc_hard(img: torch.Tensor, nbins: int, vmin: float, vmax: float, ndim: int | None = None,
+             out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Hard ECC: int64 [batch, nbins] (or [nbins] for one unbatched image) on img's device.
+
+    img: uint8 or float32 CUDA tensor [(B,) (D,) H, W]. Thresholds t_k are nbins uniform values
+    from vmin to vmax inclusive; out[b, k] = ECC of image b at t_k.
+    """
+    _need_cuda(img, "img")
+    if img.dtype == torch.uint8:
+        dt = ECC_U8
+    elif img.dtype == torch.float32:
+        dt = ECC_F32
+    else:
+        raise TypeError(f"img dtype {img.dtype}: uint8 or float32 expected")
+    ndim, batch, dims, batched = _split(img, ndim)
+    if out is None:
+        out = torch.empty((batch, nbins), dtype=torch.int64, device=img.device)
+    else:
+        _need_cuda(out, "out")
+        if out.dtype != torch.int64 or out.numel() != batch * nbins:
+            raise ValueError("out must be int64 with batch * nbins elements")
+    lib = load_library()
+    rc = lib.ecc_hard(ctypes.c_void_p(img.data_ptr()), dt, ndim, _dims_array(dims), batch,
+                      int(nbins), float(vmin), float(vmax), ctypes.c_void_p(out.data_ptr()),
+                      _stream_handle(stream))
+    _check(rc, "ecc_hard")
+    out = out.view(batch, nbins)
+    return out if batched else out[0]
+
+
+def soft_workspace_bytes(dims, batch: int, K: int) -> int:
+    lib = load_library()
+    return int(lib.ecc_soft_workspace_bytes(len(dims), _dims_array(dims), int(batch), int(K)))
+
+
+def _soft_common(img, tau, alpha, u, ndim):
+    _need_cuda(img, "img")
+    if img.dtype != torch.float32:
+        raise TypeError("soft ECC takes float32 images")
+    ndim = 2 if ndim is None else ndim
+    ndim, batch, dims, batched = _split(img, ndim)
+    for name, t in (("tau", tau), ("alpha", alpha), ("u", u)):
+        _need_cuda(t, name)
+        if t.dtype != torch.float32:
+            raise TypeError(f"{name} must be float32")
+    if alpha.numel() != 1 or u.numel() != ndim:
+        raise ValueError(f"alpha must have 1 element and u {ndim}")
+    return ndim, batch, dims, batched
+
+
+def _workspace(ws, dims, batch, K, device):
+    need = soft_workspace_bytes(dims, batch, K)
+    if need == 0:
+        raise ValueError("unsupported soft-ECC sizes")
+    if ws is None:
+        ws = torch.empty(need, dtype=torch.uint8, device=device)
+    elif ws.numel() < need:
+        raise ValueError(f"workspace of {ws.numel()} bytes, {need} needed")
+    return ws
+
+
+def ecc_soft_fwd(img, tau, lam: float, alpha, u, ws=None, out=None, ndim=None, stream=None):
+    """Soft ECC S[b, k] (float32). Returns (S, ws); pass ws unchanged to ecc_soft_bwd."""
+    ndim, batch, dims, batched = _soft_common(img, tau, alpha, u, ndim)
+    K = tau.numel()
+    ws = _workspace(ws, dims, batch, K, img.device)
+    if out is None:
+        out = torch.empty((batch, K), dtype=torch.float32, device=img.device)
+    lib = load_library()
+    rc = lib.ecc_soft_fwd(ctypes.c_void_p(img.data_ptr()), ndim, _dims_array(dims), batch,
+                          ctypes.c_void_p(tau.data_ptr()), K, float(lam),
+                          ctypes.c_void_p(alpha.data_ptr()), ctypes.c_void_p(u.data_ptr()),
+                          ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(ws.data_ptr()),
+                          ws.numel(), _stream_handle(stream))
+    _check(rc, "ecc_soft_fwd")
+    out = out.view(batch, K)
+    return (out if batched else out[0]), ws
+
+
+def ecc_soft_bwd(img, tau, lam: float, alpha, u, grad_out, ws, want_img: bool = False, ndim=None,
+                 stream=None):
+    """Analytic gradients of sum(grad_out * S): dict of float32 CUDA tensors grad_tau [K],
+    grad_alpha [1], grad_u [ndim] and, when want_img, grad_img (img's shape)."""
+    ndim, batch, dims, batched = _soft_common(img, tau, alpha, u, ndim)
+    K = tau.numel()
+    _need_cuda(grad_out, "grad_out")
+    if grad_out.dtype != torch.float32 or grad_out.numel() != batch * K:
+        raise ValueError("grad_out must be float32 with batch * K elements")
+    ws = _workspace(ws, dims, batch, K, img.device)
+    dev = img.device
+    gt = torch.empty(K, dtype=torch.float32, device=dev)
+    ga = torch.empty(1, dtype=torch.float32, device=dev)
+    gu = torch.empty(ndim, dtype=torch.float32, device=dev)
+    gi = torch.empty_like(img) if want_img else None
+    lib = load_library()
+    rc = lib.ecc_soft_bwd(ctypes.c_void_p(img.data_ptr()), ndim, _dims_array(dims), batch,
+                          ctypes.c_void_p(tau.data_ptr()), K, float(lam),
+                          ctypes.c_void_p(alpha.data_ptr()), ctypes.c_void_p(u.data_ptr()),
+                          ctypes.c_void_p(grad_out.data_ptr()), ctypes.c_void_p(gt.data_ptr()),
+                          ctypes.c_void_p(ga.data_ptr()), ctypes.c_void_p(gu.data_ptr()),
+                          ctypes.c_void_p(gi.data_ptr() if gi is not None else None),
+                          ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream_handle(stream))
+    _check(rc, "ecc_soft_bwd")
+    res = {"grad_tau": gt, "grad_alpha": ga, "grad_u": gu}
+    if want_img:
+        res["grad_img"] = gi
+    return res
+
+
+class SoftECC(torch.autograd.Function):
+    """Differentiable soft ECC layer: S = SoftECC.apply(img, tau, alpha, u, lam).
+
+    img float32 [(B,) H, W]; tau [K]; alpha [1]; u [2] (learnable); lam a Python float.
+    Gradients flow to tau, alpha, u and, when it requires grad, img.
+    """
+
+    @staticmethod
+    def forward(ctx, img, tau, alpha, u, lam):
+        img, tau, alpha, u = (t.contiguous() for t in (img, tau, alpha, u))
+        out, ws = ecc_soft_fwd(img, tau, lam, alpha, u)
+        ctx.save_for_backward(img, tau, alpha, u, ws)
+        ctx.lam = float(lam)
+        return out
+
+    @staticmethod
+    def backward(ctx, grad_out):
+        img, tau, alpha, u, ws = ctx.saved_tensors
+        res = ecc_soft_bwd(img, tau, ctx.lam, alpha, u, grad_out.contiguous().float(), ws,
+                           want_img=ctx.needs_input_grad[0])
+        gi = res.get("grad_img")
+        return (gi, res["grad_tau"], res["grad_alpha"].view_as(alpha), res["grad_u"].view_as(u),
+                None)
+
+
+def soft_ecc(img, tau, alpha, u, lam: float):
+    return SoftECC.apply(img, tau, alpha, u, lam)

@@ -1,0 +1,148 @@
+/*
+ * ecc.h -- C ABI of the GB300 (sm_103a) Euler-characteristic-curve library.
+ *
+ * Method: the paper notes "Scalable GPU-Accelerated Euler Characteristic Curves: Optimization and
+ * Differentiable Learning for PyTorch" (NeurIPS 2025 NeurReps workshop, arXiv 2510.20271):
+ *   - "Key designs -- full-scan CUDA kernel": one pass over the whole grid, a privatised histogram
+ *     of local Euler contributions per thread block, one global flush per block;
+ *   - "Key designs -- local computation of the Euler characteristic coefficient": the ECC is a sum
+ *     of per-voxel contributions c(p), each read off the 3x3 (2-D) or 3x3x3 (3-D) neighbourhood;
+ *   - "Key designs -- differentiable ECC layer (sigmoid relaxation)": 1[X <= t] becomes
+ *     sigma(lambda (t - X)) with X(p) = alpha f(p) + u . x_p; custom forward and backward kernels
+ *     return analytic gradients for the thresholds, alpha and u.
+ *
+ * Conventions shared by every entry point
+ *   - Images are C-contiguous, last axis fastest: a batch of 2-D images is [batch][H][W], of 3-D
+ *     volumes [batch][D][H][W]. `dims` is a HOST array of `ndim` extents, slowest axis first.
+ *   - Pointers named img, out, tau, alpha, u, grad_*, ws are DEVICE pointers owned by the caller;
+ *     the library never allocates, frees or retains them, and allocates no device memory itself.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL means the legacy default
+ *     stream). Arguments are validated on the host before anything is launched; an invalid call
+ *     returns a negative status and touches no memory. A failed launch returns ECC_ECUDA; errors
+ *     raised later by a kernel surface at the caller's next synchronisation.
+ *   - The library holds no state between calls and may be called from several host threads.
+ *   - Cell complex: the V-construction. Voxels are vertices; axis-aligned boxes of side 0 or 1 in
+ *     each axis whose corners all lie in the grid are cells (edges, squares, cubes); a cell's value
+ *     is the max of its vertices. Voxels outside the grid do not exist.
+ */
+#ifndef ECC_GB300_ECC_H
+#define ECC_GB300_ECC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared here so this header needs no CUDA headers. */
+struct CUstream_st;
+typedef struct CUstream_st *ecc_stream_t;
+
+/* Element types of the hard-ECC input. */
+enum ecc_dtype { ECC_U8 = 0, ECC_F32 = 1 };
+
+/* Status codes. */
+enum ecc_status {
+    ECC_OK = 0,
+    ECC_EINVAL = -1,  /* a NULL pointer, a non-positive size, vmin > vmax, a non-finite bound... */
+    ECC_EDTYPE = -2,  /* dtype is not ECC_U8 or ECC_F32 */
+    ECC_EDIM = -3,    /* ndim outside the supported set, or an extent < 1 */
+    ECC_EWS = -4,     /* workspace NULL or smaller than ecc_soft_workspace_bytes() */
+    ECC_ECUDA = -5,   /* a CUDA call failed (no device, launch failure...) */
+    ECC_ERANGE = -6   /* nbins or K above the library maximum, or a size that overflows */
+};
+
+#define ECC_MAX_NBINS 4096 /* largest nbins accepted by ecc_hard */
+#define ECC_MAX_K 8192     /* largest number of soft thresholds */
+
+/*
+ * Hard Euler characteristic curve of a batch of 2-D images or 3-D volumes.
+ *
+ * Section "Key designs -- full-scan CUDA kernel" and "local computation of the Euler
+ * characteristic coefficient" of the ECC paper notes.
+ *
+ *   out[b * nbins + k] = sum over cells sigma of image b with every vertex value <= t_k of
+ *                        (-1)^dim(sigma)                                            (int64)
+ *   t_0 = vmin, t_{nbins-1} = vmax, t_k = vmin + ((vmax - vmin) * k) / (nbins - 1) in fp64;
+ *   nbins == 1 gives the single threshold vmax.
+ *
+ * img     device pointer, batch * prod(dims) elements of type dtype (uint8 or float32), any
+ *         alignment (a 16-byte-aligned base with a row length divisible by 4 takes the
+ *         vectorised fast path). Values are compared exactly as fp64 against t_k: NaN and
+ *         values above vmax never enter; values below vmin enter at t_0.
+ * dtype   ECC_U8 or ECC_F32.
+ * ndim    2 ([H][W] per image) or 3 ([D][H][W] per image).
+ * dims    host array of ndim extents, each >= 1, slowest first.
+ * batch   number of independent images (>= 1); no cell joins two images.
+ * nbins   number of thresholds, 1 <= nbins <= ECC_MAX_NBINS.
+ * vmin, vmax  finite, vmin <= vmax.
+ * out     device pointer to batch * nbins int64; fully overwritten.
+ * Returns ECC_OK, or ECC_EINVAL / ECC_EDTYPE / ECC_EDIM / ECC_ERANGE / ECC_ECUDA.
+ */
+int ecc_hard(const void *img, int dtype, int ndim, const int64_t *dims, int64_t batch, int nbins,
+             double vmin, double vmax, int64_t *out, ecc_stream_t stream);
+
+/*
+ * Workspace bytes that ecc_soft_fwd / ecc_soft_bwd need for these sizes (0 when the sizes are
+ * invalid). The workspace holds the per-voxel critical list written by the forward call and read
+ * by the backward call, plus per-block partial sums.
+ */
+size_t ecc_soft_workspace_bytes(int ndim, const int64_t *dims, int64_t batch, int K);
+
+/*
+ * Soft (sigmoid-relaxed) ECC, forward.
+ *
+ * Section "Key designs -- differentiable ECC layer (sigmoid relaxation)" of the ECC paper notes.
+ *
+ *   X(p)        = alpha * f(p) + sum_d u[d] * x_{p,d},  x_{p,d} = (2 i_d - (n_d - 1)) / (n_d - 1)
+ *                 (0 on an axis of extent 1): coordinates centred and scaled to [-1, 1].
+ *   out[b * K + k] = sum over cells sigma of image b of
+ *                 (-1)^dim(sigma) / (1 + exp(-lambda (tau[k] - max_{v in sigma} X(v))))   (fp32)
+ *
+ * img     device float32 [batch][dims...]; finite values.
+ * ndim    2 (3-D volumes are not supported by the soft path yet: ECC_EDIM).
+ * tau     device float32 [K] thresholds, any order.
+ * K       1 <= K <= ECC_MAX_K.
+ * lambda  sigmoid sharpness, finite and > 0.
+ * alpha   device float32 [1]; u: device float32 [ndim]. tau, alpha and u are shared by the batch.
+ * out     device float32 [batch][K]; fully overwritten.
+ * ws      device workspace of at least ecc_soft_workspace_bytes(ndim, dims, batch, K) bytes,
+ *         256-byte aligned. The forward call fills it; keep it unchanged for the backward call.
+ * Returns ECC_OK or a negative status (ECC_EWS for a missing or short workspace).
+ */
+int ecc_soft_fwd(const float *img, int ndim, const int64_t *dims, int64_t batch, const float *tau,
+                 int K, float lambda, const float *alpha, const float *u, float *out, void *ws,
+                 size_t ws_bytes, ecc_stream_t stream);
+
+/*
+ * Soft ECC, backward: analytic gradients of L = sum_{b,k} grad_out[b,k] * out[b,k].
+ *
+ * Section "Key designs -- differentiable ECC layer (sigmoid relaxation)" ("a custom CUDA backward
+ * kernel computes analytic gradients") of the ECC paper notes. With s = sigma(lambda (tau_k - X))
+ * evaluated at each cell's argmax vertex o (ties: the larger linear index owns the cell):
+ *   grad_tau[k]   = sum_{b, cells} grad_out[b,k] (-1)^dim lambda s (1 - s)
+ *   dX[b, o]      = - sum_{k, cells owned by o} grad_out[b,k] (-1)^dim lambda s (1 - s)
+ *   grad_alpha[0] = sum_{b,p} dX[b,p] f[b,p];   grad_u[d] = sum_{b,p} dX[b,p] x_{p,d}
+ *   grad_img      = alpha dX                    (optional; pass NULL to skip)
+ *
+ * Arguments as for ecc_soft_fwd, with the same img, tau, K, lambda, alpha, u and the workspace
+ * filled by the forward call. grad_out: device float32 [batch][K]. grad_tau [K], grad_alpha [1],
+ * grad_u [ndim], grad_img [batch][dims...] (nullable): device float32, fully overwritten.
+ */
+int ecc_soft_bwd(const float *img, int ndim, const int64_t *dims, int64_t batch, const float *tau,
+                 int K, float lambda, const float *alpha, const float *u, const float *grad_out,
+                 float *grad_tau, float *grad_alpha, float *grad_u, float *grad_img, void *ws,
+                 size_t ws_bytes, ecc_stream_t stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *ecc_status_str(int status);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int ecc_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ECC_GB300_ECC_H */

@@ -1,0 +1,125 @@
+"""The C-ABI library on a machine without a GPU: it loads, exports every function that
+include/ecc.h declares, and its host-side validation returns the documented status codes before
+any CUDA call (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from euler_characteristic_curves_gb300 import build as libbuild
+from euler_characteristic_curves_gb300 import ecc
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "ecc.h")
+OK, EINVAL, EDTYPE, EDIM, EWS, ECUDA, ERANGE = 0, -1, -2, -3, -4, -5, -6
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return ecc.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ecc_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert {"ecc_hard", "ecc_soft_fwd", "ecc_soft_bwd", "ecc_soft_workspace_bytes",
+            "ecc_status_str", "ecc_version"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_version(lib):
+    for code in (OK, EINVAL, EDTYPE, EDIM, EWS, ECUDA, ERANGE, 12345):
+        s = lib.ecc_status_str(code)
+        assert isinstance(s, bytes) and len(s) > 0
+    assert lib.ecc_status_str(EWS).startswith(b"ECC_EWS")
+    assert lib.ecc_version() >= 10000
+
+
+def dims(*v):
+    return (ctypes.c_int64 * len(v))(*v)
+
+
+FAKE = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
+
+
+def test_hard_validation(lib):
+    d2 = dims(8, 8)
+    h = lib.ecc_hard
+    assert h(None, 1, 2, d2, 1, 4, 0.0, 1.0, FAKE, None) == EINVAL
+    assert h(FAKE, 1, 2, d2, 1, 4, 0.0, 1.0, None, None) == EINVAL
+    assert h(FAKE, 1, 2, None, 1, 4, 0.0, 1.0, FAKE, None) == EINVAL
+    assert h(FAKE, 7, 2, d2, 1, 4, 0.0, 1.0, FAKE, None) == EDTYPE
+    assert h(FAKE, 1, 1, d2, 1, 4, 0.0, 1.0, FAKE, None) == EDIM
+    assert h(FAKE, 1, 4, dims(2, 2, 2, 2), 1, 4, 0.0, 1.0, FAKE, None) == EDIM
+    assert h(FAKE, 1, 2, dims(0, 8), 1, 4, 0.0, 1.0, FAKE, None) == EDIM
+    assert h(FAKE, 1, 2, d2, 0, 4, 0.0, 1.0, FAKE, None) == EINVAL
+    assert h(FAKE, 1, 2, d2, 1, 0, 0.0, 1.0, FAKE, None) == EINVAL
+    assert h(FAKE, 1, 2, d2, 1, 4097, 0.0, 1.0, FAKE, None) == ERANGE
+    assert h(FAKE, 1, 2, d2, 1, 4, 1.0, 0.0, FAKE, None) == EINVAL
+    assert h(FAKE, 1, 2, d2, 1, 4, float("nan"), 1.0, FAKE, None) == EINVAL
+    assert h(FAKE, 1, 2, d2, 1, 4, 0.0, float("inf"), FAKE, None) == EINVAL
+    assert h(FAKE, 1, 2, d2, 1, 4, -1.7e308, 1.7e308, FAKE, None) == EINVAL
+    assert h(FAKE, 1, 2, dims(1 << 40, 1 << 30), 1, 4, 0.0, 1.0, FAKE, None) == ERANGE
+
+
+def test_soft_workspace_size(lib):
+    w = lib.ecc_soft_workspace_bytes
+    assert w(2, dims(256, 256), 64, 128) > 64 * 256 * 256 * 16
+    assert w(2, dims(256, 256), 64, 128) % 256 == 0
+    assert w(2, dims(256, 256), 64, 256) > w(2, dims(256, 256), 64, 128)
+    assert w(3, dims(8, 8, 8), 1, 4) == 0
+    assert w(2, dims(0, 8), 1, 4) == 0
+    assert w(2, dims(8, 8), 0, 4) == 0
+    assert w(2, dims(8, 8), 1, 0) == 0
+    assert w(2, dims(8, 8), 1, 8193) == 0
+
+
+def test_soft_validation(lib):
+    d2 = dims(16, 16)
+    need = lib.ecc_soft_workspace_bytes(2, d2, 1, 8)
+    ws = ctypes.c_void_p(0x100000)  # 256-byte aligned fake address
+    f = lib.ecc_soft_fwd
+    args = [FAKE, 2, d2, 1, FAKE, 8, 50.0, FAKE, FAKE, FAKE, ws, need, None]
+
+    def call(**over):
+        a = list(args)
+        names = ["img", "ndim", "dims", "batch", "tau", "K", "lam", "alpha", "u", "out", "ws",
+                 "ws_bytes", "stream"]
+        for k, v in over.items():
+            a[names.index(k)] = v
+        return f(*a)
+
+    assert call(img=None) == EINVAL
+    assert call(tau=None) == EINVAL
+    assert call(alpha=None) == EINVAL
+    assert call(u=None) == EINVAL
+    assert call(out=None) == EINVAL
+    assert call(ndim=3, dims=dims(4, 4, 4)) == EDIM
+    assert call(K=0) == EINVAL
+    assert call(K=8193) == ERANGE
+    assert call(lam=0.0) == EINVAL
+    assert call(lam=float("nan")) == EINVAL
+    assert call(ws=None) == EWS
+    assert call(ws_bytes=need - 1) == EWS
+    assert call(ws=ctypes.c_void_p(0x100010)) == EWS  # misaligned
+    b = lib.ecc_soft_bwd
+    assert b(FAKE, 2, d2, 1, FAKE, 8, 50.0, FAKE, FAKE, None, FAKE, FAKE, FAKE, None, ws, need,
+             None) == EINVAL
+    assert b(FAKE, 2, d2, 1, FAKE, 8, 50.0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, need,
+             None) == EWS
+
+
+def test_binding_rejects_cpu_tensors():
+    import torch
+
+    with pytest.raises(TypeError):
+        ecc.ecc_hard(torch.zeros(4, 4), 4, 0.0, 1.0)
+    with pytest.raises(TypeError):
+        ecc.ecc_soft_fwd(torch.zeros(4, 4), torch.zeros(3), 1.0, torch.ones(1), torch.zeros(2))

@@ -1,0 +1,226 @@
+"""GPU parity for the hard ECC: the CUDA library (through the C ABI binding) against the CPU
+oracle, bit-exact (int64), on seeded inputs.
+
+Covers small shapes spanning several tiles with ragged tails, every special case the method has
+(NaN, infinities, out-of-range values, ties, constant and checkerboard images, degenerate
+threshold ranges, misaligned buffers, nbins from 1 to the maximum), 2-D and 3-D, uint8 and
+float32, batches, and each benchmark workload at full size in the benchmark's launch
+configuration (the library derives the launch from the sizes). The 1024^3 volume is too large
+for the oracle; it is checked through inclusion-exclusion over slabs, a property of the Euler
+characteristic that holds at any size, with oracle-checked slabs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from euler_characteristic_curves_gb300 import ecc, synthetic
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def gpu_hard(img, nbins, vmin, vmax, ndim=None):
+    t = torch.from_numpy(np.ascontiguousarray(img)).to(DEV)
+    return ecc.ecc_hard(t, nbins, vmin, vmax, ndim=ndim).cpu().numpy()
+
+
+def check(img, nbins, vmin, vmax, ndim=None):
+    got = gpu_hard(img, nbins, vmin, vmax, ndim)
+    want = oracle.ecc_hard(img, nbins, vmin, vmax, ndim=ndim)
+    np.testing.assert_array_equal(got, want)
+    return got
+
+
+def rand_field(shape, seed, kind="grf"):
+    rng = np.random.default_rng(seed)
+    if kind == "grf" and len(shape) >= 2 and min(shape) >= 2:
+        return synthetic.grf(shape, seed)
+    if kind == "ties":
+        return rng.integers(0, 6, size=shape).astype(np.float32) / 5.0
+    return rng.random(shape).astype(np.float32)
+
+
+SIZES_H = [1, 2, 3, 5, 8, 17, 31, 32, 33, 67]
+SIZES_W = [1, 2, 3, 4, 5, 7, 8, 31, 127, 128, 129, 131, 260, 515]
+
+
+@pytest.mark.parametrize("h", SIZES_H)
+def test_2d_size_sweep_f32(h):
+    for i, w in enumerate(SIZES_W):
+        for kind in ("grf", "ties"):
+            f = rand_field((h, w), 100 * h + i, kind)
+            check(f, 37, 0.0, 1.0)
+
+
+@pytest.mark.parametrize("h", SIZES_H)
+def test_2d_size_sweep_u8(h):
+    rng = np.random.default_rng(h)
+    for w in SIZES_W:
+        q = rng.integers(0, 256, size=(h, w)).astype(np.uint8)
+        check(q, 256, 0.0, 255.0)
+        check(q // 40, 5, 0.0, 4.0)  # heavy ties
+        check(q, 17, 30.0, 200.0)
+
+
+def test_2d_batches_and_large_ragged():
+    f = synthetic.grf((300, 517), 5, batch=3)
+    check(f, 100, 0.0, 1.0, ndim=2)
+    q = synthetic.quantise_u8(synthetic.grf((129, 1031), 6, batch=4))
+    check(q, 256, 0.0, 255.0, ndim=2)
+    f = synthetic.grf((1000, 1000), 7)
+    check(f, 1024, 0.0, 1.0)
+
+
+@pytest.mark.parametrize("nbins", [1, 2, 3, 255, 256, 1000, 1024, 1025, 4096])
+def test_nbins_variants(nbins):
+    f = synthetic.grf((97, 203), nbins)
+    check(f, nbins, 0.0, 1.0)
+    check(f, nbins, 0.2, 0.7)
+    q = synthetic.quantise_u8(f)
+    check(q, nbins, 0.0, 255.0)
+
+
+def test_special_values():
+    f = synthetic.grf((64, 160), 8)
+    g = f.copy()
+    g[3, 4] = np.nan
+    g[10:13, 50:60] = np.inf
+    g[20, :] = -np.inf
+    g[30, 7] = 5.0
+    g[40, 100] = -3.0
+    g[63, 159] = np.nan
+    g[0, 0] = np.nan
+    check(g, 50, 0.0, 1.0)
+    check(g, 50, -4.0, 6.0)
+    check(np.full((33, 45), np.nan, np.float32), 10, 0.0, 1.0)
+    check(np.full((33, 45), 0.5, np.float32), 11, 0.0, 1.0)
+    check(np.full((33, 45), -0.0, np.float32), 3, -1.0, 0.0)
+    z = np.zeros((16, 16), np.float32)
+    z[::2, ::2] = -0.0
+    check(z, 2, -1.0, 0.0)
+    cb = (np.indices((41, 66)).sum(0) % 2).astype(np.float32)
+    check(cb, 2, 0.0, 1.0)
+    check(cb.astype(np.uint8), 2, 0.0, 1.0)
+    check(1.0 - cb, 3, 0.0, 1.0)
+
+
+def test_threshold_edges_exact():
+    # values that sit exactly on, or one ulp around, every threshold
+    H = 64
+    t = oracle.thresholds(H, 0.0, 1.0)
+    vals = []
+    for x in t:
+        x32 = np.float32(x)
+        vals += [np.nextafter(x32, np.float32(-1)), x32, np.nextafter(x32, np.float32(2))]
+    vals = np.asarray(vals, np.float32)
+    rng = np.random.default_rng(9)
+    img = rng.choice(vals, size=(50, 77)).astype(np.float32)
+    check(img, H, 0.0, 1.0)
+    img = rng.choice(np.arange(256, dtype=np.float32), size=(50, 77))
+    check(img, 256, 0.0, 255.0)  # integer thresholds: exact ties with data
+
+
+def test_degenerate_and_badly_conditioned_ranges():
+    f = synthetic.grf((40, 90), 10)
+    check(f, 5, 0.5, 0.5)  # all thresholds equal
+    check(f, 1, 0.25, 0.25)
+    big = (f.astype(np.float64) * 1e-3 + 1000.0).astype(np.float32)
+    check(big, 1024, 1000.0, 1000.001)  # offset >> range: search mode
+    check(big, 700, 1000.0002, 1000.0009)
+    check(-f, 200, -1.0, 0.0)
+    check(f * 3e38, 100, 0.0, 3e38)
+    check(f * 1e-38, 100, 0.0, 1e-38)  # subnormal thresholds
+
+
+@pytest.mark.parametrize("offset", [1, 2, 3])
+def test_misaligned_buffers(offset):
+    f = synthetic.grf((37, 128), 11 + offset)
+    base = torch.zeros(f.size + 8, dtype=torch.float32, device=DEV)
+    view = base[offset: offset + f.size].view(37, 128)
+    view.copy_(torch.from_numpy(f).to(DEV))
+    got = ecc.ecc_hard(view, 64, 0.0, 1.0).cpu().numpy()
+    np.testing.assert_array_equal(got, oracle.ecc_hard(f, 64, 0.0, 1.0))
+    q = synthetic.quantise_u8(f)
+    b8 = torch.zeros(q.size + 8, dtype=torch.uint8, device=DEV)
+    v8 = b8[offset: offset + q.size].view(37, 128)
+    v8.copy_(torch.from_numpy(q).to(DEV))
+    got = ecc.ecc_hard(v8, 256, 0.0, 255.0).cpu().numpy()
+    np.testing.assert_array_equal(got, oracle.ecc_hard(q, 256, 0.0, 255.0))
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 1), (2, 2, 2), (3, 1, 7), (1, 9, 9), (5, 6, 7),
+                                   (9, 17, 33), (4, 8, 128), (3, 9, 129), (17, 20, 131),
+                                   (2, 67, 260), (40, 12, 5)])
+def test_3d_shapes(shape):
+    for kind in ("grf", "ties", "uniform"):
+        v = rand_field(shape, sum(shape), kind)
+        check(v, 29, 0.0, 1.0)
+        check(synthetic.quantise_u8(v), 256, 0.0, 255.0)
+
+
+def test_3d_batches_special_values():
+    v = synthetic.grf((12, 20, 44), 12, batch=3)
+    v[0, 3, 4, 5] = np.nan
+    v[1, :, 7, :] = np.inf
+    v[2, 5] = -np.inf
+    check(v, 64, 0.0, 1.0, ndim=3)
+    q = synthetic.quantise_u8(synthetic.grf((7, 33, 64), 13, batch=2))
+    check(q, 256, 0.0, 255.0, ndim=3)
+    check(q, 9, 100.0, 140.0, ndim=3)
+
+
+def test_deterministic_and_stream_independent():
+    f = synthetic.grf((333, 444), 14)
+    t = torch.from_numpy(f).to(DEV)
+    a = ecc.ecc_hard(t, 512, 0.0, 1.0)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        b = ecc.ecc_hard(t, 512, 0.0, 1.0, stream=s)
+    s.synchronize()
+    assert torch.equal(a, b)
+
+
+# ------------------------------------------------------------------------ full-size workloads
+
+def test_workload_128sq_u8():
+    img = synthetic.blurred_noise_u8((128, 128), seed=1, sigma=3.0)
+    check(img, 256, 0.0, 255.0)
+
+
+def test_workload_16x1024sq_f32():
+    img = synthetic.grf((1024, 1024), seed=2, batch=16)
+    check(img, 256, 0.0, 1.0, ndim=2)
+
+
+def test_workload_8192sq_f32():
+    img = synthetic.grf((8192, 8192), seed=3)
+    check(img, 1024, 0.0, 1.0)
+
+
+def test_workload_512cube_u8():
+    v = synthetic.grf((512, 512, 512), seed=5, device=DEV)
+    q = synthetic.quantise_u8(v)
+    got = ecc.ecc_hard(q.unsqueeze(0), 256, 0.0, 255.0).cpu().numpy()[0]
+    want = oracle.ecc_hard(q.cpu().numpy(), 256, 0.0, 255.0)
+    np.testing.assert_array_equal(got, want)
+
+
+def test_workload_1024cube_f32_inclusion_exclusion():
+    """chi(V) = sum chi(slab_i) - sum chi(plane shared by slab_i and slab_{i+1}); the full
+    volume runs in the benchmark's launch, the slabs and planes in their own launches, and two
+    slabs are also checked against the oracle."""
+    v = synthetic.grf((1024, 1024, 1024), seed=4, device=DEV)
+    full = ecc.ecc_hard(v.unsqueeze(0), 256, 0.0, 1.0)[0].cpu().numpy()
+    cuts = [0, 200, 511, 777, 1023]
+    total = np.zeros(256, np.int64)
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        total += ecc.ecc_hard(v[a: b + 1].unsqueeze(0), 256, 0.0, 1.0)[0].cpu().numpy()
+    for c in cuts[1:-1]:
+        total -= ecc.ecc_hard(v[c], 256, 0.0, 1.0).cpu().numpy()
+    np.testing.assert_array_equal(full, total)
+    assert full[-1] == 1
+    for a in (0, 600):
+        slab = v[a: a + 6, 100:420, :].contiguous()
+        got = ecc.ecc_hard(slab.unsqueeze(0), 256, 0.0, 1.0)[0].cpu().numpy()
+        np.testing.assert_array_equal(got, oracle.ecc_hard(slab.cpu().numpy(), 256, 0.0, 1.0))

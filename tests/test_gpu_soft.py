@@ -1,0 +1,154 @@
+"""GPU parity for the soft ECC forward and backward against the fp64 oracle.
+
+Tolerance (per element), for S, grad_tau, grad_alpha and grad_u:
+    |gpu - oracle| <= 1e-6 + 1e-4 |oracle|.
+grad_img (an optional output) sums K terms per pixel that can cancel; its bound adds a term
+proportional to the sum of the magnitudes of those terms (returned by the oracle):
+    |gpu - oracle| <= 1e-6 + 1e-4 |oracle| + 4e-6 * sum|terms|.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from euler_characteristic_curves_gb300 import ecc, synthetic
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+RTOL, ATOL = 1e-4, 1e-6
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def assert_close(got, want, what, extra=None):
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    tol = ATOL + RTOL * np.abs(want)
+    if extra is not None:
+        tol = tol + extra
+    err = np.abs(got - want)
+    bad = err > tol
+    assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} outside tolerance; worst "
+                           f"err/tol = {np.max(err / tol):.3g}")
+
+
+def run_both(img, tau, lam, alpha, u, g, want_img=True, sample=None):
+    """GPU fwd + bwd through the C ABI, and the oracle (optionally only on sampled images)."""
+    a = np.asarray([alpha], np.float32)
+    s, ws = ecc.ecc_soft_fwd(dev(img), dev(tau), lam, dev(a), dev(u))
+    res = ecc.ecc_soft_bwd(dev(img), dev(tau), lam, dev(a), dev(u), dev(g), ws,
+                           want_img=want_img)
+    s = s.cpu().numpy()
+    res = {k: v.cpu().numpy() for k, v in res.items()}
+    imgs = img if sample is None else img[sample]
+    gs = g if sample is None else g[sample]
+    ref_s = oracle.ecc_soft_fwd(imgs, tau, lam, alpha, u, ndim=2)
+    ref = oracle.ecc_soft_bwd(imgs, tau, lam, alpha, u, gs, ndim=2, want_img=want_img)
+    return s, res, ref_s, ref
+
+
+def compare(img, tau, lam, alpha, u, g, want_img=True):
+    s, res, ref_s, ref = run_both(img, tau, lam, alpha, u, g, want_img)
+    assert_close(s, ref_s, "S")
+    assert_close(res["grad_tau"], ref["grad_tau"], "grad_tau")
+    assert_close(res["grad_alpha"][0], ref["grad_alpha"], "grad_alpha")
+    assert_close(res["grad_u"], ref["grad_u"], "grad_u")
+    if want_img:
+        assert_close(res["grad_img"], ref["grad_img"], "grad_img",
+                     extra=4e-6 * ref["grad_img_absterms"])
+
+
+@pytest.mark.parametrize("shape,batch", [((1, 1), 1), ((1, 9), 2), ((7, 1), 1), ((5, 7), 3),
+                                         ((33, 65), 2), ((64, 64), 1), ((100, 130), 2),
+                                         ((31, 257), 1)])
+def test_soft_parity_shapes(shape, batch):
+    img = synthetic.grf(shape, seed=sum(shape), batch=batch) if min(shape) > 1 else \
+        np.random.default_rng(1).random((batch,) + shape).astype(np.float32)
+    K = 24
+    tau = synthetic.uniform_thresholds(K, -0.2, 1.2)
+    u = synthetic.soft_direction(2, seed=batch)
+    g = synthetic.upstream_grad((batch, K), seed=3)
+    compare(img, tau, 50.0, 1.0, u, g)
+
+
+@pytest.mark.parametrize("K", [1, 7, 128, 129, 300])
+def test_soft_parity_K(K):
+    img = synthetic.grf((48, 80), seed=K, batch=2)
+    rng = np.random.default_rng(K)
+    tau = rng.uniform(-0.1, 1.1, size=K).astype(np.float32)  # unsorted thresholds
+    u = synthetic.soft_direction(2, seed=K)
+    g = synthetic.upstream_grad((2, K), seed=K + 1)
+    compare(img, tau, 50.0, 1.0, u, g)
+
+
+@pytest.mark.parametrize("lam,alpha", [(1.0, 1.0), (5.0, -0.7), (50.0, 2.5), (500.0, 1.0),
+                                       (3000.0, 0.3)])
+def test_soft_parity_lambda_alpha(lam, alpha):
+    img = synthetic.grf((57, 90), seed=int(lam), batch=2)
+    tau = synthetic.uniform_thresholds(32, -1.0, 1.5)
+    u = np.asarray([0.13, -0.21], np.float32)
+    g = synthetic.upstream_grad((2, 32), seed=5)
+    compare(img, tau, lam, alpha, u, g)
+
+
+def test_soft_ties_and_zero_direction():
+    q = synthetic.quantise_u8(synthetic.grf((60, 70), seed=6, batch=2)).astype(np.float32) / 255
+    tau = synthetic.uniform_thresholds(40)
+    g = synthetic.upstream_grad((2, 40), seed=7)
+    compare(q, tau, 50.0, 1.0, np.zeros(2, np.float32), g)  # exact ties in X everywhere
+    compare(q, tau, 50.0, 0.5, np.asarray([0.0, 0.3], np.float32), g)
+    const = np.full((2, 20, 30), 0.25, np.float32)
+    compare(const, tau, 50.0, 1.0, np.zeros(2, np.float32), g)
+
+
+def test_soft_large_lambda_matches_hard():
+    q = np.random.default_rng(8).integers(0, 6, size=(2, 40, 50)).astype(np.float32)
+    tau = (np.arange(7) - 0.5).astype(np.float32)
+    a = np.asarray([1.0], np.float32)
+    s, _ = ecc.ecc_soft_fwd(dev(q), dev(tau), 1.0e4, dev(a), dev(np.zeros(2, np.float32)))
+    hard = ecc.ecc_hard(dev(q), 7, -0.5, 5.5, ndim=2).cpu().numpy()
+    np.testing.assert_allclose(s.cpu().numpy(), hard.astype(np.float64), atol=1e-6)
+
+
+def test_autograd_layer_matches_direct_calls():
+    img = synthetic.grf((40, 50), seed=9, batch=2)
+    tau = dev(synthetic.uniform_thresholds(16)).requires_grad_()
+    alpha = torch.ones(1, device=DEV, requires_grad=True)
+    u = dev(np.asarray([0.05, -0.08], np.float32)).requires_grad_()
+    x = dev(img).requires_grad_()
+    g = dev(synthetic.upstream_grad((2, 16), seed=10))
+    s = ecc.soft_ecc(x, tau, alpha, u, 50.0)
+    (s * g).sum().backward()
+    s2, ws = ecc.ecc_soft_fwd(dev(img), tau.detach(), 50.0, alpha.detach(), u.detach())
+    res = ecc.ecc_soft_bwd(dev(img), tau.detach(), 50.0, alpha.detach(), u.detach(), g, ws,
+                           want_img=True)
+    assert torch.equal(s.detach(), s2)
+    assert torch.equal(tau.grad, res["grad_tau"])
+    assert torch.equal(alpha.grad, res["grad_alpha"])
+    assert torch.equal(u.grad, res["grad_u"])
+    assert torch.equal(x.grad, res["grad_img"])
+
+
+def test_workload_64x256sq_soft():
+    """The benchmark workload at full size: 64 GRF images 256^2, K = 128 thresholds on [0, 1],
+    lambda = 50, alpha = 1, u ~ N(0, 0.1^2). The oracle checks S on sampled images; for the
+    backward pass the upstream gradient is non-zero on the sampled images only, so the oracle
+    reproduces every gradient from those images while the kernels run the full launch."""
+    img = synthetic.grf((256, 256), seed=6, batch=64)
+    tau = synthetic.uniform_thresholds(128)
+    u = synthetic.soft_direction(2, seed=7)
+    g_full = synthetic.upstream_grad((64, 128), seed=8)
+    sample = np.asarray([0, 17, 42, 63])
+    g = np.zeros_like(g_full)
+    g[sample] = g_full[sample]
+    s, res, ref_s, ref = run_both(img, tau, 50.0, 1.0, u, g, want_img=True, sample=sample)
+    assert_close(s[sample], ref_s, "S")
+    assert_close(res["grad_tau"], ref["grad_tau"], "grad_tau")
+    assert_close(res["grad_alpha"][0], ref["grad_alpha"], "grad_alpha")
+    assert_close(res["grad_u"], ref["grad_u"], "grad_u")
+    assert_close(res["grad_img"][sample], ref["grad_img"], "grad_img",
+                 extra=4e-6 * ref["grad_img_absterms"])
+    others = np.setdiff1d(np.arange(64), sample)
+    assert not np.any(res["grad_img"][others])
