@@ -45,6 +45,10 @@ WORKLOADS = {
     "3d1024": [("hard", (1024, 1024, 1024), 1, "f32", 256, 0.0, 1.0, 4)],
     "3d512u8": [("hard", (512, 512, 512), 1, "u8grf", 256, 0.0, 255.0, 5)],
     "soft": [("soft", (256, 256), 64, 128, 50.0, 6, 7, 8)],
+    # smaller cases of the same kernels (inputs still larger than L2) for ncu captures
+    "3d256": [("hard", (256, 1024, 1024), 1, "f32", 256, 0.0, 1.0, 4)],
+    "2d4096": [("hard", (4096, 4096), 1, "f32", 1024, 0.0, 1.0, 3)],
+    "soft16": [("soft", (256, 256), 16, 128, 50.0, 6, 7, 8)],
 }
 WORKLOADS["headline"] = WORKLOADS["2d8192"] + WORKLOADS["3d1024"] + WORKLOADS["soft"]
 
@@ -119,7 +123,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -427,7 +431,7 @@ def max_over_ranks(x: float, world: int) -> float:
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="headline")

@@ -89,8 +89,10 @@ int ecc_hard(const void *img, int dtype, int ndim, const int64_t *dims, int64_t 
     pl.out = out;
     float table[ECC_MAX_NBINS + 2];
     const int H = nbins;
+    pl.key_err = 0.0f;
     if (dtype == ECC_U8) {
-        // key of every byte value: first k with b <= t_k (H if none)
+        // fp16 key pattern of every byte value: 0x6400 + (first k with b <= t_k; H if none)
+        uint16_t lut[256];
         for (int v = 0; v < 256; ++v) {
             int lo = 0, hi = H;
             while (lo < hi) {
@@ -100,26 +102,33 @@ int ecc_hard(const void *img, int dtype, int ndim, const int64_t *dims, int64_t 
                 else
                     lo = mid + 1;
             }
-            table[v] = (float)lo;
+            lut[v] = (uint16_t)(0x6400 + lo);
         }
+        memcpy(table, lut, sizeof(lut));
         pl.key_mode = kKeyLut;
         pl.scale = pl.offset = 0.0f;
         pl.vec_ok = ((uintptr_t)img % 4 == 0) && (W % 4 == 0);
     } else {
         for (int k = 0; k < H; ++k) table[k] = round_down_f32(threshold(k, H, vmin, vmax));
         table[H] = table[H + 1] = INFINITY;
-        // Estimator t = v * scale + offset; its error in bins (fp64 threshold rounding plus fp32
-        // evaluation) must stay below 1/4 for the two-comparison correction to be exact.
+        // Estimator t = H * sat(v * sH + oH) of the fractional bin (v - vmin) (H - 1) / (vmax -
+        // vmin), clamped to [0, H]. Its error in bins, from rounding sH, oH, the FMA, the scaling
+        // by H, the subtraction of E and the fp64 thresholds, is below
+        //     E = 2^-21 (M s + |o| + 2 H + 4),  M = max(|vmin|, |vmax|), s = (H-1)/(vmax-vmin),
+        // for every |v| <= M (values beyond saturate to t = 0 or H, where the kernel always
+        // consults the table). The kernel needs E <= 1/4; otherwise every key is searched.
         pl.key_mode = kKeySearch;
         pl.scale = pl.offset = 0.0f;
         if (H >= 2 && vmax > vmin) {
-            const double s = (double)(H - 1) / (vmax - vmin);
+            const double sc = (double)(H - 1) / (vmax - vmin);
+            const double o = -vmin * sc;
             const double M = fmax(fabs(vmin), fabs(vmax));
-            const double err = ldexp(1.0, -22) * (M * s + (double)H + 2.0);
-            if (isfinite(s) && s < 1e30 && err <= 0.25) {
+            const double err = ldexp(1.0, -21) * (M * sc + fabs(o) + 2.0 * H + 4.0);
+            if (isfinite(sc) && sc < 1e30 && err <= 0.25) {
                 pl.key_mode = kKeyEstimate;
-                pl.scale = (float)s;
-                pl.offset = (float)(-vmin * s);
+                pl.scale = (float)(sc / H);
+                pl.offset = (float)(o / H);
+                pl.key_err = (float)(err * 1.0625);
             }
         }
         pl.vec_ok = ((uintptr_t)img % 16 == 0) && (W % 4 == 0);

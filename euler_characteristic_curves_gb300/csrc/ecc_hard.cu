@@ -3,152 +3,45 @@
 // Paper notes "Scalable GPU-Accelerated Euler Characteristic Curves: Optimization and
 // Differentiable Learning for PyTorch":
 //   "Key designs -- full-scan CUDA kernel": one pass over the whole grid with no chunked
-//   re-launches; each thread block keeps a private shared-memory histogram of H bins, and only
-//   after all of its voxels does it flush, once, to global memory with atomics.
+//   re-launches; each thread block keeps a private shared-memory histogram of H bins and flushes
+//   it once, with one global atomic per non-empty bin.
 //   "Key designs -- local computation of the Euler characteristic coefficient": c(p) from the
 //   3x3 / 3x3x3 neighbourhood, accumulated at p's threshold bin.
-// The histogram's running sum over bins is the curve (second kernel).
+// The running sum of the histogram over bins is the curve (ecc_bin_scan_kernel).
 //
-// 2-D kernel: a warp owns a strip of 128 columns (4 per lane, one 16-byte load per lane per row)
-// and walks down a band of rows holding rows y-1, y, y+1 in registers; the columns left and right
-// of a lane's four come from its neighbours by shuffle, and the strip's two halo columns from
-// one extra scalar load each.
+// Both kernels first turn every voxel into its exact threshold key (ecc_keys.cuh) and then work
+// on fp16 key patterns, two pixels per instruction.
 //
-// 3-D kernel: the V-construction complex of a volume splits into the cells lying in one plane z
-// and the "vertical" cells sigma x [z, z+1], sigma a cell of the plane. A vertical cell's value is
-// the max over sigma of M_z = max(S_z, S_{z+1}) and its dimension is dim(sigma) + 1, so
-//     ECC_3D = sum_z ECC_2D(S_z) - sum_z ECC_2D(M_z).
-// Per voxel p at (x, y, z) this gives one contribution at p's bin:
-//     c(p) = c2(S_z; p) - [p owns M_z(x,y)] c2(M_z; x,y) - [p owns M_{z-1}(x,y)] c2(M_{z-1}; x,y)
-// where p owns M_z(x,y) when S_{z+1}(x,y) < S_z(x,y) (the later voxel wins ties) and owns
-// M_{z-1}(x,y) when S_{z-1}(x,y) <= S_z(x,y). With NaN for "absent / never", both ownership tests
-// fail when either value is NaN, and M propagates NaN, so such max-pixels are dropped as they
-// must be. A warp owns a 128-column row segment of a 128 x 8 tile and walks z.
+// 2-D: a warp owns a strip of 128 columns (four per lane, one 16-byte load per lane per row) and
+// walks down a band of rows; raw rows are prefetched three rows ahead in registers, and the
+// comparisons with the row below are reused as the "above" comparisons of the next row.
+//
+// 3-D: the complex of a volume splits into the cells of each plane z and the vertical cells
+// sigma x [z, z+1]; a vertical cell's value is the max over sigma of M_z = max(S_z, S_{z+1}) and
+// its dimension is dim(sigma) + 1, so ECC_3D = sum_z ECC_2D(S_z) - sum_z ECC_2D(M_z). Folding
+// each max-pixel into the voxel that carries it gives one contribution per voxel p = (x, y, z):
+//     c(p) = c2(S_z; p) - [k_{z+1} < k_z] c2(M_z; x,y) - [k_{z-1} <= k_z] c2(M_{z-1}; x,y)
+// (the later voxel wins ties; the max of two keys is the key of the max). A block owns a tile of
+// 128 columns x 8 rows and walks z; each plane's keys are computed once into a shared tile with a
+// one-pixel halo, from which every warp builds the three rows around its own row.
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "ecc_internal.cuh"
+#include "ecc_keys.cuh"
 
 namespace ecc {
 
-// ----------------------------------------------------------------------------------------------
-// Row loads: six values (x-1 .. x+4) of one row for a lane owning columns x .. x+3, x = x0 + 4 lane
-// ----------------------------------------------------------------------------------------------
-
-template <typename T>
-struct RowLoader;
-
-template <>
-struct RowLoader<float> {
-    static __device__ __forceinline__ float at(const float *__restrict__ row, int64_t x)
-    {
-        return __ldg(row + x);
-    }
-    static __device__ __forceinline__ void own4(const float *__restrict__ row, int64_t xs,
-                                                int64_t W, bool vec, float v[6])
-    {
-        if (vec) {
-            const float4 q = __ldg(reinterpret_cast<const float4 *>(row + xs));
-            v[1] = q.x;
-            v[2] = q.y;
-            v[3] = q.z;
-            v[4] = q.w;
-        } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) v[1 + j] = (xs + j < W) ? __ldg(row + xs + j) : qnan();
-        }
-    }
-};
-
-template <>
-struct RowLoader<uint8_t> {
-    static __device__ __forceinline__ float at(const uint8_t *__restrict__ row, int64_t x)
-    {
-        return u8_as_ordered_float((uint32_t)__ldg(row + x), 0);
-    }
-    static __device__ __forceinline__ void own4(const uint8_t *__restrict__ row, int64_t xs,
-                                                int64_t W, bool vec, float v[6])
-    {
-        if (vec) {
-            const uint32_t w = __ldg(reinterpret_cast<const unsigned int *>(row + xs));
-#pragma unroll
-            for (int j = 0; j < 4; ++j) v[1 + j] = u8_as_ordered_float(w, j);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                v[1 + j] = (xs + j < W) ? u8_as_ordered_float((uint32_t)__ldg(row + xs + j), 0)
-                                        : qnan();
-        }
-    }
-};
-
-// Whole-warp call (shuffles): every lane of the warp must take part with the same row/x0.
-template <typename T>
-__device__ __forceinline__ void load_row(const T *__restrict__ plane, int64_t Hy, int64_t W,
-                                         int64_t y, int64_t x0, int lane, bool vec_ok, float v[6])
-{
-    if (y < 0 || y >= Hy) {
-#pragma unroll
-        for (int j = 0; j < 6; ++j) v[j] = qnan();
-        return;
-    }
-    const T *__restrict__ row = plane + y * W;
-    const int64_t xs = x0 + 4 * lane;
-    const bool vec = vec_ok && (x0 + 128 <= W);
-    RowLoader<T>::own4(row, xs, W, vec, v);
-    float left = __shfl_up_sync(kFull, v[4], 1);
-    float right = __shfl_down_sync(kFull, v[1], 1);
-    if (lane == 0) left = (x0 > 0) ? RowLoader<T>::at(row, x0 - 1) : qnan();
-    if (lane == kWarp - 1) right = (x0 + 128 < W) ? RowLoader<T>::at(row, x0 + 128) : qnan();
-    v[0] = left;
-    v[5] = right;
-}
+constexpr int kHardThreads = 256;
+constexpr int kHardWarps = kHardThreads / kWarp;
 
 // ----------------------------------------------------------------------------------------------
-// Keys and the block histogram
+// Block setup, keys and histogram
 // ----------------------------------------------------------------------------------------------
 
-template <typename T>
-struct KeyOf;
-
-template <>
-struct KeyOf<float> {
-    template <int CAP>
-    static __device__ __forceinline__ int get(float v, const HardParams<CAP> &P,
-                                              const float *__restrict__ T)
-    {
-        if (P.key_mode == kKeyEstimate)
-            return key_estimate(v, P.scale, P.offset, (float)(P.H + 1), T);
-        return key_search(v, P.H, T);
-    }
-};
-
-template <>
-struct KeyOf<uint8_t> {
-    template <int CAP>
-    static __device__ __forceinline__ int get(float v, const HardParams<CAP> &P,
-                                              const float *__restrict__ T)
-    {
-        if (v != v) return P.H;  // absent
-        return (int)T[__float_as_int(v) & 0xff];
-    }
-};
-
-// c[j] belongs to the pixel whose value is row[1 + j].
-template <typename T, int CAP>
-__device__ __forceinline__ void accumulate4(const int c[4], const float row[6],
-                                            const HardParams<CAP> &P,
-                                            const float *__restrict__ table, int *hist)
-{
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        if (c[j] != 0) {
-            const int k = KeyOf<T>::template get<CAP>(row[1 + j], P, table);
-            if (k < P.H) atomicAdd(hist + k, c[j]);
-        }
-    }
-}
-
+// Shared layout: int hist[H], then the table: f32 thresholds T[0..H+1], or for uint8 inputs the
+// fp16 key pattern of each byte value (uint16[256]).
 template <int CAP>
 __device__ __forceinline__ void block_setup(const HardParams<CAP> &P, int *hist, float *table)
 {
@@ -157,7 +50,6 @@ __device__ __forceinline__ void block_setup(const HardParams<CAP> &P, int *hist,
     __syncthreads();
 }
 
-// One global atomic per non-empty bin per block ("one global atomic flush per block").
 template <int CAP>
 __device__ __forceinline__ void block_flush(const HardParams<CAP> &P, const int *hist, int64_t b)
 {
@@ -169,8 +61,170 @@ __device__ __forceinline__ void block_flush(const HardParams<CAP> &P, const int 
     }
 }
 
-constexpr int kHardThreads = 256;
-constexpr int kHardWarps = kHardThreads / kWarp;
+template <int CAP>
+__device__ __forceinline__ KeyConsts key_consts(const HardParams<CAP> &P)
+{
+    KeyConsts K;
+    K.sH = P.scale;
+    K.oH = P.offset;
+    K.Hf = (float)P.H;
+    K.E = P.key_err;
+    K.H = P.H;
+    K.search = P.key_mode == kKeySearch;
+    return K;
+}
+
+// Raw values of one row around a lane's four columns, plus (lanes 0 / 31) the value just left of
+// column x0 / right of column x0 + 127. `valid` has bit j set when column x + j is inside the grid.
+template <typename T>
+struct RawRow;
+
+template <>
+struct RawRow<float> {
+    float v[4];
+    float halo;
+    uint32_t valid;
+    bool present;  // row inside the grid (warp-uniform)
+};
+
+template <>
+struct RawRow<uint8_t> {
+    uint32_t bytes;
+    uint32_t halo;
+    uint32_t valid;
+    bool present;
+};
+
+__device__ __forceinline__ RawRow<float> load_raw(const float *__restrict__ plane, int64_t Hy,
+                                                  int64_t W, int64_t y, int64_t x0, int lane,
+                                                  bool vec)
+{
+    RawRow<float> r;
+    r.present = (y >= 0 && y < Hy);
+    r.valid = 0xfu;
+    r.halo = 0.0f;
+    r.v[0] = r.v[1] = r.v[2] = r.v[3] = 0.0f;
+    if (!r.present) return r;
+    const float *__restrict__ row = plane + y * W;
+    const int64_t xs = x0 + 4 * lane;
+    if (vec) {
+        const float4 q = __ldg(reinterpret_cast<const float4 *>(row + xs));
+        r.v[0] = q.x;
+        r.v[1] = q.y;
+        r.v[2] = q.z;
+        r.v[3] = q.w;
+    } else {
+        r.valid = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const bool in = xs + j < W;
+            r.v[j] = in ? __ldg(row + xs + j) : 0.0f;
+            r.valid |= in ? (1u << j) : 0u;
+        }
+    }
+    if (lane == 0 && x0 > 0) r.halo = __ldg(row + x0 - 1);
+    if (lane == kWarp - 1 && x0 + 128 < W) r.halo = __ldg(row + x0 + 128);
+    return r;
+}
+
+__device__ __forceinline__ RawRow<uint8_t> load_raw(const uint8_t *__restrict__ plane, int64_t Hy,
+                                                    int64_t W, int64_t y, int64_t x0, int lane,
+                                                    bool vec)
+{
+    RawRow<uint8_t> r;
+    r.present = (y >= 0 && y < Hy);
+    r.valid = 0xfu;
+    r.halo = 0;
+    r.bytes = 0;
+    if (!r.present) return r;
+    const uint8_t *__restrict__ row = plane + y * W;
+    const int64_t xs = x0 + 4 * lane;
+    if (vec) {
+        r.bytes = __ldg(reinterpret_cast<const unsigned int *>(row + xs));
+    } else {
+        r.valid = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const bool in = xs + j < W;
+            r.bytes |= in ? ((uint32_t)__ldg(row + xs + j) << (8 * j)) : 0u;
+            r.valid |= in ? (1u << j) : 0u;
+        }
+    }
+    if (lane == 0 && x0 > 0) r.halo = __ldg(row + x0 - 1);
+    if (lane == kWarp - 1 && x0 + 128 < W) r.halo = __ldg(row + x0 + 128);
+    return r;
+}
+
+// Key pattern of one float value (any value, NaN -> H).
+__device__ __forceinline__ uint32_t key_one(float v, const KeyConsts &K, const float *__restrict__ T)
+{
+    if (K.search) return key_search_pattern(v, K.H, T);
+    float amb = 0.0f;
+    const uint32_t k = key_fast(v, K, amb);
+    return (amb != 0.0f) ? key_fix(v, k, K, T) : k;
+}
+
+// fp16 key patterns of the lane's four values (pairs k0 | k1 << 16, k2 | k3 << 16) and of its
+// halo value (lanes 0 and 31; absent when the halo column is outside the grid). Whole-warp call.
+__device__ __forceinline__ void raw_keys(const RawRow<float> &r, const KeyConsts &K,
+                                         const float *__restrict__ T, int lane, int64_t x0,
+                                         int64_t W, uint32_t &own0, uint32_t &own1,
+                                         uint32_t &halo_key)
+{
+    uint32_t k[4];
+    if (K.search) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) k[j] = key_search_pattern(r.v[j], K.H, T);
+    } else {
+        float amb = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) k[j] = key_fast(r.v[j], K, amb);
+        if (__any_sync(kFull, amb != 0.0f)) {
+            if (amb != 0.0f) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) k[j] = key_fix(r.v[j], k[j], K, T);
+            }
+        }
+    }
+    if (r.valid != 0xfu) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (!(r.valid >> j & 1u)) k[j] = kAbsentHalf;
+    }
+    own0 = prmt(k[0], k[1], 0x5410);
+    own1 = prmt(k[2], k[3], 0x5410);
+    halo_key = kAbsentHalf;
+    if (lane == 0 && x0 > 0) halo_key = key_one(r.halo, K, T);
+    if (lane == kWarp - 1 && x0 + 128 < W) halo_key = key_one(r.halo, K, T);
+}
+
+__device__ __forceinline__ void raw_keys(const RawRow<uint8_t> &r, const KeyConsts &,
+                                         const float *__restrict__ T, int lane, int64_t x0,
+                                         int64_t W, uint32_t &own0, uint32_t &own1,
+                                         uint32_t &halo_key)
+{
+    const uint16_t *lut = reinterpret_cast<const uint16_t *>(T);
+    uint32_t k[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        k[j] = (r.valid >> j & 1u) ? (uint32_t)lut[(r.bytes >> (8 * j)) & 0xffu] : kAbsentHalf;
+    own0 = prmt(k[0], k[1], 0x5410);
+    own1 = prmt(k[2], k[3], 0x5410);
+    halo_key = kAbsentHalf;
+    if (lane == 0 && x0 > 0) halo_key = lut[r.halo & 0xffu];
+    if (lane == kWarp - 1 && x0 + 128 < W) halo_key = lut[r.halo & 0xffu];
+}
+
+template <typename T>
+__device__ __forceinline__ KeyRow key_row(const RawRow<T> &r, const KeyConsts &K,
+                                          const float *__restrict__ table, int lane, int64_t x0,
+                                          int64_t W)
+{
+    if (!r.present) return absent_row();  // warp-uniform
+    uint32_t own0, own1, hk;
+    raw_keys(r, K, table, lane, x0, W, own0, own1, hk);
+    return make_key_row(own0, own1, lane, hk, hk);
+}
 
 // ----------------------------------------------------------------------------------------------
 // 2-D kernel
@@ -195,28 +249,44 @@ __global__ void __launch_bounds__(kHardThreads) ecc_hard2d_kernel(const __grid_c
     const int64_t Tn = P.tasks_per_image;
     const int64_t t_begin = Tn * blockIdx.x / P.ctas_per_image;
     const int64_t t_end = Tn * (blockIdx.x + 1) / P.ctas_per_image;
-    const bool vec_ok = P.vec_ok != 0;
+    const KeyConsts K = key_consts(P);
+    const int64_t Hy = P.Hy, W = P.W;
+    const uint32_t limit = (kKeyBase + (uint32_t)P.H) * 0x10001u;
 
     for (int64_t t = t_begin + warp; t < t_end; t += kHardWarps) {
-        const int64_t strip = t % P.tasks_x;
-        const int64_t band = t / P.tasks_x;
-        const int64_t x0 = strip * 128;
-        const int64_t y0 = band * P.rows_per_task;
-        const int64_t y1 = min(y0 + (int64_t)P.rows_per_task, P.Hy);
-        float a[6], bb[6], d[6];
-        load_row<T>(img, P.Hy, P.W, y0 - 1, x0, lane, vec_ok, a);
-        load_row<T>(img, P.Hy, P.W, y0, x0, lane, vec_ok, bb);
-        for (int64_t y = y0; y < y1; ++y) {
-            load_row<T>(img, P.Hy, P.W, y + 1, x0, lane, vec_ok, d);
-            int c[4];
-            quad_c2d(a, bb, d, c);
-            accumulate4<T, CAP>(c, bb, P, table, hist);
-#pragma unroll
-            for (int j = 0; j < 6; ++j) {
-                a[j] = bb[j];
-                bb[j] = d[j];
-            }
+        const int64_t x0 = (t % P.tasks_x) * 128;
+        const int64_t y0 = (t / P.tasks_x) * P.rows_per_task;
+        const int64_t y1 = min(y0 + (int64_t)P.rows_per_task, Hy);
+        const bool vec = P.vec_ok && (x0 + 128 <= W);
+
+        // raw-row ring: at the start of step y, q0 / q1 / q2 (in rotation) hold rows y+1 .. y+3
+        RawRow<T> q0 = load_raw(img, Hy, W, y0 + 1, x0, lane, vec);
+        RawRow<T> q1 = load_raw(img, Hy, W, y0 + 2, x0, lane, vec);
+        RawRow<T> q2 = load_raw(img, Hy, W, y0 + 3, x0, lane, vec);
+        KeyRow ka = key_row(load_raw(img, Hy, W, y0 - 1, x0, lane, vec), K, table, lane, x0, W);
+        KeyRow kb = key_row(load_raw(img, Hy, W, y0, x0, lane, vec), K, table, lane, x0, W);
+        uint32_t Sp0, Sp1;
+        sp_init(ka, kb, Sp0, Sp1);
+
+#define ECC_2D_STEP(QS)                                                                     \
+    {                                                                                       \
+        if (y >= y1) break;                                                                 \
+        const KeyRow kd = key_row(QS, K, table, lane, x0, W);                               \
+        QS = load_raw(img, Hy, W, y + 4, x0, lane, vec);                                    \
+        uint32_t c0, c1;                                                                    \
+        c2_quad(ka, kb, kd, kBias, Sp0, Sp1, c0, c1);                                       \
+        hist_pair(kb.own0, c0, limit, hist);                                                \
+        hist_pair(kb.own1, c1, limit, hist);                                                \
+        ka = kb;                                                                            \
+        kb = kd;                                                                            \
+        ++y;                                                                                \
+    }
+        for (int64_t y = y0; y < y1;) {
+            ECC_2D_STEP(q0)
+            ECC_2D_STEP(q1)
+            ECC_2D_STEP(q2)
         }
+#undef ECC_2D_STEP
     }
     block_flush(P, hist, b);
 }
@@ -225,36 +295,73 @@ __global__ void __launch_bounds__(kHardThreads) ecc_hard2d_kernel(const __grid_c
 // 3-D kernel
 // ----------------------------------------------------------------------------------------------
 //
-// Work: CTA task = (tile of 128 columns x 8 rows) x (chunk of rows_per_task planes), tile x
-// fastest, then tile y, then chunk. Warp w owns row y0 + w of the tile; lane l columns x0+4l..+3.
+// Work: block task = (tile of 128 columns x 8 rows) x (chunk of rows_per_task planes), tile x
+// fastest, then tile y, then chunk. Warp w owns row y0 + w, lane l columns x0 + 4l .. x0 + 4l + 3.
 
-struct Plane3 {  // rows y-1, y, y+1 of one plane around a lane's four columns
-    float r[3][6];
-};
+constexpr int kTileRows = kHardWarps;                // 8
+constexpr int kKeyPitch = 136;                       // halves per shared row (272 bytes)
+constexpr int kKeyRowsHalo = kTileRows + 2;          // rows y0-1 .. y0+8
+constexpr int kKeyPlane = kKeyRowsHalo * kKeyPitch;  // halves per plane buffer
+// Tile column c (-1 .. 128) sits at half index 4 + c of a shared row, so a lane's own four keys
+// form one 8-byte-aligned word pair.
 
+// Keys of plane z of the tile plus halo into `dst` (uint16 patterns; absent outside the grid).
 template <typename T>
-__device__ __forceinline__ void load_plane(const T *__restrict__ img, int64_t D, int64_t Hy, int64_t W, int64_t z,
-                                           int64_t y, int64_t x0, int lane, bool vec_ok,
-                                           Plane3 &p)
+__device__ __forceinline__ void plane_keys(const T *__restrict__ img, int64_t D, int64_t Hy,
+                                           int64_t W, int64_t z, int64_t x0, int64_t y0,
+                                           bool vec_ok, const KeyConsts &K,
+                                           const float *__restrict__ table, uint16_t *dst)
 {
-    if (z < 0 || z >= D) {
-#pragma unroll
-        for (int i = 0; i < 3; ++i)
-#pragma unroll
-            for (int j = 0; j < 6; ++j) p.r[i][j] = qnan();
-        return;
+    const int lane = threadIdx.x & (kWarp - 1);
+    const int warp = threadIdx.x >> 5;
+    const bool zin = (z >= 0 && z < D);  // block-uniform
+    const T *__restrict__ plane = img + (zin ? z : 0) * Hy * W;
+    const bool vec = vec_ok && (x0 + 128 <= W);
+    // each warp: its own row (buffer rows 1 .. 8) with the two halo columns
+    {
+        const int64_t y = y0 + warp;
+        uint32_t own0 = kAbsentPair, own1 = kAbsentPair, hk = kAbsentHalf;
+        if (zin) {
+            const RawRow<T> r = load_raw(plane, Hy, W, y, x0, lane, vec);
+            if (r.present) raw_keys(r, K, table, lane, x0, W, own0, own1, hk);
+        }
+        uint16_t *row = dst + (1 + warp) * kKeyPitch;
+        *reinterpret_cast<uint2 *>(row + 4 + 4 * lane) = make_uint2(own0, own1);
+        if (lane == 0) row[3] = (uint16_t)hk;
+        if (lane == kWarp - 1) row[4 + 128] = (uint16_t)hk;
     }
-    const T *__restrict__ plane = img + z * Hy * W;
-#pragma unroll
-    for (int i = 0; i < 3; ++i) load_row<T>(plane, Hy, W, y - 1 + i, x0, lane, vec_ok, p.r[i]);
+    // halo rows y0 - 1 (buffer row 0) and y0 + 8 (buffer row 9): 2 x 130 keys
+    for (int i = threadIdx.x; i < 2 * 130; i += kHardThreads) {
+        const int hr = i / 130;
+        const int c = i % 130 - 1;  // tile column -1 .. 128
+        const int64_t y = (hr == 0) ? y0 - 1 : y0 + kTileRows;
+        const int64_t x = x0 + c;
+        uint32_t key = kAbsentHalf;
+        if (zin && y >= 0 && y < Hy && x >= 0 && x < W) {
+            if constexpr (sizeof(T) == 1) {
+                key = reinterpret_cast<const uint16_t *>(table)[(uint32_t)plane[y * W + x]];
+            } else {
+                key = key_one((float)plane[y * W + x], K, table);
+            }
+        }
+        dst[(hr == 0 ? 0 : kKeyRowsHalo - 1) * kKeyPitch + 4 + c] = (uint16_t)key;
+    }
 }
 
-__device__ __forceinline__ void plane_max(const Plane3 &s, const Plane3 &u, Plane3 &m)
+// Buffer row r (= tile row r - 1, r = 0 .. 9) around the lane's four columns.
+__device__ __forceinline__ KeyRow smem_key_row(const uint16_t *buf, int r, int lane)
 {
-#pragma unroll
-    for (int i = 0; i < 3; ++i)
-#pragma unroll
-        for (int j = 0; j < 6; ++j) m.r[i][j] = max_nan(s.r[i][j], u.r[i][j]);
+    const uint16_t *row = buf + r * kKeyPitch;
+    const uint2 own = *reinterpret_cast<const uint2 *>(row + 4 + 4 * lane);
+    const uint32_t left = row[3 + 4 * lane];
+    const uint32_t right = row[8 + 4 * lane];
+    KeyRow k;
+    k.own0 = own.x;
+    k.own1 = own.y;
+    k.L0 = prmt(left, own.x, 0x5410);
+    k.R0 = prmt(own.x, own.y, 0x5432);
+    k.R1 = prmt(own.y, right, 0x5432);
+    return k;
 }
 
 template <typename T, int CAP>
@@ -264,6 +371,7 @@ __global__ void __launch_bounds__(kHardThreads) ecc_hard3d_kernel(const __grid_c
     extern __shared__ int smem[];
     int *hist = smem;
     float *table = reinterpret_cast<float *>(smem + P.H);
+    __shared__ __align__(16) uint16_t keybuf[2][kKeyPlane];
     block_setup(P, hist, table);
 
     const int64_t b = blockIdx.y;
@@ -273,8 +381,11 @@ __global__ void __launch_bounds__(kHardThreads) ecc_hard3d_kernel(const __grid_c
     const int64_t Tn = P.tasks_per_image;
     const int64_t t_begin = Tn * blockIdx.x / P.ctas_per_image;
     const int64_t t_end = Tn * (blockIdx.x + 1) / P.ctas_per_image;
+    const KeyConsts K = key_consts(P);
     const bool vec_ok = P.vec_ok != 0;
     const int64_t D = P.D, Hy = P.Hy, W = P.W;
+    const uint32_t limit = (kKeyBase + (uint32_t)P.H) * 0x10001u;
+    const uint32_t kPlain = 0u;  // bias of the M stencil: plain c values
 
     for (int64_t t = t_begin; t < t_end; ++t) {
         const int64_t tx = t % P.tasks_x;
@@ -282,38 +393,65 @@ __global__ void __launch_bounds__(kHardThreads) ecc_hard3d_kernel(const __grid_c
         const int64_t ty = rest % P.tasks_y;
         const int64_t tz = rest / P.tasks_y;
         const int64_t x0 = tx * 128;
-        const int64_t y = ty * kHardWarps + warp;
-        if (y >= Hy) continue;  // warp-uniform; no block-wide barrier inside the task loop
+        const int64_t y0 = ty * kTileRows;
         const int64_t z0 = tz * P.rows_per_task;
         const int64_t z1 = min(z0 + (int64_t)P.rows_per_task, D);
+        const bool row_in = (y0 + warp) < Hy;  // warp-uniform
 
-        Plane3 prev, cur, next, m;
-        load_plane<T>(img, D, Hy, W, z0 - 1, y, x0, lane, vec_ok, prev);
-        load_plane<T>(img, D, Hy, W, z0, y, x0, lane, vec_ok, cur);
-        int cm_prev[4];
-        plane_max(prev, cur, m);
-        quad_c2d(m.r[0], m.r[1], m.r[2], cm_prev);
-        float below[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) below[j] = prev.r[1][1 + j];
+        // prologue: planes z0 - 1 (buffer 0) and z0 (buffer 1)
+        __syncthreads();  // the previous task's readers are done with both buffers
+        plane_keys<T>(img, D, Hy, W, z0 - 1, x0, y0, vec_ok, K, table, keybuf[0]);
+        plane_keys<T>(img, D, Hy, W, z0, x0, y0, vec_ok, K, table, keybuf[1]);
+        __syncthreads();
+        uint32_t cm0, cm1;  // c2(M_{z-1}) at the lane's pixels (plain values)
+        uint32_t below0, below1;  // keys of plane z - 1 at the lane's pixels
+        KeyRow ca = smem_key_row(keybuf[1], warp, lane);
+        KeyRow cb = smem_key_row(keybuf[1], warp + 1, lane);
+        KeyRow cd = smem_key_row(keybuf[1], warp + 2, lane);
+        {
+            const KeyRow pa = smem_key_row(keybuf[0], warp, lane);
+            const KeyRow pb = smem_key_row(keybuf[0], warp + 1, lane);
+            const KeyRow pd = smem_key_row(keybuf[0], warp + 2, lane);
+            const KeyRow ma = max_rows(pa, ca), mb = max_rows(pb, cb), md = max_rows(pd, cd);
+            uint32_t s0, s1;
+            sp_init(ma, mb, s0, s1);
+            c2_quad(ma, mb, md, kPlain, s0, s1, cm0, cm1);
+            below0 = pb.own0;
+            below1 = pb.own1;
+        }
 
         for (int64_t z = z0; z < z1; ++z) {
-            load_plane<T>(img, D, Hy, W, z + 1, y, x0, lane, vec_ok, next);
-            int cs[4], cm[4], c[4];
-            quad_c2d(cur.r[0], cur.r[1], cur.r[2], cs);
-            plane_max(cur, next, m);
-            quad_c2d(m.r[0], m.r[1], m.r[2], cm);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float v = cur.r[1][1 + j];
-                const bool own_up = next.r[1][1 + j] < v;
-                const bool own_dn = below[j] <= v;
-                c[j] = cs[j] - (own_up ? cm[j] : 0) - (own_dn ? cm_prev[j] : 0);
-                cm_prev[j] = cm[j];
-                below[j] = v;
+            uint16_t *nbuf = keybuf[(z - z0) & 1];  // plane z + 1 replaces plane z - 1
+            __syncthreads();
+            plane_keys<T>(img, D, Hy, W, z + 1, x0, y0, vec_ok, K, table, nbuf);
+            __syncthreads();
+            const KeyRow na = smem_key_row(nbuf, warp, lane);
+            const KeyRow nb = smem_key_row(nbuf, warp + 1, lane);
+            const KeyRow nd = smem_key_row(nbuf, warp + 2, lane);
+            if (row_in) {
+                uint32_t s0, s1, cs0, cs1, cn0, cn1;
+                sp_init(ca, cb, s0, s1);
+                c2_quad(ca, cb, cd, kBias, s0, s1, cs0, cs1);
+                const KeyRow ma = max_rows(ca, na), mb = max_rows(cb, nb), md = max_rows(cd, nd);
+                sp_init(ma, mb, s0, s1);
+                c2_quad(ma, mb, md, kPlain, s0, s1, cn0, cn1);
+                // c = cS - [k_{z+1} < k_z] c2(M_z) - [k_{z-1} <= k_z] c2(M_{z-1})
+                const uint32_t up0 = h2_lt_mask(nb.own0, cb.own0);
+                const uint32_t up1 = h2_lt_mask(nb.own1, cb.own1);
+                const uint32_t dn0 = h2_le_mask(below0, cb.own0);
+                const uint32_t dn1 = h2_le_mask(below1, cb.own1);
+                const uint32_t c0 = h2_sub(h2_sub(cs0, cn0 & up0), cm0 & dn0);
+                const uint32_t c1 = h2_sub(h2_sub(cs1, cn1 & up1), cm1 & dn1);
+                hist_pair(cb.own0, c0, limit, hist);
+                hist_pair(cb.own1, c1, limit, hist);
+                cm0 = cn0;
+                cm1 = cn1;
             }
-            accumulate4<T, CAP>(c, cur.r[1], P, table, hist);
-            cur = next;
+            below0 = cb.own0;
+            below1 = cb.own1;
+            ca = na;
+            cb = nb;
+            cd = nd;
         }
     }
     block_flush(P, hist, b);
@@ -336,7 +474,6 @@ __global__ void __launch_bounds__(kScanThreads) ecc_bin_scan_kernel(int64_t *out
     for (int base = 0; base < H; base += kScanThreads) {
         const int i = base + threadIdx.x;
         long long v = (i < H) ? (long long)row[i] : 0;
-        // inclusive warp scan
 #pragma unroll
         for (int o = 1; o < kWarp; o <<= 1) {
             long long n = __shfl_up_sync(kFull, v, o);
@@ -351,7 +488,7 @@ __global__ void __launch_bounds__(kScanThreads) ecc_bin_scan_kernel(int64_t *out
                 long long n = __shfl_up_sync(kFull, s, o);
                 if (lane >= o) s += n;
             }
-            warp_sums[lane] = s;  // inclusive prefix of warp totals
+            warp_sums[lane] = s;
         }
         __syncthreads();
         const long long before = carry + (warp > 0 ? warp_sums[warp - 1] : 0);
@@ -366,15 +503,11 @@ __global__ void __launch_bounds__(kScanThreads) ecc_bin_scan_kernel(int64_t *out
 // Host-side launch (called from the C ABI after validation)
 // ----------------------------------------------------------------------------------------------
 
-static int g_num_sms = 0;
-
 static int num_sms()
 {
-    if (g_num_sms > 0) return g_num_sms;
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 148;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) n = 148;
-    g_num_sms = n;
     return n;
 }
 
@@ -392,15 +525,17 @@ static cudaError_t launch_hard(const HardPlan &pl, cudaStream_t s)
     P.key_mode = pl.key_mode;
     P.scale = pl.scale;
     P.offset = pl.offset;
+    P.key_err = pl.key_err;
     P.vec_ok = pl.vec_ok;
-    const int ntab = (pl.dtype == ECC_U8) ? 256 : pl.H + 2;
+    const int ntab = (pl.dtype == ECC_U8) ? 128 : pl.H + 2;  // u8: 256 uint16 in 128 floats
     P.table_len = ntab;
     for (int i = 0; i < ntab; ++i) P.table[i] = pl.table[i];
     for (int i = ntab; i < CAP + 2; ++i) P.table[i] = 0.0f;
 
     const int sms = num_sms();
-    const int64_t resident = (int64_t)sms * 4;  // 4 blocks of 256 threads per SM
     const int64_t strips = (pl.W + 127) / 128;
+    const int per_sm = pl.ndim == 2 ? 4 : 3;
+    const int64_t resident = (int64_t)sms * per_sm;
     if (pl.ndim == 2) {
         // rows per warp task: aim at ~16 K warp tasks in total, at least 8 rows each
         int64_t want = (pl.Hy * strips * pl.batch + 16383) / 16384;
@@ -411,11 +546,11 @@ static cudaError_t launch_hard(const HardPlan &pl, cudaStream_t s)
         P.tasks_y = (int)((pl.Hy + R - 1) / R);
         P.tasks_z = 1;
     } else {
-        const int64_t tiles_y = (pl.Hy + kHardWarps - 1) / kHardWarps;
-        // planes per task: aim at ~8 tasks per resident block, at least 8 planes each
-        int64_t tiles = strips * tiles_y * pl.batch;
-        int64_t want = (pl.D * tiles + resident * 8 - 1) / (resident * 8);
-        int64_t R = want < 8 ? 8 : (want > 128 ? 128 : want);
+        // planes per block task: aim at ~8 tasks per resident block, at least 16 planes each
+        const int64_t tiles_y = (pl.Hy + kTileRows - 1) / kTileRows;
+        const int64_t tiles = strips * tiles_y * pl.batch;
+        const int64_t want = (pl.D * tiles + resident * 8 - 1) / (resident * 8);
+        const int64_t R = want < 16 ? 16 : (want > 256 ? 256 : want);
         P.rows_per_task = (int)R;
         P.tasks_x = (int)strips;
         P.tasks_y = (int)tiles_y;
@@ -444,7 +579,11 @@ static cudaError_t launch_hard(const HardPlan &pl, cudaStream_t s)
 
 cudaError_t hard_run(const HardPlan &pl, cudaStream_t s)
 {
-    if (pl.dtype == ECC_U8) return launch_hard<uint8_t, 256>(pl, s);
+    if (pl.dtype == ECC_U8) {
+        if (pl.H <= 256) return launch_hard<uint8_t, 256>(pl, s);
+        if (pl.H <= 1024) return launch_hard<uint8_t, 1024>(pl, s);
+        return launch_hard<uint8_t, ECC_MAX_NBINS>(pl, s);
+    }
     if (pl.H <= 256) return launch_hard<float, 256>(pl, s);
     if (pl.H <= 1024) return launch_hard<float, 1024>(pl, s);
     return launch_hard<float, ECC_MAX_NBINS>(pl, s);

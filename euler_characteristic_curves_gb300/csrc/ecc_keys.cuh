@@ -1,0 +1,248 @@
+// ecc_keys.cuh -- threshold keys carried as fp16 patterns, and the half2 local-Euler stencil.
+//
+// Paper notes "Scalable GPU-Accelerated Euler Characteristic Curves: Optimization and
+// Differentiable Learning for PyTorch", "Key designs -- local computation of the Euler
+// characteristic coefficient": c(p) from the 3x3 neighbourhood, accumulated at p's bin.
+//
+// Every voxel first gets its exact threshold key k = #{j : t_j < v} (nbins = "never"). The order
+// by (key, linear index) refines the bin order, so the vertex-centric decomposition is exact on
+// keys. A key is stored as the fp16 bit pattern 0x6400 + k, which is finite, strictly increasing
+// in k for k <= 6143, and compares correctly with fp16 comparisons; voxels outside the grid carry
+// +inf (0x7C00), which is never earlier than anything. Two keys share one 32-bit register
+// (half2), so each comparison, logic and add instruction below serves two pixels.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ecc {
+
+constexpr uint32_t kKeyBase = 0x6400u;      // fp16 pattern of key 0 (the value 1024.0)
+constexpr uint32_t kAbsentHalf = 0x7C00u;   // fp16 +inf: outside the grid
+constexpr uint32_t kAbsentPair = 0x7C007C00u;
+constexpr float kMagic = 12582912.0f;       // 1.5 * 2^23: adding it (rounding up) gives ceil
+constexpr uint32_t kMagicBits = 0x4B400000u;
+
+// Estimator constants for float32 keys (host-computed, see ecc_api.cu):
+//   t = H * sat(v * sH + oH)  approximates clamp((v - vmin) (H - 1) / (vmax - vmin), 0, H),
+//   with |t - exact| <= E (bins), E <= 1/4. The key is ceil(exact), so when
+//   ceil(t - E) == ceil(t + E) that value is the key; otherwise the table decides.
+struct KeyConsts {
+    float sH, oH, Hf, E;
+    int H;
+    bool search;  // estimator unusable (degenerate range): binary-search every value
+};
+
+// Fast part of the key: returns the fp16 pattern of ceil(t - E) and accumulates, into `amb`,
+// (ceil(t + E) - ceil(t - E)), which is non-zero when the estimate is ambiguous (also for NaN,
+// +-inf and values sitting exactly on a threshold).
+__device__ __forceinline__ uint32_t key_fast(float v, const KeyConsts &K, float &amb)
+{
+    const float u = __saturatef(fmaf(v, K.sH, K.oH));
+    const float t = u * K.Hf;
+    const float lo = __fadd_ru(t - K.E, kMagic);
+    const float hi = __fadd_ru(t + K.E, kMagic);
+    amb += hi - lo;
+    return __float_as_uint(lo) - (kMagicBits - kKeyBase);
+}
+
+// Exact key for one value given its fast estimate `hb` = kKeyBase + ceil(t - E): the key is that
+// or one more, decided by the rounded-down fp32 threshold table T (T[H] = +inf). NaN -> H.
+__device__ __forceinline__ uint32_t key_fix(float v, uint32_t hb, const KeyConsts &K,
+                                           const float *__restrict__ T)
+{
+    if (v != v) return kKeyBase + (uint32_t)K.H;
+    const int lo = min((int)(hb - kKeyBase), K.H);
+    return kKeyBase + (uint32_t)(lo + (v > T[lo] ? 1 : 0));
+}
+
+// Binary search on the table: first k with v <= T[k] (H when none, also for NaN).
+__device__ __forceinline__ uint32_t key_search_pattern(float v, int H, const float *__restrict__ T)
+{
+    int lo = 0, hi = H;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (v <= T[mid])
+            hi = mid;
+        else
+            lo = mid + 1;
+    }
+    return kKeyBase + (uint32_t)lo;
+}
+
+// ------------------------------------------------------------------------------------------
+// half2 primitives (inline PTX so that each is exactly one instruction)
+// ------------------------------------------------------------------------------------------
+
+// 1.0 / 0.0 per half: a < b, a <= b
+__device__ __forceinline__ uint32_t h2_lt(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("set.lt.f16x2.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t h2_le(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("set.le.f16x2.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t h2_add(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t h2_sub(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+// NaN-free max of two key pairs (keys are never NaN)
+__device__ __forceinline__ uint32_t h2_max(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("max.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
+{
+    return __byte_perm(a, b, sel);
+}
+
+// A row of keys around a lane's four columns x .. x+3, as half2 pairs:
+//   own0 = (k[x], k[x+1]), own1 = (k[x+2], k[x+3]),
+//   L0 = (k[x-1], k[x]), R0 = (k[x+1], k[x+2]) (= left pair of own1), R1 = (k[x+3], k[x+4]).
+struct KeyRow {
+    uint32_t own0, own1, L0, R0, R1;
+};
+
+// Builds the shifted pairs from the lane's own pairs and its neighbours' (whole-warp call).
+// left_hi: fp16 pattern of k[x-1] for lane 0 (halo), right_lo: of k[x+4] for lane 31.
+__device__ __forceinline__ KeyRow make_key_row(uint32_t own0, uint32_t own1, int lane,
+                                               uint32_t left_halo, uint32_t right_halo)
+{
+    KeyRow r;
+    r.own0 = own0;
+    r.own1 = own1;
+    uint32_t left = __shfl_up_sync(0xffffffffu, own1, 1);   // neighbour's (k[x-2], k[x-1])
+    uint32_t right = __shfl_down_sync(0xffffffffu, own0, 1);  // neighbour's (k[x+4], k[x+5])
+    if (lane == 0) left = left_halo << 16;
+    if (lane == 31) right = right_halo;
+    r.L0 = prmt(left, own0, 0x5432);
+    r.R0 = prmt(own0, own1, 0x5432);
+    r.R1 = prmt(own1, right, 0x5432);
+    return r;
+}
+
+__device__ __forceinline__ KeyRow absent_row()
+{
+    KeyRow r;
+    r.own0 = r.own1 = r.L0 = r.R0 = r.R1 = kAbsentPair;
+    return r;
+}
+
+__device__ __forceinline__ KeyRow max_rows(const KeyRow &a, const KeyRow &b)
+{
+    KeyRow r;
+    r.own0 = h2_max(a.own0, b.own0);
+    r.own1 = h2_max(a.own1, b.own1);
+    r.L0 = h2_max(a.L0, b.L0);
+    r.R0 = h2_max(a.R0, b.R0);
+    r.R1 = h2_max(a.R1, b.R1);
+    return r;
+}
+
+// The value bias + c for two pixels at once (c in [-3, 1]; fp16 sums of small integers are
+// exact). With bias 1032 the result's pattern is 0x6408 + c; with bias 0 it is the plain value.
+// p: the pixels' keys; L, R: their left and right
+// neighbours; a*, d*: the rows above and below, same alignment. Sp = [p < above] (1.0 / 0.0),
+// i.e. "the pixel above is NOT earlier", reused from the previous row when marching down.
+//   earlier flags:  W = L <= p, E = R < p, N = 1 - Sp, S = d < p, NW = aL <= p, NE = aR <= p,
+//                   SW = dL < p, SE = dR < p
+//   c = 1 - W - E - N - S + N W NW + N E NE + S W SW + S E SE
+// The squares are formed by bitwise AND of 1.0 patterns (0x3C00): ~Sp has all other bits set,
+// so at least one positive operand keeps each product a clean 0 or 1.0.
+__device__ __forceinline__ uint32_t c2_pair(uint32_t p, uint32_t L, uint32_t R, uint32_t aL,
+                                            uint32_t aR, uint32_t d, uint32_t dL, uint32_t dR,
+                                            uint32_t Sp, uint32_t bias, uint32_t &S_out)
+{
+    const uint32_t W = h2_le(L, p), E = h2_lt(R, p);
+    const uint32_t S = h2_lt(d, p);
+    const uint32_t NW = h2_le(aL, p), NE = h2_le(aR, p);
+    const uint32_t SW = h2_lt(dL, p), SE = h2_lt(dR, p);
+    const uint32_t sqNW = ~Sp & W & NW;
+    const uint32_t sqNE = ~Sp & E & NE;
+    const uint32_t sqSW = S & W & SW;
+    const uint32_t sqSE = S & E & SE;
+    S_out = S;
+    // bias + c = (bias + Sp) - W - E - S + squares   (since 1 - N = Sp)
+    uint32_t acc = h2_add(bias, Sp);
+    acc = h2_sub(acc, h2_add(W, E));
+    acc = h2_sub(acc, S);
+    acc = h2_add(acc, h2_add(h2_add(sqNW, sqNE), h2_add(sqSW, sqSE)));
+    return acc;
+}
+
+// Local Euler contributions of the lane's four pixels of row b (rows a above, d below).
+// Returns the pairs (bias + c) in c0 (pixels x, x+1) and c1 (x+2, x+3); Sp0/Sp1 carry the
+// "pixel above is not earlier" flags in, and the S flags of this row out (for the row below).
+__device__ __forceinline__ void c2_quad(const KeyRow &a, const KeyRow &b, const KeyRow &d,
+                                        uint32_t bias, uint32_t &Sp0, uint32_t &Sp1, uint32_t &c0,
+                                        uint32_t &c1)
+{
+    uint32_t S0, S1;
+    c0 = c2_pair(b.own0, b.L0, b.R0, a.L0, a.R0, d.own0, d.L0, d.R0, Sp0, bias, S0);
+    c1 = c2_pair(b.own1, b.R0, b.R1, a.R0, a.R1, d.own1, d.R0, d.R1, Sp1, bias, S1);
+    Sp0 = S0;
+    Sp1 = S1;
+}
+
+// Sp for the first row of a band: [b < a] per pixel (the row above is not earlier).
+__device__ __forceinline__ void sp_init(const KeyRow &a, const KeyRow &b, uint32_t &Sp0,
+                                        uint32_t &Sp1)
+{
+    Sp0 = h2_lt(b.own0, a.own0);
+    Sp1 = h2_lt(b.own1, a.own1);
+}
+
+// 0xFFFF / 0x0000 per half: a < b, a <= b (masks, for selecting with bitwise AND)
+__device__ __forceinline__ uint32_t h2_lt_mask(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("set.lt.u32.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t h2_le_mask(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("set.le.u32.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+constexpr uint32_t kBias = 0x64086408u;  // (1032, 1032): contributions carried as 1032 + c
+constexpr int kBiasBits = 0x6408;         // pattern of 1032; pattern - kBiasBits = c for |c| <= 8
+
+// Adds the contributions of one pair to the block histogram: pixel keys `keys` (fp16 patterns),
+// values `cv` = 1032 + c (patterns 0x6408 + c). Pixels with c = 0, with key >= H ("never") or
+// outside the grid (key pattern +inf) add nothing.
+__device__ __forceinline__ void hist_pair(uint32_t keys, uint32_t cv, uint32_t key_limit_pair,
+                                          int *hist)
+{
+    // lanes where c != 0 and key < H
+    uint32_t live;
+    asm("{\n\t.reg .b32 m1, m2;\n\t"
+        "set.ne.u32.f16x2 m1, %1, %2;\n\t"
+        "set.lt.u32.f16x2 m2, %3, %4;\n\t"
+        "and.b32 %0, m1, m2;\n\t}"
+        : "=r"(live)
+        : "r"(cv), "r"(kBias), "r"(keys), "r"(key_limit_pair));
+    if (live & 0xffffu)
+        atomicAdd(hist + ((int)(keys & 0xffffu) - (int)kKeyBase), (int)(cv & 0xffffu) - kBiasBits);
+    if (live >> 16)
+        atomicAdd(hist + ((int)(keys >> 16) - (int)kKeyBase), (int)(cv >> 16) - kBiasBits);
+}
+
+}  // namespace ecc

@@ -21,6 +21,8 @@ DEV = "cuda:0"
 
 
 def gpu_hard(img, nbins, vmin, vmax, ndim=None):
+    if ndim is None:
+        ndim = img.ndim  # an unbatched image or volume
     t = torch.from_numpy(np.ascontiguousarray(img)).to(DEV)
     return ecc.ecc_hard(t, nbins, vmin, vmax, ndim=ndim).cpu().numpy()
 
