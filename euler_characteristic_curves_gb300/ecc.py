@@ -50,6 +50,8 @@ def load_library():
         lib.ecc_soft_fwd.restype = i
         lib.ecc_soft_bwd.argtypes = [p, i, p, i64, p, i, f, p, p, p, p, p, p, p, p, sz, p]
         lib.ecc_soft_bwd.restype = i
+        lib.ecc_soft_fwd_noalloc.argtypes = [p, i, p, i64, p, i, f, p, p, p, p]
+        lib.ecc_soft_fwd_noalloc.restype = i
         lib.ecc_status_str.argtypes = [i]
         lib.ecc_status_str.restype = ctypes.c_char_p
         lib.ecc_version.argtypes = []
@@ -181,6 +183,25 @@ def ecc_soft_fwd(img, tau, lam: float, alpha, u, ws=None, out=None, ndim=None, s
     _check(rc, "ecc_soft_fwd")
     out = out.view(batch, K)
     return (out if batched else out[0]), ws
+
+
+def ecc_soft_fwd_noalloc(img, tau, lam: float, alpha, u, out=None, ndim=None, stream=None):
+    """Soft ECC S[b, k] through ecc_soft_fwd_noalloc: same result as ecc_soft_fwd, but the
+    workspace is the library's own fixed device array, so the call allocates no device memory
+    (``out`` may be passed pre-allocated too). Sizes needing more than the array raise."""
+    ndim, batch, dims, batched = _soft_common(img, tau, alpha, u, ndim)
+    K = tau.numel()
+    if out is None:
+        out = torch.empty((batch, K), dtype=torch.float32, device=img.device)
+    lib = load_library()
+    rc = lib.ecc_soft_fwd_noalloc(ctypes.c_void_p(img.data_ptr()), ndim, _dims_array(dims),
+                                  batch, ctypes.c_void_p(tau.data_ptr()), K, float(lam),
+                                  ctypes.c_void_p(alpha.data_ptr()),
+                                  ctypes.c_void_p(u.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+                                  _stream_handle(stream))
+    _check(rc, "ecc_soft_fwd_noalloc")
+    out = out.view(batch, K)
+    return out if batched else out[0]
 
 
 def ecc_soft_bwd(img, tau, lam: float, alpha, u, grad_out, ws, want_img: bool = False, ndim=None,

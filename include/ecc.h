@@ -15,12 +15,14 @@
  *   - Images are C-contiguous, last axis fastest: a batch of 2-D images is [batch][H][W], of 3-D
  *     volumes [batch][D][H][W]. `dims` is a HOST array of `ndim` extents, slowest axis first.
  *   - Pointers named img, out, tau, alpha, u, grad_*, ws are DEVICE pointers owned by the caller;
- *     the library never allocates, frees or retains them, and allocates no device memory itself.
+ *     the library never allocates, frees or retains them, and no call allocates device memory
+ *     (ecc_soft_fwd_noalloc uses a fixed array that the loaded library image holds).
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL means the legacy default
  *     stream). Arguments are validated on the host before anything is launched; an invalid call
  *     returns a negative status and touches no memory. A failed launch returns ECC_ECUDA; errors
  *     raised later by a kernel surface at the caller's next synchronisation.
- *   - The library holds no state between calls and may be called from several host threads.
+ *   - Apart from that array, the library holds no state between calls; it may be called from
+ *     several host threads.
  *   - Cell complex: the V-construction. Voxels are vertices; axis-aligned boxes of side 0 or 1 in
  *     each axis whose corners all lie in the grid are cells (edges, squares, cubes); a cell's value
  *     is the max of its vertices. Voxels outside the grid do not exist.
@@ -134,6 +136,29 @@ int ecc_soft_bwd(const float *img, int ndim, const int64_t *dims, int64_t batch,
                  int K, float lambda, const float *alpha, const float *u, const float *grad_out,
                  float *grad_tau, float *grad_alpha, float *grad_u, float *grad_img, void *ws,
                  size_t ws_bytes, ecc_stream_t stream);
+
+/*
+ * Soft ECC forward pass that allocates nothing -- no counterpart in the paper notes.
+ *
+ * For callers that cannot allocate device memory (for example a plugin inside a host framework
+ * that owns all device memory and provides no allocator, or a latency-critical loop that cannot
+ * afford cudaMalloc's device-wide synchronisation). Computes exactly what ecc_soft_fwd computes,
+ * with the same arguments minus the workspace: the workspace lives in a library-owned device
+ * array of ECC_NOALLOC_SCRATCH_BYTES bytes, which every GPU that loads the library holds until
+ * the process exits. The call allocates nothing (no cudaMalloc / cudaFree, no allocating library
+ * routine).
+ *
+ * Sizes whose workspace (ecc_soft_workspace_bytes) exceeds ECC_NOALLOC_SCRATCH_BYTES are rejected
+ * with ECC_ERANGE before anything runs. The first call on each device looks up that device's
+ * array address (cudaGetSymbolAddress) with the device current; make that first call before any
+ * stream capture. All calls on a device share one array, which keeps the last call's contents
+ * (each call overwrites whatever it reads): calls whose executions overlap on the GPU race and
+ * must be serialised by the caller, e.g. by issuing them on one stream.
+ */
+#define ECC_NOALLOC_SCRATCH_BYTES (16u << 20)
+int ecc_soft_fwd_noalloc(const float *img, int ndim, const int64_t *dims, int64_t batch,
+                         const float *tau, int K, float lambda, const float *alpha,
+                         const float *u, float *out, ecc_stream_t stream);
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *ecc_status_str(int status);
