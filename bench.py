@@ -333,13 +333,15 @@ def time_e2e(args, parts, inputs, step, device, world):
 
 # ------------------------------------------------------------------------------------ oracle arm
 
+SAMPLE_2D = 512           # 2-D parts: a 512 x 512 crop of one image
+SAMPLE_3D = (32, 128, 128)  # 3-D parts: a 32 x 128 x 128 crop
+SAMPLE_SOFT = 128        # soft part: one 128 x 128 image, all K thresholds, fwd + bwd
+SAMPLE_TEXT = ("each 2-D part cropped to 512^2 (one image), each 3-D part to 32x128x128, "
+               "the soft part one 128^2 image with all K thresholds (fwd + bwd)")
+
+
 def oracle_sample_step(parts, cache):
-    """The oracle on a bounded sample of every part of the workload; returns voxels processed.
-
-    Samples: 2-D images are cropped to at most 1024 x 1024 (one image of a batch), 3-D volumes
-    to 96 x 256 x 256 voxels, the soft part to one image with all K thresholds (fwd + bwd)."""
-    import numpy as np
-
+    """The oracle on a bounded sample of every part of the workload; returns voxels processed."""
     import oracle
     from euler_characteristic_curves_gb300 import synthetic
 
@@ -350,9 +352,9 @@ def oracle_sample_step(parts, cache):
             if p[0] == "hard":
                 _, shape, batch, kind, nbins, vmin, vmax, seed = p
                 if len(shape) == 2:
-                    sh = (min(shape[0], 1024), min(shape[1], 1024))
+                    sh = (min(shape[0], SAMPLE_2D), min(shape[1], SAMPLE_2D))
                 else:
-                    sh = (min(shape[0], 96), min(shape[1], 256), min(shape[2], 256))
+                    sh = tuple(min(a, b) for a, b in zip(shape, SAMPLE_3D))
                 if kind == "u8blur":
                     img = synthetic.blurred_noise_u8(sh, seed)
                 elif kind == "u8grf":
@@ -362,7 +364,8 @@ def oracle_sample_step(parts, cache):
                 cache[key] = img
             else:
                 _, shape, batch, K, lam, s_img, s_u, s_g = p
-                cache[key] = (synthetic.grf(shape, s_img), synthetic.uniform_thresholds(K),
+                sh = (min(shape[0], SAMPLE_SOFT), min(shape[1], SAMPLE_SOFT))
+                cache[key] = (synthetic.grf(sh, s_img), synthetic.uniform_thresholds(K),
                               synthetic.soft_direction(len(shape), s_u),
                               synthetic.upstream_grad((1, K), s_g))
         x = cache[key]
@@ -377,16 +380,18 @@ def oracle_sample_step(parts, cache):
     return vox
 
 
-def time_oracle(steps, warmup, parts):
+def time_oracle(steps, warmup, parts, min_seconds=0.0):
+    """Times `steps` sample passes (after `warmup`), continuing until min_seconds have passed."""
     cache = {}
     for _ in range(warmup):
         oracle_sample_step(parts, cache)
     t0 = time.perf_counter()
-    vox = 0
-    for _ in range(steps):
+    vox, n = 0, 0
+    while n < steps or time.perf_counter() - t0 < min_seconds:
         vox += oracle_sample_step(parts, cache)
+        n += 1
     dt = time.perf_counter() - t0
-    return vox, dt
+    return vox, dt, n
 
 
 # ------------------------------------------------------------------------------------ dist
@@ -452,7 +457,7 @@ def main(argv=None):
     if args.impl == "reference":
         if rank != 0:
             return 0
-        vox, dt = time_oracle(args.steps, args.warmup, parts)
+        vox, dt, _ = time_oracle(args.steps, args.warmup, parts)
         value = vox / dt / 1e9
         line = {"impl": "reference", "metric": METRIC, "value": round(value, 6),
                 "unit": "Gvoxels/s", "n_gpus": args.gpus, "steps": args.steps,
@@ -461,10 +466,7 @@ def main(argv=None):
                 "dtype": "f64 oracle on f32/u8 inputs", "data": "synthetic (seeded GRF)",
                 "config": config,
                 "cpu_baseline": {"value": round(value, 6), "unit": "Gvoxels/s", "cores": 1,
-                                 "kind": "oracle",
-                                 "sample": "per step: each 2-D part cropped to <= 1024^2 "
-                                           "(one image), each 3-D part to 96x256x256, soft "
-                                           "part one 256^2 image fwd+bwd"},
+                                 "kind": "oracle", "sample": "per step: " + SAMPLE_TEXT},
                 "e2e": {"value": round(value, 6), "unit": "Gvoxels/s",
                         "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
@@ -511,12 +513,10 @@ def main(argv=None):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu_steps = 1
-        vox, dt = time_oracle(cpu_steps, 0, parts)
+        vox, dt, npass = time_oracle(1, 1, parts, min_seconds=10.0)
         cpu = {"value": round(vox / dt / 1e9, 6), "unit": "Gvoxels/s", "cores": 1,
                "kind": "oracle", "seconds": round(dt, 2),
-               "sample": "one pass: each 2-D part cropped to <= 1024^2 (one image), each 3-D "
-                         "part to 96x256x256, soft part one 256^2 image fwd+bwd"}
+               "sample": f"{npass} passes (single-threaded C, ~10 s), each: " + SAMPLE_TEXT}
     soft_ms = [part_ms[i] for i, p in enumerate(parts) if p[0] == "soft"]
     line = {"metric": METRIC, "value": round(value, 3), "unit": "Gvoxels/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),

@@ -65,6 +65,30 @@ def test_linear_ramp_closed_form(axis, sign):
     # (the other component is a subgradient: X ties along that axis, so it is not checked)
 
 
+@pytest.mark.parametrize("shape,u,pixel", [((3, 4), (0.0, 0.0), (0, 0)),
+                                           ((5, 7), (0.0, 0.0), (0, 0)),
+                                           ((3, 5), (0.0, 0.3), (0, 0)),
+                                           ((3, 5), (0.0, -0.3), (0, 4)),
+                                           ((4, 3), (-0.3, 0.0), (3, 0)),
+                                           ((4, 6), (-0.2, -0.1), (3, 5))])
+def test_gradient_lands_on_the_first_entering_pixel(shape, u, pixel):
+    """f = 0, X = u . x (constant when u = 0). Every sublevel set is a box, so only the first
+    pixel to enter has a non-zero local contribution (+1), and the image gradient sits on that
+    pixel alone: the first pixel in index order when values tie ("lower index enters first"),
+    otherwise the corner where X is smallest -- which corner pins the axis order of u and x."""
+    f = np.zeros(shape, np.float32)
+    lam, tau = 4.0, np.asarray([0.1], np.float32)
+    r = oracle.ecc_soft_bwd(f, tau, lam, 1.0, np.asarray(u, np.float32), np.ones(1))
+    gi = r["grad_img"]
+    nz = np.argwhere(gi != 0)
+    assert [tuple(x) for x in nz] == [pixel]
+    x0 = -float(np.float32(abs(u[0]))) if u[0] else 0.0
+    x1 = -float(np.float32(abs(u[1]))) if u[1] else 0.0
+    s = 1.0 / (1.0 + np.exp(-lam * (0.1 - (x0 + x1))))
+    # dL/dX = -lambda s (1 - s) for the only contributing vertex, grad_img = alpha dL/dX
+    assert abs(gi[pixel] + lam * s * (1 - s)) < 1e-7
+
+
 def test_alpha_rescaling_identity():
     """With u = 0, S(f; alpha, lam, tau) = S(f; 1, lam * alpha, tau / alpha)."""
     f = synthetic.grf((10, 11), 5)
