@@ -8,7 +8,7 @@ Gvoxels per second of the whole step; the per-part device times, the roofline fr
 dominant kernel and the soft fwd+bwd milliseconds are reported beside it.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload headline|2d8192|3d1024|2d1024x16|2d128u8|3d512u8|soft]
+                    [--workload headline|2d8192|3d1024|2d1024x16|2d128u8|3d512u8|soft|soft3d]
 
 Under torchrun every rank runs the same workload on its own GPU (independent problems, no
 collective on the data path; weak scaling); the timed region is bracketed by barriers and the
@@ -49,6 +49,8 @@ WORKLOADS = {
     "3d256": [("hard", (256, 1024, 1024), 1, "f32", 256, 0.0, 1.0, 4)],
     "2d4096": [("hard", (4096, 4096), 1, "f32", 1024, 0.0, 1.0, 3)],
     "soft16": [("soft", (256, 256), 16, 128, 50.0, 6, 7, 8)],
+    # the soft path on 3-D volumes (3 x 3 x 3 neighbourhoods): 4 GRF volumes of 128^3
+    "soft3d": [("soft", (128, 128, 128), 4, 128, 50.0, 9, 10, 11)],
 }
 WORKLOADS["headline"] = WORKLOADS["2d8192"] + WORKLOADS["3d1024"] + WORKLOADS["soft"]
 
@@ -62,7 +64,7 @@ def part_name(p):
     if p[0] == "hard":
         dims = "x".join(str(s) for s in p[1])
         return f"hard_{len(p[1])}d_{p[2]}x{dims}_{p[3]}_H{p[4]}"
-    return f"soft_fwd_bwd_{p[2]}x{p[1][0]}x{p[1][1]}_K{p[3]}"
+    return f"soft_fwd_bwd_{p[2]}x{'x'.join(str(x) for x in p[1])}_K{p[3]}"
 
 
 def part_voxels(p):
@@ -167,6 +169,39 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+# Soft-path roofline. The soft kernels evaluate one sigmoid term per (listed voxel, threshold)
+# in the forward pass and again in the backward pass. A term takes one special-function (XU)
+# operation -- the reciprocal of 1 + e, with e = E_p F_k a plain product -- or two on tiles whose
+# exponents leave the factorised range (ex2 + reciprocal), plus about 4 FP32 operations forward
+# (E F, 1 + e, the select, the accumulate) and 7 backward (also w = r - r^2 and the two
+# accumulations of c w and g w). GB300 issues 16 XU and 128 FP32 operations per clock per SM on
+# 152 SMs, so at one XU operation per term the XU pipe bounds the rate:
+#     peak terms/s = 152 * 16 * f_sm.
+SM_COUNT, XU_PER_CLK, FP32_PER_CLK = 152, 16, 128
+FP32_PER_TERM = (4 + 7) / 2  # average over the forward and the backward term
+
+
+def soft_roofline(p, ms, stats, clocks):
+    n_list, n_direct, n_tiles = stats
+    K = p[3]
+    terms = 2 * n_list * K  # forward + backward
+    xu_ops = terms * (1.0 + (n_direct / n_tiles if n_tiles else 0.0))
+    f_sm = (clocks.get("sm_max_mhz") or 2070.0) * 1e6
+    xu_peak = SM_COUNT * XU_PER_CLK * f_sm
+    fp32_peak = SM_COUNT * FP32_PER_CLK * f_sm
+    achieved = terms / (ms * 1e-3)
+    return {"listed_voxels": n_list, "direct_tiles": n_direct, "tiles": n_tiles,
+            "dense_terms": 2 * part_voxels(p) * K,
+            "roofline": {"bound": "xu", "unit": "Gterms/s",
+                         "achieved": round(achieved / 1e9, 2),
+                         "peak": round(xu_peak / 1e9, 2),
+                         "frac": round(xu_ops / (ms * 1e-3) / xu_peak, 4),
+                         "fp32_frac": round(terms * FP32_PER_TERM / (ms * 1e-3) / fp32_peak, 4),
+                         "peak_source": "derived: 152 SMs x 16 XU ops/clk x max SM clock, one "
+                                        "XU op per term (two on direct-form tiles)",
+                         "timing": "CUDA events around forward + backward library calls"}}
+
+
 # ------------------------------------------------------------------------------------ our arm
 
 def make_inputs(parts, device):
@@ -236,6 +271,15 @@ class OurStep:
             o["grads"] = self.ecc.ecc_soft_bwd(x["img"], x["tau"], x["lam"], x["alpha"], x["u"],
                                                x["g"], o["ws"])
 
+    def soft_stats(self):
+        """Per soft part: [listed voxels, direct-form tiles, tiles] of the last forward pass."""
+        out = {}
+        for p, x, o in zip(self.parts, self.inputs, self.outs):
+            if p[0] == "soft":
+                st = self.ecc.ecc_soft_stats(x["img"], p[3], o["ws"], ndim=len(p[1]))
+                out[part_name(p)] = [int(v) for v in st.cpu().tolist()]
+        return out
+
     def results(self):
         res = []
         for p, o in zip(self.parts, self.outs):
@@ -279,8 +323,9 @@ def time_ours(args, parts, rank, world, device):
     part_ms = [statistics.mean(ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(args.steps))
                for i in range(len(parts))]
     total_ms = max_over_ranks(total_ms, world)
+    soft_stats = step.soft_stats()
     e2e = time_e2e(args, parts, inputs, step, device, world)
-    return total_ms, part_ms, clocks, step.launches_per_step * args.steps, e2e
+    return total_ms, part_ms, clocks, step.launches_per_step * args.steps, e2e, soft_stats
 
 
 def time_e2e(args, parts, inputs, step, device, world):
@@ -336,8 +381,10 @@ def time_e2e(args, parts, inputs, step, device, world):
 SAMPLE_2D = 512           # 2-D parts: a 512 x 512 crop of one image
 SAMPLE_3D = (32, 128, 128)  # 3-D parts: a 32 x 128 x 128 crop
 SAMPLE_SOFT = 128        # soft part: one 128 x 128 image, all K thresholds, fwd + bwd
+SAMPLE_SOFT_3D = 24      # 3-D soft part: one 24^3 volume
 SAMPLE_TEXT = ("each 2-D part cropped to 512^2 (one image), each 3-D part to 32x128x128, "
-               "the soft part one 128^2 image with all K thresholds (fwd + bwd)")
+               "a 2-D soft part one 128^2 image (a 3-D one a 24^3 volume) with all K "
+               "thresholds (fwd + bwd)")
 
 
 def oracle_sample_step(parts, cache):
@@ -364,7 +411,10 @@ def oracle_sample_step(parts, cache):
                 cache[key] = img
             else:
                 _, shape, batch, K, lam, s_img, s_u, s_g = p
-                sh = (min(shape[0], SAMPLE_SOFT), min(shape[1], SAMPLE_SOFT))
+                if len(shape) == 2:
+                    sh = (min(shape[0], SAMPLE_SOFT), min(shape[1], SAMPLE_SOFT))
+                else:
+                    sh = tuple(min(a, SAMPLE_SOFT_3D) for a in shape)
                 cache[key] = (synthetic.grf(sh, s_img), synthetic.uniform_thresholds(K),
                               synthetic.soft_direction(len(shape), s_u),
                               synthetic.upstream_grad((1, K), s_g))
@@ -480,7 +530,8 @@ def main(argv=None):
     from euler_characteristic_curves_gb300 import build as libbuild
 
     libbuild.build()
-    total_ms, part_ms, clocks, launches, e2e = time_ours(args, parts, rank, world, device)
+    total_ms, part_ms, clocks, launches, e2e, soft_stats = time_ours(args, parts, rank, world,
+                                                                     device)
     ms_step = total_ms / args.steps
     value = unit_vox * world / (ms_step * 1e-3) / 1e9
 
@@ -496,6 +547,8 @@ def main(argv=None):
             alg = part_voxels(p) * elem + 8 * p[2] * p[4]
             ent["hbm_gbs"] = round(alg / (ms * 1e-3) / 1e9, 1)
             ent["hbm_frac"] = round(alg / (ms * 1e-3) / 1e9 / peak, 4)
+        if p[0] == "soft":
+            ent.update(soft_roofline(p, ms, soft_stats[part_name(p)], clocks))
         breakdown[part_name(p)] = ent
     roofline = None
     pd = parts[dom]
@@ -525,6 +578,8 @@ def main(argv=None):
             "data": "synthetic (seeded Gaussian random fields, k^-3 spectrum)",
             "config": config, "parts": breakdown,
             "soft_fwd_bwd_ms": round(soft_ms[0], 4) if soft_ms else None,
+            "soft_roofline": next((breakdown[part_name(p)]["roofline"] for p in parts
+                                   if p[0] == "soft"), None),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches, "clocks": clocks,
             "kernel_source": kernel_source_hash()}

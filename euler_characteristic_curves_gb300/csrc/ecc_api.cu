@@ -153,7 +153,7 @@ static int soft_check(const float *img, int ndim, const int64_t *dims, int64_t b
                       void *ws, size_t ws_bytes, SoftLayout &L)
 {
     if (!img || !dims || !tau || !alpha || !u) return ECC_EINVAL;
-    if (ndim != 2) return ECC_EDIM;
+    if (ndim != 2 && ndim != 3) return ECC_EDIM;
     for (int d = 0; d < ndim; ++d)
         if (dims[d] < 1) return ECC_EDIM;
     if (batch < 1 || K < 1) return ECC_EINVAL;
@@ -190,6 +190,22 @@ int ecc_soft_bwd(const float *img, int ndim, const int64_t *dims, int64_t batch,
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (soft_run_bwd(L, img, tau, lambda, alpha, grad_out, grad_tau, grad_alpha, grad_u, grad_img,
                      ws, s) != cudaSuccess)
+        return ECC_ECUDA;
+    return ECC_OK;
+}
+
+int ecc_soft_stats(int ndim, const int64_t *dims, int64_t batch, int K, const void *ws,
+                   size_t ws_bytes, int64_t *stats, ecc_stream_t stream)
+{
+    if (!dims || !stats) return ECC_EINVAL;
+    if (ndim != 2 && ndim != 3) return ECC_EDIM;
+    for (int d = 0; d < ndim; ++d)
+        if (dims[d] < 1) return ECC_EDIM;
+    if (batch < 1 || K < 1) return ECC_EINVAL;
+    SoftLayout L;
+    if (!soft_layout(ndim, dims, batch, K, L)) return ECC_ERANGE;
+    if (!ws || ws_bytes < L.total || ((uintptr_t)ws % 256) != 0) return ECC_EWS;
+    if (soft_run_stats(L, ws, stats, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return ECC_ECUDA;
     return ECC_OK;
 }

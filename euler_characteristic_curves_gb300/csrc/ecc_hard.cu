@@ -23,7 +23,8 @@
 //     c(p) = c2(S_z; p) - [k_{z+1} < k_z] c2(M_z; x,y) - [k_{z-1} <= k_z] c2(M_{z-1}; x,y)
 // (the later voxel wins ties; the max of two keys is the key of the max). A block owns a tile of
 // 128 columns x 8 rows and walks z; each plane's keys are computed once into a shared tile with a
-// one-pixel halo, from which every warp builds the three rows around its own row.
+// one-pixel halo, from which every warp builds the three rows around its own row. The raw values
+// of the next plane are loaded into registers one plane ahead.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -35,6 +36,14 @@ namespace ecc {
 
 constexpr int kHardThreads = 256;
 constexpr int kHardWarps = kHardThreads / kWarp;
+
+// Resident blocks per SM the kernels are compiled for (register budget 65536 / (256 * blocks)).
+#ifndef ECC_2D_MIN_BLOCKS
+#define ECC_2D_MIN_BLOCKS 3
+#endif
+#ifndef ECC_3D_MIN_BLOCKS
+#define ECC_3D_MIN_BLOCKS 3
+#endif
 
 // ----------------------------------------------------------------------------------------------
 // Block setup, keys and histogram
@@ -74,8 +83,26 @@ __device__ __forceinline__ KeyConsts key_consts(const HardParams<CAP> &P)
     return K;
 }
 
-// Raw values of one row around a lane's four columns, plus (lanes 0 / 31) the value just left of
-// column x0 / right of column x0 + 127. `valid` has bit j set when column x + j is inside the grid.
+// Key pattern of one float value (any value; NaN -> H). SEARCH: binary-search every value (the
+// estimator is not usable for this threshold range).
+template <bool SEARCH>
+__device__ __forceinline__ uint32_t key_one(float v, const KeyConsts &K, const float *__restrict__ T)
+{
+    if (SEARCH) return key_search_pattern(v, K.H, T);
+    float amb = 0.0f;
+    const uint32_t k = key_fast(v, K, amb);
+    return (amb != 0.0f) ? key_fix(v, k, K, T) : k;
+}
+
+template <bool SEARCH>
+__device__ __forceinline__ uint32_t key_one(uint8_t v, const KeyConsts &, const float *__restrict__ T)
+{
+    return reinterpret_cast<const uint16_t *>(T)[v];
+}
+
+// Raw values of one row around a lane's four columns, plus (lanes 0 / 31 only) the value just
+// left of column x0 / right of column x0 + 127. `valid` has bit j set when column x + j is inside
+// the grid; `halo_in` says whether the lane's halo column exists.
 template <typename T>
 struct RawRow;
 
@@ -85,34 +112,33 @@ struct RawRow<float> {
     float halo;
     uint32_t valid;
     bool present;  // row inside the grid (warp-uniform)
+    bool halo_in;
 };
 
 template <>
 struct RawRow<uint8_t> {
     uint32_t bytes;
-    uint32_t halo;
+    uint8_t halo;
     uint32_t valid;
     bool present;
+    bool halo_in;
 };
 
-__device__ __forceinline__ RawRow<float> load_raw(const float *__restrict__ plane, int64_t Hy,
-                                                  int64_t W, int64_t y, int64_t x0, int lane,
-                                                  bool vec)
+template <typename T>
+__device__ __forceinline__ void load_own(const T *__restrict__ row, int xs, int W, bool vec,
+                                         RawRow<T> &r);
+
+template <>
+__device__ __forceinline__ void load_own<float>(const float *__restrict__ row, int xs, int W,
+                                                bool vec, RawRow<float> &r)
 {
-    RawRow<float> r;
-    r.present = (y >= 0 && y < Hy);
-    r.valid = 0xfu;
-    r.halo = 0.0f;
-    r.v[0] = r.v[1] = r.v[2] = r.v[3] = 0.0f;
-    if (!r.present) return r;
-    const float *__restrict__ row = plane + y * W;
-    const int64_t xs = x0 + 4 * lane;
     if (vec) {
         const float4 q = __ldg(reinterpret_cast<const float4 *>(row + xs));
         r.v[0] = q.x;
         r.v[1] = q.y;
         r.v[2] = q.z;
         r.v[3] = q.w;
+        r.valid = 0xfu;
     } else {
         r.valid = 0;
 #pragma unroll
@@ -122,27 +148,18 @@ __device__ __forceinline__ RawRow<float> load_raw(const float *__restrict__ plan
             r.valid |= in ? (1u << j) : 0u;
         }
     }
-    if (lane == 0 && x0 > 0) r.halo = __ldg(row + x0 - 1);
-    if (lane == kWarp - 1 && x0 + 128 < W) r.halo = __ldg(row + x0 + 128);
-    return r;
 }
 
-__device__ __forceinline__ RawRow<uint8_t> load_raw(const uint8_t *__restrict__ plane, int64_t Hy,
-                                                    int64_t W, int64_t y, int64_t x0, int lane,
-                                                    bool vec)
+template <>
+__device__ __forceinline__ void load_own<uint8_t>(const uint8_t *__restrict__ row, int xs, int W,
+                                                  bool vec, RawRow<uint8_t> &r)
 {
-    RawRow<uint8_t> r;
-    r.present = (y >= 0 && y < Hy);
-    r.valid = 0xfu;
-    r.halo = 0;
-    r.bytes = 0;
-    if (!r.present) return r;
-    const uint8_t *__restrict__ row = plane + y * W;
-    const int64_t xs = x0 + 4 * lane;
     if (vec) {
         r.bytes = __ldg(reinterpret_cast<const unsigned int *>(row + xs));
+        r.valid = 0xfu;
     } else {
         r.valid = 0;
+        r.bytes = 0;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const bool in = xs + j < W;
@@ -150,29 +167,36 @@ __device__ __forceinline__ RawRow<uint8_t> load_raw(const uint8_t *__restrict__ 
             r.valid |= in ? (1u << j) : 0u;
         }
     }
-    if (lane == 0 && x0 > 0) r.halo = __ldg(row + x0 - 1);
-    if (lane == kWarp - 1 && x0 + 128 < W) r.halo = __ldg(row + x0 + 128);
+}
+
+template <typename T>
+__device__ __forceinline__ RawRow<T> load_raw(const T *__restrict__ plane, int Hy, int W, int y,
+                                              int x0, int lane, bool vec)
+{
+    RawRow<T> r;
+    r.present = (y >= 0 && y < Hy);
+    r.halo_in = false;
+    if (!r.present) {
+        r.valid = 0;
+        return r;
+    }
+    const T *__restrict__ row = plane + (int64_t)y * W;
+    load_own<T>(row, x0 + 4 * lane, W, vec, r);
+    const int hx = (lane == 0) ? x0 - 1 : x0 + 128;
+    r.halo_in = (lane == 0 || lane == kWarp - 1) && hx >= 0 && hx < W;
+    r.halo = r.halo_in ? __ldg(row + hx) : (T)0;
     return r;
 }
 
-// Key pattern of one float value (any value, NaN -> H).
-__device__ __forceinline__ uint32_t key_one(float v, const KeyConsts &K, const float *__restrict__ T)
-{
-    if (K.search) return key_search_pattern(v, K.H, T);
-    float amb = 0.0f;
-    const uint32_t k = key_fast(v, K, amb);
-    return (amb != 0.0f) ? key_fix(v, k, K, T) : k;
-}
-
-// fp16 key patterns of the lane's four values (pairs k0 | k1 << 16, k2 | k3 << 16) and of its
-// halo value (lanes 0 and 31; absent when the halo column is outside the grid). Whole-warp call.
+// fp16 key patterns of the lane's four values as pairs (k0 | k1 << 16, k2 | k3 << 16), and of
+// its halo value (absent when there is none). Whole-warp call.
+template <bool SEARCH>
 __device__ __forceinline__ void raw_keys(const RawRow<float> &r, const KeyConsts &K,
-                                         const float *__restrict__ T, int lane, int64_t x0,
-                                         int64_t W, uint32_t &own0, uint32_t &own1,
-                                         uint32_t &halo_key)
+                                         const float *__restrict__ T, uint32_t &own0,
+                                         uint32_t &own1, uint32_t &halo_key)
 {
     uint32_t k[4];
-    if (K.search) {
+    if (SEARCH) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) k[j] = key_search_pattern(r.v[j], K.H, T);
     } else {
@@ -194,14 +218,13 @@ __device__ __forceinline__ void raw_keys(const RawRow<float> &r, const KeyConsts
     own0 = prmt(k[0], k[1], 0x5410);
     own1 = prmt(k[2], k[3], 0x5410);
     halo_key = kAbsentHalf;
-    if (lane == 0 && x0 > 0) halo_key = key_one(r.halo, K, T);
-    if (lane == kWarp - 1 && x0 + 128 < W) halo_key = key_one(r.halo, K, T);
+    if (r.halo_in) halo_key = key_one<SEARCH>(r.halo, K, T);
 }
 
-__device__ __forceinline__ void raw_keys(const RawRow<uint8_t> &r, const KeyConsts &,
-                                         const float *__restrict__ T, int lane, int64_t x0,
-                                         int64_t W, uint32_t &own0, uint32_t &own1,
-                                         uint32_t &halo_key)
+template <bool SEARCH>
+__device__ __forceinline__ void raw_keys(const RawRow<uint8_t> &r, const KeyConsts &K,
+                                         const float *__restrict__ T, uint32_t &own0,
+                                         uint32_t &own1, uint32_t &halo_key)
 {
     const uint16_t *lut = reinterpret_cast<const uint16_t *>(T);
     uint32_t k[4];
@@ -210,19 +233,16 @@ __device__ __forceinline__ void raw_keys(const RawRow<uint8_t> &r, const KeyCons
         k[j] = (r.valid >> j & 1u) ? (uint32_t)lut[(r.bytes >> (8 * j)) & 0xffu] : kAbsentHalf;
     own0 = prmt(k[0], k[1], 0x5410);
     own1 = prmt(k[2], k[3], 0x5410);
-    halo_key = kAbsentHalf;
-    if (lane == 0 && x0 > 0) halo_key = lut[r.halo & 0xffu];
-    if (lane == kWarp - 1 && x0 + 128 < W) halo_key = lut[r.halo & 0xffu];
+    halo_key = r.halo_in ? (uint32_t)lut[r.halo] : kAbsentHalf;
 }
 
-template <typename T>
+template <bool SEARCH, typename T>
 __device__ __forceinline__ KeyRow key_row(const RawRow<T> &r, const KeyConsts &K,
-                                          const float *__restrict__ table, int lane, int64_t x0,
-                                          int64_t W)
+                                          const float *__restrict__ table, int lane)
 {
     if (!r.present) return absent_row();  // warp-uniform
     uint32_t own0, own1, hk;
-    raw_keys(r, K, table, lane, x0, W, own0, own1, hk);
+    raw_keys<SEARCH>(r, K, table, own0, own1, hk);
     return make_key_row(own0, own1, lane, hk, hk);
 }
 
@@ -233,8 +253,8 @@ __device__ __forceinline__ KeyRow key_row(const RawRow<T> &r, const KeyConsts &K
 // Work: an image is cut into warp tasks (strip of 128 columns) x (band of rows_per_task rows),
 // strip index fastest. blockIdx.y = image; block g of the image takes the task range
 // [g * T / G, (g + 1) * T / G) and its warps take those tasks round-robin.
-template <typename T, int CAP>
-__global__ void __launch_bounds__(kHardThreads) ecc_hard2d_kernel(const __grid_constant__
+template <typename T, int CAP, bool SEARCH>
+__global__ void __launch_bounds__(kHardThreads, ECC_2D_MIN_BLOCKS) ecc_hard2d_kernel(const __grid_constant__
                                                                   HardParams<CAP> P)
 {
     extern __shared__ int smem[];
@@ -247,31 +267,32 @@ __global__ void __launch_bounds__(kHardThreads) ecc_hard2d_kernel(const __grid_c
     const int lane = threadIdx.x & (kWarp - 1);
     const int warp = threadIdx.x >> 5;
     const int64_t Tn = P.tasks_per_image;
-    const int64_t t_begin = Tn * blockIdx.x / P.ctas_per_image;
-    const int64_t t_end = Tn * (blockIdx.x + 1) / P.ctas_per_image;
+    const int t_begin = (int)(Tn * blockIdx.x / P.ctas_per_image);
+    const int t_end = (int)(Tn * (blockIdx.x + 1) / P.ctas_per_image);
     const KeyConsts K = key_consts(P);
-    const int64_t Hy = P.Hy, W = P.W;
+    const int Hy = (int)P.Hy, W = (int)P.W;
+    const int R = P.rows_per_task, TX = P.tasks_x;
     const uint32_t limit = (kKeyBase + (uint32_t)P.H) * 0x10001u;
 
-    for (int64_t t = t_begin + warp; t < t_end; t += kHardWarps) {
-        const int64_t x0 = (t % P.tasks_x) * 128;
-        const int64_t y0 = (t / P.tasks_x) * P.rows_per_task;
-        const int64_t y1 = min(y0 + (int64_t)P.rows_per_task, Hy);
+    for (int t = t_begin + warp; t < t_end; t += kHardWarps) {
+        const int x0 = (t % TX) * 128;
+        const int y0 = (t / TX) * R;
+        const int y1 = min(y0 + R, Hy);
         const bool vec = P.vec_ok && (x0 + 128 <= W);
 
         // raw-row ring: at the start of step y, q0 / q1 / q2 (in rotation) hold rows y+1 .. y+3
         RawRow<T> q0 = load_raw(img, Hy, W, y0 + 1, x0, lane, vec);
         RawRow<T> q1 = load_raw(img, Hy, W, y0 + 2, x0, lane, vec);
         RawRow<T> q2 = load_raw(img, Hy, W, y0 + 3, x0, lane, vec);
-        KeyRow ka = key_row(load_raw(img, Hy, W, y0 - 1, x0, lane, vec), K, table, lane, x0, W);
-        KeyRow kb = key_row(load_raw(img, Hy, W, y0, x0, lane, vec), K, table, lane, x0, W);
+        KeyRow ka = key_row<SEARCH>(load_raw(img, Hy, W, y0 - 1, x0, lane, vec), K, table, lane);
+        KeyRow kb = key_row<SEARCH>(load_raw(img, Hy, W, y0, x0, lane, vec), K, table, lane);
         uint32_t Sp0, Sp1;
         sp_init(ka, kb, Sp0, Sp1);
 
 #define ECC_2D_STEP(QS)                                                                     \
     {                                                                                       \
         if (y >= y1) break;                                                                 \
-        const KeyRow kd = key_row(QS, K, table, lane, x0, W);                               \
+        const KeyRow kd = key_row<SEARCH>(QS, K, table, lane);                                    \
         QS = load_raw(img, Hy, W, y + 4, x0, lane, vec);                                    \
         uint32_t c0, c1;                                                                    \
         c2_quad(ka, kb, kd, kBias, Sp0, Sp1, c0, c1);                                       \
@@ -281,7 +302,7 @@ __global__ void __launch_bounds__(kHardThreads) ecc_hard2d_kernel(const __grid_c
         kb = kd;                                                                            \
         ++y;                                                                                \
     }
-        for (int64_t y = y0; y < y1;) {
+        for (int y = y0; y < y1;) {
             ECC_2D_STEP(q0)
             ECC_2D_STEP(q1)
             ECC_2D_STEP(q2)
@@ -305,46 +326,62 @@ constexpr int kKeyPlane = kKeyRowsHalo * kKeyPitch;  // halves per plane buffer
 // Tile column c (-1 .. 128) sits at half index 4 + c of a shared row, so a lane's own four keys
 // form one 8-byte-aligned word pair.
 
-// Keys of plane z of the tile plus halo into `dst` (uint16 patterns; absent outside the grid).
+// The raw values one thread needs for one plane of the tile: its warp's row around its columns
+// (with the two halo columns on lanes 0 / 31) and one value of the two halo rows (thread t: row
+// y0 - 1 or y0 + 8 by t >> 7, column x0 + (t & 127)); threads 0..3 also take the halo corners.
 template <typename T>
-__device__ __forceinline__ void plane_keys(const T *__restrict__ img, int64_t D, int64_t Hy,
-                                           int64_t W, int64_t z, int64_t x0, int64_t y0,
-                                           bool vec_ok, const KeyConsts &K,
-                                           const float *__restrict__ table, uint16_t *dst)
+struct PlaneRaw {
+    RawRow<T> own;
+    T hrow, corner;
+    bool hrow_in, corner_in;
+};
+
+template <typename T>
+__device__ __forceinline__ PlaneRaw<T> load_plane(const T *__restrict__ img, int64_t D, int Hy,
+                                                  int W, int64_t z, int x0, int y0, bool vec_ok,
+                                                  int warp, int lane)
 {
-    const int lane = threadIdx.x & (kWarp - 1);
-    const int warp = threadIdx.x >> 5;
+    PlaneRaw<T> p;
     const bool zin = (z >= 0 && z < D);  // block-uniform
-    const T *__restrict__ plane = img + (zin ? z : 0) * Hy * W;
+    const T *__restrict__ plane = img + (zin ? z : 0) * (int64_t)Hy * W;
     const bool vec = vec_ok && (x0 + 128 <= W);
-    // each warp: its own row (buffer rows 1 .. 8) with the two halo columns
-    {
-        const int64_t y = y0 + warp;
-        uint32_t own0 = kAbsentPair, own1 = kAbsentPair, hk = kAbsentHalf;
-        if (zin) {
-            const RawRow<T> r = load_raw(plane, Hy, W, y, x0, lane, vec);
-            if (r.present) raw_keys(r, K, table, lane, x0, W, own0, own1, hk);
-        }
-        uint16_t *row = dst + (1 + warp) * kKeyPitch;
-        *reinterpret_cast<uint2 *>(row + 4 + 4 * lane) = make_uint2(own0, own1);
-        if (lane == 0) row[3] = (uint16_t)hk;
-        if (lane == kWarp - 1) row[4 + 128] = (uint16_t)hk;
+    if (zin) {
+        p.own = load_raw(plane, Hy, W, y0 + warp, x0, lane, vec);
+    } else {
+        p.own.present = false;
+        p.own.halo_in = false;
+        p.own.valid = 0;
     }
-    // halo rows y0 - 1 (buffer row 0) and y0 + 8 (buffer row 9): 2 x 130 keys
-    for (int i = threadIdx.x; i < 2 * 130; i += kHardThreads) {
-        const int hr = i / 130;
-        const int c = i % 130 - 1;  // tile column -1 .. 128
-        const int64_t y = (hr == 0) ? y0 - 1 : y0 + kTileRows;
-        const int64_t x = x0 + c;
-        uint32_t key = kAbsentHalf;
-        if (zin && y >= 0 && y < Hy && x >= 0 && x < W) {
-            if constexpr (sizeof(T) == 1) {
-                key = reinterpret_cast<const uint16_t *>(table)[(uint32_t)plane[y * W + x]];
-            } else {
-                key = key_one((float)plane[y * W + x], K, table);
-            }
-        }
-        dst[(hr == 0 ? 0 : kKeyRowsHalo - 1) * kKeyPitch + 4 + c] = (uint16_t)key;
+    const int t = threadIdx.x;
+    const int hy = (t >> 7) ? y0 + kTileRows : y0 - 1;
+    const int hx = x0 + (t & 127);
+    p.hrow_in = zin && hy >= 0 && hy < Hy && hx < W;
+    p.hrow = p.hrow_in ? plane[(int64_t)hy * W + hx] : (T)0;
+    const int cy = (t & 2) ? y0 + kTileRows : y0 - 1;
+    const int cx = (t & 1) ? x0 + 128 : x0 - 1;
+    p.corner_in = zin && t < 4 && cy >= 0 && cy < Hy && cx >= 0 && cx < W;
+    p.corner = p.corner_in ? plane[(int64_t)cy * W + cx] : (T)0;
+    return p;
+}
+
+// Keys of a loaded plane into the shared buffer `dst` (uint16 patterns; absent outside the grid).
+template <bool SEARCH, typename T>
+__device__ __forceinline__ void store_plane_keys(const PlaneRaw<T> &p, const KeyConsts &K,
+                                                 const float *__restrict__ table, int warp,
+                                                 int lane, uint16_t *dst)
+{
+    uint32_t own0 = kAbsentPair, own1 = kAbsentPair, hk = kAbsentHalf;
+    if (p.own.present) raw_keys<SEARCH>(p.own, K, table, own0, own1, hk);  // warp-uniform branch
+    uint16_t *row = dst + (1 + warp) * kKeyPitch;
+    *reinterpret_cast<uint2 *>(row + 4 + 4 * lane) = make_uint2(own0, own1);
+    if (lane == 0) row[3] = (uint16_t)hk;
+    if (lane == kWarp - 1) row[4 + 128] = (uint16_t)hk;
+    const int t = threadIdx.x;
+    const uint32_t hkey = p.hrow_in ? key_one<SEARCH>(p.hrow, K, table) : kAbsentHalf;
+    dst[((t >> 7) ? kKeyRowsHalo - 1 : 0) * kKeyPitch + 4 + (t & 127)] = (uint16_t)hkey;
+    if (t < 4) {
+        const uint32_t ck = p.corner_in ? key_one<SEARCH>(p.corner, K, table) : kAbsentHalf;
+        dst[((t & 2) ? kKeyRowsHalo - 1 : 0) * kKeyPitch + ((t & 1) ? 4 + 128 : 3)] = (uint16_t)ck;
     }
 }
 
@@ -364,8 +401,8 @@ __device__ __forceinline__ KeyRow smem_key_row(const uint16_t *buf, int r, int l
     return k;
 }
 
-template <typename T, int CAP>
-__global__ void __launch_bounds__(kHardThreads) ecc_hard3d_kernel(const __grid_constant__
+template <typename T, int CAP, bool SEARCH>
+__global__ void __launch_bounds__(kHardThreads, ECC_3D_MIN_BLOCKS) ecc_hard3d_kernel(const __grid_constant__
                                                                   HardParams<CAP> P)
 {
     extern __shared__ int smem[];
@@ -383,27 +420,33 @@ __global__ void __launch_bounds__(kHardThreads) ecc_hard3d_kernel(const __grid_c
     const int64_t t_end = Tn * (blockIdx.x + 1) / P.ctas_per_image;
     const KeyConsts K = key_consts(P);
     const bool vec_ok = P.vec_ok != 0;
-    const int64_t D = P.D, Hy = P.Hy, W = P.W;
+    const int64_t D = P.D;
+    const int Hy = (int)P.Hy, W = (int)P.W;
     const uint32_t limit = (kKeyBase + (uint32_t)P.H) * 0x10001u;
     const uint32_t kPlain = 0u;  // bias of the M stencil: plain c values
 
     for (int64_t t = t_begin; t < t_end; ++t) {
-        const int64_t tx = t % P.tasks_x;
+        const int tx = (int)(t % P.tasks_x);
         const int64_t rest = t / P.tasks_x;
-        const int64_t ty = rest % P.tasks_y;
+        const int ty = (int)(rest % P.tasks_y);
         const int64_t tz = rest / P.tasks_y;
-        const int64_t x0 = tx * 128;
-        const int64_t y0 = ty * kTileRows;
+        const int x0 = tx * 128;
+        const int y0 = ty * kTileRows;
         const int64_t z0 = tz * P.rows_per_task;
         const int64_t z1 = min(z0 + (int64_t)P.rows_per_task, D);
         const bool row_in = (y0 + warp) < Hy;  // warp-uniform
 
-        // prologue: planes z0 - 1 (buffer 0) and z0 (buffer 1)
+        // prologue: keys of planes z0 - 1 (buffer 0) and z0 (buffer 1); raw plane z0 + 1 in flight
         __syncthreads();  // the previous task's readers are done with both buffers
-        plane_keys<T>(img, D, Hy, W, z0 - 1, x0, y0, vec_ok, K, table, keybuf[0]);
-        plane_keys<T>(img, D, Hy, W, z0, x0, y0, vec_ok, K, table, keybuf[1]);
+        {
+            const PlaneRaw<T> pm = load_plane<T>(img, D, Hy, W, z0 - 1, x0, y0, vec_ok, warp, lane);
+            const PlaneRaw<T> p0 = load_plane<T>(img, D, Hy, W, z0, x0, y0, vec_ok, warp, lane);
+            store_plane_keys<SEARCH>(pm, K, table, warp, lane, keybuf[0]);
+            store_plane_keys<SEARCH>(p0, K, table, warp, lane, keybuf[1]);
+        }
+        PlaneRaw<T> pnext = load_plane<T>(img, D, Hy, W, z0 + 1, x0, y0, vec_ok, warp, lane);
         __syncthreads();
-        uint32_t cm0, cm1;  // c2(M_{z-1}) at the lane's pixels (plain values)
+        uint32_t cm0, cm1;        // c2(M_{z-1}) at the lane's pixels (plain values)
         uint32_t below0, below1;  // keys of plane z - 1 at the lane's pixels
         KeyRow ca = smem_key_row(keybuf[1], warp, lane);
         KeyRow cb = smem_key_row(keybuf[1], warp + 1, lane);
@@ -422,8 +465,11 @@ __global__ void __launch_bounds__(kHardThreads) ecc_hard3d_kernel(const __grid_c
 
         for (int64_t z = z0; z < z1; ++z) {
             uint16_t *nbuf = keybuf[(z - z0) & 1];  // plane z + 1 replaces plane z - 1
-            __syncthreads();
-            plane_keys<T>(img, D, Hy, W, z + 1, x0, y0, vec_ok, K, table, nbuf);
+            // One barrier per plane: the buffer written here was last read in the step before
+            // the previous one, and every warp has passed the previous step's barrier since.
+            if (z == z0) __syncthreads();  // the prologue read buffer 0
+            store_plane_keys<SEARCH>(pnext, K, table, warp, lane, nbuf);
+            if (z + 2 <= z1) pnext = load_plane<T>(img, D, Hy, W, z + 2, x0, y0, vec_ok, warp, lane);
             __syncthreads();
             const KeyRow na = smem_key_row(nbuf, warp, lane);
             const KeyRow nb = smem_key_row(nbuf, warp + 1, lane);
@@ -511,7 +557,7 @@ static int num_sms()
     return n;
 }
 
-template <typename T, int CAP>
+template <typename T, int CAP, bool SEARCH>
 static cudaError_t launch_hard(const HardPlan &pl, cudaStream_t s)
 {
     HardParams<CAP> P;
@@ -534,13 +580,13 @@ static cudaError_t launch_hard(const HardPlan &pl, cudaStream_t s)
 
     const int sms = num_sms();
     const int64_t strips = (pl.W + 127) / 128;
-    const int per_sm = pl.ndim == 2 ? 4 : 3;
+    const int per_sm = pl.ndim == 2 ? ECC_2D_MIN_BLOCKS : ECC_3D_MIN_BLOCKS;
     const int64_t resident = (int64_t)sms * per_sm;
     if (pl.ndim == 2) {
-        // rows per warp task: aim at ~16 K warp tasks in total, at least 8 rows each
-        int64_t want = (pl.Hy * strips * pl.batch + 16383) / 16384;
-        int64_t R = ((want + 7) / 8) * 8;
-        R = R < 8 ? 8 : (R > 256 ? 256 : R);
+        // rows per warp task: 8, or more for very large batches (at most ~64 K tasks per warp
+        // slot keeps the task loop short); small tasks keep the warps of a block balanced
+        int64_t R = 8;
+        while (R < 256 && pl.Hy * strips * pl.batch / R > resident * kHardWarps * 64) R *= 2;
         P.rows_per_task = (int)R;
         P.tasks_x = (int)strips;
         P.tasks_y = (int)((pl.Hy + R - 1) / R);
@@ -567,9 +613,9 @@ static cudaError_t launch_hard(const HardPlan &pl, cudaStream_t s)
     const size_t smem = (size_t)pl.H * sizeof(int) + (size_t)(CAP + 2) * sizeof(float);
     dim3 grid((unsigned)per_image_ctas, (unsigned)pl.batch);
     if (pl.ndim == 2) {
-        ecc_hard2d_kernel<T, CAP><<<grid, kHardThreads, smem, s>>>(P);
+        ecc_hard2d_kernel<T, CAP, SEARCH><<<grid, kHardThreads, smem, s>>>(P);
     } else {
-        ecc_hard3d_kernel<T, CAP><<<grid, kHardThreads, smem, s>>>(P);
+        ecc_hard3d_kernel<T, CAP, SEARCH><<<grid, kHardThreads, smem, s>>>(P);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -580,13 +626,14 @@ static cudaError_t launch_hard(const HardPlan &pl, cudaStream_t s)
 cudaError_t hard_run(const HardPlan &pl, cudaStream_t s)
 {
     if (pl.dtype == ECC_U8) {
-        if (pl.H <= 256) return launch_hard<uint8_t, 256>(pl, s);
-        if (pl.H <= 1024) return launch_hard<uint8_t, 1024>(pl, s);
-        return launch_hard<uint8_t, ECC_MAX_NBINS>(pl, s);
+        if (pl.H <= 256) return launch_hard<uint8_t, 256, false>(pl, s);
+        if (pl.H <= 1024) return launch_hard<uint8_t, 1024, false>(pl, s);
+        return launch_hard<uint8_t, ECC_MAX_NBINS, false>(pl, s);
     }
-    if (pl.H <= 256) return launch_hard<float, 256>(pl, s);
-    if (pl.H <= 1024) return launch_hard<float, 1024>(pl, s);
-    return launch_hard<float, ECC_MAX_NBINS>(pl, s);
+    if (pl.key_mode == kKeySearch) return launch_hard<float, ECC_MAX_NBINS, true>(pl, s);
+    if (pl.H <= 256) return launch_hard<float, 256, false>(pl, s);
+    if (pl.H <= 1024) return launch_hard<float, 1024, false>(pl, s);
+    return launch_hard<float, ECC_MAX_NBINS, false>(pl, s);
 }
 
 }  // namespace ecc

@@ -156,15 +156,21 @@ __device__ __forceinline__ KeyRow max_rows(const KeyRow &a, const KeyRow &b)
 }
 
 // The value bias + c for two pixels at once (c in [-3, 1]; fp16 sums of small integers are
-// exact). With bias 1032 the result's pattern is 0x6408 + c; with bias 0 it is the plain value.
-// p: the pixels' keys; L, R: their left and right
-// neighbours; a*, d*: the rows above and below, same alignment. Sp = [p < above] (1.0 / 0.0),
-// i.e. "the pixel above is NOT earlier", reused from the previous row when marching down.
+// exact). p: the pixels' keys; L, R: their left and right neighbours; a*, d*: the rows above and
+// below, same alignment. Sp = [p < above] (1.0 / 0.0), i.e. "the pixel above is NOT earlier",
+// reused from the previous row when marching down.
 //   earlier flags:  W = L <= p, E = R < p, N = 1 - Sp, S = d < p, NW = aL <= p, NE = aR <= p,
 //                   SW = dL < p, SE = dR < p
-//   c = 1 - W - E - N - S + N W NW + N E NE + S W SW + S E SE
-// The squares are formed by bitwise AND of 1.0 patterns (0x3C00): ~Sp has all other bits set,
-// so at least one positive operand keeps each product a clean 0 or 1.0.
+//   c = 1 - (W + E + N + S) + N W NW + N E NE + S W SW + S E SE
+// Attaching each square to the edge that precedes it around p (N -> E -> S -> W) gives
+//   c = 1 - N ~(E NE) - E ~(S SE) - S ~(W SW) - W ~(N NW)
+//     = (Sp | E NE) - E ~(S SE) - S ~(W SW) - W (Sp | ~NW),
+// four 3-input logic operations on 1.0 patterns (0x3C00): each has a plain (non-negated) flag
+// as an AND operand or is an OR of plain flags, so its result is exactly 0 or 1.0.
+__device__ __forceinline__ uint32_t lop_or_and(uint32_t a, uint32_t b, uint32_t c)
+{
+    return a | (b & c);
+}
 __device__ __forceinline__ uint32_t c2_pair(uint32_t p, uint32_t L, uint32_t R, uint32_t aL,
                                             uint32_t aR, uint32_t d, uint32_t dL, uint32_t dR,
                                             uint32_t Sp, uint32_t bias, uint32_t &S_out)
@@ -173,17 +179,12 @@ __device__ __forceinline__ uint32_t c2_pair(uint32_t p, uint32_t L, uint32_t R, 
     const uint32_t S = h2_lt(d, p);
     const uint32_t NW = h2_le(aL, p), NE = h2_le(aR, p);
     const uint32_t SW = h2_lt(dL, p), SE = h2_lt(dR, p);
-    const uint32_t sqNW = ~Sp & W & NW;
-    const uint32_t sqNE = ~Sp & E & NE;
-    const uint32_t sqSW = S & W & SW;
-    const uint32_t sqSE = S & E & SE;
+    const uint32_t A = lop_or_and(Sp, E, NE);
+    const uint32_t B = E & ~(S & SE);
+    const uint32_t C = S & ~(W & SW);
+    const uint32_t D = W & (Sp | ~NW);
     S_out = S;
-    // bias + c = (bias + Sp) - W - E - S + squares   (since 1 - N = Sp)
-    uint32_t acc = h2_add(bias, Sp);
-    acc = h2_sub(acc, h2_add(W, E));
-    acc = h2_sub(acc, S);
-    acc = h2_add(acc, h2_add(h2_add(sqNW, sqNE), h2_add(sqSW, sqSE)));
-    return acc;
+    return h2_sub(h2_sub(h2_add(bias, A), B), h2_add(C, D));
 }
 
 // Local Euler contributions of the lane's four pixels of row b (rows a above, d below).
@@ -222,16 +223,28 @@ __device__ __forceinline__ uint32_t h2_le_mask(uint32_t a, uint32_t b)
     return d;
 }
 
-constexpr uint32_t kBias = 0x64086408u;  // (1032, 1032): contributions carried as 1032 + c
-constexpr int kBiasBits = 0x6408;         // pattern of 1032; pattern - kBiasBits = c for |c| <= 8
+constexpr uint32_t kBias = 0x65006500u;  // (1280, 1280): contributions carried as 1280 + c
+// The pattern of 1280 + c is 0x6500 + c for |c| <= 8, so its low byte is c as a signed byte.
+
+__device__ __forceinline__ int sext_byte0(uint32_t x)
+{
+    uint32_t d;
+    asm("prmt.b32 %0, %1, 0, 0x8880;" : "=r"(d) : "r"(x));
+    return (int)d;
+}
+__device__ __forceinline__ int sext_byte2(uint32_t x)
+{
+    uint32_t d;
+    asm("prmt.b32 %0, %1, 0, 0xAAA2;" : "=r"(d) : "r"(x));
+    return (int)d;
+}
 
 // Adds the contributions of one pair to the block histogram: pixel keys `keys` (fp16 patterns),
-// values `cv` = 1032 + c (patterns 0x6408 + c). Pixels with c = 0, with key >= H ("never") or
-// outside the grid (key pattern +inf) add nothing.
+// values `cv` = 1280 + c. Pixels with c = 0, with key >= H ("never") or outside the grid (key
+// pattern +inf) add nothing.
 __device__ __forceinline__ void hist_pair(uint32_t keys, uint32_t cv, uint32_t key_limit_pair,
                                           int *hist)
 {
-    // lanes where c != 0 and key < H
     uint32_t live;
     asm("{\n\t.reg .b32 m1, m2;\n\t"
         "set.ne.u32.f16x2 m1, %1, %2;\n\t"
@@ -239,10 +252,11 @@ __device__ __forceinline__ void hist_pair(uint32_t keys, uint32_t cv, uint32_t k
         "and.b32 %0, m1, m2;\n\t}"
         : "=r"(live)
         : "r"(cv), "r"(kBias), "r"(keys), "r"(key_limit_pair));
-    if (live & 0xffffu)
-        atomicAdd(hist + ((int)(keys & 0xffffu) - (int)kKeyBase), (int)(cv & 0xffffu) - kBiasBits);
-    if (live >> 16)
-        atomicAdd(hist + ((int)(keys >> 16) - (int)kKeyBase), (int)(cv >> 16) - kBiasBits);
+    int *const a0 = hist + ((int)(keys & 0xffffu) - (int)kKeyBase);
+    int *const a1 = hist + ((int)(keys >> 16) - (int)kKeyBase);
+    const int v0 = sext_byte0(cv), v1 = sext_byte2(cv);
+    if (live & 0xffffu) atomicAdd(a0, v0);
+    if (live & 0xffff0000u) atomicAdd(a1, v1);
 }
 
 }  // namespace ecc

@@ -1,4 +1,5 @@
-// ecc_soft.cu -- sigmoid-relaxed ("soft") ECC of 2-D images with analytic gradients (sm_103a).
+// ecc_soft.cu -- sigmoid-relaxed ("soft") ECC of 2-D images and 3-D volumes with analytic
+// gradients (sm_103a).
 //
 // Paper notes "Scalable GPU-Accelerated Euler Characteristic Curves: Optimization and
 // Differentiable Learning for PyTorch", "Key designs -- differentiable ECC layer (sigmoid
@@ -12,7 +13,9 @@
 //     s_pk = sigma(lambda (tau_k - X_p)).
 // Only voxels with c_X(p) != 0 contribute, so a prep kernel computes X and c_X once per call and
 // compacts the contributing voxels ("critical list"); the forward and backward kernels then read
-// each voxel once for all K thresholds (threads own thresholds, the list is broadcast).
+// each voxel once for all K thresholds (threads own thresholds, the list is broadcast). In 2-D,
+// c_X reads the 8 neighbours; in 3-D the 26 neighbours, with c_X = sum over the 27 cells that
+// contain p and whose other vertices are all earlier of (-1)^dim (range [-5, 7]).
 //
 // Numerics (fp32 arithmetic unless noted):
 //  * X is carried as an unevaluated sum hi + lo of two floats (alpha f and u x by exact products,
@@ -39,9 +42,17 @@ namespace ecc {
 // Workspace layout
 // ---------------------------------------------------------------------------------------------
 
-constexpr int kTileX = 64;
-constexpr int kTileY = 32;
-constexpr int kTileCap = kTileX * kTileY;  // entries per tile: every pixel may contribute
+// Tiles: 64 x 32 pixels (2-D), 32 x 8 x 8 voxels (3-D); both 2048 = kTileCap cells.
+template <int NDIM> struct SoftTile;
+template <> struct SoftTile<2> {
+    static constexpr int X = 64, Y = 32, Z = 1;
+};
+template <> struct SoftTile<3> {
+    static constexpr int X = 32, Y = 8, Z = 8;
+};
+constexpr int kTileCap = 2048;  // entries per tile: every voxel may contribute
+static_assert(SoftTile<2>::X * SoftTile<2>::Y == kTileCap, "2-D tile size");
+static_assert(SoftTile<3>::X * SoftTile<3>::Y * SoftTile<3>::Z == kTileCap, "3-D tile size");
 constexpr int kPrepThreads = 256;
 constexpr int kSoftThreads = 64;           // each thread owns two thresholds per pass
 constexpr int kKPerPass = 2 * kSoftThreads;
@@ -49,26 +60,37 @@ constexpr int kChunk = 256;                // entries staged in shared memory at
 constexpr int kGroup = 8;                  // entries per backward transpose-reduce
 constexpr int kTileFlagDirect = 1 << 30;   // count flag: an exponent of this tile is out of range
 constexpr float kExpLimit = 100.0f;
+constexpr int kScal = 4;                   // backward scalar partials per tile: alpha, u_0..u_2
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 bool soft_layout(int ndim, const int64_t *dims, int64_t batch, int K, SoftLayout &L)
 {
-    if (ndim != 2 || !dims || batch < 1 || K < 1 || K > ECC_MAX_K) return false;
-    if (dims[0] < 1 || dims[1] < 1) return false;
-    L.Hy = dims[0];
-    L.W = dims[1];
+    if ((ndim != 2 && ndim != 3) || !dims || batch < 1 || K < 1 || K > ECC_MAX_K) return false;
+    for (int d = 0; d < ndim; ++d)
+        if (dims[d] < 1 || dims[d] > ((int64_t)1 << 31)) return false;
+    if (batch > 65535) return false;  // images run along gridDim.y
+    L.ndim = ndim;
+    L.D = ndim == 3 ? dims[0] : 1;
+    L.Hy = dims[ndim - 2];
+    L.W = dims[ndim - 1];
     L.batch = batch;
     L.K = K;
-    if (L.Hy * L.W >= ((int64_t)1 << 28)) return false;  // entry indices use 28 bits
-    L.tiles_x = (L.W + kTileX - 1) / kTileX;
-    L.tiles_y = (L.Hy + kTileY - 1) / kTileY;
-    L.tiles = L.tiles_x * L.tiles_y;
+    if (L.D * L.Hy > ((int64_t)1 << 40) / L.W) return false;
+    const int tx = ndim == 3 ? SoftTile<3>::X : SoftTile<2>::X;
+    const int ty = ndim == 3 ? SoftTile<3>::Y : SoftTile<2>::Y;
+    const int tz = ndim == 3 ? SoftTile<3>::Z : SoftTile<2>::Z;
+    L.tiles_x = (L.W + tx - 1) / tx;
+    L.tiles_y = (L.Hy + ty - 1) / ty;
+    L.tiles_z = (L.D + tz - 1) / tz;
+    L.tiles = L.tiles_x * L.tiles_y * L.tiles_z;
+    if (L.tiles >= ((int64_t)1 << 31)) return false;  // tiles run along gridDim.x
     const int64_t units = batch * L.tiles;
     if (units > ((int64_t)1 << 40) / kTileCap) return false;
+    const int64_t ncoord = (ndim == 3 ? L.D : 0) + L.Hy + L.W;
     size_t off = 0;
     L.off_coords = off;
-    off = align256(off + sizeof(float2) * (size_t)(L.Hy + L.W));
+    off = align256(off + sizeof(float2) * (size_t)ncoord);
     L.off_counts = off;
     off = align256(off + sizeof(int) * (size_t)units);
     L.off_entries = off;
@@ -76,10 +98,17 @@ bool soft_layout(int ndim, const int64_t *dims, int64_t batch, int K, SoftLayout
     L.off_part = off;
     off = align256(off + sizeof(double) * (size_t)units * (size_t)K);
     L.off_scal = off;
-    off = align256(off + sizeof(double) * (size_t)units * 3);
+    off = align256(off + sizeof(double) * (size_t)units * kScal);
     L.total = off;
     return true;
 }
+
+// Geometry handed to the kernels. Coordinate tables: axis 0 first (the z axis of a volume, the
+// row axis of an image), then the following axes; nz = D for volumes and 0 for images.
+struct SoftGeom {
+    int64_t D, Hy, W, nz;
+    int64_t tiles_x, tiles_y, tiles;
+};
 
 // ---------------------------------------------------------------------------------------------
 // Error-free float transformations (Knuth two-sum, FMA two-product)
@@ -114,6 +143,28 @@ __device__ __forceinline__ float2 filtration_df(float alpha, float f, float u0, 
     const float lo = __fadd_rn(__fadd_rn(t1, t2), __fadd_rn(e1, __fadd_rn(e2, e3)));
     const float hi = __fadd_rn(s2, lo);
     return make_float2(hi, __fsub_rn(lo, __fsub_rn(hi, s2)));
+}
+
+// X = alpha f + u0 x0 + u1 x1 + u2 x2 as a normalised (hi, lo) pair.
+__device__ __forceinline__ float2 filtration_df3(float alpha, float f, float u0, float2 x0, float u1,
+                                                 float2 x1, float u2, float2 x2)
+{
+    float p1, e1, p2, e2, p3, e3, p4, e4;
+    two_prod(alpha, f, p1, e1);
+    two_prod(u0, x0.x, p2, e2);
+    two_prod(u1, x1.x, p3, e3);
+    two_prod(u2, x2.x, p4, e4);
+    e2 = fmaf(u0, x0.y, e2);
+    e3 = fmaf(u1, x1.y, e3);
+    e4 = fmaf(u2, x2.y, e4);
+    float s1, t1, s2, t2, s3, t3;
+    two_sum(p1, p2, s1, t1);
+    two_sum(s1, p3, s2, t2);
+    two_sum(s2, p4, s3, t3);
+    const float lo = __fadd_rn(__fadd_rn(__fadd_rn(t1, t2), t3),
+                               __fadd_rn(e1, __fadd_rn(__fadd_rn(e2, e3), e4)));
+    const float hi = __fadd_rn(s3, lo);
+    return make_float2(hi, __fsub_rn(lo, __fsub_rn(hi, s3)));
 }
 
 // q is earlier than p under (X, linear index): X_q < X_p, or equal with q's index smaller.
@@ -183,81 +234,158 @@ __device__ float tau_midpoint(const float *__restrict__ tau, int K)
     return 0.5f * lo + 0.5f * hi;
 }
 
-// Entry: {E_p, X_hi, X_lo, (index << 3) | (c + 4)}.
-__device__ __forceinline__ int entry_c(const float4 &en) { return (__float_as_int(en.w) & 7) - 4; }
-__device__ __forceinline__ int entry_idx(const float4 &en) { return __float_as_int(en.w) >> 3; }
+// Entry: {E_p, X_hi, X_lo, (index in the tile << 4) | (c + 8)}, c in [-8, 7].
+constexpr int kPadWord = 8;  // c = 0 at index 0: a padding entry that contributes nothing
+__device__ __forceinline__ int entry_c(const float4 &en) { return (__float_as_int(en.w) & 15) - 8; }
+__device__ __forceinline__ int entry_loc(const float4 &en) { return __float_as_int(en.w) >> 4; }
+
+// The cells of the 3-D V-construction that contain a voxel p: one direction per axis in
+// {-1, 0, +1} (0 = the cell does not extend along that axis), 27 in all, of dimension = the
+// number of non-zero directions. A neighbourhood bit o = (dz + 1) 9 + (dy + 1) 3 + (dx + 1)
+// stands for the voxel at offset (dz, dy, dx); mask[s] holds the bits of the vertices of cell s.
+struct CellTable3 {
+    uint32_t mask[27];
+    int sign[27];
+};
+__host__ __device__ constexpr CellTable3 make_cell_table3()
+{
+    CellTable3 t{};
+    for (int s = 0; s < 27; ++s) {
+        const int sz = s / 9 - 1, sy = (s / 3) % 3 - 1, sx = s % 3 - 1;
+        uint32_t m = 0;
+        for (int a = 0; a <= (sz != 0); ++a)
+            for (int b = 0; b <= (sy != 0); ++b)
+                for (int c = 0; c <= (sx != 0); ++c)
+                    m |= 1u << ((a * sz + 1) * 9 + (b * sy + 1) * 3 + (c * sx + 1));
+        t.mask[s] = m;
+        const int dim = (sz != 0) + (sy != 0) + (sx != 0);
+        t.sign[s] = (dim & 1) ? -1 : 1;
+    }
+    return t;
+}
 
 // ---------------------------------------------------------------------------------------------
 // Kernels
 // ---------------------------------------------------------------------------------------------
 
-// Coordinates x_d(i) = (2 i - (n - 1)) / (n - 1) in fp64, stored as (hi, lo) float pairs:
-// axis 0 (rows) first, then axis 1 (columns).
-__global__ void soft_coords_kernel(float2 *coords, int64_t Hy, int64_t W)
+// Coordinates x_d(i) = (2 i - (n - 1)) / (n - 1) in fp64, stored as (hi, lo) float pairs, one
+// table per axis, axis 0 first: [nz z-coordinates][Hy row coordinates][W column coordinates].
+__global__ void soft_coords_kernel(float2 *coords, int64_t nz, int64_t Hy, int64_t W)
 {
     const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-    if (i >= Hy + W) return;
-    const int64_t n = (i < Hy) ? Hy : W;
-    const int64_t j = (i < Hy) ? i : i - Hy;
+    if (i >= nz + Hy + W) return;
+    int64_t n, j;
+    if (i < nz) {
+        n = nz;
+        j = i;
+    } else if (i < nz + Hy) {
+        n = Hy;
+        j = i - nz;
+    } else {
+        n = W;
+        j = i - nz - Hy;
+    }
     double x = 0.0;
     if (n > 1) x = (2.0 * (double)j - (double)(n - 1)) / (double)(n - 1);
     const float hi = (float)x;
     coords[i] = make_float2(hi, (float)(x - (double)hi));
 }
 
-// One block per (tile, image). Computes X on the tile plus a one-pixel halo, c_X per pixel, and
-// writes the contributing pixels of the tile, in pixel order, to the tile's slot of the list.
+// Local Euler contribution c_X(p) of a 2-D pixel from its 3 x 3 neighbourhood in X (row pitch HX,
+// `c` points at p). Earlier = `<=` for the neighbours with a smaller linear index, `<` otherwise.
+template <int HX>
+__device__ __forceinline__ int local_c2(const float2 *c)
+{
+    const float2 p = c[0];
+    const bool N = df_le(c[-HX], p), Wf = df_le(c[-1], p), S = df_lt(c[HX], p), E = df_lt(c[1], p);
+    const bool NW = df_le(c[-HX - 1], p), NE = df_le(c[-HX + 1], p);
+    const bool SW = df_lt(c[HX - 1], p), SE = df_lt(c[HX + 1], p);
+    return 1 - (int)N - (int)Wf - (int)S - (int)E + (int)(N && Wf && NW) + (int)(N && E && NE) +
+           (int)(S && Wf && SW) + (int)(S && E && SE);
+}
+
+// Local Euler contribution of a 3-D voxel from its 3 x 3 x 3 neighbourhood (row pitch HX, plane
+// pitch HP). Bits 0..12 of the neighbourhood are the offsets before p in row-major order (smaller
+// linear index, earlier when `<=`), bits 14..26 those after it (earlier when `<`).
+template <int HX, int HP>
+__device__ __forceinline__ int local_c3(const float2 *c)
+{
+    constexpr CellTable3 T = make_cell_table3();
+    const float2 p = c[0];
+    uint32_t earlier = 1u << 13;
+#pragma unroll
+    for (int o = 0; o < 27; ++o) {
+        if (o == 13) continue;
+        const int off = (o / 9 - 1) * HP + ((o / 3) % 3 - 1) * HX + (o % 3 - 1);
+        const float2 q = c[off];
+        const bool e = (o < 13) ? df_le(q, p) : df_lt(q, p);
+        earlier |= (uint32_t)e << o;
+    }
+    int v = 0;
+#pragma unroll
+    for (int s = 0; s < 27; ++s) v += ((earlier & T.mask[s]) == T.mask[s]) ? T.sign[s] : 0;
+    return v;
+}
+
+// One block per (tile, image). Computes X on the tile plus a one-voxel halo, c_X per voxel, and
+// writes the contributing voxels of the tile, in the tile's own raster order, to the tile's slot
+// of the list.
+template <int NDIM>
 __global__ void __launch_bounds__(kPrepThreads) soft_prep_kernel(
     const float *__restrict__ img, const float *__restrict__ alpha_p, const float *__restrict__ u_p,
     const float *__restrict__ tau, int K, float l2, const float2 *__restrict__ coords,
-    int *__restrict__ counts, float4 *__restrict__ entries, int64_t Hy, int64_t W,
-    int64_t tiles_x, int64_t tiles)
+    int *__restrict__ counts, float4 *__restrict__ entries, SoftGeom g)
 {
-    constexpr int HX = kTileX + 2, HY = kTileY + 2;
-    __shared__ float2 X[HY][HX];
+    using T = SoftTile<NDIM>;
+    constexpr int HX = T::X + 2, HY = T::Y + 2, HZ = NDIM == 3 ? T::Z + 2 : 1;
+    constexpr int HP = HX * HY;
+    constexpr int ZO = NDIM == 3 ? 1 : 0;  // halo offset along z
+    __shared__ float2 X[HZ * HP];
     __shared__ int warp_tot[kPrepThreads / kWarp];
     __shared__ int running;
 
     const int64_t b = blockIdx.y;
     const int64_t tile = blockIdx.x;
-    const int64_t x0 = (tile % tiles_x) * kTileX;
-    const int64_t y0 = (tile / tiles_x) * kTileY;
-    const float *__restrict__ f = img + b * Hy * W;
-    const float alpha = __ldg(alpha_p), u0 = __ldg(u_p), u1 = __ldg(u_p + 1);
-    const float2 *__restrict__ cy = coords;
-    const float2 *__restrict__ cx = coords + Hy;
+    const int64_t x0 = (tile % g.tiles_x) * T::X;
+    const int64_t y0 = ((tile / g.tiles_x) % g.tiles_y) * T::Y;
+    const int64_t z0 = (tile / (g.tiles_x * g.tiles_y)) * T::Z;
+    const float *__restrict__ f = img + b * g.D * g.Hy * g.W;
+    const float alpha = __ldg(alpha_p);
+    const float u0 = __ldg(u_p), u1 = __ldg(u_p + 1), u2 = NDIM == 3 ? __ldg(u_p + 2) : 0.0f;
+    const float2 *__restrict__ cz = coords;
+    const float2 *__restrict__ cy = coords + g.nz;
+    const float2 *__restrict__ cx = coords + g.nz + g.Hy;
     const float inf = __int_as_float(0x7f800000);
     const float m = tau_midpoint(tau, K);
 
-    for (int i = threadIdx.x; i < HX * HY; i += kPrepThreads) {
-        const int iy = i / HX, ix = i % HX;
-        const int64_t gy = y0 - 1 + iy, gx = x0 - 1 + ix;
+    for (int i = threadIdx.x; i < HZ * HP; i += kPrepThreads) {
+        const int iz = i / HP, iy = (i / HX) % HY, ix = i % HX;
+        const int64_t gz = z0 - ZO + iz, gy = y0 - 1 + iy, gx = x0 - 1 + ix;
         float2 v = make_float2(inf, 0.0f);  // outside the grid: never earlier
-        if (gy >= 0 && gy < Hy && gx >= 0 && gx < W)
-            v = filtration_df(alpha, __ldg(f + gy * W + gx), u0, __ldg(cy + gy), u1, __ldg(cx + gx));
-        X[iy][ix] = v;
+        if (gz >= 0 && gz < g.D && gy >= 0 && gy < g.Hy && gx >= 0 && gx < g.W) {
+            const float fv = __ldg(f + (gz * g.Hy + gy) * g.W + gx);
+            if (NDIM == 3)
+                v = filtration_df3(alpha, fv, u0, __ldg(cz + gz), u1, __ldg(cy + gy), u2,
+                                   __ldg(cx + gx));
+            else
+                v = filtration_df(alpha, fv, u0, __ldg(cy + gy), u1, __ldg(cx + gx));
+        }
+        X[i] = v;
     }
     if (threadIdx.x == 0) running = 0;
     __syncthreads();
 
     const int lane = threadIdx.x & (kWarp - 1), warp = threadIdx.x >> 5;
-    float4 *__restrict__ out = entries + (b * tiles + tile) * (int64_t)kTileCap;
+    float4 *__restrict__ out = entries + (b * g.tiles + tile) * (int64_t)kTileCap;
     bool direct = false;
     for (int r = 0; r < kTileCap / kPrepThreads; ++r) {
         const int i = r * kPrepThreads + threadIdx.x;
-        const int ly = i / kTileX, lx = i % kTileX;
-        const int64_t gy = y0 + ly, gx = x0 + lx;
+        const int lx = i % T::X, ly = (i / T::X) % T::Y, lz = i / (T::X * T::Y);
+        const float2 *cp = &X[(lz + ZO) * HP + (ly + 1) * HX + lx + 1];
+        const float2 p = cp[0];
         int c = 0;
-        const float2 p = X[ly + 1][lx + 1];
-        if (gy < Hy && gx < W) {
-            const float2 n = X[ly][lx + 1], s = X[ly + 2][lx + 1];
-            const float2 w = X[ly + 1][lx], e = X[ly + 1][lx + 2];
-            const bool N = df_le(n, p), Wf = df_le(w, p), S = df_lt(s, p), E = df_lt(e, p);
-            const bool NW = df_le(X[ly][lx], p), NE = df_le(X[ly][lx + 2], p);
-            const bool SW = df_lt(X[ly + 2][lx], p), SE = df_lt(X[ly + 2][lx + 2], p);
-            c = 1 - (int)N - (int)Wf - (int)S - (int)E + (int)(N && Wf && NW) +
-                (int)(N && E && NE) + (int)(S && Wf && SW) + (int)(S && E && SE);
-        }
+        if (z0 + lz < g.D && y0 + ly < g.Hy && x0 + lx < g.W)
+            c = NDIM == 3 ? local_c3<HX, HP>(cp) : local_c2<HX>(cp);
         const unsigned mask = __ballot_sync(kFull, c != 0);
         if (lane == 0) warp_tot[warp] = __popc(mask);
         __syncthreads();
@@ -269,7 +397,7 @@ __global__ void __launch_bounds__(kPrepThreads) soft_prep_kernel(
             two_sum(p.x, -m, s, e);  // X - m, exactly, as s + (e + lo)
             const float E = pow2_scaled(l2, s, e + p.y, ex);
             direct |= !(fabsf(ex) <= kExpLimit);
-            const int packed = ((int)(gy * W + gx) << 3) | (c + 4);
+            const int packed = (i << 4) | (c + 8);
             out[before] = make_float4(E, p.x, p.y, __int_as_float(packed));
         }
         __syncthreads();
@@ -281,7 +409,7 @@ __global__ void __launch_bounds__(kPrepThreads) soft_prep_kernel(
         __syncthreads();
     }
     direct = __syncthreads_or(direct);
-    if (threadIdx.x == 0) counts[b * tiles + tile] = running | (direct ? kTileFlagDirect : 0);
+    if (threadIdx.x == 0) counts[b * g.tiles + tile] = running | (direct ? kTileFlagDirect : 0);
 }
 
 // Per-thread threshold state: tau_k, F_k (factorised path) and whether its exponent is in range.
@@ -428,22 +556,25 @@ __device__ __forceinline__ void bwd_group(const float4 *en8, const KState &s0, c
 }
 
 // Backward: one block per (tile, image); thread t owns thresholds k = kb + t and kb + t + 64.
+template <int NDIM>
 __global__ void __launch_bounds__(kSoftThreads) soft_bwd_kernel(
     const float *__restrict__ img, const float *__restrict__ tau, int K, float lambda, float l2,
     const float *__restrict__ alpha_p, const float *__restrict__ grad_out,
     const int *__restrict__ counts, const float4 *__restrict__ entries,
     const float2 *__restrict__ coords, double *__restrict__ part, double *__restrict__ scal,
-    float *__restrict__ grad_img, int64_t Hy, int64_t W, int64_t tiles)
+    float *__restrict__ grad_img, SoftGeom g)
 {
+    using T = SoftTile<NDIM>;
     constexpr int NW = kSoftThreads / kWarp;
     __shared__ __align__(16) float4 sh[kChunk];
     __shared__ __align__(16) float qbuf[NW][kGroup][kWarp];
     __shared__ float red[NW][kChunk];
     __shared__ float dxs[kTileCap];
-    __shared__ double scal_red[NW][3];
+    __shared__ double scal_red[NW][kScal];
 
     const int64_t b = blockIdx.y;
-    const int64_t unit = b * tiles + blockIdx.x;
+    const int64_t tile = blockIdx.x;
+    const int64_t unit = b * g.tiles + tile;
     const int cnt = counts[unit];
     const int n = cnt & (kTileFlagDirect - 1);
     const float4 *__restrict__ list = entries + unit * (int64_t)kTileCap;
@@ -463,7 +594,8 @@ __global__ void __launch_bounds__(kSoftThreads) soft_bwd_kernel(
             __syncthreads();
             // stage the chunk; pad the last group with c = 0 entries
             for (int i = threadIdx.x; i < kChunk; i += kSoftThreads)
-                sh[i] = (i < m_ent) ? list[e0 + i] : make_float4(0.f, 0.f, 0.f, __int_as_float(4));
+                sh[i] = (i < m_ent) ? list[e0 + i]
+                                    : make_float4(0.f, 0.f, 0.f, __int_as_float(kPadWord));
             __syncthreads();
             for (int g = 0; g * kGroup < m_ent; ++g) {
                 float rs;
@@ -490,35 +622,48 @@ __global__ void __launch_bounds__(kSoftThreads) soft_bwd_kernel(
 
     // per-voxel gradient: dX = -lambda c sum_k g w; grad_img = alpha dX; dalpha, du partials
     const float alpha = __ldg(alpha_p);
-    const float *__restrict__ f = img + b * Hy * W;
-    float sa = 0.f, ca = 0.f, sy = 0.f, cy = 0.f, sx = 0.f, cx = 0.f;
+    const int64_t image = g.D * g.Hy * g.W;
+    const float *__restrict__ f = img + b * image;
+    const int64_t x0 = (tile % g.tiles_x) * T::X;
+    const int64_t y0 = ((tile / g.tiles_x) % g.tiles_y) * T::Y;
+    const int64_t z0 = (tile / (g.tiles_x * g.tiles_y)) * T::Z;
+    const float2 *__restrict__ cz = coords;
+    const float2 *__restrict__ cy = coords + g.nz;
+    const float2 *__restrict__ cx = coords + g.nz + g.Hy;
+    float sum[kScal] = {0.f, 0.f, 0.f, 0.f}, comp[kScal] = {0.f, 0.f, 0.f, 0.f};
     for (int i = threadIdx.x; i < n; i += kSoftThreads) {
         const float4 en = list[i];
-        const int idx = entry_idx(en);
+        const int loc = entry_loc(en);
+        const int64_t gx = x0 + loc % T::X, gy = y0 + (loc / T::X) % T::Y,
+                      gz = z0 + loc / (T::X * T::Y);
+        const int64_t idx = (gz * g.Hy + gy) * g.W + gx;
         const float dX = -lambda * (float)entry_c(en) * dxs[i];
-        if (grad_img) grad_img[b * Hy * W + idx] = alpha * dX;
-        const int64_t iy = idx / W, ix = idx % W;
-        const float2 xy = __ldg(coords + iy), xx = __ldg(coords + Hy + ix);
-        kahan_add(sa, ca, dX * __ldg(f + idx));
-        kahan_add(sy, cy, dX * (xy.x + xy.y));
-        kahan_add(sx, cx, dX * (xx.x + xx.y));
+        if (grad_img) grad_img[b * image + idx] = alpha * dX;
+        const float2 xy = __ldg(cy + gy), xx = __ldg(cx + gx);
+        kahan_add(sum[0], comp[0], dX * __ldg(f + idx));
+        if (NDIM == 3) {
+            const float2 xz = __ldg(cz + gz);
+            kahan_add(sum[1], comp[1], dX * (xz.x + xz.y));
+        }
+        kahan_add(sum[NDIM - 1], comp[NDIM - 1], dX * (xy.x + xy.y));
+        kahan_add(sum[NDIM], comp[NDIM], dX * (xx.x + xx.y));
     }
-    double v[3] = {(double)sa - (double)ca, (double)sy - (double)cy, (double)sx - (double)cx};
+    double v[kScal];
 #pragma unroll
-    for (int j = 0; j < 3; ++j) {
+    for (int j = 0; j < kScal; ++j) {
+        v[j] = (double)sum[j] - (double)comp[j];
 #pragma unroll
         for (int o = kWarp / 2; o > 0; o >>= 1) v[j] += __shfl_xor_sync(kFull, v[j], o);
     }
     if (lane == 0) {
-        scal_red[warp][0] = v[0];
-        scal_red[warp][1] = v[1];
-        scal_red[warp][2] = v[2];
+#pragma unroll
+        for (int j = 0; j < kScal; ++j) scal_red[warp][j] = v[j];
     }
     __syncthreads();
-    if (threadIdx.x < 3) {
+    if (threadIdx.x < kScal) {
         double acc = 0.0;
         for (int w2 = 0; w2 < NW; ++w2) acc += scal_red[w2][threadIdx.x];
-        scal[unit * 3 + threadIdx.x] = acc;
+        scal[unit * kScal + threadIdx.x] = acc;
     }
 }
 
@@ -537,7 +682,7 @@ __global__ void __launch_bounds__(kReduceThreads) soft_bwd_reduce_kernel(
         for (int64_t u = threadIdx.x; u < units; u += kReduceThreads) acc += part[u * K + o];
     } else {
         const int j = o - K;
-        for (int64_t u = threadIdx.x; u < units; u += kReduceThreads) acc += scal[u * 3 + j];
+        for (int64_t u = threadIdx.x; u < units; u += kReduceThreads) acc += scal[u * kScal + j];
     }
     red[threadIdx.x] = acc;
     __syncthreads();
@@ -565,6 +710,48 @@ static inline float lambda_log2e(float lambda)
     return (float)((double)lambda * 1.4426950408889634);
 }
 
+// stats = {listed voxels, tiles on the direct path, tiles}: one block, fixed-order tree.
+__global__ void __launch_bounds__(kReduceThreads) soft_stats_kernel(const int *__restrict__ counts,
+                                                                    int64_t units,
+                                                                    int64_t *__restrict__ stats)
+{
+    __shared__ long long red[2][kReduceThreads];
+    long long n = 0, direct = 0;
+    for (int64_t i = threadIdx.x; i < units; i += kReduceThreads) {
+        const int c = counts[i];
+        n += c & (kTileFlagDirect - 1);
+        direct += (c & kTileFlagDirect) ? 1 : 0;
+    }
+    red[0][threadIdx.x] = n;
+    red[1][threadIdx.x] = direct;
+    __syncthreads();
+    for (int st = kReduceThreads / 2; st > 0; st >>= 1) {
+        if (threadIdx.x < st) {
+            red[0][threadIdx.x] += red[0][threadIdx.x + st];
+            red[1][threadIdx.x] += red[1][threadIdx.x + st];
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        stats[0] = red[0][0];
+        stats[1] = red[1][0];
+        stats[2] = units;
+    }
+}
+
+static SoftGeom soft_geom(const SoftLayout &L)
+{
+    SoftGeom g;
+    g.D = L.D;
+    g.Hy = L.Hy;
+    g.W = L.W;
+    g.nz = L.ndim == 3 ? L.D : 0;
+    g.tiles_x = L.tiles_x;
+    g.tiles_y = L.tiles_y;
+    g.tiles = L.tiles;
+    return g;
+}
+
 cudaError_t soft_run_fwd(const SoftLayout &L, const float *img, const float *tau, float lambda,
                          const float *alpha, const float *u, float *out, void *ws, cudaStream_t s)
 {
@@ -574,11 +761,16 @@ cudaError_t soft_run_fwd(const SoftLayout &L, const float *img, const float *tau
     float4 *entries = reinterpret_cast<float4 *>(base + L.off_entries);
     double *part = reinterpret_cast<double *>(base + L.off_part);
     const float l2 = lambda_log2e(lambda);
-    const int64_t ncoord = L.Hy + L.W;
-    soft_coords_kernel<<<(unsigned)((ncoord + 255) / 256), 256, 0, s>>>(coords, L.Hy, L.W);
+    const SoftGeom g = soft_geom(L);
+    const int64_t ncoord = g.nz + L.Hy + L.W;
+    soft_coords_kernel<<<(unsigned)((ncoord + 255) / 256), 256, 0, s>>>(coords, g.nz, L.Hy, L.W);
     dim3 grid((unsigned)L.tiles, (unsigned)L.batch);
-    soft_prep_kernel<<<grid, kPrepThreads, 0, s>>>(img, alpha, u, tau, L.K, l2, coords, counts,
-                                                   entries, L.Hy, L.W, L.tiles_x, L.tiles);
+    if (L.ndim == 3)
+        soft_prep_kernel<3><<<grid, kPrepThreads, 0, s>>>(img, alpha, u, tau, L.K, l2, coords,
+                                                          counts, entries, g);
+    else
+        soft_prep_kernel<2><<<grid, kPrepThreads, 0, s>>>(img, alpha, u, tau, L.K, l2, coords,
+                                                          counts, entries, g);
     soft_fwd_kernel<<<grid, kSoftThreads, 0, s>>>(tau, L.K, l2, counts, entries, part, L.tiles);
     const int64_t nout = L.batch * L.K;
     soft_fwd_reduce_kernel<<<(unsigned)((nout + 255) / 256), 256, 0, s>>>(part, out, L.K, L.tiles,
@@ -597,18 +789,32 @@ cudaError_t soft_run_bwd(const SoftLayout &L, const float *img, const float *tau
     const float4 *entries = reinterpret_cast<const float4 *>(base + L.off_entries);
     double *part = reinterpret_cast<double *>(base + L.off_part);
     double *scal = reinterpret_cast<double *>(base + L.off_scal);
+    const SoftGeom g = soft_geom(L);
     if (grad_img) {
-        cudaError_t e =
-            cudaMemsetAsync(grad_img, 0, sizeof(float) * (size_t)(L.batch * L.Hy * L.W), s);
+        cudaError_t e = cudaMemsetAsync(grad_img, 0,
+                                        sizeof(float) * (size_t)(L.batch * L.D * L.Hy * L.W), s);
         if (e != cudaSuccess) return e;
     }
     dim3 grid((unsigned)L.tiles, (unsigned)L.batch);
-    soft_bwd_kernel<<<grid, kSoftThreads, 0, s>>>(img, tau, L.K, lambda, lambda_log2e(lambda),
-                                                  alpha, grad_out, counts, entries, coords, part,
-                                                  scal, grad_img, L.Hy, L.W, L.tiles);
+    const float l2 = lambda_log2e(lambda);
+    if (L.ndim == 3)
+        soft_bwd_kernel<3><<<grid, kSoftThreads, 0, s>>>(img, tau, L.K, lambda, l2, alpha,
+                                                         grad_out, counts, entries, coords, part,
+                                                         scal, grad_img, g);
+    else
+        soft_bwd_kernel<2><<<grid, kSoftThreads, 0, s>>>(img, tau, L.K, lambda, l2, alpha,
+                                                         grad_out, counts, entries, coords, part,
+                                                         scal, grad_img, g);
     const int64_t units = L.batch * L.tiles;
-    soft_bwd_reduce_kernel<<<(unsigned)(L.K + 3), kReduceThreads, 0, s>>>(
+    soft_bwd_reduce_kernel<<<(unsigned)(L.K + 1 + L.ndim), kReduceThreads, 0, s>>>(
         part, scal, L.K, units, grad_tau, grad_alpha, grad_u);
+    return cudaGetLastError();
+}
+
+cudaError_t soft_run_stats(const SoftLayout &L, const void *ws, int64_t *stats, cudaStream_t s)
+{
+    const int *counts = reinterpret_cast<const int *>(static_cast<const char *>(ws) + L.off_counts);
+    soft_stats_kernel<<<1, kReduceThreads, 0, s>>>(counts, L.batch * L.tiles, stats);
     return cudaGetLastError();
 }
 

@@ -5,7 +5,7 @@ device pointers, sizes and the current CUDA stream, and turns negative status co
 exceptions. There is no CPU path: CPU tensors are rejected, and a missing library raises.
 
 Names follow the C entry points: ``ecc_hard``, ``ecc_soft_fwd``, ``ecc_soft_bwd``,
-``soft_workspace_bytes``; ``SoftECC`` / ``soft_ecc`` wrap the soft pair as a differentiable
+``ecc_soft_stats``, ``ecc_soft_fwd_noalloc``, ``soft_workspace_bytes``; ``SoftECC`` / ``soft_ecc`` wrap the soft pair as a differentiable
 PyTorch layer ("Key designs -- differentiable ECC layer (sigmoid relaxation)" in the paper notes
 "Scalable GPU-Accelerated Euler Characteristic Curves").
 """
@@ -50,6 +50,8 @@ def load_library():
         lib.ecc_soft_fwd.restype = i
         lib.ecc_soft_bwd.argtypes = [p, i, p, i64, p, i, f, p, p, p, p, p, p, p, p, sz, p]
         lib.ecc_soft_bwd.restype = i
+        lib.ecc_soft_stats.argtypes = [i, p, i64, i, p, sz, p, p]
+        lib.ecc_soft_stats.restype = i
         lib.ecc_soft_fwd_noalloc.argtypes = [p, i, p, i64, p, i, f, p, p, p, p]
         lib.ecc_soft_fwd_noalloc.restype = i
         lib.ecc_status_str.argtypes = [i]
@@ -145,12 +147,12 @@ def _soft_common(img, tau, alpha, u, ndim):
     _need_cuda(img, "img")
     if img.dtype != torch.float32:
         raise TypeError("soft ECC takes float32 images")
-    ndim = 2 if ndim is None else ndim
-    ndim, batch, dims, batched = _split(img, ndim)
     for name, t in (("tau", tau), ("alpha", alpha), ("u", u)):
         _need_cuda(t, name)
         if t.dtype != torch.float32:
             raise TypeError(f"{name} must be float32")
+    ndim = u.numel() if ndim is None else ndim  # u has one component per image axis
+    ndim, batch, dims, batched = _split(img, ndim)
     if alpha.numel() != 1 or u.numel() != ndim:
         raise ValueError(f"alpha must have 1 element and u {ndim}")
     return ndim, batch, dims, batched
@@ -183,6 +185,21 @@ def ecc_soft_fwd(img, tau, lam: float, alpha, u, ws=None, out=None, ndim=None, s
     _check(rc, "ecc_soft_fwd")
     out = out.view(batch, K)
     return (out if batched else out[0]), ws
+
+
+def ecc_soft_stats(img, K: int, ws, ndim=None, stream=None) -> torch.Tensor:
+    """int64 CUDA tensor [3]: voxels on the soft work list (summed over the batch), tiles that
+    took the direct exponent form, and tiles, for the workspace ``ws`` that a soft forward call
+    filled for ``img`` and ``K`` thresholds (``ndim``: 2 or 3, default 2 for [B, H, W])."""
+    _need_cuda(img, "img")
+    _need_cuda(ws, "ws")
+    ndim, batch, dims, _ = _split(img, 2 if ndim is None and img.dim() != 4 else ndim)
+    stats = torch.empty(3, dtype=torch.int64, device=img.device)
+    rc = load_library().ecc_soft_stats(ndim, _dims_array(dims), batch, int(K),
+                                       ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+                                       ctypes.c_void_p(stats.data_ptr()), _stream_handle(stream))
+    _check(rc, "ecc_soft_stats")
+    return stats
 
 
 def ecc_soft_fwd_noalloc(img, tau, lam: float, alpha, u, out=None, ndim=None, stream=None):
@@ -237,7 +254,8 @@ def ecc_soft_bwd(img, tau, lam: float, alpha, u, grad_out, ws, want_img: bool = 
 class SoftECC(torch.autograd.Function):
     """Differentiable soft ECC layer: S = SoftECC.apply(img, tau, alpha, u, lam).
 
-    img float32 [(B,) H, W]; tau [K]; alpha [1]; u [2] (learnable); lam a Python float.
+    img float32 [(B,) H, W] with u [2], or [(B,) D, H, W] with u [3]; tau [K]; alpha [1]
+    (tau, alpha and u learnable); lam a Python float.
     Gradients flow to tau, alpha, u and, when it requires grad, img.
     """
 

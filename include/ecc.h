@@ -103,7 +103,7 @@ size_t ecc_soft_workspace_bytes(int ndim, const int64_t *dims, int64_t batch, in
  *                 (-1)^dim(sigma) / (1 + exp(-lambda (tau[k] - max_{v in sigma} X(v))))   (fp32)
  *
  * img     device float32 [batch][dims...]; finite values.
- * ndim    2 (3-D volumes are not supported by the soft path yet: ECC_EDIM).
+ * ndim    2 ([H][W] per image) or 3 ([D][H][W] per volume); u has ndim entries, axis 0 first.
  * tau     device float32 [K] thresholds, any order.
  * K       1 <= K <= ECC_MAX_K.
  * lambda  sigmoid sharpness, finite and > 0.
@@ -136,6 +136,23 @@ int ecc_soft_bwd(const float *img, int ndim, const int64_t *dims, int64_t batch,
                  int K, float lambda, const float *alpha, const float *u, const float *grad_out,
                  float *grad_tau, float *grad_alpha, float *grad_u, float *grad_img, void *ws,
                  size_t ws_bytes, ecc_stream_t stream);
+
+/*
+ * Size of the soft forward pass's work list -- a diagnostic with no counterpart in the paper
+ * notes, for sizing and for rooflines: the soft kernels evaluate one sigmoid per (listed voxel,
+ * threshold) pair.
+ *
+ * ws must hold the result of an ecc_soft_fwd (or ecc_soft_bwd) call with the same ndim, dims,
+ * batch and K. Writes, asynchronously on `stream`:
+ *   stats[0] = number of voxels with a non-zero local contribution c_X(p), summed over the batch
+ *   stats[1] = number of tiles whose exponents left the factorised range (their terms take the
+ *              direct form, two special-function operations per term instead of one)
+ *   stats[2] = number of tiles
+ * stats: device int64 [3], overwritten. Returns ECC_OK or a negative status (ECC_EWS for a short
+ * or misaligned workspace).
+ */
+int ecc_soft_stats(int ndim, const int64_t *dims, int64_t batch, int K, const void *ws,
+                   size_t ws_bytes, int64_t *stats, ecc_stream_t stream);
 
 /*
  * Soft ECC forward pass that allocates nothing -- no counterpart in the paper notes.

@@ -74,7 +74,9 @@ def test_soft_workspace_size(lib):
     assert w(2, dims(256, 256), 64, 128) > 64 * 256 * 256 * 16
     assert w(2, dims(256, 256), 64, 128) % 256 == 0
     assert w(2, dims(256, 256), 64, 256) > w(2, dims(256, 256), 64, 128)
-    assert w(3, dims(8, 8, 8), 1, 4) == 0
+    assert w(3, dims(8, 8, 8), 1, 4) > 8 * 8 * 8 * 16
+    assert w(4, dims(2, 2, 2, 2), 1, 4) == 0
+    assert w(2, dims(8, 8), 65536, 4) == 0  # images run along a 16-bit grid axis
     assert w(2, dims(0, 8), 1, 4) == 0
     assert w(2, dims(8, 8), 0, 4) == 0
     assert w(2, dims(8, 8), 1, 0) == 0
@@ -101,7 +103,10 @@ def test_soft_validation(lib):
     assert call(alpha=None) == EINVAL
     assert call(u=None) == EINVAL
     assert call(out=None) == EINVAL
-    assert call(ndim=3, dims=dims(4, 4, 4)) == EDIM
+    assert call(ndim=4, dims=dims(4, 4, 4, 4)) == EDIM
+    assert call(ndim=1, dims=dims(4)) == EDIM
+    assert call(ndim=3, dims=dims(4, 0, 4)) == EDIM
+    assert call(ndim=3, dims=dims(40, 40, 40)) == EWS  # 3-D volumes need their own size
     assert call(K=0) == EINVAL
     assert call(K=8193) == ERANGE
     assert call(lam=0.0) == EINVAL
@@ -114,6 +119,20 @@ def test_soft_validation(lib):
              None) == EINVAL
     assert b(FAKE, 2, d2, 1, FAKE, 8, 50.0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, need,
              None) == EWS
+
+
+def test_soft_stats_validation(lib):
+    d2 = dims(16, 16)
+    need = lib.ecc_soft_workspace_bytes(2, d2, 1, 8)
+    ws = ctypes.c_void_p(0x100000)
+    st = lib.ecc_soft_stats
+    assert st(2, d2, 1, 8, ws, need, None, None) == EINVAL
+    assert st(2, None, 1, 8, ws, need, FAKE, None) == EINVAL
+    assert st(5, d2, 1, 8, ws, need, FAKE, None) == EDIM
+    assert st(2, d2, 0, 8, ws, need, FAKE, None) == EINVAL
+    assert st(2, d2, 1, 8, None, need, FAKE, None) == EWS
+    assert st(2, d2, 1, 8, ws, need - 1, FAKE, None) == EWS
+    assert st(2, d2, 1, 8, ctypes.c_void_p(0x100008), need, FAKE, None) == EWS
 
 
 def test_binding_rejects_cpu_tensors():

@@ -1,6 +1,7 @@
 """GPU parity for the soft ECC forward and backward against the fp64 oracle.
 
-Tolerance (per element), for S, grad_tau, grad_alpha and grad_u:
+2-D images and 3-D volumes (the volume tests sit at the end). Tolerance (per element), for S,
+grad_tau, grad_alpha and grad_u:
     |gpu - oracle| <= 1e-6 + 1e-4 |oracle|.
 grad_img (an optional output) sums K terms per pixel that can cancel; its bound adds a term
 proportional to the sum of the magnitudes of those terms (returned by the oracle):
@@ -44,8 +45,9 @@ def run_both(img, tau, lam, alpha, u, g, want_img=True, sample=None):
     res = {k: v.cpu().numpy() for k, v in res.items()}
     imgs = img if sample is None else img[sample]
     gs = g if sample is None else g[sample]
-    ref_s = oracle.ecc_soft_fwd(imgs, tau, lam, alpha, u, ndim=2)
-    ref = oracle.ecc_soft_bwd(imgs, tau, lam, alpha, u, gs, ndim=2, want_img=want_img)
+    nd = len(u)
+    ref_s = oracle.ecc_soft_fwd(imgs, tau, lam, alpha, u, ndim=nd)
+    ref = oracle.ecc_soft_bwd(imgs, tau, lam, alpha, u, gs, ndim=nd, want_img=want_img)
     return s, res, ref_s, ref
 
 
@@ -152,3 +154,114 @@ def test_workload_64x256sq_soft():
                  extra=4e-6 * ref["grad_img_absterms"])
     others = np.setdiff1d(np.arange(64), sample)
     assert not np.any(res["grad_img"][others])
+
+
+# ---------------------------------------------------------------------------------------------
+# 3-D volumes (3 x 3 x 3 neighbourhoods; tiles of 8 x 8 x 32 voxels)
+# ---------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("shape,batch", [((1, 1, 1), 1), ((2, 3, 4), 2), ((1, 5, 70), 1),
+                                         ((5, 1, 1), 1), ((9, 10, 33), 1), ((17, 9, 40), 2),
+                                         ((8, 8, 32), 1), ((20, 19, 65), 1)])
+def test_soft3d_parity_shapes(shape, batch):
+    """Shapes below, at and across the tile edges along each axis, with ragged tails."""
+    img = synthetic.grf(shape, seed=sum(shape), batch=batch) if min(shape) > 1 else \
+        np.random.default_rng(2).random((batch,) + shape).astype(np.float32)
+    K = 20
+    tau = synthetic.uniform_thresholds(K, -0.3, 1.3)
+    u = synthetic.soft_direction(3, seed=batch + 10)
+    g = synthetic.upstream_grad((batch, K), seed=4)
+    compare(img, tau, 50.0, 1.0, u, g)
+
+
+@pytest.mark.parametrize("K,lam,alpha", [(1, 50.0, 1.0), (129, 50.0, 1.0), (33, 2.0, -0.6),
+                                         (33, 800.0, 1.7), (16, 4000.0, 0.4)])
+def test_soft3d_parity_K_lambda_alpha(K, lam, alpha):
+    img = synthetic.grf((12, 14, 36), seed=K, batch=2)
+    rng = np.random.default_rng(K + 1)
+    tau = rng.uniform(-0.4, 1.4, size=K).astype(np.float32)  # unsorted thresholds
+    u = np.asarray([0.11, -0.17, 0.07], np.float32)
+    g = synthetic.upstream_grad((2, K), seed=K + 2)
+    compare(img, tau, lam, alpha, u, g)
+
+
+def test_soft3d_ties_and_zero_direction():
+    q = synthetic.quantise_u8(synthetic.grf((10, 12, 40), seed=11, batch=2)).astype(np.float32)
+    q /= 255
+    tau = synthetic.uniform_thresholds(24)
+    g = synthetic.upstream_grad((2, 24), seed=12)
+    compare(q, tau, 50.0, 1.0, np.zeros(3, np.float32), g)  # exact ties in X everywhere
+    compare(q, tau, 50.0, 0.5, np.asarray([0.0, 0.0, 0.3], np.float32), g)
+    const = np.full((2, 9, 9, 33), 0.25, np.float32)
+    compare(const, tau, 50.0, 1.0, np.zeros(3, np.float32), g)
+
+
+def test_soft3d_large_lambda_matches_hard():
+    q = np.random.default_rng(13).integers(0, 6, size=(2, 11, 12, 37)).astype(np.float32)
+    tau = (np.arange(7) - 0.5).astype(np.float32)
+    a = np.asarray([1.0], np.float32)
+    s, _ = ecc.ecc_soft_fwd(dev(q), dev(tau), 1.0e4, dev(a), dev(np.zeros(3, np.float32)))
+    hard = ecc.ecc_hard(dev(q), 7, -0.5, 5.5, ndim=3).cpu().numpy()
+    np.testing.assert_allclose(s.cpu().numpy(), hard.astype(np.float64), atol=1e-6)
+
+
+def test_soft3d_autograd_layer():
+    img = synthetic.grf((10, 16, 40), seed=14, batch=2)
+    tau = dev(synthetic.uniform_thresholds(16)).requires_grad_()
+    alpha = torch.ones(1, device=DEV, requires_grad=True)
+    u = dev(np.asarray([0.05, -0.08, 0.02], np.float32)).requires_grad_()
+    x = dev(img).requires_grad_()
+    g = dev(synthetic.upstream_grad((2, 16), seed=15))
+    s = ecc.soft_ecc(x, tau, alpha, u, 50.0)
+    (s * g).sum().backward()
+    ref = oracle.ecc_soft_bwd(img, tau.detach().cpu().numpy(), 50.0, 1.0,
+                              u.detach().cpu().numpy(), g.cpu().numpy(), ndim=3)
+    assert_close(tau.grad.cpu().numpy(), ref["grad_tau"], "grad_tau")
+    assert_close(u.grad.cpu().numpy(), ref["grad_u"], "grad_u")
+    assert_close(x.grad.cpu().numpy(), ref["grad_img"], "grad_img",
+                 extra=4e-6 * ref["grad_img_absterms"])
+
+
+def test_soft3d_volume_64cubed_sampled():
+    """A larger volume batch (8 x 64^3, 64 tiles each): S on two sampled volumes, and every
+    gradient with the upstream gradient non-zero on those volumes only."""
+    img = synthetic.grf((64, 64, 64), seed=16, batch=8)
+    tau = synthetic.uniform_thresholds(64)
+    u = synthetic.soft_direction(3, seed=17)
+    g_full = synthetic.upstream_grad((8, 64), seed=18)
+    sample = np.asarray([0, 5])
+    g = np.zeros_like(g_full)
+    g[sample] = g_full[sample]
+    s, res, ref_s, ref = run_both(img, tau, 50.0, 1.0, u, g, want_img=True, sample=sample)
+    assert_close(s[sample], ref_s, "S")
+    assert_close(res["grad_tau"], ref["grad_tau"], "grad_tau")
+    assert_close(res["grad_alpha"][0], ref["grad_alpha"], "grad_alpha")
+    assert_close(res["grad_u"], ref["grad_u"], "grad_u")
+    assert_close(res["grad_img"][sample], ref["grad_img"], "grad_img",
+                 extra=4e-6 * ref["grad_img_absterms"])
+
+
+@pytest.mark.parametrize("shape,batch,ndim", [((70, 130), 3, 2), ((12, 20, 45), 2, 3)])
+def test_soft_stats_counts_the_contributing_voxels(shape, batch, ndim):
+    """stats[0] = voxels with c_X != 0. The oracle's image gradient is lambda c_X sum_k g_k w_k
+    per voxel: a random upstream gradient makes it clearly non-zero exactly there, while where
+    c_X = 0 the oracle's per-cell sum leaves only rounding residue (below 1e-9 of the sum of the
+    magnitudes of its terms), which gives the expected count."""
+    img = synthetic.grf(shape, seed=21, batch=batch)
+    K = 16
+    tau = synthetic.uniform_thresholds(K)
+    u = synthetic.soft_direction(ndim, seed=22)
+    g = synthetic.upstream_grad((batch, K), seed=23)
+    a = np.asarray([1.0], np.float32)
+    # c_X depends on the order of X only, not on lambda: one oracle run at a lambda where no
+    # sigmoid derivative underflows gives the count for both launches
+    ref = oracle.ecc_soft_bwd(img, tau, 50.0, 1.0, u, g, ndim=ndim)
+    for lam, direct in ((50.0, False), (4000.0, True)):
+        _, ws = ecc.ecc_soft_fwd(dev(img), dev(tau), lam, dev(a), dev(u))
+        st = ecc.ecc_soft_stats(dev(img), K, ws, ndim=ndim).cpu().numpy()
+        assert st[0] == np.count_nonzero(np.abs(ref["grad_img"]) >
+                                          1e-9 * ref["grad_img_absterms"])
+        tile = (64, 32) if ndim == 2 else (32, 8, 8)
+        tiles = batch * int(np.prod([-(-n // t) for n, t in zip(shape[::-1], tile)]))
+        assert st[2] == tiles
+        assert (st[1] > 0) == direct

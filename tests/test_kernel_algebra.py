@@ -100,3 +100,83 @@ def test_key_patterns_and_contribution_encoding():
     for c in range(-8, 8):
         pat = int(np.float16(1280 + c).view(np.uint16))
         assert pat == 0x6500 + c and np.array(pat & 0xFF, np.uint8).view(np.int8) == c
+
+
+# ---------------------------------------------------------------------------------------------
+# Soft path, 3-D: the prep kernel's local contribution from the 27 cells containing a voxel
+# ---------------------------------------------------------------------------------------------
+
+def cell_table_3d():
+    """Bit masks (bit (dz+1) 9 + (dy+1) 3 + (dx+1)) of the vertices of the 27 cells containing a
+    voxel, one direction in {-1, 0, +1} per axis, and their signs (-1)^dim."""
+    masks, signs = [], []
+    for s in range(27):
+        d = (s // 9 - 1, (s // 3) % 3 - 1, s % 3 - 1)
+        m = 0
+        for a in range(2 if d[0] else 1):
+            for b in range(2 if d[1] else 1):
+                for c in range(2 if d[2] else 1):
+                    m |= 1 << ((a * d[0] + 1) * 9 + (b * d[1] + 1) * 3 + (c * d[2] + 1))
+        masks.append(m)
+        signs.append((-1) ** sum(x != 0 for x in d))
+    return masks, signs
+
+
+def c3_soft_model(rank):
+    """rank: the (X, linear index) order of each voxel as an integer array (absent = ABSENT)."""
+    D, Hh, Ww = rank.shape
+    P = np.full((D + 2, Hh + 2, Ww + 2), ABSENT, np.int64)
+    P[1:-1, 1:-1, 1:-1] = rank
+    earlier = np.full(rank.shape, 1 << 13, np.int64)
+    for o in range(27):
+        if o == 13:
+            continue
+        dz, dy, dx = o // 9 - 1, (o // 3) % 3 - 1, o % 3 - 1
+        q = P[1 + dz:1 + dz + D, 1 + dy:1 + dy + Hh, 1 + dx:1 + dx + Ww]
+        earlier |= (q < rank).astype(np.int64) << o  # ranks are distinct: < is the order
+    masks, signs = cell_table_3d()
+    c = np.zeros(rank.shape, np.int64)
+    for m, sg in zip(masks, signs):
+        c += sg * ((earlier & m) == m)
+    return c
+
+
+@pytest.mark.parametrize("shape,seed", [((5, 6, 7), 0), ((3, 9, 4), 1), ((1, 6, 8), 2)])
+def test_soft3d_cell_table_matches_oracle(shape, seed):
+    """X in fp64, order by (X, linear index), c from the 27-cell masks: sum_p c sigma(...) is the
+    oracle's soft forward; quantised values make many exact ties."""
+    f = np.round(synthetic.grf(shape, seed) * 7) / 7
+    f = f.astype(np.float32)
+    u = np.asarray([0.0, 0.05, -0.1], np.float32) if seed else np.zeros(3, np.float32)
+    coords = [np.zeros(1) if n == 1 else (2.0 * np.arange(n) - (n - 1)) / (n - 1) for n in shape]
+    X = f.astype(np.float64)
+    for d in range(3):
+        sh = [1, 1, 1]
+        sh[d] = shape[d]
+        X = X + np.float64(u[d]) * coords[d].reshape(sh)
+    order = np.lexsort((np.arange(X.size), X.reshape(-1)))
+    rank = np.empty(X.size, np.int64)
+    rank[order] = np.arange(X.size)
+    c = c3_soft_model(rank.reshape(shape))
+    assert c.min() >= -5 and c.max() <= 7
+    tau = np.linspace(-0.2, 1.2, 9).astype(np.float32)
+    lam = 30.0
+    s = (c.reshape(-1, 1) / (1 + np.exp(-lam * (tau.astype(np.float64) -
+                                                X.reshape(-1, 1))))).sum(0)
+    np.testing.assert_allclose(s, oracle.ecc_soft_fwd(f, tau, lam, 1.0, u, ndim=3), rtol=1e-11,
+                               atol=1e-11)
+
+
+def test_soft3d_contribution_extremes():
+    """The local contribution spans [-5, 7], which the entry's 4-bit field (c + 8) holds: -5 when
+    only the six axis neighbours are earlier, +7 when the 18 axis and face-diagonal neighbours
+    are but no corner is."""
+    r = np.full((3, 3, 3), 100, np.int64)
+    r[1, 1, 1] = 50
+    for z, y, x in [(0, 1, 1), (2, 1, 1), (1, 0, 1), (1, 2, 1), (1, 1, 0), (1, 1, 2)]:
+        r[z, y, x] = 0
+    assert c3_soft_model(r)[1, 1, 1] == -5
+    dist = np.abs(np.indices((3, 3, 3)) - 1).sum(0)
+    r = np.where(dist <= 2, 0, 100)
+    r[1, 1, 1] = 50
+    assert c3_soft_model(r)[1, 1, 1] == 7

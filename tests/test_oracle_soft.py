@@ -70,7 +70,12 @@ def test_linear_ramp_closed_form(axis, sign):
                                            ((3, 5), (0.0, 0.3), (0, 0)),
                                            ((3, 5), (0.0, -0.3), (0, 4)),
                                            ((4, 3), (-0.3, 0.0), (3, 0)),
-                                           ((4, 6), (-0.2, -0.1), (3, 5))])
+                                           ((4, 6), (-0.2, -0.1), (3, 5)),
+                                           ((3, 4, 5), (0.0, 0.0, 0.0), (0, 0, 0)),
+                                           ((3, 4, 5), (-0.3, 0.0, 0.0), (2, 0, 0)),
+                                           ((3, 4, 5), (0.0, -0.3, 0.0), (0, 3, 0)),
+                                           ((3, 4, 5), (0.0, 0.0, -0.2), (0, 0, 4)),
+                                           ((3, 4, 5), (0.1, -0.2, -0.3), (0, 3, 4))])
 def test_gradient_lands_on_the_first_entering_pixel(shape, u, pixel):
     """f = 0, X = u . x (constant when u = 0). Every sublevel set is a box, so only the first
     pixel to enter has a non-zero local contribution (+1), and the image gradient sits on that
@@ -82,9 +87,9 @@ def test_gradient_lands_on_the_first_entering_pixel(shape, u, pixel):
     gi = r["grad_img"]
     nz = np.argwhere(gi != 0)
     assert [tuple(x) for x in nz] == [pixel]
-    x0 = -float(np.float32(abs(u[0]))) if u[0] else 0.0
-    x1 = -float(np.float32(abs(u[1]))) if u[1] else 0.0
-    s = 1.0 / (1.0 + np.exp(-lam * (0.1 - (x0 + x1))))
+    # X of that corner: each axis adds -|u_d| (coordinate -1 for u_d > 0, +1 for u_d < 0)
+    x = sum(-float(np.float32(abs(ud))) for ud in u)
+    s = 1.0 / (1.0 + np.exp(-lam * (0.1 - x)))
     # dL/dX = -lambda s (1 - s) for the only contributing vertex, grad_img = alpha dL/dX
     assert abs(gi[pixel] + lam * s * (1 - s)) < 1e-7
 
