@@ -89,7 +89,7 @@ int ecc_hard(const void *img, int dtype, int ndim, const int64_t *dims, int64_t 
     pl.out = out;
     float table[ECC_MAX_NBINS + 2];
     const int H = nbins;
-    pl.key_err = 0.0f;
+    pl.key_a = pl.key_b = pl.key_clo = pl.key_chi = 0.0f;
     if (dtype == ECC_U8) {
         // fp16 key pattern of every byte value: 0x6400 + (first k with b <= t_k; H if none)
         uint16_t lut[256];
@@ -106,29 +106,32 @@ int ecc_hard(const void *img, int dtype, int ndim, const int64_t *dims, int64_t 
         }
         memcpy(table, lut, sizeof(lut));
         pl.key_mode = kKeyLut;
-        pl.scale = pl.offset = 0.0f;
         pl.vec_ok = ((uintptr_t)img % 4 == 0) && (W % 4 == 0);
     } else {
         for (int k = 0; k < H; ++k) table[k] = round_down_f32(threshold(k, H, vmin, vmax));
         table[H] = table[H + 1] = INFINITY;
-        // Estimator t = H * sat(v * sH + oH) of the fractional bin (v - vmin) (H - 1) / (vmax -
-        // vmin), clamped to [0, H]. Its error in bins, from rounding sH, oH, the FMA, the scaling
-        // by H, the subtraction of E and the fp64 thresholds, is below
-        //     E = 2^-21 (M s + |o| + 2 H + 4),  M = max(|vmin|, |vmax|), s = (H-1)/(vmax-vmin),
-        // for every |v| <= M (values beyond saturate to t = 0 or H, where the kernel always
-        // consults the table). The kernel needs E <= 1/4; otherwise every key is searched.
+        // Estimator of the fractional bin t* = v s + o, s = (H-1)/(vmax-vmin), o = -vmin s (the
+        // key is ceil(t*) clamped to [0, H]): u = sat(v a + b), a = -s/H, b = (H - 1/2 - o)/H,
+        // t = (H - 1/2) - H u. For an unsaturated value (|v| <= M + (vmax-vmin)/(H-1),
+        // M = max(|vmin|, |vmax|)), |t - t*| collects the rounding of a and b (2^-24 |v| s and
+        // 2^-24 |H - 1/2 - o|), of the FMA for u (2^-24, times H), of the FMA for t and of the
+        // constants H - 1/2 -+ E (2^-24 H each), and the fp64 rounding of the thresholds:
+        //     |t - t*| < dev = 2^-24 (M s + |o| + 5 H + 2).
+        // The kernel proves a key when ceil(t - E) == ceil(t + E); E = 1.25 dev must stay
+        // below 1/4 (then the saturated ends t = -1/2, H - 1/2 are never ambiguous), else
+        // every key is binary-searched.
         pl.key_mode = kKeySearch;
-        pl.scale = pl.offset = 0.0f;
         if (H >= 2 && vmax > vmin) {
             const double sc = (double)(H - 1) / (vmax - vmin);
             const double o = -vmin * sc;
             const double M = fmax(fabs(vmin), fabs(vmax));
-            const double err = ldexp(1.0, -21) * (M * sc + fabs(o) + 2.0 * H + 4.0);
-            if (isfinite(sc) && sc < 1e30 && err <= 0.25) {
+            const double E = 1.25 * ldexp(1.0, -24) * (M * sc + fabs(o) + 5.0 * H + 2.0);
+            if (isfinite(sc) && sc < 1e30 && E <= 0.25) {
                 pl.key_mode = kKeyEstimate;
-                pl.scale = (float)(sc / H);
-                pl.offset = (float)(o / H);
-                pl.key_err = (float)(err * 1.0625);
+                pl.key_a = (float)(-sc / H);
+                pl.key_b = (float)((H - 0.5 - o) / H);
+                pl.key_clo = (float)(H - 0.5 - E);
+                pl.key_chi = (float)(H - 0.5 + E);
             }
         }
         pl.vec_ok = ((uintptr_t)img % 16 == 0) && (W % 4 == 0);

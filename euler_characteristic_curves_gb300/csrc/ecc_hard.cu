@@ -10,11 +10,13 @@
 // The running sum of the histogram over bins is the curve (ecc_bin_scan_kernel).
 //
 // Both kernels first turn every voxel into its exact threshold key (ecc_keys.cuh) and then work
-// on fp16 key patterns, two pixels per instruction.
+// on fp16 key patterns, two pixels per instruction. Every position outside the grid reads as NaN
+// (key H, "never"), so the steady state has no boundary branches.
 //
 // 2-D: a warp owns a strip of 128 columns (four per lane, one 16-byte load per lane per row) and
 // walks down a band of rows; raw rows are prefetched three rows ahead in registers, and the
-// comparisons with the row below are reused as the "above" comparisons of the next row.
+// comparisons with the row below are reused as the "above" comparisons of the next row. The
+// keys just left and right of the strip ride on the rotated row shuffles.
 //
 // 3-D: the complex of a volume splits into the cells of each plane z and the vertical cells
 // sigma x [z, z+1]; a vertical cell's value is the max over sigma of M_z = max(S_z, S_{z+1}) and
@@ -36,6 +38,7 @@ namespace ecc {
 
 constexpr int kHardThreads = 256;
 constexpr int kHardWarps = kHardThreads / kWarp;
+constexpr int kStrip = 128;  // columns per warp strip / block tile
 
 // Resident blocks per SM the kernels are compiled for (register budget 65536 / (256 * blocks)).
 #ifndef ECC_2D_MIN_BLOCKS
@@ -49,12 +52,14 @@ constexpr int kHardWarps = kHardThreads / kWarp;
 // Block setup, keys and histogram
 // ----------------------------------------------------------------------------------------------
 
-// Shared layout: int hist[H], then the table: f32 thresholds T[0..H+1], or for uint8 inputs the
-// fp16 key pattern of each byte value (uint16[256]).
+// Shared layout: int hist[H + 1] (bin H collects the discarded "never" contributions), then the
+// table: f32 thresholds T[0..H+1], or for uint8 inputs the fp16 key pattern of each byte value.
+__host__ __device__ constexpr int hist_words(int H) { return (H + 2) & ~1; }  // keeps 8-byte align
+
 template <int CAP>
 __device__ __forceinline__ void block_setup(const HardParams<CAP> &P, int *hist, float *table)
 {
-    for (int i = threadIdx.x; i < P.H; i += blockDim.x) hist[i] = 0;
+    for (int i = threadIdx.x; i <= P.H; i += blockDim.x) hist[i] = 0;
     for (int i = threadIdx.x; i < P.table_len; i += blockDim.x) table[i] = P.table[i];
     __syncthreads();
 }
@@ -74,240 +79,269 @@ template <int CAP>
 __device__ __forceinline__ KeyConsts key_consts(const HardParams<CAP> &P)
 {
     KeyConsts K;
-    K.sH = P.scale;
-    K.oH = P.offset;
-    K.Hf = (float)P.H;
-    K.E = P.key_err;
+    K.a = P.key_a;
+    K.b = P.key_b;
+    K.nH = -(float)P.H;
+    K.clo = P.key_clo;
+    K.chi = P.key_chi;
     K.H = P.H;
-    K.search = P.key_mode == kKeySearch;
     return K;
 }
 
-// Key pattern of one float value (any value; NaN -> H). SEARCH: binary-search every value (the
-// estimator is not usable for this threshold range).
-template <bool SEARCH>
-__device__ __forceinline__ uint32_t key_one(float v, const KeyConsts &K, const float *__restrict__ T)
-{
-    if (SEARCH) return key_search_pattern(v, K.H, T);
-    float amb = 0.0f;
-    const uint32_t k = key_fast(v, K, amb);
-    return (amb != 0.0f) ? key_fix(v, k, K, T) : k;
-}
+__device__ __forceinline__ float qnan_f() { return __int_as_float(0x7fffffff); }
 
-template <bool SEARCH>
-__device__ __forceinline__ uint32_t key_one(uint8_t v, const KeyConsts &, const float *__restrict__ T)
-{
-    return reinterpret_cast<const uint16_t *>(T)[v];
-}
-
-// Raw values of one row around a lane's four columns, plus (lanes 0 / 31 only) the value just
-// left of column x0 / right of column x0 + 127. `valid` has bit j set when column x + j is inside
-// the grid; `halo_in` says whether the lane's halo column exists.
+// Raw values one lane needs from one row: its four columns and one side value (lane 0: the
+// column right of the strip, lane 31: the column left of it; NaN where the grid has none).
 template <typename T>
-struct RawRow;
+struct Raw;
 
 template <>
-struct RawRow<float> {
+struct Raw<float> {
     float v[4];
-    float halo;
-    uint32_t valid;
-    bool present;  // row inside the grid (warp-uniform)
-    bool halo_in;
+    float side;
 };
 
 template <>
-struct RawRow<uint8_t> {
-    uint32_t bytes;
-    uint8_t halo;
-    uint32_t valid;
-    bool present;
-    bool halo_in;
+struct Raw<uint8_t> {
+    uint32_t bytes;  // four values, first column in the low byte
+    uint32_t side;   // the side value, or 256 for "none"
+    uint32_t own_ok; // bit j: column j of the lane is inside the grid (and the row exists)
 };
 
-template <typename T>
-__device__ __forceinline__ void load_own(const T *__restrict__ row, int xs, int W, bool vec,
-                                         RawRow<T> &r);
+// Columns of a lane within the strip starting at x0 (fixed for a whole task).
+struct Cols {
+    int x;        // first own column
+    int sx;       // side column, clamped into the grid
+    uint32_t own_ok;  // bit j: x + j < W
+    bool side_ok;     // the side column exists
+    bool full;        // all four own columns exist and the 16-byte (4-byte for u8) load is legal
+};
 
-template <>
-__device__ __forceinline__ void load_own<float>(const float *__restrict__ row, int xs, int W,
-                                                bool vec, RawRow<float> &r)
+__device__ __forceinline__ Cols strip_cols(int x0, int W, int lane, bool vec_ok)
 {
-    if (vec) {
-        const float4 q = __ldg(reinterpret_cast<const float4 *>(row + xs));
+    Cols c;
+    c.x = x0 + 4 * lane;
+    const int sx = (lane == 0) ? x0 + kStrip : (lane == kWarp - 1 ? x0 - 1 : c.x);
+    c.side_ok = (lane == 0 || lane == kWarp - 1) && sx >= 0 && sx < W;
+    c.sx = min(max(sx, 0), W - 1);
+    c.own_ok = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) c.own_ok |= (c.x + j < W) ? (1u << j) : 0u;
+    c.full = vec_ok && (x0 + kStrip <= W);
+    return c;
+}
+
+// Loads a lane's four values of one row (row pointer `row`, or nullptr when the row is outside
+// the grid); positions outside the grid read as NaN (f32) or are cleared from own_ok (u8).
+__device__ __forceinline__ void load_own(const float *__restrict__ row, const Cols &c,
+                                         Raw<float> &r)
+{
+    if (row == nullptr) {  // warp-uniform
+#pragma unroll
+        for (int j = 0; j < 4; ++j) r.v[j] = qnan_f();
+        return;
+    }
+    if (c.full) {  // warp-uniform
+        const float4 q = __ldg(reinterpret_cast<const float4 *>(row + c.x));
         r.v[0] = q.x;
         r.v[1] = q.y;
         r.v[2] = q.z;
         r.v[3] = q.w;
-        r.valid = 0xfu;
     } else {
-        r.valid = 0;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const bool in = xs + j < W;
-            r.v[j] = in ? __ldg(row + xs + j) : 0.0f;
-            r.valid |= in ? (1u << j) : 0u;
+            const bool in = (c.own_ok >> j) & 1u;
+            const float v = __ldg(row + (in ? c.x + j : 0));
+            r.v[j] = in ? v : qnan_f();
         }
     }
 }
 
-template <>
-__device__ __forceinline__ void load_own<uint8_t>(const uint8_t *__restrict__ row, int xs, int W,
-                                                  bool vec, RawRow<uint8_t> &r)
+__device__ __forceinline__ void load_own(const uint8_t *__restrict__ row, const Cols &c,
+                                         Raw<uint8_t> &r)
 {
-    if (vec) {
-        r.bytes = __ldg(reinterpret_cast<const unsigned int *>(row + xs));
-        r.valid = 0xfu;
+    if (row == nullptr) {
+        r.bytes = 0;
+        r.own_ok = 0;
+        return;
+    }
+    if (c.full) {
+        r.bytes = __ldg(reinterpret_cast<const unsigned int *>(row + c.x));
     } else {
-        r.valid = 0;
         r.bytes = 0;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const bool in = xs + j < W;
-            r.bytes |= in ? ((uint32_t)__ldg(row + xs + j) << (8 * j)) : 0u;
-            r.valid |= in ? (1u << j) : 0u;
+            const bool in = (c.own_ok >> j) & 1u;
+            const uint32_t v = __ldg(row + (in ? c.x + j : 0));
+            r.bytes |= in ? (v << (8 * j)) : 0u;
         }
     }
+    r.own_ok = c.own_ok;
 }
 
-template <typename T>
-__device__ __forceinline__ RawRow<T> load_raw(const T *__restrict__ plane, int Hy, int W, int y,
-                                              int x0, int lane, bool vec)
+__device__ __forceinline__ void side_value(const float *__restrict__ row, const Cols &c,
+                                           Raw<float> &r)
 {
-    RawRow<T> r;
-    r.present = (y >= 0 && y < Hy);
-    r.halo_in = false;
-    if (!r.present) {
-        r.valid = 0;
-        return r;
-    }
-    const T *__restrict__ row = plane + (int64_t)y * W;
-    load_own<T>(row, x0 + 4 * lane, W, vec, r);
-    const int hx = (lane == 0) ? x0 - 1 : x0 + 128;
-    r.halo_in = (lane == 0 || lane == kWarp - 1) && hx >= 0 && hx < W;
-    r.halo = r.halo_in ? __ldg(row + hx) : (T)0;
+    r.side = qnan_f();
+    if (row != nullptr && c.side_ok) r.side = __ldg(row + c.sx);
+}
+
+__device__ __forceinline__ void side_value(const uint8_t *__restrict__ row, const Cols &c,
+                                           Raw<uint8_t> &r)
+{
+    r.side = 256u;
+    if (row != nullptr && c.side_ok) r.side = __ldg(row + c.sx);
+}
+
+// A lane's four values and its side value of one row.
+template <typename T>
+__device__ __forceinline__ Raw<T> load_row(const T *__restrict__ row, const Cols &c)
+{
+    Raw<T> r;
+    load_own(row, c, r);
+    side_value(row, c, r);
     return r;
 }
 
-// fp16 key patterns of the lane's four values as pairs (k0 | k1 << 16, k2 | k3 << 16), and of
-// its halo value (absent when there is none). Whole-warp call.
+// Keys of a raw row: own pairs (k0 | k1 << 16, k2 | k3 << 16) and the side key (low half).
 template <bool SEARCH>
-__device__ __forceinline__ void raw_keys(const RawRow<float> &r, const KeyConsts &K,
+__device__ __forceinline__ void row_keys(const Raw<float> &r, const KeyConsts &K,
                                          const float *__restrict__ T, uint32_t &own0,
-                                         uint32_t &own1, uint32_t &halo_key)
+                                         uint32_t &own1, uint32_t &side)
 {
-    uint32_t k[4];
+    uint32_t k[5];
     if (SEARCH) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) k[j] = key_search_pattern(r.v[j], K.H, T);
+        k[4] = key_search_pattern(r.side, K.H, T);
     } else {
-        float amb = 0.0f;
+        uint32_t amb = 0;
 #pragma unroll
         for (int j = 0; j < 4; ++j) k[j] = key_fast(r.v[j], K, amb);
-        if (__any_sync(kFull, amb != 0.0f)) {
-            if (amb != 0.0f) {
+        k[4] = key_fast(r.side, K, amb);
+        if (__any_sync(kFull, amb != 0)) {  // rare: a value within E of a threshold
+            if (amb != 0) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) k[j] = key_fix(r.v[j], k[j], K, T);
+                for (int j = 0; j < 4; ++j) k[j] = key_fix(r.v[j], k[j], K.H, T);
+                k[4] = key_fix(r.side, k[4], K.H, T);
             }
         }
     }
-    if (r.valid != 0xfu) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            if (!(r.valid >> j & 1u)) k[j] = kAbsentHalf;
-    }
     own0 = prmt(k[0], k[1], 0x5410);
     own1 = prmt(k[2], k[3], 0x5410);
-    halo_key = kAbsentHalf;
-    if (r.halo_in) halo_key = key_one<SEARCH>(r.halo, K, T);
+    side = k[4];
 }
 
 template <bool SEARCH>
-__device__ __forceinline__ void raw_keys(const RawRow<uint8_t> &r, const KeyConsts &K,
+__device__ __forceinline__ void row_keys(const Raw<uint8_t> &r, const KeyConsts &K,
                                          const float *__restrict__ T, uint32_t &own0,
-                                         uint32_t &own1, uint32_t &halo_key)
+                                         uint32_t &own1, uint32_t &side)
 {
     const uint16_t *lut = reinterpret_cast<const uint16_t *>(T);
+    const uint32_t never = kKeyBase + (uint32_t)K.H;
     uint32_t k[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-        k[j] = (r.valid >> j & 1u) ? (uint32_t)lut[(r.bytes >> (8 * j)) & 0xffu] : kAbsentHalf;
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t v = lut[(r.bytes >> (8 * j)) & 0xffu];
+        k[j] = ((r.own_ok >> j) & 1u) ? v : never;
+    }
     own0 = prmt(k[0], k[1], 0x5410);
     own1 = prmt(k[2], k[3], 0x5410);
-    halo_key = r.halo_in ? (uint32_t)lut[r.halo] : kAbsentHalf;
-}
-
-template <bool SEARCH, typename T>
-__device__ __forceinline__ KeyRow key_row(const RawRow<T> &r, const KeyConsts &K,
-                                          const float *__restrict__ table, int lane)
-{
-    if (!r.present) return absent_row();  // warp-uniform
-    uint32_t own0, own1, hk;
-    raw_keys<SEARCH>(r, K, table, own0, own1, hk);
-    return make_key_row(own0, own1, lane, hk, hk);
+    side = (r.side < 256u) ? (uint32_t)lut[r.side & 0xffu] : never;
 }
 
 // ----------------------------------------------------------------------------------------------
 // 2-D kernel
 // ----------------------------------------------------------------------------------------------
 //
-// Work: an image is cut into warp tasks (strip of 128 columns) x (band of rows_per_task rows),
-// strip index fastest. blockIdx.y = image; block g of the image takes the task range
-// [g * T / G, (g + 1) * T / G) and its warps take those tasks round-robin.
+// Work: the rows of an image's 128-column strips, strip-major ("strip-rows", N = strips * Hy),
+// are split into equal contiguous ranges, one per warp of the image's blocks (blockIdx.y =
+// image). A warp walks its range as one band per strip it touches, so the only repeated work is
+// the two rows around each band, and warps that run side by side read neighbouring rows.
+
+template <typename T>
+__device__ __forceinline__ const T *row_ptr(const T *__restrict__ img, int y, int rows, int W)
+{
+    return ((unsigned)y < (unsigned)rows) ? img + (int64_t)y * W : nullptr;
+}
+
+template <typename T, bool SEARCH>
+__device__ __forceinline__ KeyRow key_row(const Raw<T> &r, const KeyConsts &K,
+                                          const float *__restrict__ table, const LaneShuffle &q)
+{
+    uint32_t own0, own1, side;
+    row_keys<SEARCH>(r, K, table, own0, own1, side);
+    return make_key_row(own0, own1, side, q);
+}
+
+// One band: rows y0 .. y1 - 1 of the strip at x0.
+template <typename T, bool SEARCH>
+__device__ __forceinline__ void band2d(const T *__restrict__ img, int Hy, int W, int x0, int y0,
+                                       int y1, bool vec_ok, int lane, const LaneShuffle &q,
+                                       const KeyConsts &K, const float *__restrict__ table,
+                                       int *hist)
+{
+    const Cols c = strip_cols(x0, W, lane, vec_ok);
+    const int ylim = min(y1 + 1, Hy);  // rows that exist and are needed (the band and the row below)
+    // raw-row ring: at the start of step y, q0 / q1 / q2 (in rotation) hold rows y+1 .. y+3
+    Raw<T> q0 = load_row(row_ptr(img, y0 + 1, ylim, W), c);
+    Raw<T> q1 = load_row(row_ptr(img, y0 + 2, ylim, W), c);
+    Raw<T> q2 = load_row(row_ptr(img, y0 + 3, ylim, W), c);
+    KeyRow ka = key_row<T, SEARCH>(load_row(row_ptr(img, y0 - 1, Hy, W), c), K, table, q);
+    KeyRow kb = key_row<T, SEARCH>(load_row(row_ptr(img, y0, Hy, W), c), K, table, q);
+    uint32_t Sp0, Sp1;
+    sp_init(ka, kb, Sp0, Sp1);
+
+#define ECC_2D_STEP(QS)                                                                     \
+    {                                                                                       \
+        if (y >= y1) break;                                                                 \
+        const KeyRow kd = key_row<T, SEARCH>(QS, K, table, q);                              \
+        QS = load_row(row_ptr(img, y + 4, ylim, W), c);                                     \
+        uint32_t c0, c1;                                                                    \
+        c2_quad(ka, kb, kd, kBias, Sp0, Sp1, c0, c1);                                       \
+        hist_pair(kb.own0, c0, hist);                                                       \
+        hist_pair(kb.own1, c1, hist);                                                       \
+        ka = kb;                                                                            \
+        kb = kd;                                                                            \
+        ++y;                                                                                \
+    }
+    for (int y = y0; y < y1;) {
+        ECC_2D_STEP(q0)
+        ECC_2D_STEP(q1)
+        ECC_2D_STEP(q2)
+    }
+#undef ECC_2D_STEP
+}
+
 template <typename T, int CAP, bool SEARCH>
 __global__ void __launch_bounds__(kHardThreads, ECC_2D_MIN_BLOCKS) ecc_hard2d_kernel(const __grid_constant__
                                                                   HardParams<CAP> P)
 {
     extern __shared__ int smem[];
     int *hist = smem;
-    float *table = reinterpret_cast<float *>(smem + P.H);
+    float *table = reinterpret_cast<float *>(smem + hist_words(P.H));
     block_setup(P, hist, table);
 
     const int64_t b = blockIdx.y;
     const T *__restrict__ img = static_cast<const T *>(P.img) + b * P.image_elems;
     const int lane = threadIdx.x & (kWarp - 1);
     const int warp = threadIdx.x >> 5;
-    const int64_t Tn = P.tasks_per_image;
-    const int t_begin = (int)(Tn * blockIdx.x / P.ctas_per_image);
-    const int t_end = (int)(Tn * (blockIdx.x + 1) / P.ctas_per_image);
     const KeyConsts K = key_consts(P);
+    const LaneShuffle q = lane_shuffle(lane);
     const int Hy = (int)P.Hy, W = (int)P.W;
-    const int R = P.rows_per_task, TX = P.tasks_x;
-    const uint32_t limit = (kKeyBase + (uint32_t)P.H) * 0x10001u;
+    const bool vec_ok = P.vec_ok != 0;
 
-    for (int t = t_begin + warp; t < t_end; t += kHardWarps) {
-        const int x0 = (t % TX) * 128;
-        const int y0 = (t / TX) * R;
-        const int y1 = min(y0 + R, Hy);
-        const bool vec = P.vec_ok && (x0 + 128 <= W);
-
-        // raw-row ring: at the start of step y, q0 / q1 / q2 (in rotation) hold rows y+1 .. y+3
-        RawRow<T> q0 = load_raw(img, Hy, W, y0 + 1, x0, lane, vec);
-        RawRow<T> q1 = load_raw(img, Hy, W, y0 + 2, x0, lane, vec);
-        RawRow<T> q2 = load_raw(img, Hy, W, y0 + 3, x0, lane, vec);
-        KeyRow ka = key_row<SEARCH>(load_raw(img, Hy, W, y0 - 1, x0, lane, vec), K, table, lane);
-        KeyRow kb = key_row<SEARCH>(load_raw(img, Hy, W, y0, x0, lane, vec), K, table, lane);
-        uint32_t Sp0, Sp1;
-        sp_init(ka, kb, Sp0, Sp1);
-
-#define ECC_2D_STEP(QS)                                                                     \
-    {                                                                                       \
-        if (y >= y1) break;                                                                 \
-        const KeyRow kd = key_row<SEARCH>(QS, K, table, lane);                                    \
-        QS = load_raw(img, Hy, W, y + 4, x0, lane, vec);                                    \
-        uint32_t c0, c1;                                                                    \
-        c2_quad(ka, kb, kd, kBias, Sp0, Sp1, c0, c1);                                       \
-        hist_pair(kb.own0, c0, limit, hist);                                                \
-        hist_pair(kb.own1, c1, limit, hist);                                                \
-        ka = kb;                                                                            \
-        kb = kd;                                                                            \
-        ++y;                                                                                \
-    }
-        for (int y = y0; y < y1;) {
-            ECC_2D_STEP(q0)
-            ECC_2D_STEP(q1)
-            ECC_2D_STEP(q2)
-        }
-#undef ECC_2D_STEP
+    const int64_t N = (int64_t)P.tasks_x * Hy;  // strip-rows of the image
+    const int64_t G = (int64_t)P.ctas_per_image * kHardWarps;
+    const int64_t g = (int64_t)blockIdx.x * kHardWarps + warp;
+    int64_t i = N * g / G;
+    const int64_t iend = N * (g + 1) / G;
+    while (i < iend) {
+        const int strip = (int)(i / Hy);
+        const int y0 = (int)(i % Hy);
+        const int y1 = (int)min((int64_t)Hy, y0 + (iend - i));
+        band2d<T, SEARCH>(img, Hy, W, strip * kStrip, y0, y1, vec_ok, lane, q, K, table, hist);
+        i += y1 - y0;
     }
     block_flush(P, hist, b);
 }
@@ -317,72 +351,149 @@ __global__ void __launch_bounds__(kHardThreads, ECC_2D_MIN_BLOCKS) ecc_hard2d_ke
 // ----------------------------------------------------------------------------------------------
 //
 // Work: block task = (tile of 128 columns x 8 rows) x (chunk of rows_per_task planes), tile x
-// fastest, then tile y, then chunk. Warp w owns row y0 + w, lane l columns x0 + 4l .. x0 + 4l + 3.
+// fastest, then tile y, then chunk; block g of an image takes tasks g, g + G, ... Warp w owns row
+// y0 + w, lane l columns x0 + 4l .. x0 + 4l + 3.
 
 constexpr int kTileRows = kHardWarps;                // 8
 constexpr int kKeyPitch = 136;                       // halves per shared row (272 bytes)
 constexpr int kKeyRowsHalo = kTileRows + 2;          // rows y0-1 .. y0+8
 constexpr int kKeyPlane = kKeyRowsHalo * kKeyPitch;  // halves per plane buffer
 // Tile column c (-1 .. 128) sits at half index 4 + c of a shared row, so a lane's own four keys
-// form one 8-byte-aligned word pair.
+// form one 8-byte-aligned word pair and its outer neighbours sit in the 4-byte words before and
+// after it.
 
-// The raw values one thread needs for one plane of the tile: its warp's row around its columns
-// (with the two halo columns on lanes 0 / 31) and one value of the two halo rows (thread t: row
-// y0 - 1 or y0 + 8 by t >> 7, column x0 + (t & 127)); threads 0..3 also take the halo corners.
+// The raw values one thread needs for one plane of the tile: its warp's row (four columns), one
+// value of the two halo rows (thread t: row y0 - 1 or y0 + 8 by t >> 7, column x0 - 1 + (t & 127)),
+// and for warp 0 one "extra" value: lanes 0..7 the column left of rows y0 .. y0+7, lanes 8..15
+// the column right of them, lanes 16..19 the halo-row columns x0 + 127 and x0 + 128.
 template <typename T>
 struct PlaneRaw {
-    RawRow<T> own;
-    T hrow, corner;
-    bool hrow_in, corner_in;
+    Raw<T> own;    // own.side unused (always absent)
+    T hrow, extra;
+    bool hrow_ok, extra_ok;
 };
+
+struct PlaneCols {
+    Cols own;
+    int hy, hx;  // halo-row position of this thread (clamped)
+    bool h_ok;
+    int ey, ex;  // extra position (warp 0)
+    bool e_ok;
+    int hrow_half;   // shared index of the halo-row key
+    int extra_half;  // shared index of the extra key (or -1)
+};
+
+__device__ __forceinline__ PlaneCols plane_cols(int x0, int y0, int Hy, int W, int warp, int lane,
+                                                bool vec_ok)
+{
+    PlaneCols pc;
+    pc.own = strip_cols(x0, W, lane, vec_ok);
+    pc.own.side_ok = false;  // row halos come from the extra values
+    pc.own.sx = min(pc.own.x, W - 1);
+    const int t = threadIdx.x;
+    const int hr = t >> 7;  // 0: row y0 - 1, 1: row y0 + 8
+    const int hy = hr ? y0 + kTileRows : y0 - 1;
+    const int hx = x0 - 1 + (t & 127);
+    pc.h_ok = hy >= 0 && hy < Hy && hx >= 0 && hx < W;
+    pc.hy = min(max(hy, 0), Hy - 1);
+    pc.hx = min(max(hx, 0), W - 1);
+    pc.hrow_half = (hr ? kKeyRowsHalo - 1 : 0) * kKeyPitch + 4 + (t & 127) - 1;
+    int ey = 0, ex = 0, eh = -1;
+    if (warp == 0 && lane < 20) {
+        if (lane < 16) {
+            ey = y0 + (lane & 7);
+            ex = (lane < 8) ? x0 - 1 : x0 + kStrip;
+            eh = (1 + (lane & 7)) * kKeyPitch + ((lane < 8) ? 3 : 4 + kStrip);
+        } else {
+            const int j = lane - 16;  // (row, column): (y0-1, x0+127), (y0-1, x0+128), ...
+            ey = (j & 2) ? y0 + kTileRows : y0 - 1;
+            ex = x0 + kStrip - 1 + (j & 1);
+            eh = ((j & 2) ? kKeyRowsHalo - 1 : 0) * kKeyPitch + 4 + kStrip - 1 + (j & 1);
+        }
+    }
+    pc.e_ok = eh >= 0 && ey >= 0 && ey < Hy && ex >= 0 && ex < W;
+    pc.ey = min(max(ey, 0), Hy - 1);
+    pc.ex = min(max(ex, 0), W - 1);
+    pc.extra_half = eh;
+    return pc;
+}
 
 template <typename T>
 __device__ __forceinline__ PlaneRaw<T> load_plane(const T *__restrict__ img, int64_t D, int Hy,
-                                                  int W, int64_t z, int x0, int y0, bool vec_ok,
-                                                  int warp, int lane)
+                                                  int W, int64_t z, int y, const PlaneCols &pc,
+                                                  bool with_extra)
 {
     PlaneRaw<T> p;
     const bool zin = (z >= 0 && z < D);  // block-uniform
     const T *__restrict__ plane = img + (zin ? z : 0) * (int64_t)Hy * W;
-    const bool vec = vec_ok && (x0 + 128 <= W);
-    if (zin) {
-        p.own = load_raw(plane, Hy, W, y0 + warp, x0, lane, vec);
-    } else {
-        p.own.present = false;
-        p.own.halo_in = false;
-        p.own.valid = 0;
+    load_own(zin ? row_ptr(plane, y, Hy, W) : nullptr, pc.own, p.own);
+    const T h = __ldg(plane + (int64_t)pc.hy * W + pc.hx);
+    p.hrow = h;
+    p.hrow_ok = zin && pc.h_ok;
+    p.extra_ok = false;
+    p.extra = h;
+    if (with_extra) {  // warp-uniform (warp 0)
+        p.extra = __ldg(plane + (int64_t)pc.ey * W + pc.ex);
+        p.extra_ok = zin && pc.e_ok;
     }
-    const int t = threadIdx.x;
-    const int hy = (t >> 7) ? y0 + kTileRows : y0 - 1;
-    const int hx = x0 + (t & 127);
-    p.hrow_in = zin && hy >= 0 && hy < Hy && hx < W;
-    p.hrow = p.hrow_in ? plane[(int64_t)hy * W + hx] : (T)0;
-    const int cy = (t & 2) ? y0 + kTileRows : y0 - 1;
-    const int cx = (t & 1) ? x0 + 128 : x0 - 1;
-    p.corner_in = zin && t < 4 && cy >= 0 && cy < Hy && cx >= 0 && cx < W;
-    p.corner = p.corner_in ? plane[(int64_t)cy * W + cx] : (T)0;
     return p;
 }
 
-// Keys of a loaded plane into the shared buffer `dst` (uint16 patterns; absent outside the grid).
-template <bool SEARCH, typename T>
-__device__ __forceinline__ void store_plane_keys(const PlaneRaw<T> &p, const KeyConsts &K,
-                                                 const float *__restrict__ table, int warp,
-                                                 int lane, uint16_t *dst)
+// Key of one value (NaN / missing -> H).
+template <bool SEARCH>
+__device__ __forceinline__ uint32_t value_key(float v, bool ok, const KeyConsts &K,
+                                              const float *__restrict__ T, uint32_t &amb)
 {
-    uint32_t own0 = kAbsentPair, own1 = kAbsentPair, hk = kAbsentHalf;
-    if (p.own.present) raw_keys<SEARCH>(p.own, K, table, own0, own1, hk);  // warp-uniform branch
+    const float x = ok ? v : qnan_f();
+    if (SEARCH) return key_search_pattern(x, K.H, T);
+    return key_fast(x, K, amb);
+}
+
+// Keys of a loaded plane into the shared buffer `dst`.
+template <bool SEARCH>
+__device__ __forceinline__ void store_plane_keys(const PlaneRaw<float> &p, const PlaneCols &pc,
+                                                 const KeyConsts &K, const float *__restrict__ T,
+                                                 int warp, int lane, bool with_extra,
+                                                 uint16_t *dst)
+{
+    uint32_t k[7];
+    uint32_t amb = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) k[j] = value_key<SEARCH>(p.own.v[j], true, K, T, amb);
+    k[4] = value_key<SEARCH>(p.hrow, p.hrow_ok, K, T, amb);
+    k[5] = with_extra ? value_key<SEARCH>(p.extra, p.extra_ok, K, T, amb) : 0u;
+    if (!SEARCH && __any_sync(kFull, amb != 0)) {
+        if (amb != 0) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) k[j] = key_fix(p.own.v[j], k[j], K.H, T);
+            k[4] = key_fix(p.hrow_ok ? p.hrow : qnan_f(), k[4], K.H, T);
+            if (with_extra) k[5] = key_fix(p.extra_ok ? p.extra : qnan_f(), k[5], K.H, T);
+        }
+    }
+    uint16_t *row = dst + (1 + warp) * kKeyPitch;
+    *reinterpret_cast<uint2 *>(row + 4 + 4 * lane) =
+        make_uint2(prmt(k[0], k[1], 0x5410), prmt(k[2], k[3], 0x5410));
+    dst[pc.hrow_half] = (uint16_t)k[4];
+    if (with_extra && pc.extra_half >= 0) dst[pc.extra_half] = (uint16_t)k[5];
+}
+
+template <bool SEARCH>
+__device__ __forceinline__ void store_plane_keys(const PlaneRaw<uint8_t> &p, const PlaneCols &pc,
+                                                 const KeyConsts &K, const float *__restrict__ T,
+                                                 int warp, int lane, bool with_extra,
+                                                 uint16_t *dst)
+{
+    const uint16_t *lut = reinterpret_cast<const uint16_t *>(T);
+    const uint32_t never = kKeyBase + (uint32_t)K.H;
+    Raw<uint8_t> r = p.own;
+    r.side = 256u;  // no side value in the plane loads
+    uint32_t own0, own1, unused;
+    row_keys<SEARCH>(r, K, T, own0, own1, unused);
     uint16_t *row = dst + (1 + warp) * kKeyPitch;
     *reinterpret_cast<uint2 *>(row + 4 + 4 * lane) = make_uint2(own0, own1);
-    if (lane == 0) row[3] = (uint16_t)hk;
-    if (lane == kWarp - 1) row[4 + 128] = (uint16_t)hk;
-    const int t = threadIdx.x;
-    const uint32_t hkey = p.hrow_in ? key_one<SEARCH>(p.hrow, K, table) : kAbsentHalf;
-    dst[((t >> 7) ? kKeyRowsHalo - 1 : 0) * kKeyPitch + 4 + (t & 127)] = (uint16_t)hkey;
-    if (t < 4) {
-        const uint32_t ck = p.corner_in ? key_one<SEARCH>(p.corner, K, table) : kAbsentHalf;
-        dst[((t & 2) ? kKeyRowsHalo - 1 : 0) * kKeyPitch + ((t & 1) ? 4 + 128 : 3)] = (uint16_t)ck;
-    }
+    dst[pc.hrow_half] = (uint16_t)(p.hrow_ok ? (uint32_t)lut[p.hrow] : never);
+    if (with_extra && pc.extra_half >= 0)
+        dst[pc.extra_half] = (uint16_t)(p.extra_ok ? (uint32_t)lut[p.extra] : never);
 }
 
 // Buffer row r (= tile row r - 1, r = 0 .. 9) around the lane's four columns.
@@ -390,12 +501,12 @@ __device__ __forceinline__ KeyRow smem_key_row(const uint16_t *buf, int r, int l
 {
     const uint16_t *row = buf + r * kKeyPitch;
     const uint2 own = *reinterpret_cast<const uint2 *>(row + 4 + 4 * lane);
-    const uint32_t left = row[3 + 4 * lane];
-    const uint32_t right = row[8 + 4 * lane];
+    const uint32_t left = *reinterpret_cast<const uint32_t *>(row + 2 + 4 * lane);   // (x-2, x-1)
+    const uint32_t right = *reinterpret_cast<const uint32_t *>(row + 8 + 4 * lane);  // (x+4, x+5)
     KeyRow k;
     k.own0 = own.x;
     k.own1 = own.y;
-    k.L0 = prmt(left, own.x, 0x5410);
+    k.L0 = prmt(left, own.x, 0x5432);
     k.R0 = prmt(own.x, own.y, 0x5432);
     k.R1 = prmt(own.y, right, 0x5432);
     return k;
@@ -407,7 +518,7 @@ __global__ void __launch_bounds__(kHardThreads, ECC_3D_MIN_BLOCKS) ecc_hard3d_ke
 {
     extern __shared__ int smem[];
     int *hist = smem;
-    float *table = reinterpret_cast<float *>(smem + P.H);
+    float *table = reinterpret_cast<float *>(smem + hist_words(P.H));
     __shared__ __align__(16) uint16_t keybuf[2][kKeyPlane];
     block_setup(P, hist, table);
 
@@ -415,36 +526,36 @@ __global__ void __launch_bounds__(kHardThreads, ECC_3D_MIN_BLOCKS) ecc_hard3d_ke
     const T *__restrict__ img = static_cast<const T *>(P.img) + b * P.image_elems;
     const int lane = threadIdx.x & (kWarp - 1);
     const int warp = threadIdx.x >> 5;
+    const bool with_extra = (warp == 0);
     const int64_t Tn = P.tasks_per_image;
-    const int64_t t_begin = Tn * blockIdx.x / P.ctas_per_image;
-    const int64_t t_end = Tn * (blockIdx.x + 1) / P.ctas_per_image;
+    const int64_t G = P.ctas_per_image;
     const KeyConsts K = key_consts(P);
     const bool vec_ok = P.vec_ok != 0;
     const int64_t D = P.D;
     const int Hy = (int)P.Hy, W = (int)P.W;
-    const uint32_t limit = (kKeyBase + (uint32_t)P.H) * 0x10001u;
     const uint32_t kPlain = 0u;  // bias of the M stencil: plain c values
 
-    for (int64_t t = t_begin; t < t_end; ++t) {
+    for (int64_t t = blockIdx.x; t < Tn; t += G) {
         const int tx = (int)(t % P.tasks_x);
         const int64_t rest = t / P.tasks_x;
         const int ty = (int)(rest % P.tasks_y);
         const int64_t tz = rest / P.tasks_y;
-        const int x0 = tx * 128;
+        const int x0 = tx * kStrip;
         const int y0 = ty * kTileRows;
+        const int y = y0 + warp;  // this warp's row
         const int64_t z0 = tz * P.rows_per_task;
         const int64_t z1 = min(z0 + (int64_t)P.rows_per_task, D);
-        const bool row_in = (y0 + warp) < Hy;  // warp-uniform
+        const PlaneCols pc = plane_cols(x0, y0, Hy, W, warp, lane, vec_ok);
 
         // prologue: keys of planes z0 - 1 (buffer 0) and z0 (buffer 1); raw plane z0 + 1 in flight
         __syncthreads();  // the previous task's readers are done with both buffers
         {
-            const PlaneRaw<T> pm = load_plane<T>(img, D, Hy, W, z0 - 1, x0, y0, vec_ok, warp, lane);
-            const PlaneRaw<T> p0 = load_plane<T>(img, D, Hy, W, z0, x0, y0, vec_ok, warp, lane);
-            store_plane_keys<SEARCH>(pm, K, table, warp, lane, keybuf[0]);
-            store_plane_keys<SEARCH>(p0, K, table, warp, lane, keybuf[1]);
+            const PlaneRaw<T> pm = load_plane<T>(img, D, Hy, W, z0 - 1, y, pc, with_extra);
+            const PlaneRaw<T> p0 = load_plane<T>(img, D, Hy, W, z0, y, pc, with_extra);
+            store_plane_keys<SEARCH>(pm, pc, K, table, warp, lane, with_extra, keybuf[0]);
+            store_plane_keys<SEARCH>(p0, pc, K, table, warp, lane, with_extra, keybuf[1]);
         }
-        PlaneRaw<T> pnext = load_plane<T>(img, D, Hy, W, z0 + 1, x0, y0, vec_ok, warp, lane);
+        PlaneRaw<T> pnext = load_plane<T>(img, D, Hy, W, z0 + 1, y, pc, with_extra);
         __syncthreads();
         uint32_t cm0, cm1;        // c2(M_{z-1}) at the lane's pixels (plain values)
         uint32_t below0, below1;  // keys of plane z - 1 at the lane's pixels
@@ -468,31 +579,30 @@ __global__ void __launch_bounds__(kHardThreads, ECC_3D_MIN_BLOCKS) ecc_hard3d_ke
             // One barrier per plane: the buffer written here was last read in the step before
             // the previous one, and every warp has passed the previous step's barrier since.
             if (z == z0) __syncthreads();  // the prologue read buffer 0
-            store_plane_keys<SEARCH>(pnext, K, table, warp, lane, nbuf);
-            if (z + 2 <= z1) pnext = load_plane<T>(img, D, Hy, W, z + 2, x0, y0, vec_ok, warp, lane);
+            store_plane_keys<SEARCH>(pnext, pc, K, table, warp, lane, with_extra, nbuf);
+            if (z + 2 <= z1)  // block-uniform: the next plane is needed
+                pnext = load_plane<T>(img, D, Hy, W, z + 2, y, pc, with_extra);
             __syncthreads();
             const KeyRow na = smem_key_row(nbuf, warp, lane);
             const KeyRow nb = smem_key_row(nbuf, warp + 1, lane);
             const KeyRow nd = smem_key_row(nbuf, warp + 2, lane);
-            if (row_in) {
-                uint32_t s0, s1, cs0, cs1, cn0, cn1;
-                sp_init(ca, cb, s0, s1);
-                c2_quad(ca, cb, cd, kBias, s0, s1, cs0, cs1);
-                const KeyRow ma = max_rows(ca, na), mb = max_rows(cb, nb), md = max_rows(cd, nd);
-                sp_init(ma, mb, s0, s1);
-                c2_quad(ma, mb, md, kPlain, s0, s1, cn0, cn1);
-                // c = cS - [k_{z+1} < k_z] c2(M_z) - [k_{z-1} <= k_z] c2(M_{z-1})
-                const uint32_t up0 = h2_lt_mask(nb.own0, cb.own0);
-                const uint32_t up1 = h2_lt_mask(nb.own1, cb.own1);
-                const uint32_t dn0 = h2_le_mask(below0, cb.own0);
-                const uint32_t dn1 = h2_le_mask(below1, cb.own1);
-                const uint32_t c0 = h2_sub(h2_sub(cs0, cn0 & up0), cm0 & dn0);
-                const uint32_t c1 = h2_sub(h2_sub(cs1, cn1 & up1), cm1 & dn1);
-                hist_pair(cb.own0, c0, limit, hist);
-                hist_pair(cb.own1, c1, limit, hist);
-                cm0 = cn0;
-                cm1 = cn1;
-            }
+            uint32_t s0, s1, cs0, cs1, cn0, cn1;
+            sp_init(ca, cb, s0, s1);
+            c2_quad(ca, cb, cd, kBias, s0, s1, cs0, cs1);
+            const KeyRow ma = max_rows(ca, na), mb = max_rows(cb, nb), md = max_rows(cd, nd);
+            sp_init(ma, mb, s0, s1);
+            c2_quad(ma, mb, md, kPlain, s0, s1, cn0, cn1);
+            // c = cS - [k_{z+1} < k_z] c2(M_z) - [k_{z-1} <= k_z] c2(M_{z-1})
+            const uint32_t up0 = h2_lt_mask(nb.own0, cb.own0);
+            const uint32_t up1 = h2_lt_mask(nb.own1, cb.own1);
+            const uint32_t dn0 = h2_le_mask(below0, cb.own0);
+            const uint32_t dn1 = h2_le_mask(below1, cb.own1);
+            const uint32_t c0 = h2_sub(h2_sub(cs0, cn0 & up0), cm0 & dn0);
+            const uint32_t c1 = h2_sub(h2_sub(cs1, cn1 & up1), cm1 & dn1);
+            hist_pair(cb.own0, c0, hist);
+            hist_pair(cb.own1, c1, hist);
+            cm0 = cn0;
+            cm1 = cn1;
             below0 = cb.own0;
             below1 = cb.own1;
             ca = na;
@@ -557,6 +667,27 @@ static int num_sms()
     return n;
 }
 
+// Planes per 3-D block task: the power of two from 32 up that maximises the useful fraction of
+// the block time -- tasks shared evenly over the blocks (the busiest block sets the time) times
+// R / (R + 2) for the two prologue planes of each task.
+static int64_t pick_chunk(int64_t D, int64_t tiles, int64_t blocks)
+{
+    int64_t best = 32;
+    double best_eff = -1.0;
+    for (int64_t R = 32;; R *= 2) {
+        const int64_t tasks = tiles * ((D + R - 1) / R);
+        const double per = (double)tasks / (double)blocks;
+        const double busiest = (double)((tasks + blocks - 1) / blocks);
+        const double eff = (per / busiest) * ((double)R / (double)(R + 2));
+        if (eff > best_eff + 1e-9) {
+            best_eff = eff;
+            best = R;
+        }
+        if (R >= D) break;
+    }
+    return best;
+}
+
 template <typename T, int CAP, bool SEARCH>
 static cudaError_t launch_hard(const HardPlan &pl, cudaStream_t s)
 {
@@ -569,9 +700,10 @@ static cudaError_t launch_hard(const HardPlan &pl, cudaStream_t s)
     P.image_elems = pl.D * pl.Hy * pl.W;
     P.H = pl.H;
     P.key_mode = pl.key_mode;
-    P.scale = pl.scale;
-    P.offset = pl.offset;
-    P.key_err = pl.key_err;
+    P.key_a = pl.key_a;
+    P.key_b = pl.key_b;
+    P.key_clo = pl.key_clo;
+    P.key_chi = pl.key_chi;
     P.vec_ok = pl.vec_ok;
     const int ntab = (pl.dtype == ECC_U8) ? 128 : pl.H + 2;  // u8: 256 uint16 in 128 floats
     P.table_len = ntab;
@@ -579,39 +711,39 @@ static cudaError_t launch_hard(const HardPlan &pl, cudaStream_t s)
     for (int i = ntab; i < CAP + 2; ++i) P.table[i] = 0.0f;
 
     const int sms = num_sms();
-    const int64_t strips = (pl.W + 127) / 128;
+    const int64_t strips = (pl.W + kStrip - 1) / kStrip;
     const int per_sm = pl.ndim == 2 ? ECC_2D_MIN_BLOCKS : ECC_3D_MIN_BLOCKS;
-    const int64_t resident = (int64_t)sms * per_sm;
+    const int64_t resident = (int64_t)sms * per_sm;  // blocks that fit at once
+    // blocks per image: the resident blocks shared out over the batch
+    int64_t per_image = (resident + pl.batch - 1) / pl.batch;
     if (pl.ndim == 2) {
-        // rows per warp task: 8, or more for very large batches (at most ~64 K tasks per warp
-        // slot keeps the task loop short); small tasks keep the warps of a block balanced
-        int64_t R = 8;
-        while (R < 256 && pl.Hy * strips * pl.batch / R > resident * kHardWarps * 64) R *= 2;
-        P.rows_per_task = (int)R;
+        // contiguous strip-row ranges, at least 32 rows per warp
+        const int64_t N = strips * pl.Hy;
+        const int64_t need = (N + 32 * kHardWarps - 1) / (32 * kHardWarps);
+        if (per_image > need) per_image = need;
+        P.rows_per_task = 0;
         P.tasks_x = (int)strips;
-        P.tasks_y = (int)((pl.Hy + R - 1) / R);
+        P.tasks_y = (int)pl.Hy;
         P.tasks_z = 1;
+        P.tasks_per_image = N;
     } else {
-        // planes per block task: aim at ~8 tasks per resident block, at least 16 planes each
         const int64_t tiles_y = (pl.Hy + kTileRows - 1) / kTileRows;
-        const int64_t tiles = strips * tiles_y * pl.batch;
-        const int64_t want = (pl.D * tiles + resident * 8 - 1) / (resident * 8);
-        const int64_t R = want < 16 ? 16 : (want > 256 ? 256 : want);
+        const int64_t tiles = strips * tiles_y;
+        if (per_image > tiles * pl.D) per_image = tiles * pl.D;
+        const int64_t R = pick_chunk(pl.D, tiles, per_image);
         P.rows_per_task = (int)R;
         P.tasks_x = (int)strips;
         P.tasks_y = (int)tiles_y;
         P.tasks_z = (int)((pl.D + R - 1) / R);
+        P.tasks_per_image = (int64_t)P.tasks_x * P.tasks_y * P.tasks_z;
+        if (per_image > P.tasks_per_image) per_image = P.tasks_per_image;
     }
-    P.tasks_per_image = (int64_t)P.tasks_x * P.tasks_y * P.tasks_z;
-    int64_t per_image_ctas = (resident + pl.batch - 1) / pl.batch;
-    const int64_t max_ctas = pl.ndim == 2 ? (P.tasks_per_image + kHardWarps - 1) / kHardWarps
-                                          : P.tasks_per_image;
-    if (per_image_ctas > max_ctas) per_image_ctas = max_ctas;
-    if (per_image_ctas < 1) per_image_ctas = 1;
-    P.ctas_per_image = (int)per_image_ctas;
+    if (per_image < 1) per_image = 1;
+    P.ctas_per_image = (int)per_image;
 
-    const size_t smem = (size_t)pl.H * sizeof(int) + (size_t)(CAP + 2) * sizeof(float);
-    dim3 grid((unsigned)per_image_ctas, (unsigned)pl.batch);
+    const size_t smem =
+        (size_t)hist_words(pl.H) * sizeof(int) + (size_t)(CAP + 2) * sizeof(float);
+    dim3 grid((unsigned)per_image, (unsigned)pl.batch);
     if (pl.ndim == 2) {
         ecc_hard2d_kernel<T, CAP, SEARCH><<<grid, kHardThreads, smem, s>>>(P);
     } else {

@@ -44,11 +44,12 @@ struct HardParams {
     int H;
     int table_len;  // entries of table[] in use
     int key_mode;
-    float scale, offset;  // estimator: t = H * sat(v * scale + offset)
-    float key_err;        // bound on |t - exact| in bins
-    int vec_ok;           // rows 16-byte (f32) / 4-byte (u8) aligned and W % 4 == 0
-    // work decomposition
-    int rows_per_task;    // 2-D: rows per warp task; 3-D: planes per CTA task
+    float key_a, key_b;      // estimator u = sat(v a + b), t = (H - 1/2) - H u
+    float key_clo, key_chi;  // (H - 1/2) -+ E, E bounding |t - exact fractional bin|
+    int vec_ok;              // rows 16-byte (f32) / 4-byte (u8) aligned and W % 4 == 0
+    // work decomposition: tasks are numbered band-major (the 128-column strip or tile fastest),
+    // and warp (2-D) / block (3-D) g of an image takes tasks g, g + G, g + 2G, ...
+    int rows_per_task;  // 2-D: rows per warp task; 3-D: planes per block task
     int tasks_x, tasks_y, tasks_z;
     int64_t tasks_per_image;
     int ctas_per_image;
@@ -65,7 +66,7 @@ struct HardPlan {
     int64_t D, Hy, W, batch;
     int H;
     int key_mode;
-    float scale, offset, key_err;
+    float key_a, key_b, key_clo, key_chi;
     int vec_ok;
     const void *img;
     int64_t *out;

@@ -7,9 +7,13 @@
 // Every voxel first gets its exact threshold key k = #{j : t_j < v} (nbins = "never"). The order
 // by (key, linear index) refines the bin order, so the vertex-centric decomposition is exact on
 // keys. A key is stored as the fp16 bit pattern 0x6400 + k, which is finite, strictly increasing
-// in k for k <= 6143, and compares correctly with fp16 comparisons; voxels outside the grid carry
-// +inf (0x7C00), which is never earlier than anything. Two keys share one 32-bit register
-// (half2), so each comparison, logic and add instruction below serves two pixels.
+// in k for k <= 6143, and compares correctly with fp16 comparisons. Two keys share one 32-bit
+// register (half2), so each comparison, logic and add instruction below serves two pixels.
+//
+// Positions outside the grid take the key H ("never enters"), the key of a NaN value: for every
+// voxel whose key is below H such a neighbour is never earlier, exactly like a missing vertex
+// (the cells through it never enter), and the contributions of voxels with key H are discarded.
+// So the kernels read NaN for every position outside the grid and need no boundary branches.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -18,42 +22,44 @@
 
 namespace ecc {
 
+constexpr int kWarpLanes = 32;
 constexpr uint32_t kKeyBase = 0x6400u;      // fp16 pattern of key 0 (the value 1024.0)
-constexpr uint32_t kAbsentHalf = 0x7C00u;   // fp16 +inf: outside the grid
-constexpr uint32_t kAbsentPair = 0x7C007C00u;
-constexpr float kMagic = 12582912.0f;       // 1.5 * 2^23: adding it (rounding up) gives ceil
-constexpr uint32_t kMagicBits = 0x4B400000u;
+// 1.5 * 2^23 + 0x6400: adding a value t in (-2^22, 2^22) with rounding up gives the float whose
+// bit pattern is kMagicKeyBits + ceil(t), so its low 16 bits are the fp16 key pattern of ceil(t).
+constexpr float kMagicKey = 12608512.0f;
+constexpr uint32_t kMagicKeyBits = 0x4B406400u;
 
-// Estimator constants for float32 keys (host-computed, see ecc_api.cu):
-//   t = H * sat(v * sH + oH)  approximates clamp((v - vmin) (H - 1) / (vmax - vmin), 0, H),
-//   with |t - exact| <= E (bins), E <= 1/4. The key is ceil(exact), so when
-//   ceil(t - E) == ceil(t + E) that value is the key; otherwise the table decides.
+// Estimator constants for float32 keys (host-computed, see ecc_api.cu). With the fractional bin
+// t* = (v - vmin) (H - 1) / (vmax - vmin) (key = ceil(t*) clamped to [0, H]) the kernels compute
+//     u = sat(v a + b) = sat((H - 1/2 - t*) / H),   t = H - 1/2 - H u,
+// so t = t* up to a rounding error below E (E <= 1/4), saturated values land on t = -1/2 (key 0)
+// or t = H - 1/2 (key H), and NaN, which saturates to u = 0, gets key H ("never enters").
+// ceil(t - E) == ceil(t + E) proves the key; otherwise the threshold table decides.
 struct KeyConsts {
-    float sH, oH, Hf, E;
+    float a, b;      // u = sat(v a + b)
+    float nH;        // -H
+    float clo, chi;  // H - 1/2 - E, H - 1/2 + E
     int H;
-    bool search;  // estimator unusable (degenerate range): binary-search every value
 };
 
-// Fast part of the key: returns the fp16 pattern of ceil(t - E) and accumulates, into `amb`,
-// (ceil(t + E) - ceil(t - E)), which is non-zero when the estimate is ambiguous (also for NaN,
-// +-inf and values sitting exactly on a threshold).
-__device__ __forceinline__ uint32_t key_fast(float v, const KeyConsts &K, float &amb)
+// Fast key of one value: returns bits whose low half is the fp16 pattern of ceil(t - E), and ORs
+// into `amb` a non-zero value when ceil(t + E) differs (the estimate is then ambiguous).
+__device__ __forceinline__ uint32_t key_fast(float v, const KeyConsts &K, uint32_t &amb)
 {
-    const float u = __saturatef(fmaf(v, K.sH, K.oH));
-    const float t = u * K.Hf;
-    const float lo = __fadd_ru(t - K.E, kMagic);
-    const float hi = __fadd_ru(t + K.E, kMagic);
-    amb += hi - lo;
-    return __float_as_uint(lo) - (kMagicBits - kKeyBase);
+    const float u = __saturatef(fmaf(v, K.a, K.b));
+    const float lo = __fadd_ru(fmaf(u, K.nH, K.clo), kMagicKey);
+    const float hi = __fadd_ru(fmaf(u, K.nH, K.chi), kMagicKey);
+    amb |= __float_as_uint(lo) ^ __float_as_uint(hi);
+    return __float_as_uint(lo);
 }
 
-// Exact key for one value given its fast estimate `hb` = kKeyBase + ceil(t - E): the key is that
-// or one more, decided by the rounded-down fp32 threshold table T (T[H] = +inf). NaN -> H.
-__device__ __forceinline__ uint32_t key_fix(float v, uint32_t hb, const KeyConsts &K,
+// Exact key given the fast estimate `lo_bits` (any value whose estimate window holds the key):
+// the key is lo or lo + 1, decided by the rounded-down fp32 threshold table T (T[H] = +inf).
+// Correct for unambiguous values too (then v <= T[lo]); NaN estimates lo = H and stays there.
+__device__ __forceinline__ uint32_t key_fix(float v, uint32_t lo_bits, int H,
                                            const float *__restrict__ T)
 {
-    if (v != v) return kKeyBase + (uint32_t)K.H;
-    const int lo = min((int)(hb - kKeyBase), K.H);
+    const int lo = min((int)(lo_bits & 0xffffu) - (int)kKeyBase, H);
     return kKeyBase + (uint32_t)(lo + (v > T[lo] ? 1 : 0));
 }
 
@@ -119,28 +125,39 @@ struct KeyRow {
     uint32_t own0, own1, L0, R0, R1;
 };
 
-// Builds the shifted pairs from the lane's own pairs and its neighbours' (whole-warp call).
-// left_hi: fp16 pattern of k[x-1] for lane 0 (halo), right_lo: of k[x+4] for lane 31.
-__device__ __forceinline__ KeyRow make_key_row(uint32_t own0, uint32_t own1, int lane,
-                                               uint32_t left_halo, uint32_t right_halo)
+// Lane constants for building rows with two shuffles. The keys just outside a warp's 128-column
+// strip travel on the rotated shuffles: lane 31 carries the key left of the strip (column x0 - 1)
+// into lane 0, and lane 0 carries the key right of it (column x0 + 128) into lane 31.
+struct LaneShuffle {
+    int src_l, src_r;    // lane - 1 and lane + 1, modulo 32
+    uint32_t sel_l, sel_r;  // byte selectors that splice the side key into the published word
+};
+
+__device__ __forceinline__ LaneShuffle lane_shuffle(int lane)
 {
+    LaneShuffle q;
+    q.src_l = (lane + kWarpLanes - 1) & (kWarpLanes - 1);
+    q.src_r = (lane + 1) & (kWarpLanes - 1);
+    q.sel_l = (lane == kWarpLanes - 1) ? 0x5410u : 0x3210u;  // lane 31: side key in the high half
+    q.sel_r = (lane == 0) ? 0x3254u : 0x3210u;               // lane 0: side key in the low half
+    return q;
+}
+
+// A lane's row from its own pairs and its side key (low half of `side`; lane 0: column x0 + 128,
+// lane 31: column x0 - 1, other lanes: ignored). Whole-warp call.
+__device__ __forceinline__ KeyRow make_key_row(uint32_t own0, uint32_t own1, uint32_t side,
+                                               const LaneShuffle &q)
+{
+    const uint32_t pub_l = prmt(own1, side, q.sel_l);
+    const uint32_t pub_r = prmt(own0, side, q.sel_r);
+    const uint32_t left = __shfl_sync(0xffffffffu, pub_l, q.src_l);   // (k[x-2], k[x-1])
+    const uint32_t right = __shfl_sync(0xffffffffu, pub_r, q.src_r);  // (k[x+4], k[x+5])
     KeyRow r;
     r.own0 = own0;
     r.own1 = own1;
-    uint32_t left = __shfl_up_sync(0xffffffffu, own1, 1);   // neighbour's (k[x-2], k[x-1])
-    uint32_t right = __shfl_down_sync(0xffffffffu, own0, 1);  // neighbour's (k[x+4], k[x+5])
-    if (lane == 0) left = left_halo << 16;
-    if (lane == 31) right = right_halo;
     r.L0 = prmt(left, own0, 0x5432);
     r.R0 = prmt(own0, own1, 0x5432);
     r.R1 = prmt(own1, right, 0x5432);
-    return r;
-}
-
-__device__ __forceinline__ KeyRow absent_row()
-{
-    KeyRow r;
-    r.own0 = r.own1 = r.L0 = r.R0 = r.R1 = kAbsentPair;
     return r;
 }
 
@@ -239,24 +256,16 @@ __device__ __forceinline__ int sext_byte2(uint32_t x)
     return (int)d;
 }
 
-// Adds the contributions of one pair to the block histogram: pixel keys `keys` (fp16 patterns),
-// values `cv` = 1280 + c. Pixels with c = 0, with key >= H ("never") or outside the grid (key
-// pattern +inf) add nothing.
-__device__ __forceinline__ void hist_pair(uint32_t keys, uint32_t cv, uint32_t key_limit_pair,
-                                          int *hist)
+// Adds the contributions of one pair to the block histogram `hist` (H + 1 bins): pixel key
+// patterns `keys`, values `cv` = 1280 + c. Pixels whose key is H ("never") land in the unused bin
+// hist[H]; pixels with c = 0 add nothing.
+__device__ __forceinline__ void hist_pair(uint32_t keys, uint32_t cv, int *hist)
 {
-    uint32_t live;
-    asm("{\n\t.reg .b32 m1, m2;\n\t"
-        "set.ne.u32.f16x2 m1, %1, %2;\n\t"
-        "set.lt.u32.f16x2 m2, %3, %4;\n\t"
-        "and.b32 %0, m1, m2;\n\t}"
-        : "=r"(live)
-        : "r"(cv), "r"(kBias), "r"(keys), "r"(key_limit_pair));
-    int *const a0 = hist + ((int)(keys & 0xffffu) - (int)kKeyBase);
-    int *const a1 = hist + ((int)(keys >> 16) - (int)kKeyBase);
     const int v0 = sext_byte0(cv), v1 = sext_byte2(cv);
-    if (live & 0xffffu) atomicAdd(a0, v0);
-    if (live & 0xffff0000u) atomicAdd(a1, v1);
+    const int k0 = (int)(keys & 0xffffu) - (int)kKeyBase;
+    const int k1 = (int)(keys >> 16) - (int)kKeyBase;
+    if (v0 != 0) atomicAdd(hist + k0, v0);
+    if (v1 != 0) atomicAdd(hist + k1, v1);
 }
 
 }  // namespace ecc
