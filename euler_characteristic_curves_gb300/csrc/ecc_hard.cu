@@ -274,21 +274,116 @@ __device__ __forceinline__ KeyRow key_row(const Raw<T> &r, const KeyConsts &K,
     return make_key_row(own0, own1, side, q);
 }
 
-// One band: rows y0 .. y1 - 1 of the strip at x0.
-template <typename T, bool SEARCH>
-__device__ __forceinline__ void band2d(const T *__restrict__ img, int Hy, int W, int x0, int y0,
-                                       int y1, bool vec_ok, int lane, const LaneShuffle &q,
-                                       const KeyConsts &K, const float *__restrict__ table,
-                                       int *hist)
+// Predicated loads (no branch): the value at p when ok, else the given default.
+__device__ __forceinline__ float ldg_if(const float *p, bool ok, float dflt)
 {
-    const Cols c = strip_cols(x0, W, lane, vec_ok);
-    const int ylim = min(y1 + 1, Hy);  // rows that exist and are needed (the band and the row below)
+    float v = dflt;
+    asm("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q ld.global.nc.f32 %0, [%1];\n\t}"
+        : "+f"(v)
+        : "l"(p), "r"((unsigned)ok));
+    return v;
+}
+__device__ __forceinline__ uint32_t ldg_if(const uint8_t *p, bool ok, uint32_t dflt)
+{
+    uint32_t v = dflt;
+    asm("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q ld.global.nc.u8 %0, [%1];\n\t}"
+        : "+r"(v)
+        : "l"(p), "r"((unsigned)ok));
+    return v;
+}
+
+// Rows of one band as a lane reads them: its own columns and its side column, one row after
+// the other; rows before 0 and from `rlim` on read as absent.
+template <typename T>
+struct RowCursor {
+    const T *own;   // the lane's first column in row r
+    const T *side;  // the lane's side column in row r
+    int r, rlim;
+    int W;
+};
+
+template <typename T>
+__device__ __forceinline__ RowCursor<T> row_cursor(const T *__restrict__ img, const Cols &c, int r0,
+                                                   int rlim, int W)
+{
+    RowCursor<T> rc;
+    rc.own = img + (int64_t)r0 * W + c.x;
+    rc.side = img + (int64_t)r0 * W + c.sx;
+    rc.r = r0;
+    rc.rlim = rlim;
+    rc.W = W;
+    return rc;
+}
+
+template <bool FULL>
+__device__ __forceinline__ Raw<float> next_row(RowCursor<float> &rc, const Cols &c)
+{
+    Raw<float> out;
+    if ((unsigned)rc.r < (unsigned)rc.rlim) {  // warp-uniform
+        if (FULL) {
+            const float4 q = __ldg(reinterpret_cast<const float4 *>(rc.own));
+            out.v[0] = q.x;
+            out.v[1] = q.y;
+            out.v[2] = q.z;
+            out.v[3] = q.w;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                out.v[j] = ldg_if(rc.own + j, (c.own_ok >> j) & 1u, qnan_f());
+        }
+        out.side = ldg_if(rc.side, c.side_ok, qnan_f());
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) out.v[j] = qnan_f();
+        out.side = qnan_f();
+    }
+    rc.own += rc.W;
+    rc.side += rc.W;
+    ++rc.r;
+    return out;
+}
+
+template <bool FULL>
+__device__ __forceinline__ Raw<uint8_t> next_row(RowCursor<uint8_t> &rc, const Cols &c)
+{
+    Raw<uint8_t> out;
+    if ((unsigned)rc.r < (unsigned)rc.rlim) {  // warp-uniform
+        if (FULL) {
+            out.bytes = __ldg(reinterpret_cast<const unsigned int *>(rc.own));
+        } else {
+            out.bytes = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                out.bytes |= ldg_if(rc.own + j, (c.own_ok >> j) & 1u, 0u) << (8 * j);
+        }
+        out.own_ok = c.own_ok;
+        out.side = ldg_if(rc.side, c.side_ok, 256u);
+    } else {
+        out.bytes = 0;
+        out.own_ok = 0;
+        out.side = 256u;
+    }
+    rc.own += rc.W;
+    rc.side += rc.W;
+    ++rc.r;
+    return out;
+}
+
+// One band: rows y0 .. y1 - 1 of the strip at x0 (FULL: all 128 columns exist and rows are
+// 16-byte / 4-byte aligned, so each lane reads its four values with one load).
+template <typename T, bool SEARCH, bool FULL>
+__device__ __forceinline__ void band2d(const T *__restrict__ img, int Hy, int W, const Cols &c,
+                                       int y0, int y1, const LaneShuffle &q, const KeyConsts &K,
+                                       const float *__restrict__ table, uint32_t hist_s)
+{
+    // rows y0 - 1 .. y1 exist-or-absent; later rows (prefetch overshoot) read as absent
+    RowCursor<T> rc = row_cursor(img, c, y0 - 1, min(y1 + 1, Hy), W);
+    KeyRow ka = key_row<T, SEARCH>(next_row<FULL>(rc, c), K, table, q);
+    KeyRow kb = key_row<T, SEARCH>(next_row<FULL>(rc, c), K, table, q);
     // raw-row ring: at the start of step y, q0 / q1 / q2 (in rotation) hold rows y+1 .. y+3
-    Raw<T> q0 = load_row(row_ptr(img, y0 + 1, ylim, W), c);
-    Raw<T> q1 = load_row(row_ptr(img, y0 + 2, ylim, W), c);
-    Raw<T> q2 = load_row(row_ptr(img, y0 + 3, ylim, W), c);
-    KeyRow ka = key_row<T, SEARCH>(load_row(row_ptr(img, y0 - 1, Hy, W), c), K, table, q);
-    KeyRow kb = key_row<T, SEARCH>(load_row(row_ptr(img, y0, Hy, W), c), K, table, q);
+    Raw<T> q0 = next_row<FULL>(rc, c);
+    Raw<T> q1 = next_row<FULL>(rc, c);
+    Raw<T> q2 = next_row<FULL>(rc, c);
     uint32_t Sp0, Sp1;
     sp_init(ka, kb, Sp0, Sp1);
 
@@ -296,11 +391,11 @@ __device__ __forceinline__ void band2d(const T *__restrict__ img, int Hy, int W,
     {                                                                                       \
         if (y >= y1) break;                                                                 \
         const KeyRow kd = key_row<T, SEARCH>(QS, K, table, q);                              \
-        QS = load_row(row_ptr(img, y + 4, ylim, W), c);                                     \
+        QS = next_row<FULL>(rc, c);                                                         \
         uint32_t c0, c1;                                                                    \
         c2_quad(ka, kb, kd, kBias, Sp0, Sp1, c0, c1);                                       \
-        hist_pair(kb.own0, c0, hist);                                                       \
-        hist_pair(kb.own1, c1, hist);                                                       \
+        hist_pair(kb.own0, c0, hist_s);                                            \
+        hist_pair(kb.own1, c1, hist_s);                                            \
         ka = kb;                                                                            \
         kb = kd;                                                                            \
         ++y;                                                                                \
@@ -330,18 +425,24 @@ __global__ void __launch_bounds__(kHardThreads, ECC_2D_MIN_BLOCKS) ecc_hard2d_ke
     const LaneShuffle q = lane_shuffle(lane);
     const int Hy = (int)P.Hy, W = (int)P.W;
     const bool vec_ok = P.vec_ok != 0;
+    const uint32_t hist_s = (uint32_t)__cvta_generic_to_shared(hist) - 4u * kKeyBase;
 
-    const int64_t N = (int64_t)P.tasks_x * Hy;  // strip-rows of the image
-    const int64_t G = (int64_t)P.ctas_per_image * kHardWarps;
-    const int64_t g = (int64_t)blockIdx.x * kHardWarps + warp;
-    int64_t i = N * g / G;
-    const int64_t iend = N * (g + 1) / G;
+    // this warp's strip-rows [i, iend): warp g gets rows_per_task consecutive strip-rows
+    // (strip-major), one more for the first rows_extra warps
+    const uint32_t g = blockIdx.x * kHardWarps + warp;
+    const uint32_t per = (uint32_t)P.rows_per_task, extra = (uint32_t)P.rows_extra;
+    uint32_t i = g * per + min(g, extra);
+    const uint32_t iend = i + per + (g < extra ? 1u : 0u);
     while (i < iend) {
-        const int strip = (int)(i / Hy);
-        const int y0 = (int)(i % Hy);
-        const int y1 = (int)min((int64_t)Hy, y0 + (iend - i));
-        band2d<T, SEARCH>(img, Hy, W, strip * kStrip, y0, y1, vec_ok, lane, q, K, table, hist);
-        i += y1 - y0;
+        const int strip = (int)(i / (uint32_t)Hy);
+        const int y0 = (int)(i - (uint32_t)strip * (uint32_t)Hy);
+        const int y1 = min(Hy, y0 + (int)(iend - i));
+        const Cols c = strip_cols(strip * kStrip, W, lane, vec_ok);
+        if (c.full)  // warp-uniform
+            band2d<T, SEARCH, true>(img, Hy, W, c, y0, y1, q, K, table, hist_s);
+        else
+            band2d<T, SEARCH, false>(img, Hy, W, c, y0, y1, q, K, table, hist_s);
+        i += (uint32_t)(y1 - y0);
     }
     block_flush(P, hist, b);
 }
@@ -534,6 +635,7 @@ __global__ void __launch_bounds__(kHardThreads, ECC_3D_MIN_BLOCKS) ecc_hard3d_ke
     const int64_t D = P.D;
     const int Hy = (int)P.Hy, W = (int)P.W;
     const uint32_t kPlain = 0u;  // bias of the M stencil: plain c values
+    const uint32_t hist_s = (uint32_t)__cvta_generic_to_shared(hist) - 4u * kKeyBase;
 
     for (int64_t t = blockIdx.x; t < Tn; t += G) {
         const int tx = (int)(t % P.tasks_x);
@@ -599,8 +701,8 @@ __global__ void __launch_bounds__(kHardThreads, ECC_3D_MIN_BLOCKS) ecc_hard3d_ke
             const uint32_t dn1 = h2_le_mask(below1, cb.own1);
             const uint32_t c0 = h2_sub(h2_sub(cs0, cn0 & up0), cm0 & dn0);
             const uint32_t c1 = h2_sub(h2_sub(cs1, cn1 & up1), cm1 & dn1);
-            hist_pair(cb.own0, c0, hist);
-            hist_pair(cb.own1, c1, hist);
+            hist_pair(cb.own0, c0, hist_s);
+            hist_pair(cb.own1, c1, hist_s);
             cm0 = cn0;
             cm1 = cn1;
             below0 = cb.own0;
@@ -719,9 +821,13 @@ static cudaError_t launch_hard(const HardPlan &pl, cudaStream_t s)
     if (pl.ndim == 2) {
         // contiguous strip-row ranges, at least 32 rows per warp
         const int64_t N = strips * pl.Hy;
+        if (N >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;  // 32-bit row arithmetic
         const int64_t need = (N + 32 * kHardWarps - 1) / (32 * kHardWarps);
         if (per_image > need) per_image = need;
-        P.rows_per_task = 0;
+        if (per_image < 1) per_image = 1;
+        const int64_t G = per_image * kHardWarps;
+        P.rows_per_task = (int)(N / G);
+        P.rows_extra = (int)(N % G);
         P.tasks_x = (int)strips;
         P.tasks_y = (int)pl.Hy;
         P.tasks_z = 1;

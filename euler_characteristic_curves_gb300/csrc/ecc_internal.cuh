@@ -47,9 +47,11 @@ struct HardParams {
     float key_a, key_b;      // estimator u = sat(v a + b), t = (H - 1/2) - H u
     float key_clo, key_chi;  // (H - 1/2) -+ E, E bounding |t - exact fractional bin|
     int vec_ok;              // rows 16-byte (f32) / 4-byte (u8) aligned and W % 4 == 0
-    // work decomposition: tasks are numbered band-major (the 128-column strip or tile fastest),
-    // and warp (2-D) / block (3-D) g of an image takes tasks g, g + G, g + 2G, ...
-    int rows_per_task;  // 2-D: rows per warp task; 3-D: planes per block task
+    // work decomposition. 2-D: warp g of an image takes rows_per_task consecutive strip-rows
+    // (one more for the first rows_extra warps); 3-D: tasks are numbered tile-major and block g
+    // takes tasks g, g + G, g + 2G, ...
+    int rows_per_task;  // 2-D: strip-rows per warp; 3-D: planes per block task
+    int rows_extra;
     int tasks_x, tasks_y, tasks_z;
     int64_t tasks_per_image;
     int ctas_per_image;
