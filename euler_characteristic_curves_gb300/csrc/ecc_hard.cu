@@ -131,78 +131,6 @@ __device__ __forceinline__ Cols strip_cols(int x0, int W, int lane, bool vec_ok)
     return c;
 }
 
-// Loads a lane's four values of one row (row pointer `row`, or nullptr when the row is outside
-// the grid); positions outside the grid read as NaN (f32) or are cleared from own_ok (u8).
-__device__ __forceinline__ void load_own(const float *__restrict__ row, const Cols &c,
-                                         Raw<float> &r)
-{
-    if (row == nullptr) {  // warp-uniform
-#pragma unroll
-        for (int j = 0; j < 4; ++j) r.v[j] = qnan_f();
-        return;
-    }
-    if (c.full) {  // warp-uniform
-        const float4 q = __ldg(reinterpret_cast<const float4 *>(row + c.x));
-        r.v[0] = q.x;
-        r.v[1] = q.y;
-        r.v[2] = q.z;
-        r.v[3] = q.w;
-    } else {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const bool in = (c.own_ok >> j) & 1u;
-            const float v = __ldg(row + (in ? c.x + j : 0));
-            r.v[j] = in ? v : qnan_f();
-        }
-    }
-}
-
-__device__ __forceinline__ void load_own(const uint8_t *__restrict__ row, const Cols &c,
-                                         Raw<uint8_t> &r)
-{
-    if (row == nullptr) {
-        r.bytes = 0;
-        r.own_ok = 0;
-        return;
-    }
-    if (c.full) {
-        r.bytes = __ldg(reinterpret_cast<const unsigned int *>(row + c.x));
-    } else {
-        r.bytes = 0;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const bool in = (c.own_ok >> j) & 1u;
-            const uint32_t v = __ldg(row + (in ? c.x + j : 0));
-            r.bytes |= in ? (v << (8 * j)) : 0u;
-        }
-    }
-    r.own_ok = c.own_ok;
-}
-
-__device__ __forceinline__ void side_value(const float *__restrict__ row, const Cols &c,
-                                           Raw<float> &r)
-{
-    r.side = qnan_f();
-    if (row != nullptr && c.side_ok) r.side = __ldg(row + c.sx);
-}
-
-__device__ __forceinline__ void side_value(const uint8_t *__restrict__ row, const Cols &c,
-                                           Raw<uint8_t> &r)
-{
-    r.side = 256u;
-    if (row != nullptr && c.side_ok) r.side = __ldg(row + c.sx);
-}
-
-// A lane's four values and its side value of one row.
-template <typename T>
-__device__ __forceinline__ Raw<T> load_row(const T *__restrict__ row, const Cols &c)
-{
-    Raw<T> r;
-    load_own(row, c, r);
-    side_value(row, c, r);
-    return r;
-}
-
 // Keys of a raw row: own pairs (k0 | k1 << 16, k2 | k3 << 16) and the side key (low half).
 template <bool SEARCH>
 __device__ __forceinline__ void row_keys(const Raw<float> &r, const KeyConsts &K,
@@ -258,12 +186,6 @@ __device__ __forceinline__ void row_keys(const Raw<uint8_t> &r, const KeyConsts 
 // are split into equal contiguous ranges, one per warp of the image's blocks (blockIdx.y =
 // image). A warp walks its range as one band per strip it touches, so the only repeated work is
 // the two rows around each band, and warps that run side by side read neighbouring rows.
-
-template <typename T>
-__device__ __forceinline__ const T *row_ptr(const T *__restrict__ img, int y, int rows, int W)
-{
-    return ((unsigned)y < (unsigned)rows) ? img + (int64_t)y * W : nullptr;
-}
 
 template <typename T, bool SEARCH>
 __device__ __forceinline__ KeyRow key_row(const Raw<T> &r, const KeyConsts &K,
@@ -466,19 +388,33 @@ constexpr int kKeyPlane = kKeyRowsHalo * kKeyPitch;  // halves per plane buffer
 // The raw values one thread needs for one plane of the tile: its warp's row (four columns), one
 // value of the two halo rows (thread t: row y0 - 1 or y0 + 8 by t >> 7, column x0 - 1 + (t & 127)),
 // and for warp 0 one "extra" value: lanes 0..7 the column left of rows y0 .. y0+7, lanes 8..15
-// the column right of them, lanes 16..19 the halo-row columns x0 + 127 and x0 + 128.
+// the column right of them, lanes 16..19 the halo-row columns x0 + 127 and x0 + 128. Positions
+// outside the grid read as NaN (f32) or 256 (u8), both meaning "never".
+template <typename T>
+struct HaloVal;
+template <>
+struct HaloVal<float> {
+    using type = float;
+    static __device__ __forceinline__ float none() { return qnan_f(); }
+};
+template <>
+struct HaloVal<uint8_t> {
+    using type = uint32_t;
+    static __device__ __forceinline__ uint32_t none() { return 256u; }
+};
+
 template <typename T>
 struct PlaneRaw {
-    Raw<T> own;    // own.side unused (always absent)
-    T hrow, extra;
-    bool hrow_ok, extra_ok;
+    Raw<T> own;  // own.side unused
+    typename HaloVal<T>::type hrow, extra;
 };
 
 struct PlaneCols {
-    Cols own;
+    Cols own;    // own.own_ok also clears every column when the warp's row is outside the grid
+    bool full;   // the warp's row exists and its four values load with one aligned load
     int hy, hx;  // halo-row position of this thread (clamped)
     bool h_ok;
-    int ey, ex;  // extra position (warp 0)
+    int ey, ex;  // extra position (warp 0, clamped)
     bool e_ok;
     int hrow_half;   // shared index of the halo-row key
     int extra_half;  // shared index of the extra key (or -1)
@@ -489,8 +425,9 @@ __device__ __forceinline__ PlaneCols plane_cols(int x0, int y0, int Hy, int W, i
 {
     PlaneCols pc;
     pc.own = strip_cols(x0, W, lane, vec_ok);
-    pc.own.side_ok = false;  // row halos come from the extra values
-    pc.own.sx = min(pc.own.x, W - 1);
+    const bool row_in = y0 + warp < Hy;
+    if (!row_in) pc.own.own_ok = 0;
+    pc.full = pc.own.full && row_in;
     const int t = threadIdx.x;
     const int hr = t >> 7;  // 0: row y0 - 1, 1: row y0 + 8
     const int hy = hr ? y0 + kTileRows : y0 - 1;
@@ -519,35 +456,89 @@ __device__ __forceinline__ PlaneCols plane_cols(int x0, int y0, int Hy, int W, i
     return pc;
 }
 
+// A thread's plane-by-plane reader: pointers into plane z that advance one plane per read;
+// planes outside [0, D) read as absent.
 template <typename T>
-__device__ __forceinline__ PlaneRaw<T> load_plane(const T *__restrict__ img, int64_t D, int Hy,
-                                                  int W, int64_t z, int y, const PlaneCols &pc,
-                                                  bool with_extra)
+struct PlaneCursor {
+    const T *own, *hrow, *extra;
+    int64_t stride;
+    int64_t z, D;
+};
+
+template <typename T>
+__device__ __forceinline__ PlaneCursor<T> plane_cursor(const T *__restrict__ img,
+                                                       const PlaneCols &pc, int y, int64_t z,
+                                                       int64_t D, int Hy, int W)
 {
-    PlaneRaw<T> p;
-    const bool zin = (z >= 0 && z < D);  // block-uniform
-    const T *__restrict__ plane = img + (zin ? z : 0) * (int64_t)Hy * W;
-    load_own(zin ? row_ptr(plane, y, Hy, W) : nullptr, pc.own, p.own);
-    const T h = __ldg(plane + (int64_t)pc.hy * W + pc.hx);
-    p.hrow = h;
-    p.hrow_ok = zin && pc.h_ok;
-    p.extra_ok = false;
-    p.extra = h;
-    if (with_extra) {  // warp-uniform (warp 0)
-        p.extra = __ldg(plane + (int64_t)pc.ey * W + pc.ex);
-        p.extra_ok = zin && pc.e_ok;
-    }
-    return p;
+    PlaneCursor<T> cur;
+    cur.stride = (int64_t)Hy * W;
+    const T *plane = img + z * cur.stride;
+    cur.own = plane + (int64_t)min(y, Hy - 1) * W + pc.own.x;
+    cur.hrow = plane + (int64_t)pc.hy * W + pc.hx;
+    cur.extra = plane + (int64_t)pc.ey * W + pc.ex;
+    cur.z = z;
+    cur.D = D;
+    return cur;
 }
 
-// Key of one value (NaN / missing -> H).
-template <bool SEARCH>
-__device__ __forceinline__ uint32_t value_key(float v, bool ok, const KeyConsts &K,
-                                              const float *__restrict__ T, uint32_t &amb)
+__device__ __forceinline__ void load_own4(const float *p, const PlaneCols &pc, Raw<float> &r)
 {
-    const float x = ok ? v : qnan_f();
-    if (SEARCH) return key_search_pattern(x, K.H, T);
-    return key_fast(x, K, amb);
+    if (pc.full) {  // warp-uniform
+        const float4 q = __ldg(reinterpret_cast<const float4 *>(p));
+        r.v[0] = q.x;
+        r.v[1] = q.y;
+        r.v[2] = q.z;
+        r.v[3] = q.w;
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) r.v[j] = ldg_if(p + j, (pc.own.own_ok >> j) & 1u, qnan_f());
+    }
+}
+
+__device__ __forceinline__ void load_own4(const uint8_t *p, const PlaneCols &pc, Raw<uint8_t> &r)
+{
+    if (pc.full) {  // warp-uniform
+        r.bytes = __ldg(reinterpret_cast<const unsigned int *>(p));
+    } else {
+        r.bytes = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            r.bytes |= ldg_if(p + j, (pc.own.own_ok >> j) & 1u, 0u) << (8 * j);
+    }
+    r.own_ok = pc.own.own_ok;
+}
+
+__device__ __forceinline__ void absent_own(Raw<float> &r)
+{
+#pragma unroll
+    for (int j = 0; j < 4; ++j) r.v[j] = qnan_f();
+}
+__device__ __forceinline__ void absent_own(Raw<uint8_t> &r)
+{
+    r.bytes = 0;
+    r.own_ok = 0;
+}
+
+template <typename T>
+__device__ __forceinline__ PlaneRaw<T> next_plane(PlaneCursor<T> &cur, const PlaneCols &pc,
+                                                  bool with_extra)
+{
+    using V = HaloVal<T>;
+    PlaneRaw<T> p;
+    p.extra = V::none();
+    if ((uint64_t)cur.z < (uint64_t)cur.D) {  // block-uniform
+        load_own4(cur.own, pc, p.own);
+        p.hrow = ldg_if(cur.hrow, pc.h_ok, V::none());
+        if (with_extra) p.extra = ldg_if(cur.extra, pc.e_ok, V::none());  // warp-uniform
+    } else {
+        absent_own(p.own);
+        p.hrow = V::none();
+    }
+    cur.own += cur.stride;
+    cur.hrow += cur.stride;
+    cur.extra += cur.stride;
+    ++cur.z;
+    return p;
 }
 
 // Keys of a loaded plane into the shared buffer `dst`.
@@ -557,18 +548,25 @@ __device__ __forceinline__ void store_plane_keys(const PlaneRaw<float> &p, const
                                                  int warp, int lane, bool with_extra,
                                                  uint16_t *dst)
 {
-    uint32_t k[7];
-    uint32_t amb = 0;
+    uint32_t k[6];
+    if (SEARCH) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) k[j] = value_key<SEARCH>(p.own.v[j], true, K, T, amb);
-    k[4] = value_key<SEARCH>(p.hrow, p.hrow_ok, K, T, amb);
-    k[5] = with_extra ? value_key<SEARCH>(p.extra, p.extra_ok, K, T, amb) : 0u;
-    if (!SEARCH && __any_sync(kFull, amb != 0)) {
-        if (amb != 0) {
+        for (int j = 0; j < 4; ++j) k[j] = key_search_pattern(p.own.v[j], K.H, T);
+        k[4] = key_search_pattern(p.hrow, K.H, T);
+        k[5] = with_extra ? key_search_pattern(p.extra, K.H, T) : 0u;
+    } else {
+        uint32_t amb = 0;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) k[j] = key_fix(p.own.v[j], k[j], K.H, T);
-            k[4] = key_fix(p.hrow_ok ? p.hrow : qnan_f(), k[4], K.H, T);
-            if (with_extra) k[5] = key_fix(p.extra_ok ? p.extra : qnan_f(), k[5], K.H, T);
+        for (int j = 0; j < 4; ++j) k[j] = key_fast(p.own.v[j], K, amb);
+        k[4] = key_fast(p.hrow, K, amb);
+        k[5] = key_fast(p.extra, K, amb);  // NaN (key H) outside warp 0
+        if (__any_sync(kFull, amb != 0)) {  // rare: a value within E of a threshold
+            if (amb != 0) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) k[j] = key_fix(p.own.v[j], k[j], K.H, T);
+                k[4] = key_fix(p.hrow, k[4], K.H, T);
+                k[5] = key_fix(p.extra, k[5], K.H, T);
+            }
         }
     }
     uint16_t *row = dst + (1 + warp) * kKeyPitch;
@@ -592,9 +590,9 @@ __device__ __forceinline__ void store_plane_keys(const PlaneRaw<uint8_t> &p, con
     row_keys<SEARCH>(r, K, T, own0, own1, unused);
     uint16_t *row = dst + (1 + warp) * kKeyPitch;
     *reinterpret_cast<uint2 *>(row + 4 + 4 * lane) = make_uint2(own0, own1);
-    dst[pc.hrow_half] = (uint16_t)(p.hrow_ok ? (uint32_t)lut[p.hrow] : never);
+    dst[pc.hrow_half] = (uint16_t)(p.hrow < 256u ? (uint32_t)lut[p.hrow] : never);
     if (with_extra && pc.extra_half >= 0)
-        dst[pc.extra_half] = (uint16_t)(p.extra_ok ? (uint32_t)lut[p.extra] : never);
+        dst[pc.extra_half] = (uint16_t)(p.extra < 256u ? (uint32_t)lut[p.extra] : never);
 }
 
 // Buffer row r (= tile row r - 1, r = 0 .. 9) around the lane's four columns.
@@ -644,20 +642,20 @@ __global__ void __launch_bounds__(kHardThreads, ECC_3D_MIN_BLOCKS) ecc_hard3d_ke
         const int64_t tz = rest / P.tasks_y;
         const int x0 = tx * kStrip;
         const int y0 = ty * kTileRows;
-        const int y = y0 + warp;  // this warp's row
         const int64_t z0 = tz * P.rows_per_task;
         const int64_t z1 = min(z0 + (int64_t)P.rows_per_task, D);
         const PlaneCols pc = plane_cols(x0, y0, Hy, W, warp, lane, vec_ok);
+        PlaneCursor<T> cur = plane_cursor(img, pc, y0 + warp, z0 - 1, D, Hy, W);
 
         // prologue: keys of planes z0 - 1 (buffer 0) and z0 (buffer 1); raw plane z0 + 1 in flight
         __syncthreads();  // the previous task's readers are done with both buffers
         {
-            const PlaneRaw<T> pm = load_plane<T>(img, D, Hy, W, z0 - 1, y, pc, with_extra);
-            const PlaneRaw<T> p0 = load_plane<T>(img, D, Hy, W, z0, y, pc, with_extra);
+            const PlaneRaw<T> pm = next_plane(cur, pc, with_extra);
+            const PlaneRaw<T> p0 = next_plane(cur, pc, with_extra);
             store_plane_keys<SEARCH>(pm, pc, K, table, warp, lane, with_extra, keybuf[0]);
             store_plane_keys<SEARCH>(p0, pc, K, table, warp, lane, with_extra, keybuf[1]);
         }
-        PlaneRaw<T> pnext = load_plane<T>(img, D, Hy, W, z0 + 1, y, pc, with_extra);
+        PlaneRaw<T> pnext = next_plane(cur, pc, with_extra);
         __syncthreads();
         uint32_t cm0, cm1;        // c2(M_{z-1}) at the lane's pixels (plain values)
         uint32_t below0, below1;  // keys of plane z - 1 at the lane's pixels
@@ -675,42 +673,46 @@ __global__ void __launch_bounds__(kHardThreads, ECC_3D_MIN_BLOCKS) ecc_hard3d_ke
             below0 = pb.own0;
             below1 = pb.own1;
         }
+        __syncthreads();  // buffer 0 is read; plane z0 + 1 may replace it
 
-        for (int64_t z = z0; z < z1; ++z) {
-            uint16_t *nbuf = keybuf[(z - z0) & 1];  // plane z + 1 replaces plane z - 1
-            // One barrier per plane: the buffer written here was last read in the step before
-            // the previous one, and every warp has passed the previous step's barrier since.
-            if (z == z0) __syncthreads();  // the prologue read buffer 0
-            store_plane_keys<SEARCH>(pnext, pc, K, table, warp, lane, with_extra, nbuf);
-            if (z + 2 <= z1)  // block-uniform: the next plane is needed
-                pnext = load_plane<T>(img, D, Hy, W, z + 2, y, pc, with_extra);
-            __syncthreads();
-            const KeyRow na = smem_key_row(nbuf, warp, lane);
-            const KeyRow nb = smem_key_row(nbuf, warp + 1, lane);
-            const KeyRow nd = smem_key_row(nbuf, warp + 2, lane);
-            uint32_t s0, s1, cs0, cs1, cn0, cn1;
-            sp_init(ca, cb, s0, s1);
-            c2_quad(ca, cb, cd, kBias, s0, s1, cs0, cs1);
-            const KeyRow ma = max_rows(ca, na), mb = max_rows(cb, nb), md = max_rows(cd, nd);
-            sp_init(ma, mb, s0, s1);
-            c2_quad(ma, mb, md, kPlain, s0, s1, cn0, cn1);
-            // c = cS - [k_{z+1} < k_z] c2(M_z) - [k_{z-1} <= k_z] c2(M_{z-1})
-            const uint32_t up0 = h2_lt_mask(nb.own0, cb.own0);
-            const uint32_t up1 = h2_lt_mask(nb.own1, cb.own1);
-            const uint32_t dn0 = h2_le_mask(below0, cb.own0);
-            const uint32_t dn1 = h2_le_mask(below1, cb.own1);
-            const uint32_t c0 = h2_sub(h2_sub(cs0, cn0 & up0), cm0 & dn0);
-            const uint32_t c1 = h2_sub(h2_sub(cs1, cn1 & up1), cm1 & dn1);
-            hist_pair(cb.own0, c0, hist_s);
-            hist_pair(cb.own1, c1, hist_s);
-            cm0 = cn0;
-            cm1 = cn1;
-            below0 = cb.own0;
-            below1 = cb.own1;
-            ca = na;
-            cb = nb;
-            cd = nd;
+        // One barrier per plane: plane z + 1 goes to buffer (z - z0) & 1, which was last read
+        // two steps before, and every warp has passed the previous step's barrier since. The loop
+        // is unrolled by two so that the buffer and the carried rows need no register moves.
+#define ECC_3D_STEP(NBUF, ZZ)                                                               \
+    {                                                                                       \
+        store_plane_keys<SEARCH>(pnext, pc, K, table, warp, lane, with_extra, NBUF);        \
+        if ((ZZ) + 2 <= z1) pnext = next_plane(cur, pc, with_extra); /* block-uniform */    \
+        __syncthreads();                                                                    \
+        const KeyRow na = smem_key_row(NBUF, warp, lane);                                   \
+        const KeyRow nb = smem_key_row(NBUF, warp + 1, lane);                               \
+        const KeyRow nd = smem_key_row(NBUF, warp + 2, lane);                               \
+        uint32_t s0, s1, cs0, cs1, cn0, cn1;                                                \
+        sp_init(ca, cb, s0, s1);                                                            \
+        c2_quad(ca, cb, cd, kBias, s0, s1, cs0, cs1);                                       \
+        const KeyRow ma = max_rows(ca, na), mb = max_rows(cb, nb), md = max_rows(cd, nd);   \
+        sp_init(ma, mb, s0, s1);                                                            \
+        c2_quad(ma, mb, md, kPlain, s0, s1, cn0, cn1);                                      \
+        /* c = cS - [k_{z+1} < k_z] c2(M_z) - [k_{z-1} <= k_z] c2(M_{z-1}) */                \
+        const uint32_t up0 = h2_lt_mask(nb.own0, cb.own0);                                  \
+        const uint32_t up1 = h2_lt_mask(nb.own1, cb.own1);                                  \
+        const uint32_t dn0 = h2_le_mask(below0, cb.own0);                                   \
+        const uint32_t dn1 = h2_le_mask(below1, cb.own1);                                   \
+        hist_pair(cb.own0, h2_sub(h2_sub(cs0, cn0 & up0), cm0 & dn0), hist_s);              \
+        hist_pair(cb.own1, h2_sub(h2_sub(cs1, cn1 & up1), cm1 & dn1), hist_s);              \
+        cm0 = cn0;                                                                          \
+        cm1 = cn1;                                                                          \
+        below0 = cb.own0;                                                                   \
+        below1 = cb.own1;                                                                   \
+        ca = na;                                                                            \
+        cb = nb;                                                                            \
+        cd = nd;                                                                            \
+    }
+        for (int64_t z = z0; z < z1; z += 2) {
+            ECC_3D_STEP(keybuf[0], z)
+            if (z + 1 >= z1) break;
+            ECC_3D_STEP(keybuf[1], z + 1)
         }
+#undef ECC_3D_STEP
     }
     block_flush(P, hist, b);
 }
