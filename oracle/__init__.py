@@ -158,3 +158,49 @@ def ecc_soft_bwd(img, tau, lam, alpha, u, grad_out, ndim=None, want_img=True):
         res["grad_img"] = gi
         res["grad_img_absterms"] = gabs
     return res
+
+
+# ---------------------------------------------------------------------------------------------
+# Soft Euler characteristic transform: the soft ECC along each of several directions
+# ---------------------------------------------------------------------------------------------
+# Paper notes "Scalable GPU-Accelerated Euler Characteristic Curves", "Limitations": the layer
+# works on one direction at a time, while the Euler characteristic transform integrates the
+# curve over many directions. By definition the transform's value for direction u_j is the
+# (soft) ECC of the filtration X_j = alpha f + u_j . x, so the oracle evaluates the pinned
+# single-direction soft ECC once per direction.
+
+def _directions(U, ndim):
+    U = np.asarray(U, np.float32)
+    if U.ndim != 2 or U.shape[1] != ndim:
+        raise ValueError(f"directions must have shape [n_dirs, {ndim}]")
+    return U
+
+
+def ecc_soft_ect_fwd(img, tau, lam, alpha, U, ndim=None):
+    """S[b, j, k] = soft ECC of image b along direction U[j] (fp64); [(B,) n_dirs, K]."""
+    nd = np.asarray(img).ndim if ndim is None else ndim
+    U = _directions(U, nd)
+    per = [ecc_soft_fwd(img, tau, lam, alpha, U[j], ndim=nd) for j in range(U.shape[0])]
+    return np.stack(per, axis=-2)
+
+
+def ecc_soft_ect_bwd(img, tau, lam, alpha, U, grad_out, ndim=None, want_img=True):
+    """Gradients of sum(grad_out * S) for the transform; grad_out [(B,) n_dirs, K]. Returns
+    grad_tau [K], grad_alpha, grad_u [n_dirs, ndim] and (want_img) grad_img, grad_img_absterms:
+    the sums over directions of the single-direction gradients, with grad_u kept per direction."""
+    nd = np.asarray(img).ndim if ndim is None else ndim
+    U = _directions(U, nd)
+    go = np.asarray(grad_out, np.float64)
+    res = {"grad_tau": 0.0, "grad_alpha": 0.0, "grad_u": np.zeros(U.shape, np.float64)}
+    if want_img:
+        res["grad_img"] = 0.0
+        res["grad_img_absterms"] = 0.0
+    for j in range(U.shape[0]):
+        r = ecc_soft_bwd(img, tau, lam, alpha, U[j], go[..., j, :], ndim=nd, want_img=want_img)
+        res["grad_tau"] = res["grad_tau"] + r["grad_tau"]
+        res["grad_alpha"] = res["grad_alpha"] + r["grad_alpha"]
+        res["grad_u"][j] = r["grad_u"]
+        if want_img:
+            res["grad_img"] = res["grad_img"] + r["grad_img"]
+            res["grad_img_absterms"] = res["grad_img_absterms"] + r["grad_img_absterms"]
+    return res

@@ -178,3 +178,44 @@ def test_u_zero_alpha_one_is_soft_ecc_of_f():
     s = oracle.ecc_soft_fwd(f, tau, 1.0e4, 1.0, [0.0, 0.0])
     hard = oracle.ecc_hard(f, 256, 0.0, 255.0)[np.arange(0, 256, 15)]
     np.testing.assert_allclose(s, hard.astype(np.float64), atol=1e-12)
+
+
+# ---------------------------------------------------------------------------------------------
+# Soft Euler characteristic transform (several directions)
+# ---------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("shape", [(4, 5), (3, 4, 5)])
+def test_ect_closed_form_on_a_flat_image(shape):
+    """f = 0: along every direction u_j each sublevel set of X_j = u_j . x is a staircase region
+    of the grid, contractible whenever non-empty, so only the first voxel to enter contributes
+    and S_j(t) = sigma(lam (t - X_min,j)), X_min,j = -sum_d |u_jd| (a corner of the grid). The
+    u-gradient of each direction follows from dX_min,j / du_jd = -sign(u_jd)."""
+    f = np.zeros(shape, np.float32)
+    rng = np.random.default_rng(len(shape))
+    U = rng.normal(0, 0.3, size=(5, len(shape))).astype(np.float32)
+    U[1, 0] = 0.0  # one direction with a tie along an axis
+    tau = np.linspace(-1.0, 1.0, 7).astype(np.float32)
+    lam = 5.0
+    s = oracle.ecc_soft_ect_fwd(f, tau, lam, 1.0, U)
+    assert s.shape == (5, 7)
+    g = rng.standard_normal((5, 7))
+    res = oracle.ecc_soft_ect_bwd(f, tau, lam, 1.0, U, g)
+    for j in range(5):
+        xmin = -sum(abs(float(x)) for x in U[j])
+        want = 1.0 / (1.0 + np.exp(-lam * (tau.astype(np.float64) - xmin)))
+        np.testing.assert_allclose(s[j], want, rtol=1e-12, atol=1e-15)
+        dsdx = -lam * want * (1 - want)  # dS/dX_min
+        for d in range(len(shape)):
+            if U[j, d] != 0.0:
+                want_gu = np.sum(g[j] * dsdx) * (-np.sign(U[j, d]))
+                np.testing.assert_allclose(res["grad_u"][j, d], want_gu, rtol=1e-10)
+
+
+def test_ect_of_one_direction_is_the_soft_ecc_and_batches_stack():
+    img = synthetic.grf((9, 11), 21, batch=3)
+    tau = synthetic.uniform_thresholds(6)
+    U = np.asarray([[0.1, -0.2], [0.0, 0.0], [-0.3, 0.05]], np.float32)
+    s = oracle.ecc_soft_ect_fwd(img, tau, 40.0, 1.0, U, ndim=2)
+    assert s.shape == (3, 3, 6)
+    for j in range(3):
+        np.testing.assert_array_equal(s[:, j], oracle.ecc_soft_fwd(img, tau, 40.0, 1.0, U[j], ndim=2))
