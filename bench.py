@@ -51,6 +51,9 @@ WORKLOADS = {
     "soft16": [("soft", (256, 256), 16, 128, 50.0, 6, 7, 8)],
     # the soft path on 3-D volumes (3 x 3 x 3 neighbourhoods): 4 GRF volumes of 128^3
     "soft3d": [("soft", (128, 128, 128), 4, 128, 50.0, 9, 10, 11)],
+    # the soft Euler characteristic transform: 16 GRF images of 256^2 along 32 directions
+    # (a soft part with a ninth field, the number of directions)
+    "ect": [("soft", (256, 256), 16, 128, 50.0, 12, 13, 14, 32)],
 }
 WORKLOADS["headline"] = WORKLOADS["2d8192"] + WORKLOADS["3d1024"] + WORKLOADS["soft"]
 
@@ -60,11 +63,17 @@ DESCRIPTION = {
 }
 
 
+def part_dirs(p):
+    """Directions of a soft part (1 for the soft ECC, more for the transform)."""
+    return p[8] if p[0] == "soft" and len(p) > 8 else 1
+
+
 def part_name(p):
     if p[0] == "hard":
         dims = "x".join(str(s) for s in p[1])
         return f"hard_{len(p[1])}d_{p[2]}x{dims}_{p[3]}_H{p[4]}"
-    return f"soft_fwd_bwd_{p[2]}x{'x'.join(str(x) for x in p[1])}_K{p[3]}"
+    name = f"soft_fwd_bwd_{p[2]}x{'x'.join(str(x) for x in p[1])}_K{p[3]}"
+    return name if part_dirs(p) == 1 else name.replace("soft_", "soft_ect_") + f"_D{part_dirs(p)}"
 
 
 def part_voxels(p):
@@ -191,7 +200,7 @@ def soft_roofline(p, ms, stats, clocks):
     fp32_peak = SM_COUNT * FP32_PER_CLK * f_sm
     achieved = terms / (ms * 1e-3)
     return {"listed_voxels": n_list, "direct_tiles": n_direct, "tiles": n_tiles,
-            "dense_terms": 2 * part_voxels(p) * K,
+            "dense_terms": 2 * part_voxels(p) * K * part_dirs(p),
             "roofline": {"bound": "xu", "unit": "Gterms/s",
                          "achieved": round(achieved / 1e9, 2),
                          "peak": round(xu_peak / 1e9, 2),
@@ -225,11 +234,17 @@ def make_inputs(parts, device):
                 img = img.unsqueeze(0)
             inputs.append({"img": img.contiguous(), "ndim": len(shape)})
         else:
-            _, shape, batch, K, lam, s_img, s_u, s_g = p
+            _, shape, batch, K, lam, s_img, s_u, s_g = p[:8]
+            nd = part_dirs(p)
             img = synthetic.grf(shape, s_img, device=device, batch=batch)
             tau = torch.from_numpy(synthetic.uniform_thresholds(K)).to(device)
-            u = torch.from_numpy(synthetic.soft_direction(len(shape), s_u)).to(device)
-            g = torch.from_numpy(synthetic.upstream_grad((batch, K), s_g)).to(device)
+            if nd == 1:
+                u = torch.from_numpy(synthetic.soft_direction(len(shape), s_u)).to(device)
+                g = torch.from_numpy(synthetic.upstream_grad((batch, K), s_g)).to(device)
+            else:
+                u = torch.from_numpy(np.stack([synthetic.soft_direction(len(shape), s_u + j)
+                                               for j in range(nd)])).to(device)
+                g = torch.from_numpy(synthetic.upstream_grad((batch, nd, K), s_g)).to(device)
             alpha = torch.ones(1, dtype=torch.float32, device=device)
             inputs.append({"img": img.contiguous(), "tau": tau, "u": u, "g": g, "alpha": alpha,
                            "lam": lam})
@@ -255,9 +270,11 @@ class OurStep:
             else:
                 K = p[3]
                 nb = x["img"].shape[0]
-                ws = torch.empty(ecc.soft_workspace_bytes(p[1], nb, K), dtype=torch.uint8,
+                nd = part_dirs(p)
+                ws = torch.empty(ecc.soft_workspace_bytes(p[1], nb, K, nd), dtype=torch.uint8,
                                  device=device)
-                s = torch.empty((nb, K), dtype=torch.float32, device=device)
+                s = torch.empty((nb, nd, K) if nd > 1 else (nb, K), dtype=torch.float32,
+                                device=device)
                 self.outs.append({"ws": ws, "s": s})
         self.launches_per_step = sum(2 if p[0] == "hard" else 6 for p in parts)
 
@@ -265,18 +282,24 @@ class OurStep:
         p, x, o = self.parts[i], self.inputs[i], self.outs[i]
         if p[0] == "hard":
             self.ecc.ecc_hard(x["img"], p[4], p[5], p[6], ndim=x["ndim"], out=o)
-        else:
+        elif part_dirs(p) == 1:
             self.ecc.ecc_soft_fwd(x["img"], x["tau"], x["lam"], x["alpha"], x["u"], ws=o["ws"],
                                   out=o["s"])
             o["grads"] = self.ecc.ecc_soft_bwd(x["img"], x["tau"], x["lam"], x["alpha"], x["u"],
                                                x["g"], o["ws"])
+        else:
+            self.ecc.ecc_soft_ect_fwd(x["img"], x["tau"], x["lam"], x["alpha"], x["u"],
+                                      ws=o["ws"], out=o["s"], ndim=len(p[1]))
+            o["grads"] = self.ecc.ecc_soft_ect_bwd(x["img"], x["tau"], x["lam"], x["alpha"],
+                                                   x["u"], x["g"], o["ws"], ndim=len(p[1]))
 
     def soft_stats(self):
         """Per soft part: [listed voxels, direct-form tiles, tiles] of the last forward pass."""
         out = {}
         for p, x, o in zip(self.parts, self.inputs, self.outs):
             if p[0] == "soft":
-                st = self.ecc.ecc_soft_stats(x["img"], p[3], o["ws"], ndim=len(p[1]))
+                st = self.ecc.ecc_soft_ect_stats(x["img"], p[3], part_dirs(p), o["ws"],
+                                                 ndim=len(p[1]))
                 out[part_name(p)] = [int(v) for v in st.cpu().tolist()]
         return out
 
@@ -382,15 +405,18 @@ SAMPLE_2D = 512           # 2-D parts: a 512 x 512 crop of one image
 SAMPLE_3D = (32, 128, 128)  # 3-D parts: a 32 x 128 x 128 crop
 SAMPLE_SOFT = 128        # soft part: one 128 x 128 image, all K thresholds, fwd + bwd
 SAMPLE_SOFT_3D = 24      # 3-D soft part: one 24^3 volume
+SAMPLE_ECT = 48          # transform part: one 48^2 image, all directions
 SAMPLE_TEXT = ("each 2-D part cropped to 512^2 (one image), each 3-D part to 32x128x128, "
-               "a 2-D soft part one 128^2 image (a 3-D one a 24^3 volume) with all K "
-               "thresholds (fwd + bwd)")
+               "a 2-D soft part one 128^2 image (a 3-D one a 24^3 volume, a transform part one "
+               "48^2 image with all directions) with all K thresholds (fwd + bwd)")
 
 
 def oracle_sample_step(parts, cache):
     """The oracle on a bounded sample of every part of the workload; returns voxels processed."""
     import oracle
     from euler_characteristic_curves_gb300 import synthetic
+
+    import numpy as np
 
     vox = 0
     for p in parts:
@@ -410,22 +436,25 @@ def oracle_sample_step(parts, cache):
                     img = synthetic.grf(sh, seed)
                 cache[key] = img
             else:
-                _, shape, batch, K, lam, s_img, s_u, s_g = p
-                if len(shape) == 2:
+                _, shape, batch, K, lam, s_img, s_u, s_g = p[:8]
+                nd = part_dirs(p)
+                if nd > 1:
+                    sh = tuple(min(a, SAMPLE_ECT) for a in shape)
+                elif len(shape) == 2:
                     sh = (min(shape[0], SAMPLE_SOFT), min(shape[1], SAMPLE_SOFT))
                 else:
                     sh = tuple(min(a, SAMPLE_SOFT_3D) for a in shape)
-                cache[key] = (synthetic.grf(sh, s_img), synthetic.uniform_thresholds(K),
-                              synthetic.soft_direction(len(shape), s_u),
-                              synthetic.upstream_grad((1, K), s_g))
+                U = np.stack([synthetic.soft_direction(len(shape), s_u + j) for j in range(nd)])
+                cache[key] = (synthetic.grf(sh, s_img), synthetic.uniform_thresholds(K), U,
+                              synthetic.upstream_grad((1, nd, K), s_g))
         x = cache[key]
         if p[0] == "hard":
             oracle.ecc_hard(x, p[4], p[5], p[6])
             vox += x.size
         else:
-            img, tau, u, g = x
-            oracle.ecc_soft_fwd(img, tau, p[4], 1.0, u)
-            oracle.ecc_soft_bwd(img, tau, p[4], 1.0, u, g, want_img=False)
+            img, tau, U, g = x
+            oracle.ecc_soft_ect_fwd(img, tau, p[4], 1.0, U)
+            oracle.ecc_soft_ect_bwd(img, tau, p[4], 1.0, U, g[0], want_img=False)
             vox += img.size
     return vox
 

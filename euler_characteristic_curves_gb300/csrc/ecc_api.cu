@@ -144,36 +144,43 @@ int ecc_hard(const void *img, int dtype, int ndim, const int64_t *dims, int64_t 
     return ECC_OK;
 }
 
-size_t ecc_soft_workspace_bytes(int ndim, const int64_t *dims, int64_t batch, int K)
+size_t ecc_soft_ect_workspace_bytes(int ndim, const int64_t *dims, int64_t batch, int K,
+                                    int ndirs)
 {
     SoftLayout L;
-    if (!soft_layout(ndim, dims, batch, K, L)) return 0;
+    if (!soft_layout(ndim, dims, batch, K, ndirs, L)) return 0;
     return L.total;
+}
+
+size_t ecc_soft_workspace_bytes(int ndim, const int64_t *dims, int64_t batch, int K)
+{
+    return ecc_soft_ect_workspace_bytes(ndim, dims, batch, K, 1);
 }
 
 static int soft_check(const float *img, int ndim, const int64_t *dims, int64_t batch,
                       const float *tau, int K, float lambda, const float *alpha, const float *u,
-                      void *ws, size_t ws_bytes, SoftLayout &L)
+                      int ndirs, void *ws, size_t ws_bytes, SoftLayout &L)
 {
     if (!img || !dims || !tau || !alpha || !u) return ECC_EINVAL;
     if (ndim != 2 && ndim != 3) return ECC_EDIM;
     for (int d = 0; d < ndim; ++d)
         if (dims[d] < 1) return ECC_EDIM;
-    if (batch < 1 || K < 1) return ECC_EINVAL;
-    if (K > ECC_MAX_K || batch > 65535) return ECC_ERANGE;
+    if (batch < 1 || K < 1 || ndirs < 1) return ECC_EINVAL;
+    if (K > ECC_MAX_K || ndirs > ECC_MAX_DIRS || batch * ndirs > 65535) return ECC_ERANGE;
     if (!(lambda > 0.0f) || !isfinite(lambda)) return ECC_EINVAL;
-    if (!soft_layout(ndim, dims, batch, K, L)) return ECC_ERANGE;
+    if (!soft_layout(ndim, dims, batch, K, ndirs, L)) return ECC_ERANGE;
     if (L.tiles > 2147483647) return ECC_ERANGE;
     if (!ws || ws_bytes < L.total || ((uintptr_t)ws % 256) != 0) return ECC_EWS;
     return ECC_OK;
 }
 
-int ecc_soft_fwd(const float *img, int ndim, const int64_t *dims, int64_t batch, const float *tau,
-                 int K, float lambda, const float *alpha, const float *u, float *out, void *ws,
-                 size_t ws_bytes, ecc_stream_t stream)
+int ecc_soft_ect_fwd(const float *img, int ndim, const int64_t *dims, int64_t batch,
+                     const float *tau, int K, float lambda, const float *alpha, const float *u,
+                     int ndirs, float *out, void *ws, size_t ws_bytes, ecc_stream_t stream)
 {
     SoftLayout L;
-    const int rc = soft_check(img, ndim, dims, batch, tau, K, lambda, alpha, u, ws, ws_bytes, L);
+    const int rc =
+        soft_check(img, ndim, dims, batch, tau, K, lambda, alpha, u, ndirs, ws, ws_bytes, L);
     if (rc != ECC_OK) return rc;
     if (!out) return ECC_EINVAL;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -181,13 +188,23 @@ int ecc_soft_fwd(const float *img, int ndim, const int64_t *dims, int64_t batch,
     return ECC_OK;
 }
 
-int ecc_soft_bwd(const float *img, int ndim, const int64_t *dims, int64_t batch, const float *tau,
-                 int K, float lambda, const float *alpha, const float *u, const float *grad_out,
-                 float *grad_tau, float *grad_alpha, float *grad_u, float *grad_img, void *ws,
+int ecc_soft_fwd(const float *img, int ndim, const int64_t *dims, int64_t batch, const float *tau,
+                 int K, float lambda, const float *alpha, const float *u, float *out, void *ws,
                  size_t ws_bytes, ecc_stream_t stream)
 {
+    return ecc_soft_ect_fwd(img, ndim, dims, batch, tau, K, lambda, alpha, u, 1, out, ws,
+                            ws_bytes, stream);
+}
+
+int ecc_soft_ect_bwd(const float *img, int ndim, const int64_t *dims, int64_t batch,
+                     const float *tau, int K, float lambda, const float *alpha, const float *u,
+                     int ndirs, const float *grad_out, float *grad_tau, float *grad_alpha,
+                     float *grad_u, float *grad_img, void *ws, size_t ws_bytes,
+                     ecc_stream_t stream)
+{
     SoftLayout L;
-    const int rc = soft_check(img, ndim, dims, batch, tau, K, lambda, alpha, u, ws, ws_bytes, L);
+    const int rc =
+        soft_check(img, ndim, dims, batch, tau, K, lambda, alpha, u, ndirs, ws, ws_bytes, L);
     if (rc != ECC_OK) return rc;
     if (!grad_out || !grad_tau || !grad_alpha || !grad_u) return ECC_EINVAL;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -197,20 +214,35 @@ int ecc_soft_bwd(const float *img, int ndim, const int64_t *dims, int64_t batch,
     return ECC_OK;
 }
 
-int ecc_soft_stats(int ndim, const int64_t *dims, int64_t batch, int K, const void *ws,
-                   size_t ws_bytes, int64_t *stats, ecc_stream_t stream)
+int ecc_soft_bwd(const float *img, int ndim, const int64_t *dims, int64_t batch, const float *tau,
+                 int K, float lambda, const float *alpha, const float *u, const float *grad_out,
+                 float *grad_tau, float *grad_alpha, float *grad_u, float *grad_img, void *ws,
+                 size_t ws_bytes, ecc_stream_t stream)
+{
+    return ecc_soft_ect_bwd(img, ndim, dims, batch, tau, K, lambda, alpha, u, 1, grad_out,
+                            grad_tau, grad_alpha, grad_u, grad_img, ws, ws_bytes, stream);
+}
+
+int ecc_soft_ect_stats(int ndim, const int64_t *dims, int64_t batch, int K, int ndirs,
+                       const void *ws, size_t ws_bytes, int64_t *stats, ecc_stream_t stream)
 {
     if (!dims || !stats) return ECC_EINVAL;
     if (ndim != 2 && ndim != 3) return ECC_EDIM;
     for (int d = 0; d < ndim; ++d)
         if (dims[d] < 1) return ECC_EDIM;
-    if (batch < 1 || K < 1) return ECC_EINVAL;
+    if (batch < 1 || K < 1 || ndirs < 1) return ECC_EINVAL;
     SoftLayout L;
-    if (!soft_layout(ndim, dims, batch, K, L)) return ECC_ERANGE;
+    if (!soft_layout(ndim, dims, batch, K, ndirs, L)) return ECC_ERANGE;
     if (!ws || ws_bytes < L.total || ((uintptr_t)ws % 256) != 0) return ECC_EWS;
     if (soft_run_stats(L, ws, stats, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return ECC_ECUDA;
     return ECC_OK;
+}
+
+int ecc_soft_stats(int ndim, const int64_t *dims, int64_t batch, int K, const void *ws,
+                   size_t ws_bytes, int64_t *stats, ecc_stream_t stream)
+{
+    return ecc_soft_ect_stats(ndim, dims, batch, K, 1, ws, ws_bytes, stats, stream);
 }
 
 }  // extern "C"

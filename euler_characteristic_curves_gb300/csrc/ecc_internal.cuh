@@ -80,10 +80,11 @@ struct SoftLayout {
     int ndim;
     int64_t D, Hy, W, batch;  // D = 1 for 2-D
     int K;
+    int ndirs;  // directions u_j (1 for the soft ECC, more for the transform)
     int64_t tiles_x, tiles_y, tiles_z, tiles;  // tiles per image
     size_t off_coords, off_counts, off_entries, off_part, off_scal, total;
 };
-bool soft_layout(int ndim, const int64_t *dims, int64_t batch, int K, SoftLayout &L);
+bool soft_layout(int ndim, const int64_t *dims, int64_t batch, int K, int ndirs, SoftLayout &L);
 cudaError_t soft_run_fwd(const SoftLayout &L, const float *img, const float *tau, float lambda,
                          const float *alpha, const float *u, float *out, void *ws, cudaStream_t s);
 cudaError_t soft_run_stats(const SoftLayout &L, const void *ws, int64_t *stats, cudaStream_t s);

@@ -61,7 +61,7 @@ extern "C" int ecc_soft_fwd_noalloc(const float *img, int ndim, const int64_t *d
     if (K > ECC_MAX_K || batch > 65535) return ECC_ERANGE;
     if (!(lambda > 0.0f) || !isfinite(lambda)) return ECC_EINVAL;
     SoftLayout L;
-    if (!soft_layout(ndim, dims, batch, K, L)) return ECC_ERANGE;
+    if (!soft_layout(ndim, dims, batch, K, 1, L)) return ECC_ERANGE;
     if (L.total > (size_t)ECC_NOALLOC_SCRATCH_BYTES) return ECC_ERANGE;
     void *ws = nullptr;
     const int rc = scratch_address(&ws);

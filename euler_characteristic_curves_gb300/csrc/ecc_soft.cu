@@ -64,12 +64,14 @@ constexpr int kScal = 4;                   // backward scalar partials per tile:
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-bool soft_layout(int ndim, const int64_t *dims, int64_t batch, int K, SoftLayout &L)
+bool soft_layout(int ndim, const int64_t *dims, int64_t batch, int K, int ndirs, SoftLayout &L)
 {
     if ((ndim != 2 && ndim != 3) || !dims || batch < 1 || K < 1 || K > ECC_MAX_K) return false;
     for (int d = 0; d < ndim; ++d)
         if (dims[d] < 1 || dims[d] > ((int64_t)1 << 31)) return false;
-    if (batch > 65535) return false;  // images run along gridDim.y
+    if (ndirs < 1 || ndirs > ECC_MAX_DIRS) return false;
+    if (batch * ndirs > 65535) return false;  // (image, direction) pairs run along gridDim.y
+    L.ndirs = ndirs;
     L.ndim = ndim;
     L.D = ndim == 3 ? dims[0] : 1;
     L.Hy = dims[ndim - 2];
@@ -85,7 +87,7 @@ bool soft_layout(int ndim, const int64_t *dims, int64_t batch, int K, SoftLayout
     L.tiles_z = (L.D + tz - 1) / tz;
     L.tiles = L.tiles_x * L.tiles_y * L.tiles_z;
     if (L.tiles >= ((int64_t)1 << 31)) return false;  // tiles run along gridDim.x
-    const int64_t units = batch * L.tiles;
+    const int64_t units = batch * ndirs * L.tiles;
     if (units > ((int64_t)1 << 40) / kTileCap) return false;
     const int64_t ncoord = (ndim == 3 ? L.D : 0) + L.Hy + L.W;
     size_t off = 0;
@@ -327,19 +329,21 @@ __device__ __forceinline__ int local_c3(const float2 *c)
     return v;
 }
 
-// One block per (tile, image). Computes X on the tile plus a one-voxel halo, c_X per voxel, and
-// writes the contributing voxels of the tile, in the tile's own raster order, to the tile's slot
-// of the list.
+// One block per (tile, image). Reads f on the tile plus a one-voxel halo once, then for each
+// direction u_j computes X_j = alpha f + u_j . x there, c_X per voxel, and writes the contributing
+// voxels of the tile, in the tile's own raster order, to the slot of unit (image, direction,
+// tile).
 template <int NDIM>
 __global__ void __launch_bounds__(kPrepThreads) soft_prep_kernel(
     const float *__restrict__ img, const float *__restrict__ alpha_p, const float *__restrict__ u_p,
-    const float *__restrict__ tau, int K, float l2, const float2 *__restrict__ coords,
+    int ndirs, const float *__restrict__ tau, int K, float l2, const float2 *__restrict__ coords,
     int *__restrict__ counts, float4 *__restrict__ entries, SoftGeom g)
 {
     using T = SoftTile<NDIM>;
     constexpr int HX = T::X + 2, HY = T::Y + 2, HZ = NDIM == 3 ? T::Z + 2 : 1;
     constexpr int HP = HX * HY;
     constexpr int ZO = NDIM == 3 ? 1 : 0;  // halo offset along z
+    __shared__ float Fv[HZ * HP];  // f on the tile and its halo; NaN outside the grid
     __shared__ float2 X[HZ * HP];
     __shared__ int warp_tot[kPrepThreads / kWarp];
     __shared__ int running;
@@ -351,65 +355,79 @@ __global__ void __launch_bounds__(kPrepThreads) soft_prep_kernel(
     const int64_t z0 = (tile / (g.tiles_x * g.tiles_y)) * T::Z;
     const float *__restrict__ f = img + b * g.D * g.Hy * g.W;
     const float alpha = __ldg(alpha_p);
-    const float u0 = __ldg(u_p), u1 = __ldg(u_p + 1), u2 = NDIM == 3 ? __ldg(u_p + 2) : 0.0f;
     const float2 *__restrict__ cz = coords;
     const float2 *__restrict__ cy = coords + g.nz;
     const float2 *__restrict__ cx = coords + g.nz + g.Hy;
     const float inf = __int_as_float(0x7f800000);
     const float m = tau_midpoint(tau, K);
+    const int lane = threadIdx.x & (kWarp - 1), warp = threadIdx.x >> 5;
 
     for (int i = threadIdx.x; i < HZ * HP; i += kPrepThreads) {
         const int iz = i / HP, iy = (i / HX) % HY, ix = i % HX;
         const int64_t gz = z0 - ZO + iz, gy = y0 - 1 + iy, gx = x0 - 1 + ix;
-        float2 v = make_float2(inf, 0.0f);  // outside the grid: never earlier
-        if (gz >= 0 && gz < g.D && gy >= 0 && gy < g.Hy && gx >= 0 && gx < g.W) {
-            const float fv = __ldg(f + (gz * g.Hy + gy) * g.W + gx);
-            if (NDIM == 3)
-                v = filtration_df3(alpha, fv, u0, __ldg(cz + gz), u1, __ldg(cy + gy), u2,
-                                   __ldg(cx + gx));
-            else
-                v = filtration_df(alpha, fv, u0, __ldg(cy + gy), u1, __ldg(cx + gx));
-        }
-        X[i] = v;
+        float fv = qnan();
+        if (gz >= 0 && gz < g.D && gy >= 0 && gy < g.Hy && gx >= 0 && gx < g.W)
+            fv = __ldg(f + (gz * g.Hy + gy) * g.W + gx);
+        Fv[i] = fv;
     }
-    if (threadIdx.x == 0) running = 0;
-    __syncthreads();
 
-    const int lane = threadIdx.x & (kWarp - 1), warp = threadIdx.x >> 5;
-    float4 *__restrict__ out = entries + (b * g.tiles + tile) * (int64_t)kTileCap;
-    bool direct = false;
-    for (int r = 0; r < kTileCap / kPrepThreads; ++r) {
-        const int i = r * kPrepThreads + threadIdx.x;
-        const int lx = i % T::X, ly = (i / T::X) % T::Y, lz = i / (T::X * T::Y);
-        const float2 *cp = &X[(lz + ZO) * HP + (ly + 1) * HX + lx + 1];
-        const float2 p = cp[0];
-        int c = 0;
-        if (z0 + lz < g.D && y0 + ly < g.Hy && x0 + lx < g.W)
-            c = NDIM == 3 ? local_c3<HX, HP>(cp) : local_c2<HX>(cp);
-        const unsigned mask = __ballot_sync(kFull, c != 0);
-        if (lane == 0) warp_tot[warp] = __popc(mask);
-        __syncthreads();
-        int before = running;
-        for (int w2 = 0; w2 < warp; ++w2) before += warp_tot[w2];
-        before += __popc(mask & ((1u << lane) - 1u));
-        if (c != 0) {
-            float s, e, ex;
-            two_sum(p.x, -m, s, e);  // X - m, exactly, as s + (e + lo)
-            const float E = pow2_scaled(l2, s, e + p.y, ex);
-            direct |= !(fabsf(ex) <= kExpLimit);
-            const int packed = (i << 4) | (c + 8);
-            out[before] = make_float4(E, p.x, p.y, __int_as_float(packed));
+    for (int j = 0; j < ndirs; ++j) {
+        const float *u = u_p + j * NDIM;
+        const float u0 = __ldg(u), u1 = __ldg(u + 1), u2 = NDIM == 3 ? __ldg(u + 2) : 0.0f;
+        __syncthreads();  // Fv is complete; the previous direction is done with X and running
+        for (int i = threadIdx.x; i < HZ * HP; i += kPrepThreads) {
+            const int iz = i / HP, iy = (i / HX) % HY, ix = i % HX;
+            const int64_t gz = z0 - ZO + iz, gy = y0 - 1 + iy, gx = x0 - 1 + ix;
+            const float fv = Fv[i];
+            float2 v = make_float2(inf, 0.0f);  // outside the grid: never earlier
+            if (fv == fv) {  // inside the grid (NaN marks outside; inputs are finite)
+                if (NDIM == 3)
+                    v = filtration_df3(alpha, fv, u0, __ldg(cz + gz), u1, __ldg(cy + gy), u2,
+                                       __ldg(cx + gx));
+                else
+                    v = filtration_df(alpha, fv, u0, __ldg(cy + gy), u1, __ldg(cx + gx));
+            }
+            X[i] = v;
         }
+        if (threadIdx.x == 0) running = 0;
         __syncthreads();
-        if (threadIdx.x == 0) {
-            int tot = 0;
-            for (int w2 = 0; w2 < kPrepThreads / kWarp; ++w2) tot += warp_tot[w2];
-            running += tot;
+
+        const int64_t unit = ((int64_t)b * ndirs + j) * g.tiles + tile;
+        float4 *__restrict__ out = entries + unit * (int64_t)kTileCap;
+        bool direct = false;
+        for (int r = 0; r < kTileCap / kPrepThreads; ++r) {
+            const int i = r * kPrepThreads + threadIdx.x;
+            const int lx = i % T::X, ly = (i / T::X) % T::Y, lz = i / (T::X * T::Y);
+            const float2 *cp = &X[(lz + ZO) * HP + (ly + 1) * HX + lx + 1];
+            const float2 p = cp[0];
+            int c = 0;
+            if (z0 + lz < g.D && y0 + ly < g.Hy && x0 + lx < g.W)
+                c = NDIM == 3 ? local_c3<HX, HP>(cp) : local_c2<HX>(cp);
+            const unsigned mask = __ballot_sync(kFull, c != 0);
+            if (lane == 0) warp_tot[warp] = __popc(mask);
+            __syncthreads();
+            int before = running;
+            for (int w2 = 0; w2 < warp; ++w2) before += warp_tot[w2];
+            before += __popc(mask & ((1u << lane) - 1u));
+            if (c != 0) {
+                float s, e, ex;
+                two_sum(p.x, -m, s, e);  // X - m, exactly, as s + (e + lo)
+                const float E = pow2_scaled(l2, s, e + p.y, ex);
+                direct |= !(fabsf(ex) <= kExpLimit);
+                const int packed = (i << 4) | (c + 8);
+                out[before] = make_float4(E, p.x, p.y, __int_as_float(packed));
+            }
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                int tot = 0;
+                for (int w2 = 0; w2 < kPrepThreads / kWarp; ++w2) tot += warp_tot[w2];
+                running += tot;
+            }
+            __syncthreads();
         }
-        __syncthreads();
+        direct = __syncthreads_or(direct);
+        if (threadIdx.x == 0) counts[unit] = running | (direct ? kTileFlagDirect : 0);
     }
-    direct = __syncthreads_or(direct);
-    if (threadIdx.x == 0) counts[b * g.tiles + tile] = running | (direct ? kTileFlagDirect : 0);
 }
 
 // Per-thread threshold state: tau_k, F_k (factorised path) and whether its exponent is in range.
@@ -555,11 +573,13 @@ __device__ __forceinline__ void bwd_group(const float4 *en8, const KState &s0, c
     __syncwarp();
 }
 
-// Backward: one block per (tile, image); thread t owns thresholds k = kb + t and kb + t + 64.
+// Backward: one block per (tile, image), looping over the directions; thread t owns thresholds
+// k = kb + t and kb + t + 64. The image gradient of the tile collects alpha dX over the
+// directions in shared memory in a fixed order and is written once, for every voxel of the tile.
 template <int NDIM>
 __global__ void __launch_bounds__(kSoftThreads) soft_bwd_kernel(
-    const float *__restrict__ img, const float *__restrict__ tau, int K, float lambda, float l2,
-    const float *__restrict__ alpha_p, const float *__restrict__ grad_out,
+    const float *__restrict__ img, const float *__restrict__ tau, int K, int ndirs, float lambda,
+    float l2, const float *__restrict__ alpha_p, const float *__restrict__ grad_out,
     const int *__restrict__ counts, const float4 *__restrict__ entries,
     const float2 *__restrict__ coords, double *__restrict__ part, double *__restrict__ scal,
     float *__restrict__ grad_img, SoftGeom g)
@@ -570,57 +590,13 @@ __global__ void __launch_bounds__(kSoftThreads) soft_bwd_kernel(
     __shared__ __align__(16) float qbuf[NW][kGroup][kWarp];
     __shared__ float red[NW][kChunk];
     __shared__ float dxs[kTileCap];
+    __shared__ float gacc[kTileCap];
     __shared__ double scal_red[NW][kScal];
 
     const int64_t b = blockIdx.y;
     const int64_t tile = blockIdx.x;
-    const int64_t unit = b * g.tiles + tile;
-    const int cnt = counts[unit];
-    const int n = cnt & (kTileFlagDirect - 1);
-    const float4 *__restrict__ list = entries + unit * (int64_t)kTileCap;
     const int lane = threadIdx.x & (kWarp - 1), warp = threadIdx.x >> 5;
     const float m = tau_midpoint(tau, K);
-    for (int i = threadIdx.x; i < n; i += kSoftThreads) dxs[i] = 0.0f;
-
-    for (int kb = 0; kb < K; kb += kKPerPass) {
-        const int k0 = kb + threadIdx.x, k1 = k0 + kSoftThreads;
-        const KState s0 = k_state(tau, k0, K, l2, m), s1 = k_state(tau, k1, K, l2, m);
-        const float g0 = (k0 < K) ? __ldg(grad_out + b * K + k0) : 0.0f;
-        const float g1 = (k1 < K) ? __ldg(grad_out + b * K + k1) : 0.0f;
-        const bool fact = __syncthreads_and(s0.ok && s1.ok && !(cnt & kTileFlagDirect));
-        float a0 = 0.f, c0 = 0.f, a1 = 0.f, c1 = 0.f;
-        for (int e0 = 0; e0 < n; e0 += kChunk) {
-            const int m_ent = min(kChunk, n - e0);
-            __syncthreads();
-            // stage the chunk; pad the last group with c = 0 entries
-            for (int i = threadIdx.x; i < kChunk; i += kSoftThreads)
-                sh[i] = (i < m_ent) ? list[e0 + i]
-                                    : make_float4(0.f, 0.f, 0.f, __int_as_float(kPadWord));
-            __syncthreads();
-            for (int g = 0; g * kGroup < m_ent; ++g) {
-                float rs;
-                if (fact)
-                    bwd_group<true>(sh + g * kGroup, s0, s1, g0, g1, l2, a0, c0, a1, c1,
-                                    qbuf[warp], lane, rs);
-                else
-                    bwd_group<false>(sh + g * kGroup, s0, s1, g0, g1, l2, a0, c0, a1, c1,
-                                     qbuf[warp], lane, rs);
-                if ((lane & 3) == 0) red[warp][g * kGroup + (lane >> 2)] = rs;
-            }
-            __syncthreads();
-            for (int i = threadIdx.x; i < m_ent; i += kSoftThreads) {
-                float q = 0.0f;
-#pragma unroll
-                for (int w2 = 0; w2 < NW; ++w2) q += red[w2][i];
-                dxs[e0 + i] += q;
-            }
-        }
-        if (k0 < K) part[unit * K + k0] = (double)lambda * (double)g0 * ((double)a0 - (double)c0);
-        if (k1 < K) part[unit * K + k1] = (double)lambda * (double)g1 * ((double)a1 - (double)c1);
-    }
-    __syncthreads();
-
-    // per-voxel gradient: dX = -lambda c sum_k g w; grad_img = alpha dX; dalpha, du partials
     const float alpha = __ldg(alpha_p);
     const int64_t image = g.D * g.Hy * g.W;
     const float *__restrict__ f = img + b * image;
@@ -630,40 +606,101 @@ __global__ void __launch_bounds__(kSoftThreads) soft_bwd_kernel(
     const float2 *__restrict__ cz = coords;
     const float2 *__restrict__ cy = coords + g.nz;
     const float2 *__restrict__ cx = coords + g.nz + g.Hy;
-    float sum[kScal] = {0.f, 0.f, 0.f, 0.f}, comp[kScal] = {0.f, 0.f, 0.f, 0.f};
-    for (int i = threadIdx.x; i < n; i += kSoftThreads) {
-        const float4 en = list[i];
-        const int loc = entry_loc(en);
-        const int64_t gx = x0 + loc % T::X, gy = y0 + (loc / T::X) % T::Y,
-                      gz = z0 + loc / (T::X * T::Y);
-        const int64_t idx = (gz * g.Hy + gy) * g.W + gx;
-        const float dX = -lambda * (float)entry_c(en) * dxs[i];
-        if (grad_img) grad_img[b * image + idx] = alpha * dX;
-        const float2 xy = __ldg(cy + gy), xx = __ldg(cx + gx);
-        kahan_add(sum[0], comp[0], dX * __ldg(f + idx));
-        if (NDIM == 3) {
-            const float2 xz = __ldg(cz + gz);
-            kahan_add(sum[1], comp[1], dX * (xz.x + xz.y));
+    if (grad_img)
+        for (int i = threadIdx.x; i < kTileCap; i += kSoftThreads) gacc[i] = 0.0f;
+
+    for (int j = 0; j < ndirs; ++j) {
+        const int64_t bj = b * ndirs + j;
+        const int64_t unit = bj * g.tiles + tile;
+        const int cnt = counts[unit];
+        const int n = cnt & (kTileFlagDirect - 1);
+        const float4 *__restrict__ list = entries + unit * (int64_t)kTileCap;
+        __syncthreads();  // the previous direction is done with dxs
+        for (int i = threadIdx.x; i < n; i += kSoftThreads) dxs[i] = 0.0f;
+
+        for (int kb = 0; kb < K; kb += kKPerPass) {
+            const int k0 = kb + threadIdx.x, k1 = k0 + kSoftThreads;
+            const KState s0 = k_state(tau, k0, K, l2, m), s1 = k_state(tau, k1, K, l2, m);
+            const float g0 = (k0 < K) ? __ldg(grad_out + bj * K + k0) : 0.0f;
+            const float g1 = (k1 < K) ? __ldg(grad_out + bj * K + k1) : 0.0f;
+            const bool fact = __syncthreads_and(s0.ok && s1.ok && !(cnt & kTileFlagDirect));
+            float a0 = 0.f, c0 = 0.f, a1 = 0.f, c1 = 0.f;
+            for (int e0 = 0; e0 < n; e0 += kChunk) {
+                const int m_ent = min(kChunk, n - e0);
+                __syncthreads();
+                // stage the chunk; pad the last group with c = 0 entries
+                for (int i = threadIdx.x; i < kChunk; i += kSoftThreads)
+                    sh[i] = (i < m_ent) ? list[e0 + i]
+                                        : make_float4(0.f, 0.f, 0.f, __int_as_float(kPadWord));
+                __syncthreads();
+                for (int gi = 0; gi * kGroup < m_ent; ++gi) {
+                    float rs;
+                    if (fact)
+                        bwd_group<true>(sh + gi * kGroup, s0, s1, g0, g1, l2, a0, c0, a1, c1,
+                                        qbuf[warp], lane, rs);
+                    else
+                        bwd_group<false>(sh + gi * kGroup, s0, s1, g0, g1, l2, a0, c0, a1, c1,
+                                         qbuf[warp], lane, rs);
+                    if ((lane & 3) == 0) red[warp][gi * kGroup + (lane >> 2)] = rs;
+                }
+                __syncthreads();
+                for (int i = threadIdx.x; i < m_ent; i += kSoftThreads) {
+                    float q = 0.0f;
+#pragma unroll
+                    for (int w2 = 0; w2 < NW; ++w2) q += red[w2][i];
+                    dxs[e0 + i] += q;
+                }
+            }
+            if (k0 < K)
+                part[unit * K + k0] = (double)lambda * (double)g0 * ((double)a0 - (double)c0);
+            if (k1 < K)
+                part[unit * K + k1] = (double)lambda * (double)g1 * ((double)a1 - (double)c1);
         }
-        kahan_add(sum[NDIM - 1], comp[NDIM - 1], dX * (xy.x + xy.y));
-        kahan_add(sum[NDIM], comp[NDIM], dX * (xx.x + xx.y));
-    }
-    double v[kScal];
+        __syncthreads();
+
+        // per-voxel gradient: dX = -lambda c sum_k g w; grad_img += alpha dX; dalpha, du partials
+        float sum[kScal] = {0.f, 0.f, 0.f, 0.f}, comp[kScal] = {0.f, 0.f, 0.f, 0.f};
+        for (int i = threadIdx.x; i < n; i += kSoftThreads) {
+            const float4 en = list[i];
+            const int loc = entry_loc(en);
+            const int64_t gx = x0 + loc % T::X, gy = y0 + (loc / T::X) % T::Y,
+                          gz = z0 + loc / (T::X * T::Y);
+            const int64_t idx = (gz * g.Hy + gy) * g.W + gx;
+            const float dX = -lambda * (float)entry_c(en) * dxs[i];
+            if (grad_img) gacc[loc] += alpha * dX;  // one entry per voxel and direction
+            const float2 xy = __ldg(cy + gy), xx = __ldg(cx + gx);
+            kahan_add(sum[0], comp[0], dX * __ldg(f + idx));
+            if (NDIM == 3) {
+                const float2 xz = __ldg(cz + gz);
+                kahan_add(sum[1], comp[1], dX * (xz.x + xz.y));
+            }
+            kahan_add(sum[NDIM - 1], comp[NDIM - 1], dX * (xy.x + xy.y));
+            kahan_add(sum[NDIM], comp[NDIM], dX * (xx.x + xx.y));
+        }
+        double v[kScal];
 #pragma unroll
-    for (int j = 0; j < kScal; ++j) {
-        v[j] = (double)sum[j] - (double)comp[j];
+        for (int q = 0; q < kScal; ++q) {
+            v[q] = (double)sum[q] - (double)comp[q];
 #pragma unroll
-        for (int o = kWarp / 2; o > 0; o >>= 1) v[j] += __shfl_xor_sync(kFull, v[j], o);
-    }
-    if (lane == 0) {
+            for (int o = kWarp / 2; o > 0; o >>= 1) v[q] += __shfl_xor_sync(kFull, v[q], o);
+        }
+        if (lane == 0) {
 #pragma unroll
-        for (int j = 0; j < kScal; ++j) scal_red[warp][j] = v[j];
+            for (int q = 0; q < kScal; ++q) scal_red[warp][q] = v[q];
+        }
+        __syncthreads();
+        if (threadIdx.x < kScal) {
+            double acc = 0.0;
+            for (int w2 = 0; w2 < NW; ++w2) acc += scal_red[w2][threadIdx.x];
+            scal[unit * kScal + threadIdx.x] = acc;
+        }
     }
+    if (!grad_img) return;
     __syncthreads();
-    if (threadIdx.x < kScal) {
-        double acc = 0.0;
-        for (int w2 = 0; w2 < NW; ++w2) acc += scal_red[w2][threadIdx.x];
-        scal[unit * kScal + threadIdx.x] = acc;
+    for (int i = threadIdx.x; i < kTileCap; i += kSoftThreads) {
+        const int64_t gx = x0 + i % T::X, gy = y0 + (i / T::X) % T::Y, gz = z0 + i / (T::X * T::Y);
+        if (gz < g.D && gy < g.Hy && gx < g.W)
+            grad_img[b * image + (gz * g.Hy + gy) * g.W + gx] = gacc[i];
     }
 }
 
@@ -672,17 +709,26 @@ __global__ void __launch_bounds__(kSoftThreads) soft_bwd_kernel(
 constexpr int kReduceThreads = 256;
 
 __global__ void __launch_bounds__(kReduceThreads) soft_bwd_reduce_kernel(
-    const double *__restrict__ part, const double *__restrict__ scal, int K, int64_t units,
-    float *__restrict__ grad_tau, float *__restrict__ grad_alpha, float *__restrict__ grad_u)
+    const double *__restrict__ part, const double *__restrict__ scal, int K, int ndim, int ndirs,
+    int64_t images, int64_t tiles, float *__restrict__ grad_tau, float *__restrict__ grad_alpha,
+    float *__restrict__ grad_u)
 {
     __shared__ double red[kReduceThreads];
-    const int o = blockIdx.x;  // 0..K-1: grad_tau[o]; K: grad_alpha; K+1..: grad_u
+    // o in 0..K-1: grad_tau[o]; K: grad_alpha; K + 1 + j ndim + d: grad_u[j][d]
+    const int o = blockIdx.x;
+    const int64_t units = images * ndirs * tiles;
     double acc = 0.0;
     if (o < K) {
         for (int64_t u = threadIdx.x; u < units; u += kReduceThreads) acc += part[u * K + o];
+    } else if (o == K) {
+        for (int64_t u = threadIdx.x; u < units; u += kReduceThreads) acc += scal[u * kScal];
     } else {
-        const int j = o - K;
-        for (int64_t u = threadIdx.x; u < units; u += kReduceThreads) acc += scal[u * kScal + j];
+        const int j = (o - K - 1) / ndim, d = (o - K - 1) % ndim;
+        // the units of direction j: (image b, tile t) -> ((b ndirs + j) tiles + t)
+        for (int64_t i = threadIdx.x; i < images * tiles; i += kReduceThreads) {
+            const int64_t b = i / tiles, t = i % tiles;
+            acc += scal[((b * ndirs + j) * tiles + t) * kScal + 1 + d];
+        }
     }
     red[threadIdx.x] = acc;
     __syncthreads();
@@ -764,17 +810,19 @@ cudaError_t soft_run_fwd(const SoftLayout &L, const float *img, const float *tau
     const SoftGeom g = soft_geom(L);
     const int64_t ncoord = g.nz + L.Hy + L.W;
     soft_coords_kernel<<<(unsigned)((ncoord + 255) / 256), 256, 0, s>>>(coords, g.nz, L.Hy, L.W);
-    dim3 grid((unsigned)L.tiles, (unsigned)L.batch);
+    const dim3 grid((unsigned)L.tiles, (unsigned)L.batch);
     if (L.ndim == 3)
-        soft_prep_kernel<3><<<grid, kPrepThreads, 0, s>>>(img, alpha, u, tau, L.K, l2, coords,
-                                                          counts, entries, g);
+        soft_prep_kernel<3><<<grid, kPrepThreads, 0, s>>>(img, alpha, u, L.ndirs, tau, L.K, l2,
+                                                          coords, counts, entries, g);
     else
-        soft_prep_kernel<2><<<grid, kPrepThreads, 0, s>>>(img, alpha, u, tau, L.K, l2, coords,
-                                                          counts, entries, g);
-    soft_fwd_kernel<<<grid, kSoftThreads, 0, s>>>(tau, L.K, l2, counts, entries, part, L.tiles);
-    const int64_t nout = L.batch * L.K;
+        soft_prep_kernel<2><<<grid, kPrepThreads, 0, s>>>(img, alpha, u, L.ndirs, tau, L.K, l2,
+                                                          coords, counts, entries, g);
+    // one block per unit (tile, image x direction)
+    const dim3 ugrid((unsigned)L.tiles, (unsigned)(L.batch * L.ndirs));
+    soft_fwd_kernel<<<ugrid, kSoftThreads, 0, s>>>(tau, L.K, l2, counts, entries, part, L.tiles);
+    const int64_t nout = L.batch * L.ndirs * L.K;
     soft_fwd_reduce_kernel<<<(unsigned)((nout + 255) / 256), 256, 0, s>>>(part, out, L.K, L.tiles,
-                                                                          L.batch);
+                                                                          L.batch * L.ndirs);
     return cudaGetLastError();
 }
 
@@ -790,31 +838,25 @@ cudaError_t soft_run_bwd(const SoftLayout &L, const float *img, const float *tau
     double *part = reinterpret_cast<double *>(base + L.off_part);
     double *scal = reinterpret_cast<double *>(base + L.off_scal);
     const SoftGeom g = soft_geom(L);
-    if (grad_img) {
-        cudaError_t e = cudaMemsetAsync(grad_img, 0,
-                                        sizeof(float) * (size_t)(L.batch * L.D * L.Hy * L.W), s);
-        if (e != cudaSuccess) return e;
-    }
-    dim3 grid((unsigned)L.tiles, (unsigned)L.batch);
+    const dim3 grid((unsigned)L.tiles, (unsigned)L.batch);
     const float l2 = lambda_log2e(lambda);
     if (L.ndim == 3)
-        soft_bwd_kernel<3><<<grid, kSoftThreads, 0, s>>>(img, tau, L.K, lambda, l2, alpha,
-                                                         grad_out, counts, entries, coords, part,
-                                                         scal, grad_img, g);
+        soft_bwd_kernel<3><<<grid, kSoftThreads, 0, s>>>(img, tau, L.K, L.ndirs, lambda, l2,
+                                                         alpha, grad_out, counts, entries, coords,
+                                                         part, scal, grad_img, g);
     else
-        soft_bwd_kernel<2><<<grid, kSoftThreads, 0, s>>>(img, tau, L.K, lambda, l2, alpha,
-                                                         grad_out, counts, entries, coords, part,
-                                                         scal, grad_img, g);
-    const int64_t units = L.batch * L.tiles;
-    soft_bwd_reduce_kernel<<<(unsigned)(L.K + 1 + L.ndim), kReduceThreads, 0, s>>>(
-        part, scal, L.K, units, grad_tau, grad_alpha, grad_u);
+        soft_bwd_kernel<2><<<grid, kSoftThreads, 0, s>>>(img, tau, L.K, L.ndirs, lambda, l2,
+                                                         alpha, grad_out, counts, entries, coords,
+                                                         part, scal, grad_img, g);
+    soft_bwd_reduce_kernel<<<(unsigned)(L.K + 1 + L.ndirs * L.ndim), kReduceThreads, 0, s>>>(
+        part, scal, L.K, L.ndim, L.ndirs, L.batch, L.tiles, grad_tau, grad_alpha, grad_u);
     return cudaGetLastError();
 }
 
 cudaError_t soft_run_stats(const SoftLayout &L, const void *ws, int64_t *stats, cudaStream_t s)
 {
     const int *counts = reinterpret_cast<const int *>(static_cast<const char *>(ws) + L.off_counts);
-    soft_stats_kernel<<<1, kReduceThreads, 0, s>>>(counts, L.batch * L.tiles, stats);
+    soft_stats_kernel<<<1, kReduceThreads, 0, s>>>(counts, L.batch * L.ndirs * L.tiles, stats);
     return cudaGetLastError();
 }
 

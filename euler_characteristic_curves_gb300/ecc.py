@@ -5,7 +5,8 @@ device pointers, sizes and the current CUDA stream, and turns negative status co
 exceptions. There is no CPU path: CPU tensors are rejected, and a missing library raises.
 
 Names follow the C entry points: ``ecc_hard``, ``ecc_soft_fwd``, ``ecc_soft_bwd``,
-``ecc_soft_stats``, ``ecc_soft_fwd_noalloc``, ``soft_workspace_bytes``; ``SoftECC`` / ``soft_ecc`` wrap the soft pair as a differentiable
+``ecc_soft_stats``, ``ecc_soft_fwd_noalloc``, ``ecc_soft_ect_fwd``, ``ecc_soft_ect_bwd``,
+``ecc_soft_ect_stats``, ``soft_workspace_bytes``; ``SoftECT`` / ``soft_ect`` wrap the transform; ``SoftECC`` / ``soft_ecc`` wrap the soft pair as a differentiable
 PyTorch layer ("Key designs -- differentiable ECC layer (sigmoid relaxation)" in the paper notes
 "Scalable GPU-Accelerated Euler Characteristic Curves").
 """
@@ -50,6 +51,14 @@ def load_library():
         lib.ecc_soft_fwd.restype = i
         lib.ecc_soft_bwd.argtypes = [p, i, p, i64, p, i, f, p, p, p, p, p, p, p, p, sz, p]
         lib.ecc_soft_bwd.restype = i
+        lib.ecc_soft_ect_workspace_bytes.argtypes = [i, p, i64, i, i]
+        lib.ecc_soft_ect_workspace_bytes.restype = sz
+        lib.ecc_soft_ect_fwd.argtypes = [p, i, p, i64, p, i, f, p, p, i, p, p, sz, p]
+        lib.ecc_soft_ect_fwd.restype = i
+        lib.ecc_soft_ect_bwd.argtypes = [p, i, p, i64, p, i, f, p, p, i, p, p, p, p, p, p, sz, p]
+        lib.ecc_soft_ect_bwd.restype = i
+        lib.ecc_soft_ect_stats.argtypes = [i, p, i64, i, i, p, sz, p, p]
+        lib.ecc_soft_ect_stats.restype = i
         lib.ecc_soft_stats.argtypes = [i, p, i64, i, p, sz, p, p]
         lib.ecc_soft_stats.restype = i
         lib.ecc_soft_fwd_noalloc.argtypes = [p, i, p, i64, p, i, f, p, p, p, p]
@@ -138,9 +147,10 @@ def ecc_hard(img: torch.Tensor, nbins: int, vmin: float, vmax: float, ndim: int 
     return out if batched else out[0]
 
 
-def soft_workspace_bytes(dims, batch: int, K: int) -> int:
+def soft_workspace_bytes(dims, batch: int, K: int, ndirs: int = 1) -> int:
     lib = load_library()
-    return int(lib.ecc_soft_workspace_bytes(len(dims), _dims_array(dims), int(batch), int(K)))
+    return int(lib.ecc_soft_ect_workspace_bytes(len(dims), _dims_array(dims), int(batch), int(K),
+                                                int(ndirs)))
 
 
 def _soft_common(img, tau, alpha, u, ndim):
@@ -158,8 +168,8 @@ def _soft_common(img, tau, alpha, u, ndim):
     return ndim, batch, dims, batched
 
 
-def _workspace(ws, dims, batch, K, device):
-    need = soft_workspace_bytes(dims, batch, K)
+def _workspace(ws, dims, batch, K, device, ndirs=1):
+    need = soft_workspace_bytes(dims, batch, K, ndirs)
     if need == 0:
         raise ValueError("unsupported soft-ECC sizes")
     if ws is None:
@@ -249,6 +259,121 @@ def ecc_soft_bwd(img, tau, lam: float, alpha, u, grad_out, ws, want_img: bool = 
     if want_img:
         res["grad_img"] = gi
     return res
+
+
+def _ect_common(img, tau, alpha, U, ndim):
+    _need_cuda(U, "u")
+    if U.dim() != 2:
+        raise ValueError("directions must have shape [n_dirs, ndim]")
+    ndim = U.shape[1] if ndim is None else ndim
+    if U.shape[1] != ndim:
+        raise ValueError(f"directions must have {ndim} components")
+    for name, t in (("tau", tau), ("alpha", alpha)):
+        _need_cuda(t, name)
+        if t.dtype != torch.float32:
+            raise TypeError(f"{name} must be float32")
+    if U.dtype != torch.float32:
+        raise TypeError("u must be float32")
+    _need_cuda(img, "img")
+    if img.dtype != torch.float32:
+        raise TypeError("soft ECC takes float32 images")
+    if alpha.numel() != 1:
+        raise ValueError("alpha must have 1 element")
+    ndim, batch, dims, batched = _split(img, ndim)
+    return ndim, batch, dims, batched, U.shape[0]
+
+
+def ecc_soft_ect_fwd(img, tau, lam: float, alpha, U, ws=None, out=None, ndim=None, stream=None):
+    """Soft Euler characteristic transform S[b, j, k]: the soft ECC of image b along direction
+    U[j] (U: float32 CUDA [n_dirs, ndim]). Returns (S, ws); pass ws unchanged to the backward."""
+    ndim, batch, dims, batched, nd = _ect_common(img, tau, alpha, U, ndim)
+    K = tau.numel()
+    ws = _workspace(ws, dims, batch, K, img.device, nd)
+    if out is None:
+        out = torch.empty((batch, nd, K), dtype=torch.float32, device=img.device)
+    lib = load_library()
+    rc = lib.ecc_soft_ect_fwd(ctypes.c_void_p(img.data_ptr()), ndim, _dims_array(dims), batch,
+                              ctypes.c_void_p(tau.data_ptr()), K, float(lam),
+                              ctypes.c_void_p(alpha.data_ptr()), ctypes.c_void_p(U.data_ptr()),
+                              nd, ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(ws.data_ptr()),
+                              ws.numel(), _stream_handle(stream))
+    _check(rc, "ecc_soft_ect_fwd")
+    out = out.view(batch, nd, K)
+    return (out if batched else out[0]), ws
+
+
+def ecc_soft_ect_bwd(img, tau, lam: float, alpha, U, grad_out, ws, want_img: bool = False,
+                     ndim=None, stream=None):
+    """Gradients of sum(grad_out * S) for the transform: grad_tau [K], grad_alpha [1],
+    grad_u [n_dirs, ndim] and, when want_img, grad_img (summed over directions)."""
+    ndim, batch, dims, batched, nd = _ect_common(img, tau, alpha, U, ndim)
+    K = tau.numel()
+    _need_cuda(grad_out, "grad_out")
+    if grad_out.dtype != torch.float32 or grad_out.numel() != batch * nd * K:
+        raise ValueError("grad_out must be float32 with batch * n_dirs * K elements")
+    ws = _workspace(ws, dims, batch, K, img.device, nd)
+    dev = img.device
+    gt = torch.empty(K, dtype=torch.float32, device=dev)
+    ga = torch.empty(1, dtype=torch.float32, device=dev)
+    gu = torch.empty((nd, ndim), dtype=torch.float32, device=dev)
+    gi = torch.empty_like(img) if want_img else None
+    lib = load_library()
+    rc = lib.ecc_soft_ect_bwd(ctypes.c_void_p(img.data_ptr()), ndim, _dims_array(dims), batch,
+                              ctypes.c_void_p(tau.data_ptr()), K, float(lam),
+                              ctypes.c_void_p(alpha.data_ptr()), ctypes.c_void_p(U.data_ptr()),
+                              nd, ctypes.c_void_p(grad_out.data_ptr()),
+                              ctypes.c_void_p(gt.data_ptr()), ctypes.c_void_p(ga.data_ptr()),
+                              ctypes.c_void_p(gu.data_ptr()),
+                              ctypes.c_void_p(gi.data_ptr() if gi is not None else None),
+                              ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream_handle(stream))
+    _check(rc, "ecc_soft_ect_bwd")
+    res = {"grad_tau": gt, "grad_alpha": ga, "grad_u": gu}
+    if want_img:
+        res["grad_img"] = gi
+    return res
+
+
+def ecc_soft_ect_stats(img, K: int, ndirs: int, ws, ndim=None, stream=None) -> torch.Tensor:
+    """ecc_soft_stats for a workspace filled by ecc_soft_ect_fwd."""
+    _need_cuda(img, "img")
+    _need_cuda(ws, "ws")
+    ndim, batch, dims, _ = _split(img, 2 if ndim is None and img.dim() != 4 else ndim)
+    stats = torch.empty(3, dtype=torch.int64, device=img.device)
+    rc = load_library().ecc_soft_ect_stats(ndim, _dims_array(dims), batch, int(K), int(ndirs),
+                                           ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+                                           ctypes.c_void_p(stats.data_ptr()),
+                                           _stream_handle(stream))
+    _check(rc, "ecc_soft_ect_stats")
+    return stats
+
+
+class SoftECT(torch.autograd.Function):
+    """Differentiable soft Euler characteristic transform: S = SoftECT.apply(img, tau, alpha, U, lam).
+
+    img float32 [(B,) H, W] or [(B,) D, H, W]; U [n_dirs, ndim] directions; tau [K]; alpha [1];
+    returns [(B,) n_dirs, K]. Gradients flow to tau, alpha, U and, when it requires grad, img.
+    """
+
+    @staticmethod
+    def forward(ctx, img, tau, alpha, U, lam):
+        img, tau, alpha, U = (t.contiguous() for t in (img, tau, alpha, U))
+        out, ws = ecc_soft_ect_fwd(img, tau, lam, alpha, U)
+        ctx.save_for_backward(img, tau, alpha, U, ws)
+        ctx.lam = float(lam)
+        return out
+
+    @staticmethod
+    def backward(ctx, grad_out):
+        img, tau, alpha, U, ws = ctx.saved_tensors
+        res = ecc_soft_ect_bwd(img, tau, ctx.lam, alpha, U, grad_out.contiguous().float(), ws,
+                               want_img=ctx.needs_input_grad[0])
+        gi = res.get("grad_img")
+        return (gi, res["grad_tau"], res["grad_alpha"].view_as(alpha), res["grad_u"].view_as(U),
+                None)
+
+
+def soft_ect(img, tau, alpha, U, lam: float):
+    return SoftECT.apply(img, tau, alpha, U, lam)
 
 
 class SoftECC(torch.autograd.Function):

@@ -57,6 +57,7 @@ enum ecc_status {
 
 #define ECC_MAX_NBINS 4096 /* largest nbins accepted by ecc_hard */
 #define ECC_MAX_K 8192     /* largest number of soft thresholds */
+#define ECC_MAX_DIRS 4096  /* largest number of directions of the soft transform */
 
 /*
  * Hard Euler characteristic curve of a batch of 2-D images or 3-D volumes.
@@ -136,6 +137,46 @@ int ecc_soft_bwd(const float *img, int ndim, const int64_t *dims, int64_t batch,
                  int K, float lambda, const float *alpha, const float *u, const float *grad_out,
                  float *grad_tau, float *grad_alpha, float *grad_u, float *grad_img, void *ws,
                  size_t ws_bytes, ecc_stream_t stream);
+
+/*
+ * Soft Euler characteristic transform: the soft ECC along several directions at once.
+ *
+ * Section "Limitations" of the ECC paper notes: the layer takes one direction, while the Euler
+ * characteristic transform integrates the curve over many. For direction j (u_j = u[j * ndim ..])
+ * the transform's curve is the soft ECC of the filtration X_j = alpha f + u_j . x, exactly as
+ * ecc_soft_fwd defines it:
+ *   out[(b * ndirs + j) * K + k] = ecc_soft_fwd(image b, u_j)[k]
+ * One pass reads each image tile once for all directions.
+ *
+ * Arguments as for ecc_soft_fwd, plus:
+ * u       device float32 [ndirs][ndim] directions (any length, zero allowed).
+ * ndirs   1 <= ndirs <= ECC_MAX_DIRS, and batch * ndirs <= 65535.
+ * out     device float32 [batch][ndirs][K]; fully overwritten.
+ * ws      at least ecc_soft_ect_workspace_bytes(ndim, dims, batch, K, ndirs) bytes, 256-aligned.
+ * With ndirs = 1 the calls compute exactly what ecc_soft_fwd / ecc_soft_bwd compute.
+ */
+size_t ecc_soft_ect_workspace_bytes(int ndim, const int64_t *dims, int64_t batch, int K,
+                                    int ndirs);
+int ecc_soft_ect_fwd(const float *img, int ndim, const int64_t *dims, int64_t batch,
+                     const float *tau, int K, float lambda, const float *alpha, const float *u,
+                     int ndirs, float *out, void *ws, size_t ws_bytes, ecc_stream_t stream);
+
+/*
+ * Backward pass of the transform: analytic gradients of
+ * L = sum_{b,j,k} grad_out[(b * ndirs + j) * K + k] * out[(b * ndirs + j) * K + k].
+ * grad_tau [K] and grad_alpha [1] sum over images and directions; grad_u [ndirs][ndim] holds one
+ * gradient per direction; grad_img (nullable, [batch][dims...]) sums over directions. All device
+ * float32, fully overwritten. Same arguments and workspace as the forward call.
+ */
+int ecc_soft_ect_bwd(const float *img, int ndim, const int64_t *dims, int64_t batch,
+                     const float *tau, int K, float lambda, const float *alpha, const float *u,
+                     int ndirs, const float *grad_out, float *grad_tau, float *grad_alpha,
+                     float *grad_u, float *grad_img, void *ws, size_t ws_bytes,
+                     ecc_stream_t stream);
+
+/* ecc_soft_stats for a workspace filled by ecc_soft_ect_fwd (stats[0] sums over directions). */
+int ecc_soft_ect_stats(int ndim, const int64_t *dims, int64_t batch, int K, int ndirs,
+                       const void *ws, size_t ws_bytes, int64_t *stats, ecc_stream_t stream);
 
 /*
  * Size of the soft forward pass's work list -- a diagnostic with no counterpart in the paper

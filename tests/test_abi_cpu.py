@@ -135,6 +135,26 @@ def test_soft_stats_validation(lib):
     assert st(2, d2, 1, 8, ctypes.c_void_p(0x100008), need, FAKE, None) == EWS
 
 
+def test_ect_validation(lib):
+    d2 = dims(16, 16)
+    w = lib.ecc_soft_ect_workspace_bytes
+    assert w(2, d2, 1, 8, 1) == lib.ecc_soft_workspace_bytes(2, d2, 1, 8)
+    assert w(2, d2, 1, 8, 4) > w(2, d2, 1, 8, 1)
+    assert w(2, d2, 1, 8, 0) == 0
+    assert w(2, d2, 1, 8, 4097) == 0
+    assert w(2, d2, 300, 8, 300) == 0  # batch * directions above 65535
+    need = w(2, d2, 1, 8, 4)
+    ws = ctypes.c_void_p(0x100000)
+    f = lib.ecc_soft_ect_fwd
+    assert f(FAKE, 2, d2, 1, FAKE, 8, 50.0, FAKE, FAKE, 0, FAKE, ws, need, None) == EINVAL
+    assert f(FAKE, 2, d2, 1, FAKE, 8, 50.0, FAKE, FAKE, 4097, FAKE, ws, need, None) == ERANGE
+    assert f(FAKE, 2, d2, 1, FAKE, 8, 50.0, FAKE, None, 4, FAKE, ws, need, None) == EINVAL
+    assert f(FAKE, 2, d2, 1, FAKE, 8, 50.0, FAKE, FAKE, 4, FAKE, ws, need - 1, None) == EWS
+    b = lib.ecc_soft_ect_bwd
+    assert b(FAKE, 2, d2, 1, FAKE, 8, 50.0, FAKE, FAKE, 4, None, FAKE, FAKE, FAKE, None, ws,
+             need, None) == EINVAL
+
+
 def test_binding_rejects_cpu_tensors():
     import torch
 
