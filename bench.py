@@ -54,6 +54,9 @@ WORKLOADS = {
     # the soft Euler characteristic transform: 16 GRF images of 256^2 along 32 directions
     # (a soft part with a ninth field, the number of directions)
     "ect": [("soft", (256, 256), 16, 128, 50.0, 12, 13, 14, 32)],
+    # the 1024^3 volume streamed from page-locked host memory in 64-plane slabs (a hard part
+    # with a ninth field, the slab length): the out-of-core path, bound by the host link
+    "3d1024stream": [("hard", (1024, 1024, 1024), 1, "f32", 256, 0.0, 1.0, 4, 64)],
 }
 WORKLOADS["headline"] = WORKLOADS["2d8192"] + WORKLOADS["3d1024"] + WORKLOADS["soft"]
 
@@ -61,6 +64,11 @@ DESCRIPTION = {
     "headline": "hard ECC 2D 8192^2 f32 nbins 1024 + 3D 1024^3 f32 nbins 256; "
                 "soft ECC fwd+bwd 64x256^2 f32 K 128 lambda 50",
 }
+
+
+def part_slab(p):
+    """Slab length of a streamed hard part (0: the volume is resident on the device)."""
+    return p[8] if p[0] == "hard" and len(p) > 8 else 0
 
 
 def part_dirs(p):
@@ -222,7 +230,12 @@ def make_inputs(parts, device):
     inputs = []
     for p in parts:
         if p[0] == "hard":
-            _, shape, batch, kind, nbins, vmin, vmax, seed = p
+            _, shape, batch, kind, nbins, vmin, vmax, seed = p[:8]
+            if part_slab(p):
+                img = synthetic.grf(shape, seed, device=device)
+                inputs.append({"host": img.cpu().pin_memory(), "ndim": len(shape)})
+                del img
+                continue
             if kind == "u8blur":
                 img = torch.from_numpy(synthetic.blurred_noise_u8(shape, seed)).to(device)
             elif kind == "u8grf":
@@ -264,7 +277,11 @@ class OurStep:
         self.parts, self.inputs = parts, inputs
         self.outs = []
         for p, x in zip(parts, inputs):
-            if p[0] == "hard":
+            if p[0] == "hard" and part_slab(p):
+                nbytes = ecc.hard_stream_buffer_bytes(p[1], torch.float32, part_slab(p))
+                self.outs.append({"out": torch.empty(p[4], dtype=torch.int64, device=device),
+                                  "buf": torch.empty(nbytes, dtype=torch.uint8, device=device)})
+            elif p[0] == "hard":
                 self.outs.append(torch.empty((x["img"].shape[0], p[4]), dtype=torch.int64,
                                              device=device))
             else:
@@ -280,7 +297,10 @@ class OurStep:
 
     def run_part(self, i):
         p, x, o = self.parts[i], self.inputs[i], self.outs[i]
-        if p[0] == "hard":
+        if p[0] == "hard" and part_slab(p):
+            self.ecc.ecc_hard_stream(x["host"], p[4], p[5], p[6], slab_planes=part_slab(p),
+                                     buf=o["buf"], out=o["out"])
+        elif p[0] == "hard":
             self.ecc.ecc_hard(x["img"], p[4], p[5], p[6], ndim=x["ndim"], out=o)
         elif part_dirs(p) == 1:
             self.ecc.ecc_soft_fwd(x["img"], x["tau"], x["lam"], x["alpha"], x["u"], ws=o["ws"],
@@ -307,7 +327,7 @@ class OurStep:
         res = []
         for p, o in zip(self.parts, self.outs):
             if p[0] == "hard":
-                res.append(o)
+                res.append(o["out"] if part_slab(p) else o)
             else:
                 res.append(o["s"])
                 res.extend(o["grads"].values())
@@ -361,7 +381,10 @@ def time_e2e(args, parts, inputs, step, device, world):
     for x in inputs:
         hx = {}
         for k, v in x.items():
-            if isinstance(v, torch.Tensor):
+            if isinstance(v, torch.Tensor) and not v.is_cuda:
+                # a streamed volume already lives in host memory: the call copies it itself
+                h2d += v.numel() * v.element_size()
+            elif isinstance(v, torch.Tensor):
                 hv = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
                 hv.copy_(v)
                 hx[k] = hv
@@ -423,7 +446,7 @@ def oracle_sample_step(parts, cache):
         key = part_name(p)
         if key not in cache:
             if p[0] == "hard":
-                _, shape, batch, kind, nbins, vmin, vmax, seed = p
+                _, shape, batch, kind, nbins, vmin, vmax, seed = p[:8]
                 if len(shape) == 2:
                     sh = (min(shape[0], SAMPLE_2D), min(shape[1], SAMPLE_2D))
                 else:
@@ -575,6 +598,8 @@ def main(argv=None):
             elem = 1 if p[3].startswith("u8") else 4
             alg = part_voxels(p) * elem + 8 * p[2] * p[4]
             ent["hbm_gbs"] = round(alg / (ms * 1e-3) / 1e9, 1)
+            if part_slab(p):  # streamed: every voxel crosses the host link once per step
+                ent["link_gbs"] = ent["hbm_gbs"]
             ent["hbm_frac"] = round(alg / (ms * 1e-3) / 1e9 / peak, 4)
         if p[0] == "soft":
             ent.update(soft_roofline(p, ms, soft_stats[part_name(p)], clocks))

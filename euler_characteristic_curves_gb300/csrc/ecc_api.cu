@@ -35,6 +35,59 @@ static bool mul_ok(int64_t a, int64_t b, int64_t &r)
     return true;
 }
 
+// Key constants and threshold table of a hard ECC call (shared by the resident and the streamed
+// entry points): the u8 key table, or the fp32 thresholds and the estimator constants.
+void hard_keys(int dtype, int nbins, double vmin, double vmax, HardPlan &pl, float *table)
+{
+    const int H = nbins;
+    pl.key_a = pl.key_b = pl.key_clo = pl.key_chi = 0.0f;
+    if (dtype == ECC_U8) {
+        // fp16 key pattern of every byte value: 0x6400 + (first k with b <= t_k; H if none)
+        uint16_t lut[256];
+        for (int v = 0; v < 256; ++v) {
+            int lo = 0, hi = H;
+            while (lo < hi) {
+                const int mid = (lo + hi) / 2;
+                if ((double)v <= threshold(mid, H, vmin, vmax))
+                    hi = mid;
+                else
+                    lo = mid + 1;
+            }
+            lut[v] = (uint16_t)(0x6400 + lo);
+        }
+        memcpy(table, lut, sizeof(lut));
+        pl.key_mode = kKeyLut;
+    } else {
+        for (int k = 0; k < H; ++k) table[k] = round_down_f32(threshold(k, H, vmin, vmax));
+        table[H] = table[H + 1] = INFINITY;
+        // Estimator of the fractional bin t* = v s + o, s = (H-1)/(vmax-vmin), o = -vmin s (the
+        // key is ceil(t*) clamped to [0, H]): u = sat(v a + b), a = -s/H, b = (H - 1/2 - o)/H,
+        // t = (H - 1/2) - H u. For an unsaturated value (|v| <= M + (vmax-vmin)/(H-1),
+        // M = max(|vmin|, |vmax|)), |t - t*| collects the rounding of a and b (2^-24 |v| s and
+        // 2^-24 |H - 1/2 - o|), of the FMA for u (2^-24, times H), of the FMA for t and of the
+        // constants H - 1/2 -+ E (2^-24 H each), and the fp64 rounding of the thresholds:
+        //     |t - t*| < dev = 2^-24 (M s + |o| + 5 H + 2).
+        // The kernel proves a key when ceil(t - E) == ceil(t + E); E = 1.25 dev must stay
+        // below 1/4 (then the saturated ends t = -1/2, H - 1/2 are never ambiguous), else
+        // every key is binary-searched.
+        pl.key_mode = kKeySearch;
+        if (H >= 2 && vmax > vmin) {
+            const double sc = (double)(H - 1) / (vmax - vmin);
+            const double o = -vmin * sc;
+            const double M = fmax(fabs(vmin), fabs(vmax));
+            const double E = 1.25 * ldexp(1.0, -24) * (M * sc + fabs(o) + 5.0 * H + 2.0);
+            if (isfinite(sc) && sc < 1e30 && E <= 0.25) {
+                pl.key_mode = kKeyEstimate;
+                pl.key_a = (float)(-sc / H);
+                pl.key_b = (float)((H - 0.5 - o) / H);
+                pl.key_clo = (float)(H - 0.5 - E);
+                pl.key_chi = (float)(H - 0.5 + E);
+            }
+        }
+    }
+    pl.table = table;
+}
+
 }  // namespace ecc
 
 using namespace ecc;
@@ -88,54 +141,9 @@ int ecc_hard(const void *img, int dtype, int ndim, const int64_t *dims, int64_t 
     pl.img = img;
     pl.out = out;
     float table[ECC_MAX_NBINS + 2];
-    const int H = nbins;
-    pl.key_a = pl.key_b = pl.key_clo = pl.key_chi = 0.0f;
-    if (dtype == ECC_U8) {
-        // fp16 key pattern of every byte value: 0x6400 + (first k with b <= t_k; H if none)
-        uint16_t lut[256];
-        for (int v = 0; v < 256; ++v) {
-            int lo = 0, hi = H;
-            while (lo < hi) {
-                const int mid = (lo + hi) / 2;
-                if ((double)v <= threshold(mid, H, vmin, vmax))
-                    hi = mid;
-                else
-                    lo = mid + 1;
-            }
-            lut[v] = (uint16_t)(0x6400 + lo);
-        }
-        memcpy(table, lut, sizeof(lut));
-        pl.key_mode = kKeyLut;
-        pl.vec_ok = ((uintptr_t)img % 4 == 0) && (W % 4 == 0);
-    } else {
-        for (int k = 0; k < H; ++k) table[k] = round_down_f32(threshold(k, H, vmin, vmax));
-        table[H] = table[H + 1] = INFINITY;
-        // Estimator of the fractional bin t* = v s + o, s = (H-1)/(vmax-vmin), o = -vmin s (the
-        // key is ceil(t*) clamped to [0, H]): u = sat(v a + b), a = -s/H, b = (H - 1/2 - o)/H,
-        // t = (H - 1/2) - H u. For an unsaturated value (|v| <= M + (vmax-vmin)/(H-1),
-        // M = max(|vmin|, |vmax|)), |t - t*| collects the rounding of a and b (2^-24 |v| s and
-        // 2^-24 |H - 1/2 - o|), of the FMA for u (2^-24, times H), of the FMA for t and of the
-        // constants H - 1/2 -+ E (2^-24 H each), and the fp64 rounding of the thresholds:
-        //     |t - t*| < dev = 2^-24 (M s + |o| + 5 H + 2).
-        // The kernel proves a key when ceil(t - E) == ceil(t + E); E = 1.25 dev must stay
-        // below 1/4 (then the saturated ends t = -1/2, H - 1/2 are never ambiguous), else
-        // every key is binary-searched.
-        pl.key_mode = kKeySearch;
-        if (H >= 2 && vmax > vmin) {
-            const double sc = (double)(H - 1) / (vmax - vmin);
-            const double o = -vmin * sc;
-            const double M = fmax(fabs(vmin), fabs(vmax));
-            const double E = 1.25 * ldexp(1.0, -24) * (M * sc + fabs(o) + 5.0 * H + 2.0);
-            if (isfinite(sc) && sc < 1e30 && E <= 0.25) {
-                pl.key_mode = kKeyEstimate;
-                pl.key_a = (float)(-sc / H);
-                pl.key_b = (float)((H - 0.5 - o) / H);
-                pl.key_clo = (float)(H - 0.5 - E);
-                pl.key_chi = (float)(H - 0.5 + E);
-            }
-        }
-        pl.vec_ok = ((uintptr_t)img % 16 == 0) && (W % 4 == 0);
-    }
+    hard_keys(dtype, nbins, vmin, vmax, pl, table);
+    const size_t align = dtype == ECC_U8 ? 4 : 16;
+    pl.vec_ok = ((uintptr_t)img % align == 0) && (W % 4 == 0);
     pl.table = table;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(out, 0, sizeof(int64_t) * (size_t)outn, s) != cudaSuccess)

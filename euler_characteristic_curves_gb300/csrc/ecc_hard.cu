@@ -71,7 +71,7 @@ __device__ __forceinline__ void block_flush(const HardParams<CAP> &P, const int 
     unsigned long long *dst = reinterpret_cast<unsigned long long *>(P.out + b * (int64_t)P.H);
     for (int i = threadIdx.x; i < P.H; i += blockDim.x) {
         const int v = hist[i];
-        if (v != 0) atomicAdd(dst + i, (unsigned long long)(long long)v);
+        if (v != 0) atomicAdd(dst + i, (unsigned long long)(long long)(P.sign * v));
     }
 }
 
@@ -809,6 +809,7 @@ static cudaError_t launch_hard(const HardPlan &pl, cudaStream_t s)
     P.key_clo = pl.key_clo;
     P.key_chi = pl.key_chi;
     P.vec_ok = pl.vec_ok;
+    P.sign = pl.sign;
     const int ntab = (pl.dtype == ECC_U8) ? 128 : pl.H + 2;  // u8: 256 uint16 in 128 floats
     P.table_len = ntab;
     for (int i = 0; i < ntab; ++i) P.table[i] = pl.table[i];
@@ -858,8 +859,13 @@ static cudaError_t launch_hard(const HardPlan &pl, cudaStream_t s)
         ecc_hard3d_kernel<T, CAP, SEARCH><<<grid, kHardThreads, smem, s>>>(P);
     }
     cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    ecc_bin_scan_kernel<<<(unsigned)pl.batch, kScanThreads, 0, s>>>(pl.out, pl.H);
+    if (e != cudaSuccess || !pl.scan) return e;
+    return hard_scan(pl.out, pl.H, pl.batch, s);
+}
+
+cudaError_t hard_scan(int64_t *out, int H, int64_t batch, cudaStream_t s)
+{
+    ecc_bin_scan_kernel<<<(unsigned)batch, kScanThreads, 0, s>>>(out, H);
     return cudaGetLastError();
 }
 

@@ -47,6 +47,7 @@ struct HardParams {
     float key_a, key_b;      // estimator u = sat(v a + b), t = (H - 1/2) - H u
     float key_clo, key_chi;  // (H - 1/2) -+ E, E bounding |t - exact fractional bin|
     int vec_ok;              // rows 16-byte (f32) / 4-byte (u8) aligned and W % 4 == 0
+    int sign;                // +1, or -1 to subtract this launch's histogram from out
     // work decomposition. 2-D: warp g of an image takes rows_per_task consecutive strip-rows
     // (one more for the first rows_extra warps); 3-D: tasks are numbered tile-major and block g
     // takes tasks g, g + G, g + 2G, ...
@@ -73,8 +74,14 @@ struct HardPlan {
     const void *img;
     int64_t *out;
     const float *table;  // H + 2 thresholds (f32), or 256 uint16 key patterns (u8) in 128 floats
+    int sign = 1;        // -1: subtract the histogram from out
+    bool scan = true;    // false: leave out as a histogram (the caller scans once at the end)
 };
 cudaError_t hard_run(const HardPlan &pl, cudaStream_t s);
+// out[b][k] = running sum over k of out[b][k], for batch rows of H bins
+cudaError_t hard_scan(int64_t *out, int H, int64_t batch, cudaStream_t s);
+// key constants and threshold table of a hard ECC call (table: ECC_MAX_NBINS + 2 floats)
+void hard_keys(int dtype, int nbins, double vmin, double vmax, HardPlan &pl, float *table);
 
 struct SoftLayout {
     int ndim;

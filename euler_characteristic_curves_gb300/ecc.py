@@ -4,7 +4,7 @@ Every computation runs in the CUDA library libecc_gb300.so; this module checks s
 device pointers, sizes and the current CUDA stream, and turns negative status codes into
 exceptions. There is no CPU path: CPU tensors are rejected, and a missing library raises.
 
-Names follow the C entry points: ``ecc_hard``, ``ecc_soft_fwd``, ``ecc_soft_bwd``,
+Names follow the C entry points: ``ecc_hard``, ``ecc_hard_stream``, ``ecc_soft_fwd``, ``ecc_soft_bwd``,
 ``ecc_soft_stats``, ``ecc_soft_fwd_noalloc``, ``ecc_soft_ect_fwd``, ``ecc_soft_ect_bwd``,
 ``ecc_soft_ect_stats``, ``soft_workspace_bytes``; ``SoftECT`` / ``soft_ect`` wrap the transform; ``SoftECC`` / ``soft_ecc`` wrap the soft pair as a differentiable
 PyTorch layer ("Key designs -- differentiable ECC layer (sigmoid relaxation)" in the paper notes
@@ -45,6 +45,10 @@ def load_library():
                                ctypes.c_float, ctypes.c_size_t)
         lib.ecc_hard.argtypes = [p, i, i, p, i64, i, d, d, p, p]
         lib.ecc_hard.restype = i
+        lib.ecc_hard_stream_buffer_bytes.argtypes = [i, p, i]
+        lib.ecc_hard_stream_buffer_bytes.restype = sz
+        lib.ecc_hard_stream.argtypes = [p, i, p, i, d, d, i, p, sz, p, p]
+        lib.ecc_hard_stream.restype = i
         lib.ecc_soft_workspace_bytes.argtypes = [i, p, i64, i]
         lib.ecc_soft_workspace_bytes.restype = sz
         lib.ecc_soft_fwd.argtypes = [p, i, p, i64, p, i, f, p, p, p, p, sz, p]
@@ -145,6 +149,52 @@ def ecc_hard(img: torch.Tensor, nbins: int, vmin: float, vmax: float, ndim: int 
     _check(rc, "ecc_hard")
     out = out.view(batch, nbins)
     return out if batched else out[0]
+
+
+def hard_stream_buffer_bytes(dims, dtype, slab_planes: int) -> int:
+    """Device bytes that ecc_hard_stream needs for a [D, H, W] volume of this dtype."""
+    dt = ECC_U8 if dtype == torch.uint8 else ECC_F32
+    return int(load_library().ecc_hard_stream_buffer_bytes(dt, _dims_array(dims),
+                                                           int(slab_planes)))
+
+
+def ecc_hard_stream(img: torch.Tensor, nbins: int, vmin: float, vmax: float,
+                    slab_planes: int = 64, buf: torch.Tensor | None = None,
+                    out: torch.Tensor | None = None, device=None, stream=None) -> torch.Tensor:
+    """Hard ECC of one [D, H, W] volume that need not fit on the device: the volume (a CPU
+    tensor, page-locked for overlapped copies, or a CUDA tensor) is streamed through two slab
+    buffers of `slab_planes` planes. Returns int64 [nbins] on `device` (default cuda:0)."""
+    if not isinstance(img, torch.Tensor) or img.dim() != 3 or not img.is_contiguous():
+        raise ValueError("img must be a contiguous [D, H, W] tensor")
+    if img.dtype == torch.uint8:
+        dt = ECC_U8
+    elif img.dtype == torch.float32:
+        dt = ECC_F32
+    else:
+        raise TypeError(f"img dtype {img.dtype}: uint8 or float32 expected")
+    dev = torch.device(device) if device is not None else (
+        img.device if img.is_cuda else torch.device("cuda", 0))
+    if dev.type != "cuda":
+        raise TypeError("the streamed ECC runs on a CUDA device (there is no CPU path)")
+    dims = tuple(img.shape)
+    need = hard_stream_buffer_bytes(dims, img.dtype, slab_planes)
+    if need == 0:
+        raise ValueError("unsupported sizes for the streamed ECC")
+    if buf is None:
+        buf = torch.empty(need, dtype=torch.uint8, device=dev)
+    elif not buf.is_cuda or buf.numel() < need:
+        raise ValueError(f"buf must be a CUDA tensor of at least {need} bytes")
+    if out is None:
+        out = torch.empty(nbins, dtype=torch.int64, device=dev)
+    with torch.cuda.device(dev):
+        rc = load_library().ecc_hard_stream(ctypes.c_void_p(img.data_ptr()), dt,
+                                            _dims_array(dims), int(nbins), float(vmin),
+                                            float(vmax), int(slab_planes),
+                                            ctypes.c_void_p(buf.data_ptr()), buf.numel(),
+                                            ctypes.c_void_p(out.data_ptr()),
+                                            _stream_handle(stream))
+    _check(rc, "ecc_hard_stream")
+    return out
 
 
 def soft_workspace_bytes(dims, batch: int, K: int, ndirs: int = 1) -> int:

@@ -87,6 +87,36 @@ int ecc_hard(const void *img, int dtype, int ndim, const int64_t *dims, int64_t 
              double vmin, double vmax, int64_t *out, ecc_stream_t stream);
 
 /*
+ * Hard ECC of one 3-D volume read in slabs of planes from memory the device need not hold
+ * (host memory, pinned or pageable, or device memory), for volumes larger than device memory.
+ *
+ * Section "Limitations" of the ECC paper notes: the full scan is limited by device memory on
+ * very large 3-D grids. Cut the volume into slabs of planes [a_i, b_i] with b_i = a_{i+1}
+ * (consecutive slabs share one plane). Every cell of the volume lies in a slab, and the cells of
+ * two consecutive slabs overlap in the cells of their shared plane, so for every threshold
+ *   ECC(volume) = sum_i ECC_3D(slab i) - sum_{i > 0} ECC_2D(plane a_i).
+ * The call computes exactly ecc_hard(volume) this way: slab i is copied into one of two device
+ * buffers on a second stream while slab i - 1 is processed on `stream`, every slab and shared
+ * plane adds or subtracts its histogram in `out`, and one running sum ends the call.
+ *
+ * img          the volume [D][H][W] (batch 1), uint8 or float32, in any memory the device can
+ *              copy from; page-locked host memory lets the copies overlap the kernels.
+ * dims         host array {D, H, W}, each >= 1.
+ * nbins, vmin, vmax   as for ecc_hard.
+ * slab_planes  planes per slab, >= 2 (each slab after the first advances slab_planes - 1 planes).
+ * dev_buf      device scratch of at least ecc_hard_stream_buffer_bytes(dtype, dims,
+ *              slab_planes) bytes, 256-byte aligned, caller-owned; contents are overwritten.
+ * out          device int64 [nbins]; fully overwritten.
+ * The call creates and destroys one stream and four events of its own; it returns once the
+ * work is queued (the copies from pageable host memory wait for the host, as cudaMemcpyAsync
+ * does). Returns ECC_OK or a negative status (ECC_EWS for a short or misaligned dev_buf).
+ */
+size_t ecc_hard_stream_buffer_bytes(int dtype, const int64_t *dims, int slab_planes);
+int ecc_hard_stream(const void *img, int dtype, const int64_t *dims, int nbins, double vmin,
+                    double vmax, int slab_planes, void *dev_buf, size_t dev_buf_bytes,
+                    int64_t *out, ecc_stream_t stream);
+
+/*
  * Workspace bytes that ecc_soft_fwd / ecc_soft_bwd need for these sizes (0 when the sizes are
  * invalid). The workspace holds the per-voxel critical list written by the forward call and read
  * by the backward call, plus per-block partial sums.

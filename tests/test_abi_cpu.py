@@ -155,6 +155,27 @@ def test_ect_validation(lib):
              need, None) == EINVAL
 
 
+def test_stream_validation(lib):
+    d3 = dims(10, 16, 16)
+    bb = lib.ecc_hard_stream_buffer_bytes
+    assert bb(1, d3, 4) == 2 * 4 * 16 * 16 * 4  # two buffers of four f32 planes (256-aligned)
+    assert bb(0, d3, 4) == 2 * 1024  # u8: 4 * 16 * 16 bytes, rounded to 256, twice
+    assert bb(1, d3, 64) == 2 * 10 * 16 * 16 * 4  # at most the whole volume
+    assert bb(1, d3, 1) == 0 and bb(7, d3, 4) == 0 and bb(1, dims(0, 4, 4), 4) == 0
+    need = bb(1, d3, 4)
+    buf = ctypes.c_void_p(0x100000)
+    st = lib.ecc_hard_stream
+    assert st(None, 1, d3, 8, 0.0, 1.0, 4, buf, need, FAKE, None) == EINVAL
+    assert st(FAKE, 1, d3, 8, 0.0, 1.0, 4, buf, need, None, None) == EINVAL
+    assert st(FAKE, 5, d3, 8, 0.0, 1.0, 4, buf, need, FAKE, None) == EDTYPE
+    assert st(FAKE, 1, dims(10, 0, 16), 8, 0.0, 1.0, 4, buf, need, FAKE, None) == EDIM
+    assert st(FAKE, 1, d3, 8, 0.0, 1.0, 1, buf, need, FAKE, None) == EINVAL
+    assert st(FAKE, 1, d3, 4097, 0.0, 1.0, 4, buf, need, FAKE, None) == ERANGE
+    assert st(FAKE, 1, d3, 8, 1.0, 0.0, 4, buf, need, FAKE, None) == EINVAL
+    assert st(FAKE, 1, d3, 8, 0.0, 1.0, 4, buf, need - 1, FAKE, None) == EWS
+    assert st(FAKE, 1, d3, 8, 0.0, 1.0, 4, ctypes.c_void_p(0x100010), need, FAKE, None) == EWS
+
+
 def test_binding_rejects_cpu_tensors():
     import torch
 
