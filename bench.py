@@ -313,6 +313,29 @@ class OurStep:
             o["grads"] = self.ecc.ecc_soft_ect_bwd(x["img"], x["tau"], x["lam"], x["alpha"],
                                                    x["u"], x["g"], o["ws"], ndim=len(p[1]))
 
+    def link_peaks(self):
+        """Per streamed part: the host-to-device copy rate of its whole host volume in one
+        cudaMemcpyAsync (GB/s), the ceiling of the streamed path."""
+        import torch
+
+        out = {}
+        for p, x, o in zip(self.parts, self.inputs, self.outs):
+            if p[0] == "hard" and part_slab(p):
+                h = x["host"]
+                d = torch.empty(h.shape, dtype=h.dtype, device=o["out"].device)
+                d.copy_(h, non_blocking=True)
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for _ in range(3):
+                    d.copy_(h, non_blocking=True)
+                e1.record()
+                torch.cuda.synchronize()
+                ms = e0.elapsed_time(e1) / 3
+                out[part_name(p)] = round(h.numel() * h.element_size() / (ms * 1e-3) / 1e9, 1)
+                del d
+        return out
+
     def soft_stats(self):
         """Per soft part: [listed voxels, direct-form tiles, tiles] of the last forward pass."""
         out = {}
@@ -367,6 +390,7 @@ def time_ours(args, parts, rank, world, device):
                for i in range(len(parts))]
     total_ms = max_over_ranks(total_ms, world)
     soft_stats = step.soft_stats()
+    soft_stats["_link_peaks"] = step.link_peaks()
     e2e = time_e2e(args, parts, inputs, step, device, world)
     return total_ms, part_ms, clocks, step.launches_per_step * args.steps, e2e, soft_stats
 
@@ -600,6 +624,10 @@ def main(argv=None):
             ent["hbm_gbs"] = round(alg / (ms * 1e-3) / 1e9, 1)
             if part_slab(p):  # streamed: every voxel crosses the host link once per step
                 ent["link_gbs"] = ent["hbm_gbs"]
+                lp = soft_stats["_link_peaks"].get(part_name(p))
+                if lp:
+                    ent["link_peak_gbs"] = lp  # one plain copy of the host volume, measured
+                    ent["link_frac"] = round(ent["link_gbs"] / lp, 4)
             ent["hbm_frac"] = round(alg / (ms * 1e-3) / 1e9 / peak, 4)
         if p[0] == "soft":
             ent.update(soft_roofline(p, ms, soft_stats[part_name(p)], clocks))

@@ -14,7 +14,7 @@
 // (key H, "never"), so the steady state has no boundary branches.
 //
 // 2-D: a warp owns a strip of 128 columns (four per lane, one 16-byte load per lane per row) and
-// walks down a band of rows; raw rows are prefetched three rows ahead in registers, and the
+// walks down a band of rows; raw rows are prefetched four rows ahead in registers, and the
 // comparisons with the row below are reused as the "above" comparisons of the next row. The
 // keys just left and right of the strip ride on the rotated row shuffles.
 //
@@ -302,10 +302,11 @@ __device__ __forceinline__ void band2d(const T *__restrict__ img, int Hy, int W,
     RowCursor<T> rc = row_cursor(img, c, y0 - 1, min(y1 + 1, Hy), W);
     KeyRow ka = key_row<T, SEARCH>(next_row<FULL>(rc, c), K, table, q);
     KeyRow kb = key_row<T, SEARCH>(next_row<FULL>(rc, c), K, table, q);
-    // raw-row ring: at the start of step y, q0 / q1 / q2 (in rotation) hold rows y+1 .. y+3
+    // raw-row ring: at the start of step y, q0 .. q3 (in rotation) hold rows y+1 .. y+4
     Raw<T> q0 = next_row<FULL>(rc, c);
     Raw<T> q1 = next_row<FULL>(rc, c);
     Raw<T> q2 = next_row<FULL>(rc, c);
+    Raw<T> q3 = next_row<FULL>(rc, c);
     uint32_t Sp0, Sp1;
     sp_init(ka, kb, Sp0, Sp1);
 
@@ -326,6 +327,7 @@ __device__ __forceinline__ void band2d(const T *__restrict__ img, int Hy, int W,
         ECC_2D_STEP(q0)
         ECC_2D_STEP(q1)
         ECC_2D_STEP(q2)
+        ECC_2D_STEP(q3)
     }
 #undef ECC_2D_STEP
 }
