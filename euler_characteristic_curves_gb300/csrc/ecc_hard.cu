@@ -39,6 +39,9 @@ namespace ecc {
 constexpr int kHardThreads = 256;
 constexpr int kHardWarps = kHardThreads / kWarp;
 constexpr int kStrip = 128;  // columns per warp strip / block tile
+// Tables of at most this many bins take the stencil's flags from the FMA pipe (exact for keys
+// up to 1024; see flag_lt / flag_le), larger ones from fp16 compares.
+constexpr int kSatMaxBins = 1024;
 
 // Resident blocks per SM the kernels are compiled for (register budget 65536 / (256 * blocks)).
 #ifndef ECC_2D_MIN_BLOCKS
@@ -293,7 +296,7 @@ __device__ __forceinline__ Raw<uint8_t> next_row(RowCursor<uint8_t> &rc, const C
 
 // One band: rows y0 .. y1 - 1 of the strip at x0 (FULL: all 128 columns exist and rows are
 // 16-byte / 4-byte aligned, so each lane reads its four values with one load).
-template <typename T, bool SEARCH, bool FULL>
+template <typename T, bool SEARCH, bool FULL, bool SAT>
 __device__ __forceinline__ void band2d(const T *__restrict__ img, int Hy, int W, const Cols &c,
                                        int y0, int y1, const LaneShuffle &q, const KeyConsts &K,
                                        const float *__restrict__ table, uint32_t hist_s)
@@ -308,7 +311,7 @@ __device__ __forceinline__ void band2d(const T *__restrict__ img, int Hy, int W,
     Raw<T> q2 = next_row<FULL>(rc, c);
     Raw<T> q3 = next_row<FULL>(rc, c);
     uint32_t Sp0, Sp1;
-    sp_init(ka, kb, Sp0, Sp1);
+    sp_init<SAT>(ka, kb, Sp0, Sp1);
 
 #define ECC_2D_STEP(QS)                                                                     \
     {                                                                                       \
@@ -316,7 +319,7 @@ __device__ __forceinline__ void band2d(const T *__restrict__ img, int Hy, int W,
         const KeyRow kd = key_row<T, SEARCH>(QS, K, table, q);                              \
         QS = next_row<FULL>(rc, c);                                                         \
         uint32_t c0, c1;                                                                    \
-        c2_quad(ka, kb, kd, kBias, Sp0, Sp1, c0, c1);                                       \
+        c2_quad<SAT>(ka, kb, kd, kBias, Sp0, Sp1, c0, c1);                                  \
         hist_pair(kb.own0, c0, hist_s);                                            \
         hist_pair(kb.own1, c1, hist_s);                                            \
         ka = kb;                                                                            \
@@ -362,10 +365,11 @@ __global__ void __launch_bounds__(kHardThreads, ECC_2D_MIN_BLOCKS) ecc_hard2d_ke
         const int y0 = (int)(i - (uint32_t)strip * (uint32_t)Hy);
         const int y1 = min(Hy, y0 + (int)(iend - i));
         const Cols c = strip_cols(strip * kStrip, W, lane, vec_ok);
+        constexpr bool SAT = CAP <= kSatMaxBins;
         if (c.full)  // warp-uniform
-            band2d<T, SEARCH, true>(img, Hy, W, c, y0, y1, q, K, table, hist_s);
+            band2d<T, SEARCH, true, SAT>(img, Hy, W, c, y0, y1, q, K, table, hist_s);
         else
-            band2d<T, SEARCH, false>(img, Hy, W, c, y0, y1, q, K, table, hist_s);
+            band2d<T, SEARCH, false, SAT>(img, Hy, W, c, y0, y1, q, K, table, hist_s);
         i += (uint32_t)(y1 - y0);
     }
     block_flush(P, hist, b);
@@ -597,6 +601,25 @@ __device__ __forceinline__ void store_plane_keys(const PlaneRaw<uint8_t> &p, con
         dst[pc.extra_half] = (uint16_t)(p.extra < 256u ? (uint32_t)lut[p.extra] : never);
 }
 
+// The 3-D fold for one pair: c = cS - [k_{z+1} < k_z] c2(M_z) - [k_{z-1} <= k_z] c2(M_{z-1}),
+// from cs = 1280 + c2(S_z), cn = c2(M_z), cm = c2(M_{z-1}) (plain fp16 values) and the keys of the
+// voxel (k), of the voxel above (up_k) and below (dn_k). SAT: flags and products on the FMA pipe.
+template <bool SAT>
+__device__ __forceinline__ uint32_t fold3(uint32_t cs, uint32_t cn, uint32_t cm, uint32_t up_k,
+                                          uint32_t dn_k, uint32_t k)
+{
+    if (SAT) {
+        const uint32_t up = h2_sub_sat(k, up_k);                     // [k_{z+1} < k_z]
+        const uint32_t dn = h2_sub_sat(h2_add(k, kOnePair), dn_k);  // [k_{z-1} <= k_z]
+        uint32_t t;
+        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(t) : "r"(cm), "r"(dn));
+        asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(t) : "r"(cn), "r"(up), "r"(t));
+        return h2_sub(cs, t);
+    }
+    const uint32_t up = h2_lt_mask(up_k, k), dn = h2_le_mask(dn_k, k);
+    return h2_sub(h2_sub(cs, cn & up), cm & dn);
+}
+
 // Buffer row r (= tile row r - 1, r = 0 .. 9) around the lane's four columns.
 __device__ __forceinline__ KeyRow smem_key_row(const uint16_t *buf, int r, int lane)
 {
@@ -635,6 +658,7 @@ __global__ void __launch_bounds__(kHardThreads, ECC_3D_MIN_BLOCKS) ecc_hard3d_ke
     const int64_t D = P.D;
     const int Hy = (int)P.Hy, W = (int)P.W;
     const uint32_t kPlain = 0u;  // bias of the M stencil: plain c values
+    constexpr bool SAT = CAP <= kSatMaxBins;
     const uint32_t hist_s = (uint32_t)__cvta_generic_to_shared(hist) - 4u * kKeyBase;
 
     for (int64_t t = blockIdx.x; t < Tn; t += G) {
@@ -670,8 +694,8 @@ __global__ void __launch_bounds__(kHardThreads, ECC_3D_MIN_BLOCKS) ecc_hard3d_ke
             const KeyRow pd = smem_key_row(keybuf[0], warp + 2, lane);
             const KeyRow ma = max_rows(pa, ca), mb = max_rows(pb, cb), md = max_rows(pd, cd);
             uint32_t s0, s1;
-            sp_init(ma, mb, s0, s1);
-            c2_quad(ma, mb, md, kPlain, s0, s1, cm0, cm1);
+            sp_init<SAT>(ma, mb, s0, s1);
+            c2_quad<SAT>(ma, mb, md, kPlain, s0, s1, cm0, cm1);
             below0 = pb.own0;
             below1 = pb.own1;
         }
@@ -689,18 +713,14 @@ __global__ void __launch_bounds__(kHardThreads, ECC_3D_MIN_BLOCKS) ecc_hard3d_ke
         const KeyRow nb = smem_key_row(NBUF, warp + 1, lane);                               \
         const KeyRow nd = smem_key_row(NBUF, warp + 2, lane);                               \
         uint32_t s0, s1, cs0, cs1, cn0, cn1;                                                \
-        sp_init(ca, cb, s0, s1);                                                            \
-        c2_quad(ca, cb, cd, kBias, s0, s1, cs0, cs1);                                       \
+        sp_init<SAT>(ca, cb, s0, s1);                                                       \
+        c2_quad<SAT>(ca, cb, cd, kBias, s0, s1, cs0, cs1);                                  \
         const KeyRow ma = max_rows(ca, na), mb = max_rows(cb, nb), md = max_rows(cd, nd);   \
-        sp_init(ma, mb, s0, s1);                                                            \
-        c2_quad(ma, mb, md, kPlain, s0, s1, cn0, cn1);                                      \
+        sp_init<SAT>(ma, mb, s0, s1);                                                       \
+        c2_quad<SAT>(ma, mb, md, kPlain, s0, s1, cn0, cn1);                                 \
         /* c = cS - [k_{z+1} < k_z] c2(M_z) - [k_{z-1} <= k_z] c2(M_{z-1}) */                \
-        const uint32_t up0 = h2_lt_mask(nb.own0, cb.own0);                                  \
-        const uint32_t up1 = h2_lt_mask(nb.own1, cb.own1);                                  \
-        const uint32_t dn0 = h2_le_mask(below0, cb.own0);                                   \
-        const uint32_t dn1 = h2_le_mask(below1, cb.own1);                                   \
-        hist_pair(cb.own0, h2_sub(h2_sub(cs0, cn0 & up0), cm0 & dn0), hist_s);              \
-        hist_pair(cb.own1, h2_sub(h2_sub(cs1, cn1 & up1), cm1 & dn1), hist_s);              \
+        hist_pair(cb.own0, fold3<SAT>(cs0, cn0, cm0, nb.own0, below0, cb.own0), hist_s);   \
+        hist_pair(cb.own1, fold3<SAT>(cs1, cn1, cm1, nb.own1, below1, cb.own1), hist_s);   \
         cm0 = cn0;                                                                          \
         cm1 = cn1;                                                                          \
         below0 = cb.own0;                                                                   \

@@ -188,14 +188,40 @@ __device__ __forceinline__ uint32_t lop_or_and(uint32_t a, uint32_t b, uint32_t 
 {
     return a | (b & c);
 }
+// The same 1.0 / 0.0 flags from the FMA pipe instead of the (half-rate) ALU pipe. Key patterns
+// of keys k <= 1024 are the fp16 values 1024 + k, integers below 2048 and so exact, as are their
+// differences. Hence [a < p] = sat(p - a), and [a <= p] = sat((p + 1) - a) wherever p + 1 is
+// exact, i.e. for every centre with key < 1024. Centres whose key is H ("never") may get a wrong
+// flag, but their contributions are discarded. So the forms hold for every table of at most 1024
+// bins (checked exhaustively over all key pairs in tests/test_kernel_algebra.py).
+__device__ __forceinline__ uint32_t h2_sub_sat(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("sub.rn.sat.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+constexpr uint32_t kOnePair = 0x3C003C00u;  // (1.0, 1.0)
+template <bool SAT>
+__device__ __forceinline__ uint32_t flag_lt(uint32_t a, uint32_t p)  // [a < p]
+{
+    return SAT ? h2_sub_sat(p, a) : h2_lt(a, p);
+}
+template <bool SAT>
+__device__ __forceinline__ uint32_t flag_le(uint32_t a, uint32_t p, uint32_t p1)  // [a <= p]
+{
+    return SAT ? h2_sub_sat(p1, a) : h2_le(a, p);
+}
+
+template <bool SAT>
 __device__ __forceinline__ uint32_t c2_pair(uint32_t p, uint32_t L, uint32_t R, uint32_t aL,
                                             uint32_t aR, uint32_t d, uint32_t dL, uint32_t dR,
                                             uint32_t Sp, uint32_t bias, uint32_t &S_out)
 {
-    const uint32_t W = h2_le(L, p), E = h2_lt(R, p);
-    const uint32_t S = h2_lt(d, p);
-    const uint32_t NW = h2_le(aL, p), NE = h2_le(aR, p);
-    const uint32_t SW = h2_lt(dL, p), SE = h2_lt(dR, p);
+    const uint32_t p1 = SAT ? h2_add(p, kOnePair) : p;
+    const uint32_t W = flag_le<SAT>(L, p, p1), E = flag_lt<SAT>(R, p);
+    const uint32_t S = flag_lt<SAT>(d, p);
+    const uint32_t NW = flag_le<SAT>(aL, p, p1), NE = flag_le<SAT>(aR, p, p1);
+    const uint32_t SW = flag_lt<SAT>(dL, p), SE = flag_lt<SAT>(dR, p);
     const uint32_t A = lop_or_and(Sp, E, NE);
     const uint32_t B = E & ~(S & SE);
     const uint32_t C = S & ~(W & SW);
@@ -207,23 +233,25 @@ __device__ __forceinline__ uint32_t c2_pair(uint32_t p, uint32_t L, uint32_t R, 
 // Local Euler contributions of the lane's four pixels of row b (rows a above, d below).
 // Returns the pairs (bias + c) in c0 (pixels x, x+1) and c1 (x+2, x+3); Sp0/Sp1 carry the
 // "pixel above is not earlier" flags in, and the S flags of this row out (for the row below).
+template <bool SAT>
 __device__ __forceinline__ void c2_quad(const KeyRow &a, const KeyRow &b, const KeyRow &d,
                                         uint32_t bias, uint32_t &Sp0, uint32_t &Sp1, uint32_t &c0,
                                         uint32_t &c1)
 {
     uint32_t S0, S1;
-    c0 = c2_pair(b.own0, b.L0, b.R0, a.L0, a.R0, d.own0, d.L0, d.R0, Sp0, bias, S0);
-    c1 = c2_pair(b.own1, b.R0, b.R1, a.R0, a.R1, d.own1, d.R0, d.R1, Sp1, bias, S1);
+    c0 = c2_pair<SAT>(b.own0, b.L0, b.R0, a.L0, a.R0, d.own0, d.L0, d.R0, Sp0, bias, S0);
+    c1 = c2_pair<SAT>(b.own1, b.R0, b.R1, a.R0, a.R1, d.own1, d.R0, d.R1, Sp1, bias, S1);
     Sp0 = S0;
     Sp1 = S1;
 }
 
 // Sp for the first row of a band: [b < a] per pixel (the row above is not earlier).
+template <bool SAT>
 __device__ __forceinline__ void sp_init(const KeyRow &a, const KeyRow &b, uint32_t &Sp0,
                                         uint32_t &Sp1)
 {
-    Sp0 = h2_lt(b.own0, a.own0);
-    Sp1 = h2_lt(b.own1, a.own1);
+    Sp0 = flag_lt<SAT>(b.own0, a.own0);
+    Sp1 = flag_lt<SAT>(b.own1, a.own1);
 }
 
 // 0xFFFF / 0x0000 per half: a < b, a <= b (masks, for selecting with bitwise AND)

@@ -180,3 +180,33 @@ def test_soft3d_contribution_extremes():
     r = np.where(dist <= 2, 0, 100)
     r[1, 1, 1] = 50
     assert c3_soft_model(r)[1, 1, 1] == 7
+
+
+# ---------------------------------------------------------------------------------------------
+# Stencil flags from saturating fp16 subtraction (tables of at most 1024 bins)
+# ---------------------------------------------------------------------------------------------
+
+def test_saturating_flags_equal_the_comparisons_for_every_key_pair():
+    """For key patterns 0x6400 + k (k <= 1024, fp16 value 1024 + k) the kernels take
+    [a < p] = sat(p - a) and [a <= p] = sat((p + 1) - a). Check every pair of keys exhaustively
+    in fp16 arithmetic: both are exact for every centre p with key below 1024 (a counted voxel of
+    a table of at most 1024 bins), and the flags are the bit patterns 0x3C00 (1.0) / 0x0000."""
+    k = np.arange(0, 1025)
+    vals = (np.uint16(0x6400) + k.astype(np.uint16)).view(np.float16)
+    a, p = vals[:, None], vals[None, :]
+    one = np.float16(1.0)
+
+    def sat(x):
+        return np.clip(x, np.float16(0), np.float16(1)).astype(np.float16)
+
+    lt = sat((p - a).astype(np.float16))
+    le = sat(((p + one).astype(np.float16) - a).astype(np.float16))
+    ka, kp = k[:, None], k[None, :]
+    np.testing.assert_array_equal(lt == 1, ka < kp)
+    counted = k < 1024
+    np.testing.assert_array_equal((le == 1)[:, counted], (ka <= kp)[:, counted])
+    assert set(np.unique(lt.view(np.uint16))) == {0, 0x3C00}
+    assert set(np.unique(le.view(np.uint16))) == {0, 0x3C00}
+    # beyond key 1023 the +1 is no longer exact in fp16, which is why larger tables compare
+    v = (np.uint16(0x6400) + np.arange(1024, 1100).astype(np.uint16)).view(np.float16)
+    assert not np.all((v + one).astype(np.float16) - v == one)
