@@ -74,6 +74,17 @@ def test_2d_batches_and_large_ragged():
     check(f, 1024, 0.0, 1.0)
 
 
+@pytest.mark.parametrize("nbins", [1023, 1024, 1025, 4096])
+def test_nbins_variants_3d(nbins):
+    """3-D at the boundary between the saturating flags (tables of up to 1024 bins) and the fp16
+    compares (larger tables), f32 and uint8."""
+    f = synthetic.grf((19, 37, 140), nbins)
+    check(f, nbins, 0.0, 1.0)
+    check(f, nbins, 0.3, 0.6)
+    q = synthetic.quantise_u8(f)
+    check(q, nbins, 0.0, 255.0)
+
+
 @pytest.mark.parametrize("nbins", [1, 2, 3, 255, 256, 1000, 1024, 1025, 4096])
 def test_nbins_variants(nbins):
     f = synthetic.grf((97, 203), nbins)
