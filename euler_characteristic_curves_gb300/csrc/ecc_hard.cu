@@ -24,9 +24,11 @@
 // each max-pixel into the voxel that carries it gives one contribution per voxel p = (x, y, z):
 //     c(p) = c2(S_z; p) - [k_{z+1} < k_z] c2(M_z; x,y) - [k_{z-1} <= k_z] c2(M_{z-1}; x,y)
 // (the later voxel wins ties; the max of two keys is the key of the max). A block owns a tile of
-// 128 columns x 8 rows and walks z; each plane's keys are computed once into a shared tile with a
-// one-pixel halo, from which every warp builds the three rows around its own row. The raw values
-// of the next plane are loaded into registers one plane ahead.
+// 128 columns x 32 rows and walks z; each plane's keys are computed once into a shared tile with a
+// one-pixel halo. A warp owns eight consecutive rows: it builds the rows around them from the
+// shared keys of planes z and z + 1 once per plane and reuses them down its rows, so the row
+// building, the max rows and the first-row flags are paid once per eight rows. The raw values of
+// the next plane are loaded into registers one plane ahead.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -43,7 +45,8 @@ constexpr int kStrip = 128;  // columns per warp strip / block tile
 // up to 1024; see flag_lt / flag_le), larger ones from fp16 compares.
 constexpr int kSatMaxBins = 1024;
 
-// Resident blocks per SM the kernels are compiled for (register budget 65536 / (256 * blocks)).
+// Resident blocks per SM the kernels are compiled for (register budget 65536 / (threads * blocks);
+// 2-D blocks have 256 threads, 3-D blocks k3Threads).
 #ifndef ECC_2D_MIN_BLOCKS
 #define ECC_2D_MIN_BLOCKS 3
 #endif
@@ -379,23 +382,64 @@ __global__ void __launch_bounds__(kHardThreads, ECC_2D_MIN_BLOCKS) ecc_hard2d_ke
 // 3-D kernel
 // ----------------------------------------------------------------------------------------------
 //
-// Work: block task = (tile of 128 columns x 8 rows) x (chunk of rows_per_task planes), tile x
-// fastest, then tile y, then chunk; block g of an image takes tasks g, g + G, ... Warp w owns row
-// y0 + w, lane l columns x0 + 4l .. x0 + 4l + 3.
+// Work: block task = (tile of 128 columns x kTileRows rows) x (chunk of rows_per_task planes),
+// tile x fastest, then tile y, then chunk; block g of an image takes tasks g, g + G, ... Warp w
+// owns the k3Rows rows y0 + w k3Rows .. y0 + (w + 1) k3Rows - 1 of the tile, lane l columns
+// x0 + 4l .. x0 + 4l + 3 of each. A warp builds the rows around its own rows once per plane and
+// reuses them down its rows, like the 2-D bands. Of the shapes measured (one to eight rows per
+// warp, two to eight warps per block), eight rows in four-warp blocks, three blocks per SM, was
+// the fastest.
 
-constexpr int kTileRows = kHardWarps;                // 8
+#ifndef ECC_3D_ROWS
+#define ECC_3D_ROWS 8
+#endif
+#ifndef ECC_3D_WARPS
+#define ECC_3D_WARPS 4
+#endif
+constexpr int k3Rows = ECC_3D_ROWS;    // rows per warp
+constexpr int k3Warps = ECC_3D_WARPS;  // warps per block
+constexpr int k3Threads = k3Warps * kWarp;
+constexpr int kTileRows = k3Warps * k3Rows;
 constexpr int kKeyPitch = 136;                       // halves per shared row (272 bytes)
-constexpr int kKeyRowsHalo = kTileRows + 2;          // rows y0-1 .. y0+8
+constexpr int kKeyRowsHalo = kTileRows + 2;          // rows y0 - 1 .. y0 + kTileRows
 constexpr int kKeyPlane = kKeyRowsHalo * kKeyPitch;  // halves per plane buffer
 // Tile column c (-1 .. 128) sits at half index 4 + c of a shared row, so a lane's own four keys
 // form one 8-byte-aligned word pair and its outer neighbours sit in the 4-byte words before and
 // after it.
+static_assert(kKeyPitch >= 4 + kStrip + 1 && kKeyPitch % 4 == 0, "shared key row layout");
 
-// The raw values one thread needs for one plane of the tile: its warp's row (four columns), one
-// value of the two halo rows (thread t: row y0 - 1 or y0 + 8 by t >> 7, column x0 - 1 + (t & 127)),
-// and for warp 0 one "extra" value: lanes 0..7 the column left of rows y0 .. y0+7, lanes 8..15
-// the column right of them, lanes 16..19 the halo-row columns x0 + 127 and x0 + 128. Positions
-// outside the grid read as NaN (f32) or 256 (u8), both meaning "never".
+// The halo of a plane: the rows above and below the tile (130 columns each, x0 - 1 .. x0 + 128),
+// then the columns left and right of the tile (kTileRows rows each). Thread t loads halo items
+// t, t + k3Threads, ... ("slots"); only the last slot is partly empty.
+constexpr int kHaloRowItems = kStrip + 2;
+constexpr int kHaloItems = 2 * kHaloRowItems + 2 * kTileRows;
+constexpr int kHaloSlots = (kHaloItems + k3Threads - 1) / k3Threads;
+
+__device__ __forceinline__ void halo_item(int i, int x0, int y0, int &y, int &x, int &half)
+{
+    if (i < 2 * kHaloRowItems) {
+        const int below = i >= kHaloRowItems;
+        const int c = i - below * kHaloRowItems - 1;  // -1 .. 128
+        y = below ? y0 + kTileRows : y0 - 1;
+        x = x0 + c;
+        half = (below ? kKeyRowsHalo - 1 : 0) * kKeyPitch + 4 + c;
+    } else {
+        const int j = i - 2 * kHaloRowItems;
+        const int right = j >= kTileRows;
+        const int r = j - right * kTileRows;
+        y = y0 + r;
+        x = right ? x0 + kStrip : x0 - 1;
+        half = (1 + r) * kKeyPitch + (right ? 4 + kStrip : 3);
+    }
+}
+
+// Whether some lane of `warp` has an item in halo slot s (warp-uniform; constant but for the
+// last slot).
+__device__ __forceinline__ bool slot_active(int s, int warp)
+{
+    return s * k3Threads + warp * kWarp < kHaloItems;
+}
+
 template <typename T>
 struct HaloVal;
 template <>
@@ -409,87 +453,77 @@ struct HaloVal<uint8_t> {
     static __device__ __forceinline__ uint32_t none() { return 256u; }
 };
 
+// The raw values one thread loads from one plane: its warp's rows (four columns each; side
+// unused) and its halo items. Absent slots and positions outside the grid read as NaN (f32) or
+// 256 (u8), both meaning "never".
 template <typename T>
 struct PlaneRaw {
-    Raw<T> own;  // own.side unused
-    typename HaloVal<T>::type hrow, extra;
+    Raw<T> own[k3Rows];
+    typename HaloVal<T>::type halo[kHaloSlots];
 };
 
-struct PlaneCols {
-    Cols own;    // own.own_ok also clears every column when the warp's row is outside the grid
-    bool full;   // the warp's row exists and its four values load with one aligned load
-    int hy, hx;  // halo-row position of this thread (clamped)
-    bool h_ok;
-    int ey, ex;  // extra position (warp 0, clamped)
-    bool e_ok;
-    int hrow_half;   // shared index of the halo-row key
-    int extra_half;  // shared index of the extra key (or -1)
+// A thread's positions within a task's tile (fixed for the task).
+struct TileCols {
+    Cols own;          // own.own_ok: the lane's columns inside the grid
+    uint32_t rows_in;  // bit i: the warp's row i exists
+    int hy[kHaloSlots], hx[kHaloSlots];  // halo item positions, clamped into the grid
+    bool h_ok[kHaloSlots];               // the item exists and lies inside the grid
+    int h_half[kHaloSlots];              // shared index of the item (-1: no item)
 };
 
-__device__ __forceinline__ PlaneCols plane_cols(int x0, int y0, int Hy, int W, int warp, int lane,
-                                                bool vec_ok)
+__device__ __forceinline__ TileCols tile_cols(int x0, int y0, int Hy, int W, int warp, int lane,
+                                              bool vec_ok)
 {
-    PlaneCols pc;
-    pc.own = strip_cols(x0, W, lane, vec_ok);
-    const bool row_in = y0 + warp < Hy;
-    if (!row_in) pc.own.own_ok = 0;
-    pc.full = pc.own.full && row_in;
-    const int t = threadIdx.x;
-    const int hr = t >> 7;  // 0: row y0 - 1, 1: row y0 + 8
-    const int hy = hr ? y0 + kTileRows : y0 - 1;
-    const int hx = x0 - 1 + (t & 127);
-    pc.h_ok = hy >= 0 && hy < Hy && hx >= 0 && hx < W;
-    pc.hy = min(max(hy, 0), Hy - 1);
-    pc.hx = min(max(hx, 0), W - 1);
-    pc.hrow_half = (hr ? kKeyRowsHalo - 1 : 0) * kKeyPitch + 4 + (t & 127) - 1;
-    int ey = 0, ex = 0, eh = -1;
-    if (warp == 0 && lane < 20) {
-        if (lane < 16) {
-            ey = y0 + (lane & 7);
-            ex = (lane < 8) ? x0 - 1 : x0 + kStrip;
-            eh = (1 + (lane & 7)) * kKeyPitch + ((lane < 8) ? 3 : 4 + kStrip);
-        } else {
-            const int j = lane - 16;  // (row, column): (y0-1, x0+127), (y0-1, x0+128), ...
-            ey = (j & 2) ? y0 + kTileRows : y0 - 1;
-            ex = x0 + kStrip - 1 + (j & 1);
-            eh = ((j & 2) ? kKeyRowsHalo - 1 : 0) * kKeyPitch + 4 + kStrip - 1 + (j & 1);
-        }
+    TileCols tc;
+    tc.own = strip_cols(x0, W, lane, vec_ok);
+    tc.rows_in = 0;
+#pragma unroll
+    for (int i = 0; i < k3Rows; ++i)
+        if (y0 + warp * k3Rows + i < Hy) tc.rows_in |= 1u << i;
+#pragma unroll
+    for (int s = 0; s < kHaloSlots; ++s) {
+        const int i = (int)threadIdx.x + s * k3Threads;
+        int y = -1, x = -1, half = -1;
+        if (i < kHaloItems) halo_item(i, x0, y0, y, x, half);
+        tc.h_ok[s] = half >= 0 && y >= 0 && y < Hy && x >= 0 && x < W;
+        tc.hy[s] = min(max(y, 0), Hy - 1);
+        tc.hx[s] = min(max(x, 0), W - 1);
+        tc.h_half[s] = half;
     }
-    pc.e_ok = eh >= 0 && ey >= 0 && ey < Hy && ex >= 0 && ex < W;
-    pc.ey = min(max(ey, 0), Hy - 1);
-    pc.ex = min(max(ex, 0), W - 1);
-    pc.extra_half = eh;
-    return pc;
+    return tc;
 }
 
 // A thread's plane-by-plane reader: pointers into plane z that advance one plane per read;
 // planes outside [0, D) read as absent.
 template <typename T>
-struct PlaneCursor {
-    const T *own, *hrow, *extra;
-    int64_t stride;
-    int64_t z, D;
+struct TileCursor {
+    const T *own;  // the lane's first column in the warp's first row (row clamped into the grid)
+    const T *halo[kHaloSlots];
+    int64_t stride, z, D;
+    int W;
 };
 
 template <typename T>
-__device__ __forceinline__ PlaneCursor<T> plane_cursor(const T *__restrict__ img,
-                                                       const PlaneCols &pc, int y, int64_t z,
-                                                       int64_t D, int Hy, int W)
+__device__ __forceinline__ TileCursor<T> tile_cursor(const T *__restrict__ img, const TileCols &tc,
+                                                     int y, int64_t z, int64_t D, int Hy, int W)
 {
-    PlaneCursor<T> cur;
+    TileCursor<T> cur;
     cur.stride = (int64_t)Hy * W;
     const T *plane = img + z * cur.stride;
-    cur.own = plane + (int64_t)min(y, Hy - 1) * W + pc.own.x;
-    cur.hrow = plane + (int64_t)pc.hy * W + pc.hx;
-    cur.extra = plane + (int64_t)pc.ey * W + pc.ex;
+    cur.own = plane + (int64_t)min(y, Hy - 1) * W + tc.own.x;
+#pragma unroll
+    for (int s = 0; s < kHaloSlots; ++s) cur.halo[s] = plane + (int64_t)tc.hy[s] * W + tc.hx[s];
     cur.z = z;
     cur.D = D;
+    cur.W = W;
     return cur;
 }
 
-__device__ __forceinline__ void load_own4(const float *p, const PlaneCols &pc, Raw<float> &r)
+// Four values of one row (`full`: one aligned load; else per-column predicated loads).
+__device__ __forceinline__ void load_own4(const float *p, const Cols &c, bool full,
+                                          Raw<float> &r)
 {
-    if (pc.full) {  // warp-uniform
+    if (full) {  // warp-uniform
         const float4 q = __ldg(reinterpret_cast<const float4 *>(p));
         r.v[0] = q.x;
         r.v[1] = q.y;
@@ -497,21 +531,22 @@ __device__ __forceinline__ void load_own4(const float *p, const PlaneCols &pc, R
         r.v[3] = q.w;
     } else {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) r.v[j] = ldg_if(p + j, (pc.own.own_ok >> j) & 1u, qnan_f());
+        for (int j = 0; j < 4; ++j) r.v[j] = ldg_if(p + j, (c.own_ok >> j) & 1u, qnan_f());
     }
 }
 
-__device__ __forceinline__ void load_own4(const uint8_t *p, const PlaneCols &pc, Raw<uint8_t> &r)
+__device__ __forceinline__ void load_own4(const uint8_t *p, const Cols &c, bool full,
+                                          Raw<uint8_t> &r)
 {
-    if (pc.full) {  // warp-uniform
+    if (full) {  // warp-uniform
         r.bytes = __ldg(reinterpret_cast<const unsigned int *>(p));
     } else {
         r.bytes = 0;
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-            r.bytes |= ldg_if(p + j, (pc.own.own_ok >> j) & 1u, 0u) << (8 * j);
+            r.bytes |= ldg_if(p + j, (c.own_ok >> j) & 1u, 0u) << (8 * j);
     }
-    r.own_ok = pc.own.own_ok;
+    r.own_ok = c.own_ok;
 }
 
 __device__ __forceinline__ void absent_own(Raw<float> &r)
@@ -526,84 +561,108 @@ __device__ __forceinline__ void absent_own(Raw<uint8_t> &r)
 }
 
 template <typename T>
-__device__ __forceinline__ PlaneRaw<T> next_plane(PlaneCursor<T> &cur, const PlaneCols &pc,
-                                                  bool with_extra)
+__device__ __forceinline__ PlaneRaw<T> next_plane(TileCursor<T> &cur, const TileCols &tc,
+                                                  int warp)
 {
     using V = HaloVal<T>;
     PlaneRaw<T> p;
-    p.extra = V::none();
-    if ((uint64_t)cur.z < (uint64_t)cur.D) {  // block-uniform
-        load_own4(cur.own, pc, p.own);
-        p.hrow = ldg_if(cur.hrow, pc.h_ok, V::none());
-        if (with_extra) p.extra = ldg_if(cur.extra, pc.e_ok, V::none());  // warp-uniform
-    } else {
-        absent_own(p.own);
-        p.hrow = V::none();
+    const bool in = (uint64_t)cur.z < (uint64_t)cur.D;  // block-uniform
+#pragma unroll
+    for (int i = 0; i < k3Rows; ++i) {
+        if (in && ((tc.rows_in >> i) & 1u))  // warp-uniform
+            load_own4(cur.own + (int64_t)i * cur.W, tc.own, tc.own.full, p.own[i]);
+        else
+            absent_own(p.own[i]);
+    }
+#pragma unroll
+    for (int s = 0; s < kHaloSlots; ++s) {
+        p.halo[s] = V::none();
+        if (slot_active(s, warp)) p.halo[s] = ldg_if(cur.halo[s], in && tc.h_ok[s], V::none());
     }
     cur.own += cur.stride;
-    cur.hrow += cur.stride;
-    cur.extra += cur.stride;
+#pragma unroll
+    for (int s = 0; s < kHaloSlots; ++s) cur.halo[s] += cur.stride;
     ++cur.z;
     return p;
 }
 
 // Keys of a loaded plane into the shared buffer `dst`.
 template <bool SEARCH>
-__device__ __forceinline__ void store_plane_keys(const PlaneRaw<float> &p, const PlaneCols &pc,
+__device__ __forceinline__ void store_plane_keys(const PlaneRaw<float> &p, const TileCols &tc,
                                                  const KeyConsts &K, const float *__restrict__ T,
-                                                 int warp, int lane, bool with_extra,
-                                                 uint16_t *dst)
+                                                 int warp, int lane, uint16_t *dst)
 {
-    uint32_t k[6];
+    uint32_t k[k3Rows][4], h[kHaloSlots];
     if (SEARCH) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) k[j] = key_search_pattern(p.own.v[j], K.H, T);
-        k[4] = key_search_pattern(p.hrow, K.H, T);
-        k[5] = with_extra ? key_search_pattern(p.extra, K.H, T) : 0u;
+        for (int i = 0; i < k3Rows; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) k[i][j] = key_search_pattern(p.own[i].v[j], K.H, T);
+#pragma unroll
+        for (int s = 0; s < kHaloSlots; ++s)
+            h[s] = slot_active(s, warp) ? key_search_pattern(p.halo[s], K.H, T) : 0u;
     } else {
         uint32_t amb = 0;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) k[j] = key_fast(p.own.v[j], K, amb);
-        k[4] = key_fast(p.hrow, K, amb);
-        k[5] = key_fast(p.extra, K, amb);  // NaN (key H) outside warp 0
+        for (int i = 0; i < k3Rows; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) k[i][j] = key_fast(p.own[i].v[j], K, amb);
+#pragma unroll
+        for (int s = 0; s < kHaloSlots; ++s) {
+            h[s] = kKeyBase + (uint32_t)K.H;  // "never" in warps without an item in slot s
+            if (slot_active(s, warp)) h[s] = key_fast(p.halo[s], K, amb);
+        }
         if (__any_sync(kFull, amb != 0)) {  // rare: a value within E of a threshold
             if (amb != 0) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) k[j] = key_fix(p.own.v[j], k[j], K.H, T);
-                k[4] = key_fix(p.hrow, k[4], K.H, T);
-                k[5] = key_fix(p.extra, k[5], K.H, T);
+                for (int i = 0; i < k3Rows; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) k[i][j] = key_fix(p.own[i].v[j], k[i][j], K.H, T);
+#pragma unroll
+                for (int s = 0; s < kHaloSlots; ++s)
+                    if (slot_active(s, warp)) h[s] = key_fix(p.halo[s], h[s], K.H, T);
             }
         }
     }
-    uint16_t *row = dst + (1 + warp) * kKeyPitch;
-    *reinterpret_cast<uint2 *>(row + 4 + 4 * lane) =
-        make_uint2(prmt(k[0], k[1], 0x5410), prmt(k[2], k[3], 0x5410));
-    dst[pc.hrow_half] = (uint16_t)k[4];
-    if (with_extra && pc.extra_half >= 0) dst[pc.extra_half] = (uint16_t)k[5];
+    uint16_t *row = dst + (1 + warp * k3Rows) * kKeyPitch + 4 + 4 * lane;
+#pragma unroll
+    for (int i = 0; i < k3Rows; ++i)
+        *reinterpret_cast<uint2 *>(row + i * kKeyPitch) =
+            make_uint2(prmt(k[i][0], k[i][1], 0x5410), prmt(k[i][2], k[i][3], 0x5410));
+#pragma unroll
+    for (int s = 0; s < kHaloSlots; ++s)
+        if (tc.h_half[s] >= 0) dst[tc.h_half[s]] = (uint16_t)h[s];
 }
 
 template <bool SEARCH>
-__device__ __forceinline__ void store_plane_keys(const PlaneRaw<uint8_t> &p, const PlaneCols &pc,
+__device__ __forceinline__ void store_plane_keys(const PlaneRaw<uint8_t> &p, const TileCols &tc,
                                                  const KeyConsts &K, const float *__restrict__ T,
-                                                 int warp, int lane, bool with_extra,
-                                                 uint16_t *dst)
+                                                 int warp, int lane, uint16_t *dst)
 {
     const uint16_t *lut = reinterpret_cast<const uint16_t *>(T);
     const uint32_t never = kKeyBase + (uint32_t)K.H;
-    Raw<uint8_t> r = p.own;
-    r.side = 256u;  // no side value in the plane loads
-    uint32_t own0, own1, unused;
-    row_keys<SEARCH>(r, K, T, own0, own1, unused);
-    uint16_t *row = dst + (1 + warp) * kKeyPitch;
-    *reinterpret_cast<uint2 *>(row + 4 + 4 * lane) = make_uint2(own0, own1);
-    dst[pc.hrow_half] = (uint16_t)(p.hrow < 256u ? (uint32_t)lut[p.hrow] : never);
-    if (with_extra && pc.extra_half >= 0)
-        dst[pc.extra_half] = (uint16_t)(p.extra < 256u ? (uint32_t)lut[p.extra] : never);
+    uint16_t *row = dst + (1 + warp * k3Rows) * kKeyPitch + 4 + 4 * lane;
+#pragma unroll
+    for (int i = 0; i < k3Rows; ++i) {
+        Raw<uint8_t> r = p.own[i];
+        r.side = 256u;  // no side value in the plane loads
+        uint32_t own0, own1, unused;
+        row_keys<SEARCH>(r, K, T, own0, own1, unused);
+        *reinterpret_cast<uint2 *>(row + i * kKeyPitch) = make_uint2(own0, own1);
+    }
+#pragma unroll
+    for (int s = 0; s < kHaloSlots; ++s)
+        if (tc.h_half[s] >= 0)
+            dst[tc.h_half[s]] =
+                (uint16_t)(p.halo[s] < 256u ? (uint32_t)lut[p.halo[s]] : never);
 }
 
-// The 3-D fold for one pair: c = cS - [k_{z+1} < k_z] c2(M_z) - [k_{z-1} <= k_z] c2(M_{z-1}),
-// from cs = 1280 + c2(S_z), cn = c2(M_z), cm = c2(M_{z-1}) (plain fp16 values) and the keys of the
-// voxel (k), of the voxel above (up_k) and below (dn_k). SAT: flags and products on the FMA pipe.
+// The 3-D fold for one pair: 1280 + c with c = cS - [k_{z+1} < k_z] c2(M_z) - [k_{z-1} <= k_z]
+// c2(M_{z-1}), from cn = c2(M_z), cm = c2(M_{z-1}) (plain fp16 values), cs = c2(S_z) (SAT: plain;
+// else 1280 + c2(S_z)) and the keys of the voxel (k), of the voxel above (up_k) and below (dn_k).
+// SAT: flags and products on the FMA pipe, the bias entering through the first product (every
+// value is an integer below 2048 in magnitude, so each fp16 step is exact).
+constexpr uint32_t kNegBias = 0xE500E500u;  // (-1280, -1280)
 template <bool SAT>
 __device__ __forceinline__ uint32_t fold3(uint32_t cs, uint32_t cn, uint32_t cm, uint32_t up_k,
                                           uint32_t dn_k, uint32_t k)
@@ -612,7 +671,7 @@ __device__ __forceinline__ uint32_t fold3(uint32_t cs, uint32_t cn, uint32_t cm,
         const uint32_t up = h2_sub_sat(k, up_k);                     // [k_{z+1} < k_z]
         const uint32_t dn = h2_sub_sat(h2_add(k, kOnePair), dn_k);  // [k_{z-1} <= k_z]
         uint32_t t;
-        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(t) : "r"(cm), "r"(dn));
+        asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(t) : "r"(cm), "r"(dn), "r"(kNegBias));
         asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(t) : "r"(cn), "r"(up), "r"(t));
         return h2_sub(cs, t);
     }
@@ -620,7 +679,7 @@ __device__ __forceinline__ uint32_t fold3(uint32_t cs, uint32_t cn, uint32_t cm,
     return h2_sub(h2_sub(cs, cn & up), cm & dn);
 }
 
-// Buffer row r (= tile row r - 1, r = 0 .. 9) around the lane's four columns.
+// Buffer row r (= tile row r - 1, r = 0 .. kTileRows + 1) around the lane's four columns.
 __device__ __forceinline__ KeyRow smem_key_row(const uint16_t *buf, int r, int lane)
 {
     const uint16_t *row = buf + r * kKeyPitch;
@@ -637,20 +696,20 @@ __device__ __forceinline__ KeyRow smem_key_row(const uint16_t *buf, int r, int l
 }
 
 template <typename T, int CAP, bool SEARCH>
-__global__ void __launch_bounds__(kHardThreads, ECC_3D_MIN_BLOCKS) ecc_hard3d_kernel(const __grid_constant__
+__global__ void __launch_bounds__(k3Threads, ECC_3D_MIN_BLOCKS) ecc_hard3d_kernel(const __grid_constant__
                                                                   HardParams<CAP> P)
 {
     extern __shared__ int smem[];
     int *hist = smem;
     float *table = reinterpret_cast<float *>(smem + hist_words(P.H));
-    __shared__ __align__(16) uint16_t keybuf[2][kKeyPlane];
+    __shared__ __align__(16) uint16_t keybuf[3][kKeyPlane];
     block_setup(P, hist, table);
 
     const int64_t b = blockIdx.y;
     const T *__restrict__ img = static_cast<const T *>(P.img) + b * P.image_elems;
     const int lane = threadIdx.x & (kWarp - 1);
     const int warp = threadIdx.x >> 5;
-    const bool with_extra = (warp == 0);
+    const int r0 = warp * k3Rows;  // buffer row of the row above the warp's first row
     const int64_t Tn = P.tasks_per_image;
     const int64_t G = P.ctas_per_image;
     const KeyConsts K = key_consts(P);
@@ -670,71 +729,81 @@ __global__ void __launch_bounds__(kHardThreads, ECC_3D_MIN_BLOCKS) ecc_hard3d_ke
         const int y0 = ty * kTileRows;
         const int64_t z0 = tz * P.rows_per_task;
         const int64_t z1 = min(z0 + (int64_t)P.rows_per_task, D);
-        const PlaneCols pc = plane_cols(x0, y0, Hy, W, warp, lane, vec_ok);
-        PlaneCursor<T> cur = plane_cursor(img, pc, y0 + warp, z0 - 1, D, Hy, W);
+        const TileCols tc = tile_cols(x0, y0, Hy, W, warp, lane, vec_ok);
+        TileCursor<T> cur = tile_cursor(img, tc, y0 + r0, z0 - 1, D, Hy, W);
 
         // prologue: keys of planes z0 - 1 (buffer 0) and z0 (buffer 1); raw plane z0 + 1 in flight
         __syncthreads();  // the previous task's readers are done with both buffers
         {
-            const PlaneRaw<T> pm = next_plane(cur, pc, with_extra);
-            const PlaneRaw<T> p0 = next_plane(cur, pc, with_extra);
-            store_plane_keys<SEARCH>(pm, pc, K, table, warp, lane, with_extra, keybuf[0]);
-            store_plane_keys<SEARCH>(p0, pc, K, table, warp, lane, with_extra, keybuf[1]);
+            const PlaneRaw<T> pm = next_plane(cur, tc, warp);
+            const PlaneRaw<T> p0 = next_plane(cur, tc, warp);
+            store_plane_keys<SEARCH>(pm, tc, K, table, warp, lane, keybuf[0]);
+            store_plane_keys<SEARCH>(p0, tc, K, table, warp, lane, keybuf[1]);
         }
-        PlaneRaw<T> pnext = next_plane(cur, pc, with_extra);
+        PlaneRaw<T> pnext = next_plane(cur, tc, warp);
         __syncthreads();
-        uint32_t cm0, cm1;        // c2(M_{z-1}) at the lane's pixels (plain values)
-        uint32_t below0, below1;  // keys of plane z - 1 at the lane's pixels
-        KeyRow ca = smem_key_row(keybuf[1], warp, lane);
-        KeyRow cb = smem_key_row(keybuf[1], warp + 1, lane);
-        KeyRow cd = smem_key_row(keybuf[1], warp + 2, lane);
+        // cm: c2(M_{z-1}) and below: the keys of plane z - 1, at the warp's own pixels.
+        uint32_t cm[k3Rows][2], below[k3Rows][2];
         {
-            const KeyRow pa = smem_key_row(keybuf[0], warp, lane);
-            const KeyRow pb = smem_key_row(keybuf[0], warp + 1, lane);
-            const KeyRow pd = smem_key_row(keybuf[0], warp + 2, lane);
-            const KeyRow ma = max_rows(pa, ca), mb = max_rows(pb, cb), md = max_rows(pd, cd);
+            KeyRow M[k3Rows + 2];
+#pragma unroll
+            for (int j = 0; j < k3Rows + 2; ++j) {
+                const KeyRow pj = smem_key_row(keybuf[0], r0 + j, lane);
+                M[j] = max_rows(pj, smem_key_row(keybuf[1], r0 + j, lane));
+                if (j >= 1 && j <= k3Rows) {
+                    below[j - 1][0] = pj.own0;
+                    below[j - 1][1] = pj.own1;
+                }
+            }
             uint32_t s0, s1;
-            sp_init<SAT>(ma, mb, s0, s1);
-            c2_quad<SAT>(ma, mb, md, kPlain, s0, s1, cm0, cm1);
-            below0 = pb.own0;
-            below1 = pb.own1;
+            sp_init<SAT>(M[0], M[1], s0, s1);
+#pragma unroll
+            for (int i = 0; i < k3Rows; ++i)
+                c2_quad<SAT, false>(M[i], M[i + 1], M[i + 2], kPlain, s0, s1, cm[i][0], cm[i][1]);
         }
-        __syncthreads();  // buffer 0 is read; plane z0 + 1 may replace it
 
-        // One barrier per plane: plane z + 1 goes to buffer (z - z0) & 1, which was last read
-        // two steps before, and every warp has passed the previous step's barrier since. The loop
-        // is unrolled by two so that the buffer and the carried rows need no register moves.
-#define ECC_3D_STEP(NBUF, ZZ)                                                               \
-    {                                                                                       \
-        store_plane_keys<SEARCH>(pnext, pc, K, table, warp, lane, with_extra, NBUF);        \
-        if ((ZZ) + 2 <= z1) pnext = next_plane(cur, pc, with_extra); /* block-uniform */    \
-        __syncthreads();                                                                    \
-        const KeyRow na = smem_key_row(NBUF, warp, lane);                                   \
-        const KeyRow nb = smem_key_row(NBUF, warp + 1, lane);                               \
-        const KeyRow nd = smem_key_row(NBUF, warp + 2, lane);                               \
-        uint32_t s0, s1, cs0, cs1, cn0, cn1;                                                \
-        sp_init<SAT>(ca, cb, s0, s1);                                                       \
-        c2_quad<SAT>(ca, cb, cd, kBias, s0, s1, cs0, cs1);                                  \
-        const KeyRow ma = max_rows(ca, na), mb = max_rows(cb, nb), md = max_rows(cd, nd);   \
-        sp_init<SAT>(ma, mb, s0, s1);                                                       \
-        c2_quad<SAT>(ma, mb, md, kPlain, s0, s1, cn0, cn1);                                 \
-        /* c = cS - [k_{z+1} < k_z] c2(M_z) - [k_{z-1} <= k_z] c2(M_{z-1}) */                \
-        hist_pair(cb.own0, fold3<SAT>(cs0, cn0, cm0, nb.own0, below0, cb.own0), hist_s);   \
-        hist_pair(cb.own1, fold3<SAT>(cs1, cn1, cm1, nb.own1, below1, cb.own1), hist_s);   \
-        cm0 = cn0;                                                                          \
-        cm1 = cn1;                                                                          \
-        below0 = cb.own0;                                                                   \
-        below1 = cb.own1;                                                                   \
-        ca = na;                                                                            \
-        cb = nb;                                                                            \
-        cd = nd;                                                                            \
-    }
-        for (int64_t z = z0; z < z1; z += 2) {
-            ECC_3D_STEP(keybuf[0], z)
-            if (z + 1 >= z1) break;
-            ECC_3D_STEP(keybuf[1], z + 1)
+        // Three buffers in a ring: at step z plane z + 1 goes to the buffer of plane z - 2, read
+        // last at step z - 1, before the barrier of step z - 1 that every warp has passed. Both
+        // planes z and z + 1 are read from shared memory, so no rows are carried in registers.
+        const uint16_t *bc = keybuf[1];
+        uint16_t *bn = keybuf[2], *bo = keybuf[0];
+        for (int64_t z = z0; z < z1; ++z) {
+            store_plane_keys<SEARCH>(pnext, tc, K, table, warp, lane, bn);
+            if (z + 2 <= z1) pnext = next_plane(cur, tc, warp);  // block-uniform
+            __syncthreads();
+            KeyRow c0 = smem_key_row(bc, r0, lane), c1 = smem_key_row(bc, r0 + 1, lane);
+            KeyRow n1 = smem_key_row(bn, r0 + 1, lane);
+            KeyRow Ma = max_rows(c0, smem_key_row(bn, r0, lane)), Mb = max_rows(c1, n1);
+            uint32_t ss0, ss1, sm0, sm1;
+            sp_init<SAT>(c0, c1, ss0, ss1);
+            sp_init<SAT>(Ma, Mb, sm0, sm1);
+#pragma unroll
+            for (int i = 0; i < k3Rows; ++i) {
+                const KeyRow c2 = smem_key_row(bc, r0 + i + 2, lane);
+                const KeyRow n2 = smem_key_row(bn, r0 + i + 2, lane);
+                uint32_t cs0, cs1, cn0, cn1;
+                c2_quad<SAT, !SAT>(c0, c1, c2, kBias, ss0, ss1, cs0, cs1);
+                const KeyRow Md = max_rows(c2, n2);
+                c2_quad<SAT, false>(Ma, Mb, Md, kPlain, sm0, sm1, cn0, cn1);
+                hist_pair(c1.own0, fold3<SAT>(cs0, cn0, cm[i][0], n1.own0, below[i][0], c1.own0),
+                          hist_s);
+                hist_pair(c1.own1, fold3<SAT>(cs1, cn1, cm[i][1], n1.own1, below[i][1], c1.own1),
+                          hist_s);
+                cm[i][0] = cn0;
+                cm[i][1] = cn1;
+                below[i][0] = c1.own0;
+                below[i][1] = c1.own1;
+                c0 = c1;
+                c1 = c2;
+                n1 = n2;
+                Ma = Mb;
+                Mb = Md;
+            }
+            const uint16_t *t = bc;
+            bc = bn;
+            bn = bo;
+            bo = const_cast<uint16_t *>(t);
         }
-#undef ECC_3D_STEP
     }
     block_flush(P, hist, b);
 }
@@ -878,7 +947,14 @@ static cudaError_t launch_hard(const HardPlan &pl, cudaStream_t s)
     if (pl.ndim == 2) {
         ecc_hard2d_kernel<T, CAP, SEARCH><<<grid, kHardThreads, smem, s>>>(P);
     } else {
-        ecc_hard3d_kernel<T, CAP, SEARCH><<<grid, kHardThreads, smem, s>>>(P);
+        // the key buffers are static shared memory; past 48 KB in all the launch must opt in
+        if (smem + sizeof(uint16_t) * 3 * kKeyPlane > 48 * 1024) {
+            const cudaError_t e = cudaFuncSetAttribute(
+                ecc_hard3d_kernel<T, CAP, SEARCH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                (int)smem);
+            if (e != cudaSuccess) return e;
+        }
+        ecc_hard3d_kernel<T, CAP, SEARCH><<<grid, k3Threads, smem, s>>>(P);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || !pl.scan) return e;

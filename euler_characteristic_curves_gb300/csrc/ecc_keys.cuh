@@ -212,7 +212,8 @@ __device__ __forceinline__ uint32_t flag_le(uint32_t a, uint32_t p, uint32_t p1)
     return SAT ? h2_sub_sat(p1, a) : h2_le(a, p);
 }
 
-template <bool SAT>
+// BIAS: return bias + c; otherwise the plain c (one add fewer).
+template <bool SAT, bool BIAS>
 __device__ __forceinline__ uint32_t c2_pair(uint32_t p, uint32_t L, uint32_t R, uint32_t aL,
                                             uint32_t aR, uint32_t d, uint32_t dL, uint32_t dR,
                                             uint32_t Sp, uint32_t bias, uint32_t &S_out)
@@ -227,20 +228,20 @@ __device__ __forceinline__ uint32_t c2_pair(uint32_t p, uint32_t L, uint32_t R, 
     const uint32_t C = S & ~(W & SW);
     const uint32_t D = W & (Sp | ~NW);
     S_out = S;
-    return h2_sub(h2_sub(h2_add(bias, A), B), h2_add(C, D));
+    return h2_sub(h2_sub(BIAS ? h2_add(bias, A) : A, B), h2_add(C, D));
 }
 
 // Local Euler contributions of the lane's four pixels of row b (rows a above, d below).
 // Returns the pairs (bias + c) in c0 (pixels x, x+1) and c1 (x+2, x+3); Sp0/Sp1 carry the
 // "pixel above is not earlier" flags in, and the S flags of this row out (for the row below).
-template <bool SAT>
+template <bool SAT, bool BIAS = true>
 __device__ __forceinline__ void c2_quad(const KeyRow &a, const KeyRow &b, const KeyRow &d,
                                         uint32_t bias, uint32_t &Sp0, uint32_t &Sp1, uint32_t &c0,
                                         uint32_t &c1)
 {
     uint32_t S0, S1;
-    c0 = c2_pair<SAT>(b.own0, b.L0, b.R0, a.L0, a.R0, d.own0, d.L0, d.R0, Sp0, bias, S0);
-    c1 = c2_pair<SAT>(b.own1, b.R0, b.R1, a.R0, a.R1, d.own1, d.R0, d.R1, Sp1, bias, S1);
+    c0 = c2_pair<SAT, BIAS>(b.own0, b.L0, b.R0, a.L0, a.R0, d.own0, d.L0, d.R0, Sp0, bias, S0);
+    c1 = c2_pair<SAT, BIAS>(b.own1, b.R0, b.R1, a.R0, a.R1, d.own1, d.R0, d.R1, Sp1, bias, S1);
     Sp0 = S0;
     Sp1 = S1;
 }

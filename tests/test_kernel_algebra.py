@@ -210,3 +210,26 @@ def test_saturating_flags_equal_the_comparisons_for_every_key_pair():
     # beyond key 1023 the +1 is no longer exact in fp16, which is why larger tables compare
     v = (np.uint16(0x6400) + np.arange(1024, 1100).astype(np.uint16)).view(np.float16)
     assert not np.all((v + one).astype(np.float16) - v == one)
+
+
+def test_fold_with_the_bias_in_the_first_product_is_exact():
+    """The 3-D kernels (tables of at most 1024 bins) form 1280 + c as
+    cs - fma(cn, up, fma(cm, dn, -1280)), with cs = c2(S_z), cn = c2(M_z), cm = c2(M_{z-1}) and
+    the 0/1 flags up, dn. Every intermediate is an integer below 2048 in magnitude, so each fp16
+    step (round to nearest) is exact; checked over every value the stencils and flags take, and
+    the low byte of the result is c as a signed byte (the histogram's sign extension)."""
+    f16 = np.float16
+    c2_vals = np.arange(-4, 5)  # c2 of a 3 x 3 neighbourhood lies in [-3, 1]; a margin around it
+    cs, cn, cm, up, dn = np.meshgrid(c2_vals, c2_vals, c2_vals, [0, 1], [0, 1], indexing="ij")
+    cs, cn, cm, up, dn = (x.ravel() for x in (cs, cn, cm, up, dn))
+
+    def h(x):
+        return np.asarray(x, dtype=np.float64).astype(f16)
+
+    t = h(h(cm) * h(dn) + h(-1280.0))     # products of small integers are exact: one rounding
+    t = h(h(cn) * h(up) + t.astype(np.float64))
+    res = h(h(cs).astype(np.float64) - t.astype(np.float64))
+    c = cs - up * cn - dn * cm
+    np.testing.assert_array_equal(res.astype(np.float64), 1280.0 + c)
+    low = (res.view(np.uint16) & 0xFF).astype(np.int64)
+    np.testing.assert_array_equal(np.where(low >= 128, low - 256, low), c)
