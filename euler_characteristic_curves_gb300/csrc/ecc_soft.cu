@@ -238,7 +238,11 @@ __device__ float tau_midpoint(const float *__restrict__ tau, int K)
 
 // Entry: {E_p, X_hi, X_lo, (index in the tile << 4) | (c + 8)}, c in [-8, 7].
 constexpr int kPadWord = 8;  // c = 0 at index 0: a padding entry that contributes nothing
-__device__ __forceinline__ int entry_c(const float4 &en) { return (__float_as_int(en.w) & 15) - 8; }
+// c as a float without a conversion instruction: 2^23 + (c + 8) is exact in fp32.
+__device__ __forceinline__ float entry_cf(const float4 &en)
+{
+    return __int_as_float(0x4B000000 | (__float_as_int(en.w) & 15)) - 8388616.0f;
+}
 __device__ __forceinline__ int entry_loc(const float4 &en) { return __float_as_int(en.w) >> 4; }
 
 // The cells of the 3-D V-construction that contain a voxel p: one direction per axis in
@@ -448,12 +452,13 @@ __device__ __forceinline__ KState k_state(const float *__restrict__ tau, int k, 
 }
 
 // r = sigma(-lambda |tau - X|) and below = [X <= tau], by the factorised or the direct form.
+// e may overflow to +inf (r = 1 * 0 = 0) or underflow to 0 (r = 0); min(e, 1) / (1 + e) is r.
 __device__ __forceinline__ float small_sigma_fact(float E, float F, bool &below)
 {
     const float e = E * F;  // exp(lambda (X - tau))
     below = e <= 1.0f;
     const float rc = rcp_approx(1.0f + e);
-    return (below ? e : 1.0f) * rc;
+    return fminf(e, 1.0f) * rc;
 }
 __device__ __forceinline__ float small_sigma_direct(const float4 &en, float t, float l2,
                                                     bool &below)
@@ -471,26 +476,34 @@ __device__ __forceinline__ void kahan_add(float &s, float &comp, float x)
     comp = (t - s) - y;
     s = t;
 }
+// Kahan step for the term a b, the product entering through one fused multiply-add.
+__device__ __forceinline__ void kahan_fma(float &s, float &comp, float a, float b)
+{
+    const float y = fmaf(a, b, -comp);
+    const float t = s + y;
+    comp = (t - s) - y;
+    s = t;
+}
 
 // Forward inner loop over staged entries for the thread's two thresholds.
+// The integer parts w0, w1 are sums of small integers (|w| <= 8 kTileCap < 2^24), exact in fp32.
 template <bool FACT>
 __device__ __forceinline__ void fwd_loop(const float4 *sh, int m_ent, const KState &s0,
-                                         const KState &s1, float l2, int &w0, int &w1, float &a0,
-                                         float &c0, float &a1, float &c1)
+                                         const KState &s1, float l2, float &w0, float &w1,
+                                         float &a0, float &c0, float &a1, float &c1)
 {
     for (int i = 0; i < m_ent; ++i) {
         const float4 en = sh[i];
-        const int c = entry_c(en);
-        const float cf = (float)c;
+        const float cf = entry_cf(en);
         bool b0, b1;
         const float r0 =
             FACT ? small_sigma_fact(en.x, s0.F, b0) : small_sigma_direct(en, s0.tau, l2, b0);
         const float r1 =
             FACT ? small_sigma_fact(en.x, s1.F, b1) : small_sigma_direct(en, s1.tau, l2, b1);
-        w0 += b0 ? c : 0;
-        w1 += b1 ? c : 0;
-        kahan_add(a0, c0, (b0 ? -cf : cf) * r0);
-        kahan_add(a1, c1, (b1 ? -cf : cf) * r1);
+        w0 += b0 ? cf : 0.0f;
+        w1 += b1 ? cf : 0.0f;
+        kahan_fma(a0, c0, b0 ? -cf : cf, r0);
+        kahan_fma(a1, c1, b1 ? -cf : cf, r1);
     }
 }
 
@@ -509,7 +522,7 @@ __global__ void __launch_bounds__(kSoftThreads) soft_fwd_kernel(
         const int k0 = kb + threadIdx.x, k1 = k0 + kSoftThreads;
         const KState s0 = k_state(tau, k0, K, l2, m), s1 = k_state(tau, k1, K, l2, m);
         const bool fact = __syncthreads_and(s0.ok && s1.ok && !(cnt & kTileFlagDirect));
-        int w0 = 0, w1 = 0;
+        float w0 = 0.f, w1 = 0.f;
         float a0 = 0.f, c0 = 0.f, a1 = 0.f, c1 = 0.f;
         for (int e0 = 0; e0 < n; e0 += kChunk) {
             const int m_ent = min(kChunk, n - e0);
@@ -552,15 +565,15 @@ __device__ __forceinline__ void bwd_group(const float4 *en8, const KState &s0, c
 #pragma unroll
     for (int j = 0; j < kGroup; ++j) {
         const float4 en = en8[j];
-        const float cf = (float)entry_c(en);
+        const float cf = entry_cf(en);
         bool b0, b1;
         const float r0 =
             FACT ? small_sigma_fact(en.x, s0.F, b0) : small_sigma_direct(en, s0.tau, l2, b0);
         const float r1 =
             FACT ? small_sigma_fact(en.x, s1.F, b1) : small_sigma_direct(en, s1.tau, l2, b1);
         const float w0 = fmaf(-r0, r0, r0), w1 = fmaf(-r1, r1, r1);
-        kahan_add(a0, c0, cf * w0);
-        kahan_add(a1, c1, cf * w1);
+        kahan_fma(a0, c0, cf, w0);
+        kahan_fma(a1, c1, cf, w1);
         qw[j][lane] = fmaf(g0, w0, g1 * w1);
     }
     __syncwarp();
@@ -666,7 +679,7 @@ __global__ void __launch_bounds__(kSoftThreads) soft_bwd_kernel(
             const int64_t gx = x0 + loc % T::X, gy = y0 + (loc / T::X) % T::Y,
                           gz = z0 + loc / (T::X * T::Y);
             const int64_t idx = (gz * g.Hy + gy) * g.W + gx;
-            const float dX = -lambda * (float)entry_c(en) * dxs[i];
+            const float dX = -lambda * entry_cf(en) * dxs[i];
             if (grad_img) gacc[loc] += alpha * dX;  // one entry per voxel and direction
             const float2 xy = __ldg(cy + gy), xx = __ldg(cx + gx);
             kahan_add(sum[0], comp[0], dX * __ldg(f + idx));
