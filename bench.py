@@ -102,10 +102,14 @@ def load_peaks():
     return 6800.0, "fallback"
 
 
-def kernel_source_hash():
+# Sources that make up the hard kernels (their recorded traffic stays valid while these hold).
+HARD_SOURCES = ("ecc_hard.cu", "ecc_internal.cuh", "ecc_keys.cuh")
+
+
+def kernel_source_hash(files=HARD_SOURCES):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "euler_characteristic_curves_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in sorted(files):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode())
             h.update(fh.read())
