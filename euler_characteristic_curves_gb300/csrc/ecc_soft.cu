@@ -57,6 +57,9 @@ constexpr int kPrepThreads = 256;
 constexpr int kSoftThreads = 64;           // each thread owns two thresholds per pass
 constexpr int kKPerPass = 2 * kSoftThreads;
 constexpr int kChunk = 256;                // entries staged in shared memory at a time
+// The backward kernel stages half as many, so that its shared memory (and registers) let a
+// full wave of blocks be resident on a 64-image batch of 256^2 images.
+constexpr int kBwdChunk = 128;
 constexpr int kGroup = 8;                  // entries per backward transpose-reduce
 constexpr int kTileFlagDirect = 1 << 30;   // count flag: an exponent of this tile is out of range
 constexpr float kExpLimit = 100.0f;
@@ -492,6 +495,7 @@ __device__ __forceinline__ void fwd_loop(const float4 *sh, int m_ent, const KSta
                                          const KState &s1, float l2, float &w0, float &w1,
                                          float &a0, float &c0, float &a1, float &c1)
 {
+#pragma unroll 4
     for (int i = 0; i < m_ent; ++i) {
         const float4 en = sh[i];
         const float cf = entry_cf(en);
@@ -599,11 +603,11 @@ __global__ void __launch_bounds__(kSoftThreads) soft_bwd_kernel(
 {
     using T = SoftTile<NDIM>;
     constexpr int NW = kSoftThreads / kWarp;
-    __shared__ __align__(16) float4 sh[kChunk];
+    __shared__ __align__(16) float4 sh[kBwdChunk];
     __shared__ __align__(16) float qbuf[NW][kGroup][kWarp];
-    __shared__ float red[NW][kChunk];
+    __shared__ float red[NW][kBwdChunk];
     __shared__ float dxs[kTileCap];
-    __shared__ float gacc[kTileCap];
+    extern __shared__ float gacc[];  // kTileCap floats, present only when grad_img is wanted
     __shared__ double scal_red[NW][kScal];
 
     const int64_t b = blockIdx.y;
@@ -638,11 +642,11 @@ __global__ void __launch_bounds__(kSoftThreads) soft_bwd_kernel(
             const float g1 = (k1 < K) ? __ldg(grad_out + bj * K + k1) : 0.0f;
             const bool fact = __syncthreads_and(s0.ok && s1.ok && !(cnt & kTileFlagDirect));
             float a0 = 0.f, c0 = 0.f, a1 = 0.f, c1 = 0.f;
-            for (int e0 = 0; e0 < n; e0 += kChunk) {
-                const int m_ent = min(kChunk, n - e0);
+            for (int e0 = 0; e0 < n; e0 += kBwdChunk) {
+                const int m_ent = min(kBwdChunk, n - e0);
                 __syncthreads();
                 // stage the chunk; pad the last group with c = 0 entries
-                for (int i = threadIdx.x; i < kChunk; i += kSoftThreads)
+                for (int i = threadIdx.x; i < kBwdChunk; i += kSoftThreads)
                     sh[i] = (i < m_ent) ? list[e0 + i]
                                         : make_float4(0.f, 0.f, 0.f, __int_as_float(kPadWord));
                 __syncthreads();
@@ -853,14 +857,16 @@ cudaError_t soft_run_bwd(const SoftLayout &L, const float *img, const float *tau
     const SoftGeom g = soft_geom(L);
     const dim3 grid((unsigned)L.tiles, (unsigned)L.batch);
     const float l2 = lambda_log2e(lambda);
+    // the image-gradient accumulator costs shared memory (and so resident blocks) only when asked
+    const size_t dyn = grad_img ? sizeof(float) * kTileCap : 0;
     if (L.ndim == 3)
-        soft_bwd_kernel<3><<<grid, kSoftThreads, 0, s>>>(img, tau, L.K, L.ndirs, lambda, l2,
-                                                         alpha, grad_out, counts, entries, coords,
-                                                         part, scal, grad_img, g);
+        soft_bwd_kernel<3><<<grid, kSoftThreads, dyn, s>>>(img, tau, L.K, L.ndirs, lambda, l2,
+                                                           alpha, grad_out, counts, entries,
+                                                           coords, part, scal, grad_img, g);
     else
-        soft_bwd_kernel<2><<<grid, kSoftThreads, 0, s>>>(img, tau, L.K, L.ndirs, lambda, l2,
-                                                         alpha, grad_out, counts, entries, coords,
-                                                         part, scal, grad_img, g);
+        soft_bwd_kernel<2><<<grid, kSoftThreads, dyn, s>>>(img, tau, L.K, L.ndirs, lambda, l2,
+                                                           alpha, grad_out, counts, entries,
+                                                           coords, part, scal, grad_img, g);
     soft_bwd_reduce_kernel<<<(unsigned)(L.K + 1 + L.ndirs * L.ndim), kReduceThreads, 0, s>>>(
         part, scal, L.K, L.ndim, L.ndirs, L.batch, L.tiles, grad_tau, grad_alpha, grad_u);
     return cudaGetLastError();
