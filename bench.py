@@ -395,7 +395,7 @@ def time_ours(args, parts, rank, world, device):
     total_ms = max_over_ranks(total_ms, world)
     soft_stats = step.soft_stats()
     soft_stats["_link_peaks"] = step.link_peaks()
-    e2e = time_e2e(args, parts, inputs, step, device, world)
+    e2e = None if args.no_e2e else time_e2e(args, parts, inputs, step, device, world)
     return total_ms, part_ms, clocks, step.launches_per_step * args.steps, e2e, soft_stats
 
 
@@ -452,6 +452,7 @@ def time_e2e(args, parts, inputs, step, device, world):
 
     one()
     torch.cuda.synchronize()
+    link = host_link_gbs(device)
     barrier(world)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
@@ -465,12 +466,33 @@ def time_e2e(args, parts, inputs, step, device, world):
     return {"value": round(hard_vox * world / (ms * 1e-3) / 1e9, 3), "unit": "Gvoxels/s",
             "ms_per_step": round(ms, 3), "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": steps,
+            "link_gbs": link, "link_floor_ms": round(h2d / (link * 1e9) * 1e3, 3),
             "path": ("3-D volumes through ecc_hard_stream from pinned host memory in "
                      f"{E2E_SLAB}-plane slabs; other parts copied and run on a second stream"
                      if streamed else "inputs copied from pinned host memory, then the step")}
 
 
 E2E_SLAB = 64  # planes per slab of a 3-D volume in the end-to-end timing
+
+
+def host_link_gbs(device, nbytes=1 << 30):
+    """Host-to-device copy rate of this machine (GB/s): one pinned buffer copied three times. The
+    end-to-end step cannot beat its input bytes at this rate; it varies between boxes."""
+    import torch
+
+    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    d.copy_(h, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(3):
+        d.copy_(h, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / 3
+    del h, d
+    return round(nbytes / (ms * 1e-3) / 1e9, 1)
 
 
 # ------------------------------------------------------------------------------------ oracle arm
@@ -618,6 +640,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="headline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the end-to-end timing (for profiler launch lists of the step)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

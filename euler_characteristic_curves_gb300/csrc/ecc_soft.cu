@@ -550,8 +550,17 @@ __global__ void soft_fwd_reduce_kernel(const double *__restrict__ part, float *_
     const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
     if (i >= batch * K) return;
     const int64_t b = i / K, k = i % K;
+    const double *__restrict__ p = part + b * tiles * K + k;
     double acc = 0.0;
-    for (int64_t t = 0; t < tiles; ++t) acc += part[(b * tiles + t) * K + k];
+    int64_t t = 0;
+    for (; t + 8 <= tiles; t += 8) {  // eight loads in flight, added in tile order
+        double v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = p[(t + j) * K];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc += v[j];
+    }
+    for (; t < tiles; ++t) acc += p[t * K];
     out[i] = (float)acc;
 }
 
@@ -612,6 +621,7 @@ __global__ void __launch_bounds__(kSoftThreads) soft_bwd_kernel(
 
     const int64_t b = blockIdx.y;
     const int64_t tile = blockIdx.x;
+    const int64_t units = (int64_t)gridDim.y * ndirs * g.tiles;  // threshold-major partials
     const int lane = threadIdx.x & (kWarp - 1), warp = threadIdx.x >> 5;
     const float m = tau_midpoint(tau, K);
     const float alpha = __ldg(alpha_p);
@@ -669,9 +679,9 @@ __global__ void __launch_bounds__(kSoftThreads) soft_bwd_kernel(
                 }
             }
             if (k0 < K)
-                part[unit * K + k0] = (double)lambda * (double)g0 * ((double)a0 - (double)c0);
+                part[k0 * units + unit] = (double)lambda * (double)g0 * ((double)a0 - (double)c0);
             if (k1 < K)
-                part[unit * K + k1] = (double)lambda * (double)g1 * ((double)a1 - (double)c1);
+                part[k1 * units + unit] = (double)lambda * (double)g1 * ((double)a1 - (double)c1);
         }
         __syncthreads();
 
@@ -725,18 +735,31 @@ __global__ void __launch_bounds__(kSoftThreads) soft_bwd_kernel(
 // output: threads take strided partials in fp64, then a fixed-order tree (deterministic).
 constexpr int kReduceThreads = 256;
 
+// One block per output: o < K grad_tau[o] (the backward kernel stores its threshold partials
+// threshold-major, so a block reads one contiguous row), o = K grad_alpha, o = K + 1 + j ndim + d
+// grad_u[j][d]. Threads take strided partials (four loads in flight, added in order), then a
+// fixed-order tree: results are deterministic.
 __global__ void __launch_bounds__(kReduceThreads) soft_bwd_reduce_kernel(
     const double *__restrict__ part, const double *__restrict__ scal, int K, int ndim, int ndirs,
     int64_t images, int64_t tiles, float *__restrict__ grad_tau, float *__restrict__ grad_alpha,
     float *__restrict__ grad_u)
 {
     __shared__ double red[kReduceThreads];
-    // o in 0..K-1: grad_tau[o]; K: grad_alpha; K + 1 + j ndim + d: grad_u[j][d]
-    const int o = blockIdx.x;
     const int64_t units = images * ndirs * tiles;
+    const int o = blockIdx.x;
     double acc = 0.0;
     if (o < K) {
-        for (int64_t u = threadIdx.x; u < units; u += kReduceThreads) acc += part[u * K + o];
+        const double *__restrict__ row = part + (int64_t)o * units;
+        int64_t u = threadIdx.x;
+        for (; u + 3 * kReduceThreads < units; u += 4 * kReduceThreads) {
+            const double v0 = row[u], v1 = row[u + kReduceThreads];
+            const double v2 = row[u + 2 * kReduceThreads], v3 = row[u + 3 * kReduceThreads];
+            acc += v0;
+            acc += v1;
+            acc += v2;
+            acc += v3;
+        }
+        for (; u < units; u += kReduceThreads) acc += row[u];
     } else if (o == K) {
         for (int64_t u = threadIdx.x; u < units; u += kReduceThreads) acc += scal[u * kScal];
     } else {
@@ -867,7 +890,8 @@ cudaError_t soft_run_bwd(const SoftLayout &L, const float *img, const float *tau
         soft_bwd_kernel<2><<<grid, kSoftThreads, dyn, s>>>(img, tau, L.K, L.ndirs, lambda, l2,
                                                            alpha, grad_out, counts, entries,
                                                            coords, part, scal, grad_img, g);
-    soft_bwd_reduce_kernel<<<(unsigned)(L.K + 1 + L.ndirs * L.ndim), kReduceThreads, 0, s>>>(
+    const unsigned rblocks = (unsigned)(L.K + 1 + L.ndirs * L.ndim);
+    soft_bwd_reduce_kernel<<<rblocks, kReduceThreads, 0, s>>>(
         part, scal, L.K, L.ndim, L.ndirs, L.batch, L.tiles, grad_tau, grad_alpha, grad_u);
     return cudaGetLastError();
 }
