@@ -454,15 +454,8 @@ __device__ __forceinline__ KState k_state(const float *__restrict__ tau, int k, 
     return s;
 }
 
-// r = sigma(-lambda |tau - X|) and below = [X <= tau], by the factorised or the direct form.
-// e may overflow to +inf (r = 1 * 0 = 0) or underflow to 0 (r = 0); min(e, 1) / (1 + e) is r.
-__device__ __forceinline__ float small_sigma_fact(float E, float F, bool &below)
-{
-    const float e = E * F;  // exp(lambda (X - tau))
-    below = e <= 1.0f;
-    const float rc = rcp_approx(1.0f + e);
-    return fminf(e, 1.0f) * rc;
-}
+// r = sigma(-lambda |tau - X|) and below = [X <= tau] by the direct form (the factorised form,
+// for both thresholds at once, is small_sigma_fact2).
 __device__ __forceinline__ float small_sigma_direct(const float4 &en, float t, float l2,
                                                     bool &below)
 {
@@ -488,27 +481,113 @@ __device__ __forceinline__ void kahan_fma(float &s, float &comp, float a, float 
     s = t;
 }
 
-// Forward inner loop over staged entries for the thread's two thresholds.
-// The integer parts w0, w1 are sums of small integers (|w| <= 8 kTileCap < 2^24), exact in fp32.
-template <bool FACT>
-__device__ __forceinline__ void fwd_loop(const float4 *sh, int m_ent, const KState &s0,
-                                         const KState &s1, float l2, float &w0, float &w1,
-                                         float &a0, float &c0, float &a1, float &c1)
+// Packed fp32 pairs: a thread's two thresholds in one 64-bit register pair, so that one
+// instruction does both. Each element is rounded exactly as the scalar operation would round it,
+// so the packed loops below give the same bits as their scalar forms.
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 pk2(float a, float b)
+{
+    f32x2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void upk2(f32x2 r, float &a, float &b)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b)
+{
+    f32x2 r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f32x2 sub2(f32x2 a, f32x2 b)
+{
+    f32x2 r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b)
+{
+    f32x2 r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c)
+{
+    f32x2 r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+// The factorised r for both thresholds: e = E F_k = exp(lambda (X - tau_k)),
+// r = min(e, 1) / (1 + e), below_k = [e <= 1]. e may overflow to +inf (r = 1 * 0 = 0) or
+// underflow to 0 (r = 0).
+__device__ __forceinline__ f32x2 small_sigma_fact2(float E, f32x2 F, bool &b0, bool &b1)
+{
+    float e0, e1, d0, d1;
+    const f32x2 e = mul2(pk2(E, E), F);
+    upk2(e, e0, e1);
+    upk2(add2(e, pk2(1.0f, 1.0f)), d0, d1);
+    b0 = e0 <= 1.0f;
+    b1 = e1 <= 1.0f;
+    return mul2(pk2(fminf(e0, 1.0f), fminf(e1, 1.0f)), pk2(rcp_approx(d0), rcp_approx(d1)));
+}
+
+// Kahan step for both thresholds with the compensation carried negated (nc = -comp), which
+// makes every step one packed add, subtract or fused multiply-add; same bits as kahan_fma.
+__device__ __forceinline__ void kahan_fma2(f32x2 &s, f32x2 &nc, f32x2 a, f32x2 b)
+{
+    const f32x2 y = fma2(a, b, nc);
+    const f32x2 t = add2(s, y);
+    nc = sub2(y, sub2(t, s));
+    s = t;
+}
+
+// Forward inner loop over staged entries for the thread's two thresholds, direct form (tiles
+// whose exponents leave the factorised range). The integer parts w0, w1 are sums of small
+// integers (|w| <= 8 kTileCap < 2^24), exact in fp32.
+__device__ __forceinline__ void fwd_loop_direct(const float4 *sh, int m_ent, const KState &s0,
+                                                const KState &s1, float l2, float &w0, float &w1,
+                                                float &a0, float &c0, float &a1, float &c1)
 {
 #pragma unroll 4
     for (int i = 0; i < m_ent; ++i) {
         const float4 en = sh[i];
         const float cf = entry_cf(en);
         bool b0, b1;
-        const float r0 =
-            FACT ? small_sigma_fact(en.x, s0.F, b0) : small_sigma_direct(en, s0.tau, l2, b0);
-        const float r1 =
-            FACT ? small_sigma_fact(en.x, s1.F, b1) : small_sigma_direct(en, s1.tau, l2, b1);
+        const float r0 = small_sigma_direct(en, s0.tau, l2, b0);
+        const float r1 = small_sigma_direct(en, s1.tau, l2, b1);
         w0 += b0 ? cf : 0.0f;
         w1 += b1 ? cf : 0.0f;
         kahan_fma(a0, c0, b0 ? -cf : cf, r0);
         kahan_fma(a1, c1, b1 ? -cf : cf, r1);
     }
+}
+
+// The factorised forward loop with both thresholds in packed pairs (the same bits as the scalar
+// form: e = E F_k, r = min(e, 1) / (1 + e), w += [e <= 1] c, Kahan over -+c r).
+__device__ __forceinline__ void fwd_loop_packed(const float4 *sh, int m_ent, const KState &s0,
+                                                const KState &s1, float &w0, float &w1,
+                                                float &a0, float &c0, float &a1, float &c1)
+{
+    const f32x2 F = pk2(s0.F, s1.F);
+    f32x2 w = pk2(w0, w1), a = pk2(a0, a1), nc = pk2(-c0, -c1);
+#pragma unroll 4
+    for (int i = 0; i < m_ent; ++i) {
+        const float4 en = sh[i];
+        const float cf = entry_cf(en);
+        bool b0, b1;
+        const f32x2 r = small_sigma_fact2(en.x, F, b0, b1);
+        w = add2(w, pk2(b0 ? cf : 0.0f, b1 ? cf : 0.0f));
+        kahan_fma2(a, nc, pk2(b0 ? -cf : cf, b1 ? -cf : cf), r);
+    }
+    float n0, n1;
+    upk2(w, w0, w1);
+    upk2(a, a0, a1);
+    upk2(nc, n0, n1);
+    c0 = -n0;
+    c1 = -n1;
 }
 
 // Forward: one block per (tile, image); thread t owns thresholds k = kb + t and kb + t + 64.
@@ -534,9 +613,9 @@ __global__ void __launch_bounds__(kSoftThreads) soft_fwd_kernel(
             for (int i = threadIdx.x; i < m_ent; i += kSoftThreads) sh[i] = list[e0 + i];
             __syncthreads();
             if (fact)
-                fwd_loop<true>(sh, m_ent, s0, s1, l2, w0, w1, a0, c0, a1, c1);
+                fwd_loop_packed(sh, m_ent, s0, s1, w0, w1, a0, c0, a1, c1);
             else
-                fwd_loop<false>(sh, m_ent, s0, s1, l2, w0, w1, a0, c0, a1, c1);
+                fwd_loop_direct(sh, m_ent, s0, s1, l2, w0, w1, a0, c0, a1, c1);
         }
         if (k0 < K) part[unit * K + k0] = (double)w0 + ((double)a0 - (double)c0);
         if (k1 < K) part[unit * K + k1] = (double)w1 + ((double)a1 - (double)c1);
@@ -564,26 +643,23 @@ __global__ void soft_fwd_reduce_kernel(const double *__restrict__ part, float *_
     out[i] = (float)acc;
 }
 
-// Backward group of eight staged entries for the thread's two thresholds:
+// Backward group of eight staged entries for the thread's two thresholds (direct form):
 //   dtau partial[k] += c_p w_pk,   w = s (1 - s) = r (1 - r)      (times lambda g_k at the end)
 //   row sum (per entry, over the warp's thresholds) of g_k w_pk   (for dX_p)
 // Each lane writes its eight values to a shared 8 x 32 block; lane l sums eight entries of row
 // l / 4, and two xor shuffles combine the four lanes of the row.
-template <bool FACT>
-__device__ __forceinline__ void bwd_group(const float4 *en8, const KState &s0, const KState &s1,
-                                          float g0, float g1, float l2, float &a0, float &c0,
-                                          float &a1, float &c1, float (*qw)[kWarp], int lane,
-                                          float &row_sum)
+__device__ __forceinline__ void bwd_group_direct(const float4 *en8, const KState &s0,
+                                                 const KState &s1, float g0, float g1, float l2,
+                                                 float &a0, float &c0, float &a1, float &c1,
+                                                 float (*qw)[kWarp], int lane, float &row_sum)
 {
 #pragma unroll
     for (int j = 0; j < kGroup; ++j) {
         const float4 en = en8[j];
         const float cf = entry_cf(en);
         bool b0, b1;
-        const float r0 =
-            FACT ? small_sigma_fact(en.x, s0.F, b0) : small_sigma_direct(en, s0.tau, l2, b0);
-        const float r1 =
-            FACT ? small_sigma_fact(en.x, s1.F, b1) : small_sigma_direct(en, s1.tau, l2, b1);
+        const float r0 = small_sigma_direct(en, s0.tau, l2, b0);
+        const float r1 = small_sigma_direct(en, s1.tau, l2, b1);
         const float w0 = fmaf(-r0, r0, r0), w1 = fmaf(-r1, r1, r1);
         kahan_fma(a0, c0, cf, w0);
         kahan_fma(a1, c1, cf, w1);
@@ -596,6 +672,34 @@ __device__ __forceinline__ void bwd_group(const float4 *en8, const KState &s0, c
     s += __shfl_xor_sync(kFull, s, 1);
     s += __shfl_xor_sync(kFull, s, 2);
     row_sum = s;  // the warp's partial of sum_k g_k w for entry lane / 4 of the group
+    __syncwarp();
+}
+
+// The factorised backward group with both thresholds in packed pairs (the same bits as the
+// scalar form); the dtau sums stay packed in (a, nc) across groups.
+__device__ __forceinline__ void bwd_group_packed(const float4 *en8, f32x2 F, float g0, float g1,
+                                                 f32x2 &a, f32x2 &nc, float (*qw)[kWarp],
+                                                 int lane, float &row_sum)
+{
+#pragma unroll
+    for (int j = 0; j < kGroup; ++j) {
+        const float4 en = en8[j];
+        const float cf = entry_cf(en);
+        bool b0, b1;
+        const f32x2 r = small_sigma_fact2(en.x, F, b0, b1);
+        const f32x2 w = fma2(sub2(0ull, r), r, r);  // r - r^2, one rounding as fmaf(-r, r, r)
+        kahan_fma2(a, nc, pk2(cf, cf), w);
+        float w0, w1;
+        upk2(w, w0, w1);
+        qw[j][lane] = fmaf(g0, w0, g1 * w1);
+    }
+    __syncwarp();
+    const float4 *rowp = reinterpret_cast<const float4 *>(&qw[lane >> 2][(lane & 3) * 8]);
+    const float4 x = rowp[0], y = rowp[1];
+    float s = ((x.x + x.y) + (x.z + x.w)) + ((y.x + y.y) + (y.z + y.w));
+    s += __shfl_xor_sync(kFull, s, 1);
+    s += __shfl_xor_sync(kFull, s, 2);
+    row_sum = s;
     __syncwarp();
 }
 
@@ -652,6 +756,8 @@ __global__ void __launch_bounds__(kSoftThreads) soft_bwd_kernel(
             const float g1 = (k1 < K) ? __ldg(grad_out + bj * K + k1) : 0.0f;
             const bool fact = __syncthreads_and(s0.ok && s1.ok && !(cnt & kTileFlagDirect));
             float a0 = 0.f, c0 = 0.f, a1 = 0.f, c1 = 0.f;
+            const f32x2 F = pk2(s0.F, s1.F);
+            f32x2 ap = 0ull, ncp = 0ull;  // packed dtau sums (+0.0f pairs) of the factorised form
             for (int e0 = 0; e0 < n; e0 += kBwdChunk) {
                 const int m_ent = min(kBwdChunk, n - e0);
                 __syncthreads();
@@ -663,10 +769,10 @@ __global__ void __launch_bounds__(kSoftThreads) soft_bwd_kernel(
                 for (int gi = 0; gi * kGroup < m_ent; ++gi) {
                     float rs;
                     if (fact)
-                        bwd_group<true>(sh + gi * kGroup, s0, s1, g0, g1, l2, a0, c0, a1, c1,
-                                        qbuf[warp], lane, rs);
+                        bwd_group_packed(sh + gi * kGroup, F, g0, g1, ap, ncp, qbuf[warp], lane,
+                                         rs);
                     else
-                        bwd_group<false>(sh + gi * kGroup, s0, s1, g0, g1, l2, a0, c0, a1, c1,
+                        bwd_group_direct(sh + gi * kGroup, s0, s1, g0, g1, l2, a0, c0, a1, c1,
                                          qbuf[warp], lane, rs);
                     if ((lane & 3) == 0) red[warp][gi * kGroup + (lane >> 2)] = rs;
                 }
@@ -677,6 +783,13 @@ __global__ void __launch_bounds__(kSoftThreads) soft_bwd_kernel(
                     for (int w2 = 0; w2 < NW; ++w2) q += red[w2][i];
                     dxs[e0 + i] += q;
                 }
+            }
+            if (fact) {
+                float n0, n1;
+                upk2(ap, a0, a1);
+                upk2(ncp, n0, n1);
+                c0 = -n0;
+                c1 = -n1;
             }
             if (k0 < K)
                 part[k0 * units + unit] = (double)lambda * (double)g0 * ((double)a0 - (double)c0);
