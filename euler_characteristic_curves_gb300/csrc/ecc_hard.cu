@@ -910,8 +910,10 @@ static cudaError_t launch_hard(const HardPlan &pl, cudaStream_t s)
     const int64_t strips = (pl.W + kStrip - 1) / kStrip;
     const int per_sm = pl.ndim == 2 ? ECC_2D_MIN_BLOCKS : ECC_3D_MIN_BLOCKS;
     const int64_t resident = (int64_t)sms * per_sm;  // blocks that fit at once
-    // blocks per image: the resident blocks shared out over the batch
-    int64_t per_image = (resident + pl.batch - 1) / pl.batch;
+    // blocks per image: the resident blocks shared out over the batch, rounded down so that the
+    // whole grid is one wave (rounding up left a few blocks to run alone in a second wave)
+    int64_t per_image = resident / pl.batch;
+    if (per_image < 1) per_image = 1;  // batches larger than a wave run in several waves
     if (pl.ndim == 2) {
         // contiguous strip-row ranges, at least 32 rows per warp
         const int64_t N = strips * pl.Hy;
