@@ -429,7 +429,7 @@ def time_e2e(args, parts, inputs, step, device, world):
     res_dev = step.results()
     d2h = sum(t.numel() * t.element_size() for t in res_dev)
     res_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in res_dev]
-    steps = max(1, min(args.steps, 5))
+    steps = max(1, min(args.steps, 8))
     stream = torch.cuda.current_stream()
     side = torch.cuda.Stream(device=device)
 
@@ -454,19 +454,24 @@ def time_e2e(args, parts, inputs, step, device, world):
     torch.cuda.synchronize()
     link = host_link_gbs(device)
     barrier(world)
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for _ in range(steps):
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    marks[0].record(stream)
+    for i in range(steps):
         one()
-    end.record(stream)
+        marks[i + 1].record(stream)
     torch.cuda.synchronize()
-    ms = max_over_ranks(start.elapsed_time(end) / steps, world)
+    per_step = [marks[i].elapsed_time(marks[i + 1]) for i in range(steps)]
+    ms = max_over_ranks(marks[0].elapsed_time(marks[-1]) / steps, world)
+    med = max_over_ranks(statistics.median(per_step), world)
     hard_vox = sum(part_voxels(p) for p in parts if p[0] == "hard") or \
         sum(part_voxels(p) for p in parts)
     return {"value": round(hard_vox * world / (ms * 1e-3) / 1e9, 3), "unit": "Gvoxels/s",
             "ms_per_step": round(ms, 3), "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": steps,
             "link_gbs": link, "link_floor_ms": round(h2d / (link * 1e9) * 1e3, 3),
+            "ms_per_step_median": round(med, 3),
+            "value_median": round(hard_vox * world / (med * 1e-3) / 1e9, 3),
+            "ms_steps": [round(x, 2) for x in per_step],
             "path": ("3-D volumes through ecc_hard_stream from pinned host memory in "
                      f"{E2E_SLAB}-plane slabs; other parts copied and run on a second stream"
                      if streamed else "inputs copied from pinned host memory, then the step")}
