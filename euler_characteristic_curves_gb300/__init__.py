@@ -4,8 +4,10 @@ The compute runs in the CUDA library built from ``csrc/`` behind the C ABI in
 ``include/ecc.h``; this package only marshals arguments (``ecc`` module). The native library is
 loaded on first use and a missing library raises immediately: there is no CPU fallback.
 """
-__all__ = ["ecc_hard", "ecc_soft_fwd", "ecc_soft_bwd", "soft_workspace_bytes", "SoftECC",
-           "soft_ecc"]
+__all__ = ["ecc_hard", "ecc_hard_stream", "hard_stream_buffer_bytes", "ecc_soft_fwd",
+           "ecc_soft_bwd", "ecc_soft_stats", "ecc_soft_fwd_noalloc", "soft_workspace_bytes",
+           "SoftECC", "soft_ecc", "ecc_soft_ect_fwd", "ecc_soft_ect_bwd", "ecc_soft_ect_stats",
+           "SoftECT", "soft_ect"]
 
 
 def __getattr__(name):
