@@ -265,3 +265,26 @@ def test_soft_stats_counts_the_contributing_voxels(shape, batch, ndim):
         tiles = batch * int(np.prod([-(-n // t) for n, t in zip(shape[::-1], tile)]))
         assert st[2] == tiles
         assert (st[1] > 0) == direct
+
+
+@pytest.mark.parametrize("ndim", [2, 3])
+def test_dense_critical_lists(ndim):
+    """Inputs where most voxels contribute: a checkerboard (with a tiny ramp so that no two values
+    tie) and white noise. Every tile's list is then far longer than one staging chunk, so the
+    forward and backward walk many chunks and groups per tile; the whole curve and every gradient
+    must still match the oracle."""
+    shape = (64, 128) if ndim == 2 else (16, 16, 64)
+    idx = np.indices(shape)
+    cb = (idx.sum(0) % 2).astype(np.float64)
+    ramp = np.arange(int(np.prod(shape)), dtype=np.float64).reshape(shape) / np.prod(shape)
+    noise = np.random.default_rng(31).random(shape)
+    img = np.stack([0.5 * cb + 0.4 * ramp, noise]).astype(np.float32)
+    K = 64
+    tau = synthetic.uniform_thresholds(K)
+    u = (synthetic.soft_direction(ndim, seed=32) * 0.1).astype(np.float32)
+    g = synthetic.upstream_grad((2, K), seed=33)
+    a = np.asarray([1.0], np.float32)
+    _, ws = ecc.ecc_soft_fwd(dev(img), dev(tau), 50.0, dev(a), dev(u))
+    st = ecc.ecc_soft_stats(dev(img), K, ws, ndim=ndim).cpu().numpy()
+    assert st[0] > 0.4 * img.size  # dense lists: most voxels contribute
+    compare(img, tau, 50.0, 1.0, u, g)
