@@ -432,11 +432,16 @@ __device__ __forceinline__ void halo_item(int i, int x0, int y0, int &y, int &x,
     }
 }
 
-// Whether some lane of `warp` has an item in halo slot s (warp-uniform; constant but for the
-// last slot).
+// Whether some lane of `warp` has an item in halo slot s (warp-uniform): every lane has one in
+// all but the last slot, which the compiler sees as a constant.
 __device__ __forceinline__ bool slot_active(int s, int warp)
 {
-    return s * k3Threads + warp * kWarp < kHaloItems;
+    return s + 1 < kHaloSlots || s * k3Threads + warp * kWarp < kHaloItems;
+}
+// Whether this thread has an item in halo slot s.
+__device__ __forceinline__ bool slot_item(int s, const int *h_half)
+{
+    return s + 1 < kHaloSlots || h_half[s] >= 0;
 }
 
 template <typename T>
@@ -566,12 +571,18 @@ __device__ __forceinline__ PlaneRaw<T> next_plane(TileCursor<T> &cur, const Tile
     using V = HaloVal<T>;
     PlaneRaw<T> p;
     const bool in = (uint64_t)cur.z < (uint64_t)cur.D;  // block-uniform
+    if (in && tc.own.full && tc.rows_in == (1u << k3Rows) - 1u) {  // warp-uniform common case
 #pragma unroll
-    for (int i = 0; i < k3Rows; ++i) {
-        if (in && ((tc.rows_in >> i) & 1u))  // warp-uniform
-            load_own4(cur.own + (int64_t)i * cur.W, tc.own, tc.own.full, p.own[i]);
-        else
-            absent_own(p.own[i]);
+        for (int i = 0; i < k3Rows; ++i)
+            load_own4(cur.own + (int64_t)i * cur.W, tc.own, true, p.own[i]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < k3Rows; ++i) {
+            if (in && ((tc.rows_in >> i) & 1u))  // warp-uniform
+                load_own4(cur.own + (int64_t)i * cur.W, tc.own, tc.own.full, p.own[i]);
+            else
+                absent_own(p.own[i]);
+        }
     }
 #pragma unroll
     for (int s = 0; s < kHaloSlots; ++s) {
@@ -630,7 +641,7 @@ __device__ __forceinline__ void store_plane_keys(const PlaneRaw<float> &p, const
             make_uint2(prmt(k[i][0], k[i][1], 0x5410), prmt(k[i][2], k[i][3], 0x5410));
 #pragma unroll
     for (int s = 0; s < kHaloSlots; ++s)
-        if (tc.h_half[s] >= 0) dst[tc.h_half[s]] = (uint16_t)h[s];
+        if (slot_item(s, tc.h_half)) dst[tc.h_half[s]] = (uint16_t)h[s];
 }
 
 template <bool SEARCH>
@@ -651,7 +662,7 @@ __device__ __forceinline__ void store_plane_keys(const PlaneRaw<uint8_t> &p, con
     }
 #pragma unroll
     for (int s = 0; s < kHaloSlots; ++s)
-        if (tc.h_half[s] >= 0)
+        if (slot_item(s, tc.h_half))
             dst[tc.h_half[s]] =
                 (uint16_t)(p.halo[s] < 256u ? (uint32_t)lut[p.halo[s]] : never);
 }
