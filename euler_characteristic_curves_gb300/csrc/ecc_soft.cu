@@ -352,8 +352,11 @@ __global__ void __launch_bounds__(kPrepThreads) soft_prep_kernel(
     constexpr int ZO = NDIM == 3 ? 1 : 0;  // halo offset along z
     __shared__ float Fv[HZ * HP];  // f on the tile and its halo; NaN outside the grid
     __shared__ float2 X[HZ * HP];
-    __shared__ int warp_tot[kPrepThreads / kWarp];
-    __shared__ int running;
+    constexpr int kRounds = kTileCap / kPrepThreads;  // pixels per thread
+    constexpr int kPrepWarps = kPrepThreads / kWarp;
+    static_assert(kRounds * kPrepWarps == 2 * kWarp, "one warp scans the (round, warp) counts");
+    __shared__ int wcount[kRounds * kPrepWarps];  // contributing pixels per (round, warp)
+    __shared__ int running;                       // the tile's list length
 
     const int64_t b = blockIdx.y;
     const int64_t tile = blockIdx.x;
@@ -396,41 +399,60 @@ __global__ void __launch_bounds__(kPrepThreads) soft_prep_kernel(
             }
             X[i] = v;
         }
-        if (threadIdx.x == 0) running = 0;
         __syncthreads();
 
         const int64_t unit = ((int64_t)b * ndirs + j) * g.tiles + tile;
         float4 *__restrict__ out = entries + unit * (int64_t)kTileCap;
-        bool direct = false;
-        for (int r = 0; r < kTileCap / kPrepThreads; ++r) {
+        // Pixel i = r kPrepThreads + thread (round r). A pixel's slot in the list is the number of
+        // contributing pixels before it in raster order: those of earlier rounds, of earlier
+        // warps in its round and of earlier lanes in its warp. The (round, warp) counts are
+        // scanned once for the whole tile.
+        int cr[kRounds];
+        unsigned bal[kRounds];
+#pragma unroll
+        for (int r = 0; r < kRounds; ++r) {
             const int i = r * kPrepThreads + threadIdx.x;
             const int lx = i % T::X, ly = (i / T::X) % T::Y, lz = i / (T::X * T::Y);
             const float2 *cp = &X[(lz + ZO) * HP + (ly + 1) * HX + lx + 1];
-            const float2 p = cp[0];
             int c = 0;
             if (z0 + lz < g.D && y0 + ly < g.Hy && x0 + lx < g.W)
                 c = NDIM == 3 ? local_c3<HX, HP>(cp) : local_c2<HX>(cp);
-            const unsigned mask = __ballot_sync(kFull, c != 0);
-            if (lane == 0) warp_tot[warp] = __popc(mask);
-            __syncthreads();
-            int before = running;
-            for (int w2 = 0; w2 < warp; ++w2) before += warp_tot[w2];
-            before += __popc(mask & ((1u << lane) - 1u));
-            if (c != 0) {
+            cr[r] = c;
+            bal[r] = __ballot_sync(kFull, c != 0);
+            if (lane == 0) wcount[r * kPrepWarps + warp] = __popc(bal[r]);
+        }
+        __syncthreads();
+        if (warp == 0) {  // exclusive scan of the 64 counts in (round, warp) order, two per lane
+            const int a = wcount[2 * lane], b2 = wcount[2 * lane + 1];
+            int incl = a + b2;
+#pragma unroll
+            for (int o = 1; o < kWarp; o <<= 1) {
+                const int t = __shfl_up_sync(kFull, incl, o);
+                if (lane >= o) incl += t;
+            }
+            const int excl = incl - (a + b2);
+            __syncwarp();
+            wcount[2 * lane] = excl;
+            wcount[2 * lane + 1] = excl + a;
+            if (lane == kWarp - 1) running = incl;
+        }
+        __syncthreads();
+        bool direct = false;
+#pragma unroll
+        for (int r = 0; r < kRounds; ++r) {
+            if (cr[r] != 0) {
+                const int i = r * kPrepThreads + threadIdx.x;
+                const int lx = i % T::X, ly = (i / T::X) % T::Y, lz = i / (T::X * T::Y);
+                const float2 p = X[(lz + ZO) * HP + (ly + 1) * HX + lx + 1];
+                const int slot =
+                    wcount[r * kPrepWarps + warp] + __popc(bal[r] & ((1u << lane) - 1u));
                 float s, e, ex;
                 two_sum(p.x, -m, s, e);  // X - m, exactly, as s + (e + lo)
                 const float E = pow2_scaled(l2, s, e + p.y, ex);
                 direct |= !(fabsf(ex) <= kExpLimit);
-                const int packed = (i << 4) | (c + 8);
-                out[before] = make_float4(E, p.x, p.y, __int_as_float(packed));
+                const int packed = (i << 4) | (cr[r] + 8);
+                out[slot] = make_float4(E, p.x, p.y, __int_as_float(packed));
             }
-            __syncthreads();
-            if (threadIdx.x == 0) {
-                int tot = 0;
-                for (int w2 = 0; w2 < kPrepThreads / kWarp; ++w2) tot += warp_tot[w2];
-                running += tot;
-            }
-            __syncthreads();
         }
         direct = __syncthreads_or(direct);
         if (threadIdx.x == 0) counts[unit] = running | (direct ? kTileFlagDirect : 0);
