@@ -725,9 +725,10 @@ __device__ __forceinline__ void bwd_group_packed(const float4 *en8, f32x2 F, flo
     __syncwarp();
 }
 
-// Backward: one block per (tile, image), looping over the directions; thread t owns thresholds
-// k = kb + t and kb + t + 64. The image gradient of the tile collects alpha dX over the
-// directions in shared memory in a fixed order and is written once, for every voxel of the tile.
+// Backward: one block per (tile, image, direction), or, when the image gradient is wanted, one
+// per (tile, image) looping over the directions; thread t owns thresholds k = kb + t and
+// kb + t + 64. The image gradient of the tile collects alpha dX over the directions in shared
+// memory in a fixed order and is written once, for every voxel of the tile.
 template <int NDIM>
 __global__ void __launch_bounds__(kSoftThreads) soft_bwd_kernel(
     const float *__restrict__ img, const float *__restrict__ tau, int K, int ndirs, float lambda,
@@ -745,9 +746,15 @@ __global__ void __launch_bounds__(kSoftThreads) soft_bwd_kernel(
     extern __shared__ float gacc[];  // kTileCap floats, present only when grad_img is wanted
     __shared__ double scal_red[NW][kScal];
 
-    const int64_t b = blockIdx.y;
+    // Without an image gradient every (image, direction) pair is a block of its own
+    // (blockIdx.y = b ndirs + j); with one, a block walks all directions of its image so that the
+    // gradient collects them in a fixed order in shared memory (blockIdx.y = b).
+    const bool per_dir = grad_img == nullptr;
+    const int64_t b = per_dir ? blockIdx.y / ndirs : blockIdx.y;
+    const int jbeg = per_dir ? (int)(blockIdx.y % ndirs) : 0;
+    const int jend = per_dir ? jbeg + 1 : ndirs;
     const int64_t tile = blockIdx.x;
-    const int64_t units = (int64_t)gridDim.y * ndirs * g.tiles;  // threshold-major partials
+    const int64_t units = (int64_t)(per_dir ? gridDim.y : gridDim.y * ndirs) * g.tiles;
     const int lane = threadIdx.x & (kWarp - 1), warp = threadIdx.x >> 5;
     const float m = tau_midpoint(tau, K);
     const float alpha = __ldg(alpha_p);
@@ -762,7 +769,7 @@ __global__ void __launch_bounds__(kSoftThreads) soft_bwd_kernel(
     if (grad_img)
         for (int i = threadIdx.x; i < kTileCap; i += kSoftThreads) gacc[i] = 0.0f;
 
-    for (int j = 0; j < ndirs; ++j) {
+    for (int j = jbeg; j < jend; ++j) {
         const int64_t bj = b * ndirs + j;
         const int64_t unit = bj * g.tiles + tile;
         const int cnt = counts[unit];
@@ -1013,7 +1020,9 @@ cudaError_t soft_run_bwd(const SoftLayout &L, const float *img, const float *tau
     double *part = reinterpret_cast<double *>(base + L.off_part);
     double *scal = reinterpret_cast<double *>(base + L.off_scal);
     const SoftGeom g = soft_geom(L);
-    const dim3 grid((unsigned)L.tiles, (unsigned)L.batch);
+    // one block per (tile, image, direction) unless the image gradient is asked for: then one per
+    // (tile, image), walking the directions (see soft_bwd_kernel)
+    const dim3 grid((unsigned)L.tiles, (unsigned)(grad_img ? L.batch : L.batch * L.ndirs));
     const float l2 = lambda_log2e(lambda);
     // the image-gradient accumulator costs shared memory (and so resident blocks) only when asked
     const size_t dyn = grad_img ? sizeof(float) * kTileCap : 0;
