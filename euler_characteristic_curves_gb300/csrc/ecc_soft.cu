@@ -34,6 +34,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "ecc_internal.cuh"
 
 namespace ecc {
@@ -54,6 +56,7 @@ constexpr int kTileCap = 2048;  // entries per tile: every voxel may contribute
 static_assert(SoftTile<2>::X * SoftTile<2>::Y == kTileCap, "2-D tile size");
 static_assert(SoftTile<3>::X * SoftTile<3>::Y * SoftTile<3>::Z == kTileCap, "3-D tile size");
 constexpr int kPrepThreads = 256;
+constexpr int64_t kPrepBlocks = 4096;      // prep grid size aimed at when directions are grouped
 constexpr int kSoftThreads = 64;           // each thread owns two thresholds per pass
 constexpr int kKPerPass = 2 * kSoftThreads;
 constexpr int kChunk = 256;                // entries staged in shared memory at a time
@@ -343,8 +346,9 @@ __device__ __forceinline__ int local_c3(const float2 *c)
 template <int NDIM>
 __global__ void __launch_bounds__(kPrepThreads) soft_prep_kernel(
     const float *__restrict__ img, const float *__restrict__ alpha_p, const float *__restrict__ u_p,
-    int ndirs, const float *__restrict__ tau, int K, float l2, const float2 *__restrict__ coords,
-    int *__restrict__ counts, float4 *__restrict__ entries, SoftGeom g)
+    int ndirs, int dirs_per_block, const float *__restrict__ tau, int K, float l2,
+    const float2 *__restrict__ coords, int *__restrict__ counts, float4 *__restrict__ entries,
+    SoftGeom g)
 {
     using T = SoftTile<NDIM>;
     constexpr int HX = T::X + 2, HY = T::Y + 2, HZ = NDIM == 3 ? T::Z + 2 : 1;
@@ -358,7 +362,11 @@ __global__ void __launch_bounds__(kPrepThreads) soft_prep_kernel(
     __shared__ int wcount[kRounds * kPrepWarps];  // contributing pixels per (round, warp)
     __shared__ int running;                       // the tile's list length
 
-    const int64_t b = blockIdx.y;
+    // blockIdx.y = b groups + group: the block's directions are one group of dirs_per_block
+    const int groups = (ndirs + dirs_per_block - 1) / dirs_per_block;
+    const int64_t b = blockIdx.y / groups;
+    const int jbeg = (int)(blockIdx.y % groups) * dirs_per_block;
+    const int jend = min(jbeg + dirs_per_block, ndirs);
     const int64_t tile = blockIdx.x;
     const int64_t x0 = (tile % g.tiles_x) * T::X;
     const int64_t y0 = ((tile / g.tiles_x) % g.tiles_y) * T::Y;
@@ -381,7 +389,7 @@ __global__ void __launch_bounds__(kPrepThreads) soft_prep_kernel(
         Fv[i] = fv;
     }
 
-    for (int j = 0; j < ndirs; ++j) {
+    for (int j = jbeg; j < jend; ++j) {
         const float *u = u_p + j * NDIM;
         const float u0 = __ldg(u), u1 = __ldg(u + 1), u2 = NDIM == 3 ? __ldg(u + 2) : 0.0f;
         __syncthreads();  // Fv is complete; the previous direction is done with X and running
@@ -992,13 +1000,21 @@ cudaError_t soft_run_fwd(const SoftLayout &L, const float *img, const float *tau
     const SoftGeom g = soft_geom(L);
     const int64_t ncoord = g.nz + L.Hy + L.W;
     soft_coords_kernel<<<(unsigned)((ncoord + 255) / 256), 256, 0, s>>>(coords, g.nz, L.Hy, L.W);
-    const dim3 grid((unsigned)L.tiles, (unsigned)L.batch);
+    // Directions in groups, each prep block reading its tile of f once for a whole group: as
+    // many groups as give about kPrepBlocks blocks (the tile list of a single direction and of
+    // a small transform stays one group).
+    const int64_t tile_images = L.tiles * L.batch;
+    const int groups = (int)std::min<int64_t>(
+        L.ndirs, std::max<int64_t>(1, (kPrepBlocks + tile_images - 1) / tile_images));
+    const int dpb = (L.ndirs + groups - 1) / groups;
+    const int ngroups = (L.ndirs + dpb - 1) / dpb;
+    const dim3 grid((unsigned)L.tiles, (unsigned)(L.batch * ngroups));
     if (L.ndim == 3)
-        soft_prep_kernel<3><<<grid, kPrepThreads, 0, s>>>(img, alpha, u, L.ndirs, tau, L.K, l2,
-                                                          coords, counts, entries, g);
+        soft_prep_kernel<3><<<grid, kPrepThreads, 0, s>>>(img, alpha, u, L.ndirs, dpb, tau, L.K,
+                                                          l2, coords, counts, entries, g);
     else
-        soft_prep_kernel<2><<<grid, kPrepThreads, 0, s>>>(img, alpha, u, L.ndirs, tau, L.K, l2,
-                                                          coords, counts, entries, g);
+        soft_prep_kernel<2><<<grid, kPrepThreads, 0, s>>>(img, alpha, u, L.ndirs, dpb, tau, L.K,
+                                                          l2, coords, counts, entries, g);
     // one block per unit (tile, image x direction)
     const dim3 ugrid((unsigned)L.tiles, (unsigned)(L.batch * L.ndirs));
     soft_fwd_kernel<<<ugrid, kSoftThreads, 0, s>>>(tau, L.K, l2, counts, entries, part, L.tiles);
