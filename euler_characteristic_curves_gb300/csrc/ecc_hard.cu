@@ -612,25 +612,35 @@ __device__ __forceinline__ void store_plane_keys(const PlaneRaw<float> &p, const
         for (int s = 0; s < kHaloSlots; ++s)
             h[s] = slot_active(s, warp) ? key_search_pattern(p.halo[s], K.H, T) : 0u;
     } else {
-        uint32_t amb = 0;
+        // ambiguity flags in two groups (the first half of the rows with the halo items, the
+        // second half), so that the rare fix-up only revisits the group that needs it
+        constexpr int kHalf = k3Rows / 2;
+        uint32_t amb0 = 0, amb1 = 0;
 #pragma unroll
         for (int i = 0; i < k3Rows; ++i)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) k[i][j] = key_fast(p.own[i].v[j], K, amb);
+            for (int j = 0; j < 4; ++j)
+                k[i][j] = key_fast(p.own[i].v[j], K, i < kHalf ? amb0 : amb1);
 #pragma unroll
         for (int s = 0; s < kHaloSlots; ++s) {
             h[s] = kKeyBase + (uint32_t)K.H;  // "never" in warps without an item in slot s
-            if (slot_active(s, warp)) h[s] = key_fast(p.halo[s], K, amb);
+            if (slot_active(s, warp)) h[s] = key_fast(p.halo[s], K, amb0);
         }
-        if (__any_sync(kFull, amb != 0)) {  // rare: a value within E of a threshold
-            if (amb != 0) {
+        if (__any_sync(kFull, (amb0 | amb1) != 0)) {  // rare: a value within E of a threshold
+            if (amb0 != 0) {
 #pragma unroll
-                for (int i = 0; i < k3Rows; ++i)
+                for (int i = 0; i < kHalf; ++i)
 #pragma unroll
                     for (int j = 0; j < 4; ++j) k[i][j] = key_fix(p.own[i].v[j], k[i][j], K.H, T);
 #pragma unroll
                 for (int s = 0; s < kHaloSlots; ++s)
                     if (slot_active(s, warp)) h[s] = key_fix(p.halo[s], h[s], K.H, T);
+            }
+            if (amb1 != 0) {
+#pragma unroll
+                for (int i = kHalf; i < k3Rows; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) k[i][j] = key_fix(p.own[i].v[j], k[i][j], K.H, T);
             }
         }
     }
