@@ -612,35 +612,40 @@ __device__ __forceinline__ void store_plane_keys(const PlaneRaw<float> &p, const
         for (int s = 0; s < kHaloSlots; ++s)
             h[s] = slot_active(s, warp) ? key_search_pattern(p.halo[s], K.H, T) : 0u;
     } else {
-        // ambiguity flags in two groups (the first half of the rows with the halo items, the
-        // second half), so that the rare fix-up only revisits the group that needs it
-        constexpr int kHalf = k3Rows / 2;
-        uint32_t amb0 = 0, amb1 = 0;
+        // ambiguity flags per group of kFixRows rows (the halo items join the first group), so
+        // that the rare fix-up only revisits the groups that need it
+        constexpr int kFixRows = k3Rows >= 2 ? 2 : 1;
+        constexpr int kGroups = k3Rows / kFixRows;
+        uint32_t amb[kGroups];
+#pragma unroll
+        for (int q = 0; q < kGroups; ++q) amb[q] = 0;
 #pragma unroll
         for (int i = 0; i < k3Rows; ++i)
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                k[i][j] = key_fast(p.own[i].v[j], K, i < kHalf ? amb0 : amb1);
+            for (int j = 0; j < 4; ++j) k[i][j] = key_fast(p.own[i].v[j], K, amb[i / kFixRows]);
 #pragma unroll
         for (int s = 0; s < kHaloSlots; ++s) {
             h[s] = kKeyBase + (uint32_t)K.H;  // "never" in warps without an item in slot s
-            if (slot_active(s, warp)) h[s] = key_fast(p.halo[s], K, amb0);
+            if (slot_active(s, warp)) h[s] = key_fast(p.halo[s], K, amb[0]);
         }
-        if (__any_sync(kFull, (amb0 | amb1) != 0)) {  // rare: a value within E of a threshold
-            if (amb0 != 0) {
+        uint32_t any = 0;
 #pragma unroll
-                for (int i = 0; i < kHalf; ++i)
+        for (int q = 0; q < kGroups; ++q) any |= amb[q];
+        if (__any_sync(kFull, any != 0)) {  // rare: a value within E of a threshold
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) k[i][j] = key_fix(p.own[i].v[j], k[i][j], K.H, T);
+            for (int q = 0; q < kGroups; ++q) {
+                if (amb[q] != 0) {
 #pragma unroll
-                for (int s = 0; s < kHaloSlots; ++s)
-                    if (slot_active(s, warp)) h[s] = key_fix(p.halo[s], h[s], K.H, T);
-            }
-            if (amb1 != 0) {
+                    for (int i = q * kFixRows; i < (q + 1) * kFixRows; ++i)
 #pragma unroll
-                for (int i = kHalf; i < k3Rows; ++i)
+                        for (int j = 0; j < 4; ++j)
+                            k[i][j] = key_fix(p.own[i].v[j], k[i][j], K.H, T);
+                    if (q == 0) {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) k[i][j] = key_fix(p.own[i].v[j], k[i][j], K.H, T);
+                        for (int s = 0; s < kHaloSlots; ++s)
+                            if (slot_active(s, warp)) h[s] = key_fix(p.halo[s], h[s], K.H, T);
+                    }
+                }
             }
         }
     }
