@@ -653,24 +653,42 @@ __global__ void __launch_bounds__(kSoftThreads) soft_fwd_kernel(
 }
 
 // out[b][k] = sum over the image's tiles of the partial sums, in tile order.
-__global__ void soft_fwd_reduce_kernel(const double *__restrict__ part, float *__restrict__ out,
-                                       int K, int64_t tiles, int64_t batch)
+constexpr int kFwdRedMaxWarps = 32;  // forward-reduction block: up to 32 warps share the tiles
+
+// Block (threshold group, image row bj) of nw = blockDim.x / 32 warps: lane l of warp w adds the
+// partials of threshold 32 blockIdx.x + l over tiles w, w + nw, ... in order (each load a
+// 256-byte row of 32 thresholds), then the nw warp sums are added in warp order: deterministic
+// for a given shape (the host picks nw from the tile count).
+__global__ void __launch_bounds__(kFwdRedMaxWarps * kWarp) soft_fwd_reduce_kernel(
+    const double *__restrict__ part, float *__restrict__ out, int K, int64_t tiles,
+    int64_t batch)
 {
-    const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-    if (i >= batch * K) return;
-    const int64_t b = i / K, k = i % K;
-    const double *__restrict__ p = part + b * tiles * K + k;
+    __shared__ double red[kFwdRedMaxWarps][kWarp + 1];
+    const int lane = threadIdx.x & (kWarp - 1), warp = threadIdx.x >> 5;
+    const int nw = blockDim.x >> 5;
+    const int k = blockIdx.x * kWarp + lane;
+    const int64_t bj = blockIdx.y;
     double acc = 0.0;
-    int64_t t = 0;
-    for (; t + 8 <= tiles; t += 8) {  // eight loads in flight, added in tile order
-        double v[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = p[(t + j) * K];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc += v[j];
+    if (k < K) {
+        const double *__restrict__ p = part + bj * tiles * K + k;
+        int64_t t = warp;
+        for (; t + 3 * nw < tiles; t += 4 * nw) {  // four loads in flight, added in order
+            const double v0 = p[t * K], v1 = p[(t + nw) * K];
+            const double v2 = p[(t + 2 * nw) * K], v3 = p[(t + 3 * nw) * K];
+            acc += v0;
+            acc += v1;
+            acc += v2;
+            acc += v3;
+        }
+        for (; t < tiles; t += nw) acc += p[t * K];
     }
-    for (; t < tiles; ++t) acc += p[t * K];
-    out[i] = (float)acc;
+    red[warp][lane] = acc;
+    __syncthreads();
+    if (warp == 0 && k < K) {
+        double sum = 0.0;
+        for (int w = 0; w < nw; ++w) sum += red[w][lane];
+        out[bj * K + k] = (float)sum;
+    }
 }
 
 // Backward group of eight staged entries for the thread's two thresholds (direct form):
@@ -1018,9 +1036,12 @@ cudaError_t soft_run_fwd(const SoftLayout &L, const float *img, const float *tau
     // one block per unit (tile, image x direction)
     const dim3 ugrid((unsigned)L.tiles, (unsigned)(L.batch * L.ndirs));
     soft_fwd_kernel<<<ugrid, kSoftThreads, 0, s>>>(tau, L.K, l2, counts, entries, part, L.tiles);
-    const int64_t nout = L.batch * L.ndirs * L.K;
-    soft_fwd_reduce_kernel<<<(unsigned)((nout + 255) / 256), 256, 0, s>>>(part, out, L.K, L.tiles,
-                                                                          L.batch * L.ndirs);
+    // about eight tiles per warp, 1 to 32 warps
+    const int rwarps =
+        (int)std::min<int64_t>(kFwdRedMaxWarps, std::max<int64_t>(1, (L.tiles + 7) / 8));
+    const dim3 rgrid((unsigned)((L.K + kWarp - 1) / kWarp), (unsigned)(L.batch * L.ndirs));
+    soft_fwd_reduce_kernel<<<rgrid, rwarps * kWarp, 0, s>>>(part, out, L.K, L.tiles,
+                                                            L.batch * L.ndirs);
     return cudaGetLastError();
 }
 
