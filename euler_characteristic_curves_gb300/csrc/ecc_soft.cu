@@ -251,30 +251,43 @@ __device__ __forceinline__ float entry_cf(const float4 &en)
 }
 __device__ __forceinline__ int entry_loc(const float4 &en) { return __float_as_int(en.w) >> 4; }
 
-// The cells of the 3-D V-construction that contain a voxel p: one direction per axis in
-// {-1, 0, +1} (0 = the cell does not extend along that axis), 27 in all, of dimension = the
-// number of non-zero directions. A neighbourhood bit o = (dz + 1) 9 + (dy + 1) 3 + (dx + 1)
-// stands for the voxel at offset (dz, dy, dx); mask[s] holds the bits of the vertices of cell s.
-struct CellTable3 {
-    uint32_t mask[27];
-    int sign[27];
+// The 3-D local contribution by the slice fold, in bits. The cells of the V-construction that
+// contain a voxel p split into those of its plane z and those reaching plane z - 1 or z + 1; a
+// cell reaching z - 1 is an in-plane cell sigma times [z - 1, z], of sign -(-1)^dim(sigma), and
+// counts when p is the latest vertex of sigma in plane z, the voxel straight below is earlier,
+// and so are sigma's vertices in plane z - 1. With m_z, m_b, m_a the 8 neighbour bits of planes
+// z, z - 1, z + 1 and e_b, e_a the voxels below and above,
+//     c3 = T2[m_z] - e_b T2[m_z & m_b] - e_a T2[m_z & m_a],
+// T2[m] the signed count of the in-plane cells around a centre whose other vertices are in m
+// (checked against the 27 cells for every mask in tests/test_kernel_algebra.py).
+// Neighbour bit order in a plane: (dy, dx) = (-1,-1), (-1,0), (-1,1), (0,-1), (0,1), (1,-1),
+// (1,0), (1,1).
+struct C2Table {
+    int8_t v[256];
 };
-__host__ __device__ constexpr CellTable3 make_cell_table3()
+__host__ __device__ constexpr int plane_bit(int dy, int dx)
 {
-    CellTable3 t{};
-    for (int s = 0; s < 27; ++s) {
-        const int sz = s / 9 - 1, sy = (s / 3) % 3 - 1, sx = s % 3 - 1;
-        uint32_t m = 0;
-        for (int a = 0; a <= (sz != 0); ++a)
-            for (int b = 0; b <= (sy != 0); ++b)
-                for (int c = 0; c <= (sx != 0); ++c)
-                    m |= 1u << ((a * sz + 1) * 9 + (b * sy + 1) * 3 + (c * sx + 1));
-        t.mask[s] = m;
-        const int dim = (sz != 0) + (sy != 0) + (sx != 0);
-        t.sign[s] = (dim & 1) ? -1 : 1;
+    return (dy + 1) * 3 + (dx + 1) < 4 ? (dy + 1) * 3 + (dx + 1) : (dy + 1) * 3 + (dx + 1) - 1;
+}
+__host__ __device__ constexpr C2Table make_c2_table()
+{
+    C2Table t{};
+    for (int m = 0; m < 256; ++m) {
+        int v = 0;
+        for (int sy = -1; sy <= 1; ++sy)
+            for (int sx = -1; sx <= 1; ++sx) {
+                int need = 0;
+                for (int a = 0; a <= (sy != 0); ++a)
+                    for (int b = 0; b <= (sx != 0); ++b)
+                        if (a * sy != 0 || b * sx != 0) need |= 1 << plane_bit(a * sy, b * sx);
+                if ((m & need) == need) v += ((sy != 0) + (sx != 0)) & 1 ? -1 : 1;
+            }
+        t.v[m] = (int8_t)v;
     }
     return t;
 }
+
+__constant__ C2Table kC2Table = make_c2_table();
 
 // ---------------------------------------------------------------------------------------------
 // Kernels
@@ -317,25 +330,28 @@ __device__ __forceinline__ int local_c2(const float2 *c)
 }
 
 // Local Euler contribution of a 3-D voxel from its 3 x 3 x 3 neighbourhood (row pitch HX, plane
-// pitch HP). Bits 0..12 of the neighbourhood are the offsets before p in row-major order (smaller
-// linear index, earlier when `<=`), bits 14..26 those after it (earlier when `<`).
+// pitch HP) by the bit slice fold above; c2tab is the table T2 in shared memory. Neighbours with
+// a smaller linear index are earlier when `<=`, those after it when `<`.
 template <int HX, int HP>
-__device__ __forceinline__ int local_c3(const float2 *c)
+__device__ __forceinline__ int local_c3(const float2 *c, const int8_t *c2tab)
 {
-    constexpr CellTable3 T = make_cell_table3();
     const float2 p = c[0];
-    uint32_t earlier = 1u << 13;
+    uint32_t mb = 0, mz = 0, ma = 0;  // neighbour bits of planes z - 1, z, z + 1
 #pragma unroll
-    for (int o = 0; o < 27; ++o) {
-        if (o == 13) continue;
-        const int off = (o / 9 - 1) * HP + ((o / 3) % 3 - 1) * HX + (o % 3 - 1);
-        const float2 q = c[off];
-        const bool e = (o < 13) ? df_le(q, p) : df_lt(q, p);
-        earlier |= (uint32_t)e << o;
-    }
-    int v = 0;
+    for (int dy = -1; dy <= 1; ++dy)
 #pragma unroll
-    for (int s = 0; s < 27; ++s) v += ((earlier & T.mask[s]) == T.mask[s]) ? T.sign[s] : 0;
+        for (int dx = -1; dx <= 1; ++dx) {
+            if (dy == 0 && dx == 0) continue;
+            const int bit = plane_bit(dy, dx);
+            const int off = dy * HX + dx;
+            mb |= (uint32_t)df_le(c[off - HP], p) << bit;  // plane z - 1: smaller index
+            mz |= (uint32_t)(off < 0 ? df_le(c[off], p) : df_lt(c[off], p)) << bit;
+            ma |= (uint32_t)df_lt(c[off + HP], p) << bit;  // plane z + 1: larger index
+        }
+    const bool eb = df_le(c[-HP], p), ea = df_lt(c[HP], p);
+    int v = c2tab[mz];
+    if (eb) v -= c2tab[mz & mb];
+    if (ea) v -= c2tab[mz & ma];
     return v;
 }
 
@@ -361,6 +377,7 @@ __global__ void __launch_bounds__(kPrepThreads) soft_prep_kernel(
     static_assert(kRounds * kPrepWarps == 2 * kWarp, "one warp scans the (round, warp) counts");
     __shared__ int wcount[kRounds * kPrepWarps];  // contributing pixels per (round, warp)
     __shared__ int running;                       // the tile's list length
+    __shared__ int8_t c2tab[256];                 // T2 of the 3-D slice fold
 
     // blockIdx.y = b groups + group: the block's directions are one group of dirs_per_block
     const int groups = (ndirs + dirs_per_block - 1) / dirs_per_block;
@@ -380,6 +397,8 @@ __global__ void __launch_bounds__(kPrepThreads) soft_prep_kernel(
     const float m = tau_midpoint(tau, K);
     const int lane = threadIdx.x & (kWarp - 1), warp = threadIdx.x >> 5;
 
+    if (NDIM == 3)
+        for (int i = threadIdx.x; i < 256; i += kPrepThreads) c2tab[i] = kC2Table.v[i];
     for (int i = threadIdx.x; i < HZ * HP; i += kPrepThreads) {
         const int iz = i / HP, iy = (i / HX) % HY, ix = i % HX;
         const int64_t gz = z0 - ZO + iz, gy = y0 - 1 + iy, gx = x0 - 1 + ix;
@@ -424,7 +443,7 @@ __global__ void __launch_bounds__(kPrepThreads) soft_prep_kernel(
             const float2 *cp = &X[(lz + ZO) * HP + (ly + 1) * HX + lx + 1];
             int c = 0;
             if (z0 + lz < g.D && y0 + ly < g.Hy && x0 + lx < g.W)
-                c = NDIM == 3 ? local_c3<HX, HP>(cp) : local_c2<HX>(cp);
+                c = NDIM == 3 ? local_c3<HX, HP>(cp, c2tab) : local_c2<HX>(cp);
             cr[r] = c;
             bal[r] = __ballot_sync(kFull, c != 0);
             if (lane == 0) wcount[r * kPrepWarps + warp] = __popc(bal[r]);

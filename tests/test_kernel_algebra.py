@@ -233,3 +233,58 @@ def test_fold_with_the_bias_in_the_first_product_is_exact():
     np.testing.assert_array_equal(res.astype(np.float64), 1280.0 + c)
     low = (res.view(np.uint16) & 0xFF).astype(np.int64)
     np.testing.assert_array_equal(np.where(low >= 128, low - 256, low), c)
+
+
+def c2_neighbour_table():
+    """T2[m]: the in-plane cells containing the centre of a 3 x 3 patch, summed with signs
+    (-1)^dim over the cells whose other vertices are all in the 8-bit neighbour mask m (bits
+    0..7: (dy, dx) = (-1,-1), (-1,0), (-1,1), (0,-1), (0,1), (1,-1), (1,0), (1,1))."""
+    nb = [(dy, dx) for dy in (-1, 0, 1) for dx in (-1, 0, 1) if (dy, dx) != (0, 0)]
+    bit = {d: i for i, d in enumerate(nb)}
+    t = np.zeros(256, np.int64)
+    for m in range(256):
+        v = 0
+        for sy in (-1, 0, 1):
+            for sx in (-1, 0, 1):
+                need = 0
+                for a in range(2 if sy else 1):
+                    for b in range(2 if sx else 1):
+                        if (a * sy, b * sx) != (0, 0):
+                            need |= 1 << bit[(a * sy, b * sx)]
+                if m & need == need:
+                    v += (-1) ** ((sy != 0) + (sx != 0))
+        t[m] = v
+    return t
+
+
+def test_slice_fold_of_the_27_cells_in_bits():
+    """The 3-D soft prep forms c3 from the 26-bit 'earlier' mask as
+        c3 = T2[m0] - e_below T2[m0 & m_below] - e_above T2[m0 & m_above],
+    with m0, m_below, m_above the 8 neighbour bits of the planes z, z - 1, z + 1 and e_below,
+    e_above the voxels straight below and above (the slice fold of the hard path, in bits). The
+    27 cells split into those of plane z, those reaching z - 1 and those reaching z + 1, so it
+    suffices to check every (plane z, plane z - 1) mask pair with plane z + 1 empty and every
+    (plane z, plane z + 1) pair with plane z - 1 empty: 2 x 2^17 masks, all of them."""
+    masks, signs = cell_table_3d()
+    t2 = c2_neighbour_table()
+
+    def compress9(x):  # 9 plane bits without the centre (bit 4) -> 8 bits
+        return (x & 0xF) | ((x >> 1) & 0xF0)
+
+    def expand8(m):  # 8 neighbour bits -> 9 plane bits with the centre bit clear
+        return (m & 0xF) | ((m & 0xF0) << 1)
+
+    m0 = np.repeat(np.arange(256, dtype=np.int64), 512)
+    other = np.tile(np.arange(512, dtype=np.int64), 256)
+    for shift in (0, 18):  # plane z - 1 or plane z + 1 populated
+        earlier = (expand8(m0) << 9) | (1 << 13) | (other << shift)
+        want = np.zeros(earlier.shape, np.int64)
+        for m, sg in zip(masks, signs):
+            want += sg * ((earlier & m) == m)
+        xb, xa = earlier & 0x1FF, (earlier >> 18) & 0x1FF
+        mz = compress9((earlier >> 9) & 0x1FF)
+        got = (t2[mz] - ((xb >> 4) & 1) * t2[mz & compress9(xb)]
+               - ((xa >> 4) & 1) * t2[mz & compress9(xa)])
+        np.testing.assert_array_equal(got, want)
+    # the table is the 2-D local contribution: its range is [-3, 1]
+    assert t2.min() == -3 and t2.max() == 1
