@@ -372,6 +372,7 @@ __global__ void __launch_bounds__(kPrepThreads) soft_prep_kernel(
     constexpr int ZO = NDIM == 3 ? 1 : 0;  // halo offset along z
     __shared__ float Fv[HZ * HP];  // f on the tile and its halo; NaN outside the grid
     __shared__ float2 X[HZ * HP];
+    __shared__ float2 ctile[HX + HY + HZ];  // coordinates of the tile's columns, rows, planes
     constexpr int kRounds = kTileCap / kPrepThreads;  // pixels per thread
     constexpr int kPrepWarps = kPrepThreads / kWarp;
     static_assert(kRounds * kPrepWarps == 2 * kWarp, "one warp scans the (round, warp) counts");
@@ -399,6 +400,21 @@ __global__ void __launch_bounds__(kPrepThreads) soft_prep_kernel(
 
     if (NDIM == 3)
         for (int i = threadIdx.x; i < 256; i += kPrepThreads) c2tab[i] = kC2Table.v[i];
+    // the tile's coordinates (its halo included) once, then f on the tile and its halo
+    for (int i = threadIdx.x; i < HX + HY + HZ; i += kPrepThreads) {
+        float2 cv = make_float2(0.0f, 0.0f);  // outside the grid: unused (f reads as NaN there)
+        if (i < HX) {
+            const int64_t gx = x0 - 1 + i;
+            if (gx >= 0 && gx < g.W) cv = __ldg(cx + gx);
+        } else if (i < HX + HY) {
+            const int64_t gy = y0 - 1 + (i - HX);
+            if (gy >= 0 && gy < g.Hy) cv = __ldg(cy + gy);
+        } else if (NDIM == 3) {
+            const int64_t gz = z0 - ZO + (i - HX - HY);
+            if (gz >= 0 && gz < g.D) cv = __ldg(cz + gz);
+        }
+        ctile[i] = cv;
+    }
     for (int i = threadIdx.x; i < HZ * HP; i += kPrepThreads) {
         const int iz = i / HP, iy = (i / HX) % HY, ix = i % HX;
         const int64_t gz = z0 - ZO + iz, gy = y0 - 1 + iy, gx = x0 - 1 + ix;
@@ -414,15 +430,14 @@ __global__ void __launch_bounds__(kPrepThreads) soft_prep_kernel(
         __syncthreads();  // Fv is complete; the previous direction is done with X and running
         for (int i = threadIdx.x; i < HZ * HP; i += kPrepThreads) {
             const int iz = i / HP, iy = (i / HX) % HY, ix = i % HX;
-            const int64_t gz = z0 - ZO + iz, gy = y0 - 1 + iy, gx = x0 - 1 + ix;
             const float fv = Fv[i];
             float2 v = make_float2(inf, 0.0f);  // outside the grid: never earlier
             if (fv == fv) {  // inside the grid (NaN marks outside; inputs are finite)
                 if (NDIM == 3)
-                    v = filtration_df3(alpha, fv, u0, __ldg(cz + gz), u1, __ldg(cy + gy), u2,
-                                       __ldg(cx + gx));
+                    v = filtration_df3(alpha, fv, u0, ctile[HX + HY + iz], u1, ctile[HX + iy],
+                                       u2, ctile[ix]);
                 else
-                    v = filtration_df(alpha, fv, u0, __ldg(cy + gy), u1, __ldg(cx + gx));
+                    v = filtration_df(alpha, fv, u0, ctile[HX + iy], u1, ctile[ix]);
             }
             X[i] = v;
         }
