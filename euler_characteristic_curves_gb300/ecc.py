@@ -263,9 +263,10 @@ def ecc_soft_stats(img, K: int, ws, ndim=None, stream=None) -> torch.Tensor:
 
 
 def ecc_soft_fwd_noalloc(img, tau, lam: float, alpha, u, out=None, ndim=None, stream=None):
-    """Soft ECC S[b, k] through ecc_soft_fwd_noalloc: same result as ecc_soft_fwd, but the
-    workspace is the library's own fixed device array, so the call allocates no device memory
-    (``out`` may be passed pre-allocated too). Sizes needing more than the array raise."""
+    """Soft ECC S[b, k] of 2-D images through ecc_soft_fwd_noalloc: same result as
+    ecc_soft_fwd, but the workspace is the library's own fixed device array, so the call
+    allocates no device memory (``out`` may be passed pre-allocated too). Volumes and sizes
+    needing more than the array raise."""
     ndim, batch, dims, batched = _soft_common(img, tau, alpha, u, ndim)
     K = tau.numel()
     if out is None:

@@ -230,11 +230,11 @@ int ecc_soft_stats(int ndim, const int64_t *dims, int64_t batch, int K, const vo
  *
  * For callers that cannot allocate device memory (for example a plugin inside a host framework
  * that owns all device memory and provides no allocator, or a latency-critical loop that cannot
- * afford cudaMalloc's device-wide synchronisation). Computes exactly what ecc_soft_fwd computes,
- * with the same arguments minus the workspace: the workspace lives in a library-owned device
- * array of ECC_NOALLOC_SCRATCH_BYTES bytes, which every GPU that loads the library holds until
- * the process exits. The call allocates nothing (no cudaMalloc / cudaFree, no allocating library
- * routine).
+ * afford cudaMalloc's device-wide synchronisation). For 2-D images (ndim must be 2; anything else
+ * returns ECC_EDIM) it computes exactly what ecc_soft_fwd computes, with the same arguments minus
+ * the workspace: the workspace lives in a library-owned device array of
+ * ECC_NOALLOC_SCRATCH_BYTES bytes, which every GPU that loads the library holds until the process
+ * exits. The call allocates nothing (no cudaMalloc / cudaFree, no allocating library routine).
  *
  * Sizes whose workspace (ecc_soft_workspace_bytes) exceeds ECC_NOALLOC_SCRATCH_BYTES are rejected
  * with ECC_ERANGE before anything runs. The first call on each device looks up that device's

@@ -77,18 +77,21 @@ def run(img, tau, lam, alpha, U, g, ndim, want_img=True):
     return s.cpu().numpy(), {k: v.cpu().numpy() for k, v in res.items()}
 
 
-def compare(img, tau, lam, alpha, U, g, ndim):
-    s, res = run(img, tau, lam, alpha, U, g, ndim)
+def compare(img, tau, lam, alpha, U, g, ndim, want_img=True):
+    s, res = run(img, tau, lam, alpha, U, g, ndim, want_img)
     ref_s = oracle.ecc_soft_ect_fwd(img, tau, lam, alpha, U, ndim=ndim)
-    ref = oracle.ecc_soft_ect_bwd(img, tau, lam, alpha, U, g, ndim=ndim)
+    ref = oracle.ecc_soft_ect_bwd(img, tau, lam, alpha, U, g, ndim=ndim, want_img=want_img)
     assert s.shape == ref_s.shape
     assert_close(s, ref_s, "S")
     assert_close(res["grad_tau"], ref["grad_tau"], "grad_tau")
     assert_close(res["grad_alpha"][0], ref["grad_alpha"], "grad_alpha")
     assert_close(res["grad_u"], ref["grad_u"], "grad_u",
                  extra=grad_u_allowance(img, tau, lam, alpha, U, g, ndim))
-    assert_close(res["grad_img"], ref["grad_img"], "grad_img",
-                 extra=4e-6 * ref["grad_img_absterms"])
+    if want_img:
+        assert_close(res["grad_img"], ref["grad_img"], "grad_img",
+                     extra=4e-6 * ref["grad_img_absterms"])
+    else:
+        assert "grad_img" not in res
 
 
 @pytest.mark.parametrize("shape,batch,ndirs", [((33, 70), 2, 5), ((64, 64), 1, 8), ((5, 7), 3, 3),
@@ -101,6 +104,29 @@ def test_ect_parity(shape, batch, ndirs):
     tau = synthetic.uniform_thresholds(K, -0.4, 1.4)
     U = directions(ndirs, len(shape), seed=ndirs)
     g = synthetic.upstream_grad((batch, ndirs, K), seed=5)
+    compare(img, tau, 40.0, 1.0, U, g, len(shape))
+
+
+@pytest.mark.parametrize("shape,batch,ndirs,K", [((33, 70), 2, 5, 16), ((5, 7), 3, 3, 200),
+                                                 ((64, 64), 1, 8, 129), ((9, 10, 33), 2, 3, 16),
+                                                 ((8, 8, 32), 1, 6, 300)])
+def test_ect_parity_without_the_image_gradient(shape, batch, ndirs, K):
+    """The backward the transform takes when no image gradient is wanted runs one block per
+    (tile, image, direction) instead of one per (tile, image); threshold counts past one chunk
+    of the backward (128) included."""
+    img = synthetic.grf(shape, seed=sum(shape) + K, batch=batch)
+    tau = synthetic.uniform_thresholds(K, -0.4, 1.4)
+    U = directions(ndirs, len(shape), seed=ndirs + K)
+    g = synthetic.upstream_grad((batch, ndirs, K), seed=K)
+    compare(img, tau, 40.0, 1.0, U, g, len(shape), want_img=False)
+
+
+@pytest.mark.parametrize("shape,K", [((20, 45), 129), ((6, 9, 40), 300)])
+def test_ect_parity_many_thresholds_with_the_image_gradient(shape, K):
+    img = synthetic.grf(shape, seed=K, batch=2)
+    tau = synthetic.uniform_thresholds(K, -0.4, 1.4)
+    U = directions(3, len(shape), seed=K + 1)
+    g = synthetic.upstream_grad((2, 3, K), seed=K + 2)
     compare(img, tau, 40.0, 1.0, U, g, len(shape))
 
 

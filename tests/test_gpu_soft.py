@@ -60,6 +60,8 @@ def compare(img, tau, lam, alpha, u, g, want_img=True):
     if want_img:
         assert_close(res["grad_img"], ref["grad_img"], "grad_img",
                      extra=4e-6 * ref["grad_img_absterms"])
+    else:
+        assert "grad_img" not in res
 
 
 @pytest.mark.parametrize("shape,batch", [((1, 1), 1), ((1, 9), 2), ((7, 1), 1), ((5, 7), 3),
@@ -83,6 +85,20 @@ def test_soft_parity_K(K):
     u = synthetic.soft_direction(2, seed=K)
     g = synthetic.upstream_grad((2, K), seed=K + 1)
     compare(img, tau, 50.0, 1.0, u, g)
+
+
+@pytest.mark.parametrize("shape,batch,K", [((1, 9), 2, 24), ((33, 65), 2, 24), ((48, 80), 1, 129),
+                                           ((31, 257), 1, 300), ((2, 3, 4), 2, 24),
+                                           ((9, 17, 33), 1, 129), ((12, 20, 45), 2, 300)])
+def test_soft_parity_without_the_image_gradient(shape, batch, K):
+    """The backward without an image gradient (the one a loss on S alone takes) keeps no
+    per-pixel accumulator; threshold counts past one chunk of the backward (128) included."""
+    img = synthetic.grf(shape, seed=sum(shape) + K, batch=batch) if min(shape) > 1 else \
+        np.random.default_rng(K).random((batch,) + shape).astype(np.float32)
+    tau = synthetic.uniform_thresholds(K, -0.2, 1.2)
+    u = synthetic.soft_direction(len(shape), seed=K)
+    g = synthetic.upstream_grad((batch, K), seed=K + 1)
+    compare(img, tau, 50.0, 1.0, u, g, want_img=False)
 
 
 @pytest.mark.parametrize("lam,alpha", [(1.0, 1.0), (5.0, -0.7), (50.0, 2.5), (500.0, 1.0),
