@@ -450,9 +450,10 @@ def time_e2e(args, parts, inputs, step, device, world):
         for hr, t in zip(res_host, step.results()):
             hr.copy_(t, non_blocking=True)
 
-    one()
-    torch.cuda.synchronize()
     link = host_link_gbs(device)
+    for _ in range(max(1, args.warmup)):  # the same warm-up count as the device-side timing
+        one()
+    torch.cuda.synchronize()
     barrier(world)
     marks = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     marks[0].record(stream)
