@@ -350,15 +350,48 @@ class OurStep:
                 out[part_name(p)] = [int(v) for v in st.cpu().tolist()]
         return out
 
+    def results_of(self, i):
+        p, o = self.parts[i], self.outs[i]
+        if p[0] == "hard":
+            return [o["out"] if part_slab(p) else o]
+        return [o["s"], *o["grads"].values()]
+
     def results(self):
-        res = []
-        for p, o in zip(self.parts, self.outs):
-            if p[0] == "hard":
-                res.append(o["out"] if part_slab(p) else o)
-            else:
-                res.append(o["s"])
-                res.extend(o["grads"].values())
-        return res
+        return [t for i in range(len(self.parts)) for t in self.results_of(i)]
+
+
+def capture_parts(step, parts, device):
+    """Captures each part's library calls into its own CUDA graph and returns a runner that
+    replays part i. Every replay launches all of the part's kernels again; what it removes is the
+    host's per-call work (argument checks, ctypes, launch submission), which for small parts
+    takes longer than the GPU work and leaves the GPU idle between calls. Before returning it
+    checks that a replay gives the same bits as an eager call of the same part."""
+    import torch
+
+    if any(part_slab(p) for p in parts):
+        raise SystemExit("--graph: the streamed part copies from host memory with its own "
+                         "streams and is not captured")
+    graphs, captured = [], []
+    for i in range(len(parts)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step.run_part(i)
+        graphs.append(g)
+        o = step.outs[i]
+        captured.append(dict(o["grads"]) if isinstance(o, dict) and "grads" in o else None)
+    for i, g in enumerate(graphs):
+        g.replay()
+        torch.cuda.synchronize()
+        got = [t.clone() for t in step.results_of(i)]
+        step.run_part(i)
+        torch.cuda.synchronize()
+        want = step.results_of(i)
+        if len(got) != len(want) or not all(torch.equal(a, b) for a, b in zip(got, want)):
+            raise SystemExit(f"--graph: replay of part {part_name(parts[i])} differs from the "
+                             "eager call")
+        if captured[i] is not None:  # the eager call made new gradient tensors
+            step.outs[i]["grads"] = captured[i]
+    return lambda i: graphs[i].replay()
 
 
 def time_ours(args, parts, rank, world, device):
@@ -374,6 +407,9 @@ def time_ours(args, parts, rank, world, device):
     barrier(world)
     sampler = ClockSampler(torch.cuda.current_device())
     sampler.start()
+    run = step.run_part
+    if args.graph:
+        run = capture_parts(step, parts, device)
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in parts] for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -383,7 +419,7 @@ def time_ours(args, parts, rank, world, device):
     for s in range(args.steps):
         for i in range(len(parts)):
             ev[s][i][0].record(stream)
-            step.run_part(i)
+            run(i)
             ev[s][i][1].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
@@ -648,6 +684,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true",
                     help="skip the end-to-end timing (for profiler launch lists of the step)")
+    ap.add_argument("--graph", action="store_true",
+                    help="time replays of one CUDA graph per part (the same library calls, "
+                         "captured once) instead of eager calls")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -659,7 +698,9 @@ def main(argv=None):
               "parts": [part_name(p) for p in parts],
               "l2": "inputs larger than L2 (the 268 MB image and the 4 GiB volume evict L2 "
                     "between passes)" if args.workload == "headline" else "not flushed",
-              "parallelism": f"independent replicas x{world}"}
+              "parallelism": f"independent replicas x{world}",
+              "timing": ("one CUDA graph per part (its library calls captured once), replayed "
+                         "every step" if args.graph else "eager library calls")}
 
     if args.impl == "reference":
         if rank != 0:
