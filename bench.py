@@ -269,6 +269,28 @@ def make_inputs(parts, device):
     return inputs
 
 
+def hard_launches(p, sms):
+    """Kernels one hard-ECC call launches: the pass and the scan, or the pass alone when a 2-D
+    image gets a single block (which stores its curve itself). Mirrors the library's grid
+    choice: 2-D blocks of 8 warps, 128-column strips, 3 blocks per SM."""
+    if part_slab(p):  # slabs sharing one plane: a 3-D pass each, a plane pass from the second
+        D, S, n, a = p[1][0], part_slab(p), 0, 0  # slab on, and one scan at the end
+        while True:
+            b = min(a + S - 1, D - 1)
+            n += 1
+            if b == D - 1:
+                return 2 * n
+            a = b
+    if len(p[1]) != 2:
+        return 2
+    Hy, W = p[1]
+    strips = -(-W // 128)
+    per_image = max(1, sms * 3 // p[2])
+    per_image = min(per_image, max(1, -(-strips * Hy // (32 * 8))))
+    R = min(max(1, per_image * 8 // strips), Hy)
+    return 1 if -(-strips * R // 8) == 1 else 2
+
+
 class OurStep:
     """One pass of the hot path through the library's public binding (device-resident)."""
 
@@ -297,7 +319,9 @@ class OurStep:
                 s = torch.empty((nb, nd, K) if nd > 1 else (nb, K), dtype=torch.float32,
                                 device=device)
                 self.outs.append({"ws": ws, "s": s})
-        self.launches_per_step = sum(2 if p[0] == "hard" else 6 for p in parts)
+        sms = torch.cuda.get_device_properties(device).multi_processor_count
+        self.launches_per_step = sum(hard_launches(p, sms) if p[0] == "hard" else 6
+                                     for p in parts)
 
     def run_part(self, i):
         p, x, o = self.parts[i], self.inputs[i], self.outs[i]

@@ -145,9 +145,8 @@ int ecc_hard(const void *img, int dtype, int ndim, const int64_t *dims, int64_t 
     const size_t align = dtype == ECC_U8 ? 4 : 16;
     pl.vec_ok = ((uintptr_t)img % align == 0) && (W % 4 == 0);
     pl.table = table;
+    pl.zero_out = true;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(out, 0, sizeof(int64_t) * (size_t)outn, s) != cudaSuccess)
-        return ECC_ECUDA;
     if (hard_run(pl, s) != cudaSuccess) return ECC_ECUDA;
     return ECC_OK;
 }

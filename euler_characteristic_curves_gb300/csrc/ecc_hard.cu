@@ -70,10 +70,46 @@ __device__ __forceinline__ void block_setup(const HardParams<CAP> &P, int *hist,
     __syncthreads();
 }
 
-template <int CAP>
+// The image's only block (P.direct) writes the curve itself: warp w of the nw warps takes the
+// contiguous bins [w per, (w + 1) per), adds the totals of the warps before it, and walks its
+// bins 32 at a time with a shuffle scan and a running carry.
+__device__ __forceinline__ void block_store_curve(const int *hist, int H, int64_t *dst)
+{
+    __shared__ long long warp_total[32];
+    const int lane = threadIdx.x & (kWarp - 1), warp = threadIdx.x >> 5;
+    const int nw = blockDim.x >> 5;
+    const int per = (H + nw - 1) / nw;
+    const int lo = min(H, warp * per), hi = min(H, lo + per);
+    long long t = 0;
+    for (int i = lo + lane; i < hi; i += kWarp) t += hist[i];
+#pragma unroll
+    for (int o = kWarp / 2; o > 0; o >>= 1) t += __shfl_xor_sync(kFull, t, o);
+    if (lane == 0) warp_total[warp] = t;
+    __syncthreads();
+    long long carry = 0;
+    for (int w = 0; w < warp; ++w) carry += warp_total[w];
+    for (int c = lo; c < hi; c += kWarp) {  // warp-uniform bounds
+        const int i = c + lane;
+        long long v = i < hi ? (long long)hist[i] : 0;
+#pragma unroll
+        for (int o = 1; o < kWarp; o <<= 1) {
+            const long long n = __shfl_up_sync(kFull, v, o);
+            if (lane >= o) v += n;
+        }
+        if (i < hi) dst[i] = (int64_t)(carry + v);
+        carry += __shfl_sync(kFull, v, kWarp - 1);
+    }
+}
+
+// DIRECT_OK: the kernel may run with P.direct (the 2-D kernel; the 3-D kernel always flushes).
+template <bool DIRECT_OK, int CAP>
 __device__ __forceinline__ void block_flush(const HardParams<CAP> &P, const int *hist, int64_t b)
 {
     __syncthreads();
+    if (DIRECT_OK && P.direct) {  // grid-uniform
+        block_store_curve(hist, P.H, P.out + b * (int64_t)P.H);
+        return;
+    }
     unsigned long long *dst = reinterpret_cast<unsigned long long *>(P.out + b * (int64_t)P.H);
     for (int i = threadIdx.x; i < P.H; i += blockDim.x) {
         const int v = hist[i];
@@ -374,7 +410,7 @@ __global__ void __launch_bounds__(kHardThreads, ECC_2D_MIN_BLOCKS) ecc_hard2d_ke
         else
             band2d<T, SEARCH, false, SAT>(img, Hy, W, c, y0, y1, q, K, table, hist_s);
     }
-    block_flush(P, hist, b);
+    block_flush<true>(P, hist, b);
 }
 
 // ----------------------------------------------------------------------------------------------
@@ -830,7 +866,7 @@ __global__ void __launch_bounds__(k3Threads, ECC_3D_MIN_BLOCKS) ecc_hard3d_kerne
             bo = const_cast<uint16_t *>(t);
         }
     }
-    block_flush(P, hist, b);
+    block_flush<false>(P, hist, b);
 }
 
 // ----------------------------------------------------------------------------------------------
@@ -970,6 +1006,13 @@ static cudaError_t launch_hard(const HardPlan &pl, cudaStream_t s)
     }
     if (per_image < 1) per_image = 1;
     P.ctas_per_image = (int)per_image;
+    // 2-D, one block per image: it holds the whole histogram and stores the curve itself
+    P.direct = (pl.ndim == 2 && per_image == 1 && pl.scan && pl.sign == 1) ? 1 : 0;
+    if (!P.direct && pl.zero_out) {
+        const cudaError_t m =
+            cudaMemsetAsync(pl.out, 0, sizeof(int64_t) * (size_t)(pl.batch * pl.H), s);
+        if (m != cudaSuccess) return m;
+    }
 
     const size_t smem =
         (size_t)hist_words(pl.H) * sizeof(int) + (size_t)(CAP + 2) * sizeof(float);
@@ -987,7 +1030,7 @@ static cudaError_t launch_hard(const HardPlan &pl, cudaStream_t s)
         ecc_hard3d_kernel<T, CAP, SEARCH><<<grid, k3Threads, smem, s>>>(P);
     }
     cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess || !pl.scan) return e;
+    if (e != cudaSuccess || !pl.scan || P.direct) return e;
     return hard_scan(pl.out, pl.H, pl.batch, s);
 }
 

@@ -38,7 +38,7 @@ enum KeyMode : int { kKeyEstimate = 0, kKeySearch = 1, kKeyLut = 2 };
 template <int CAP>
 struct HardParams {
     const void *img;
-    int64_t *out;      // [batch][H] int64, zeroed before the launch
+    int64_t *out;      // [batch][H] int64: zeroed before the launch, unless direct
     int64_t D, Hy, W;  // extents (D = 1 for 2-D)
     int64_t image_elems;
     int H;
@@ -56,6 +56,7 @@ struct HardParams {
     int tasks_x, tasks_y, tasks_z;
     int64_t tasks_per_image;
     int ctas_per_image;
+    int direct;  // 1: one block per image, which stores the running sum itself (no memset, scan)
     float table[CAP + 2];  // f32: T_0..T_{H-1}, +inf, +inf;  u8: uint16 key pattern per byte
 };
 
@@ -76,6 +77,7 @@ struct HardPlan {
     const float *table;  // H + 2 thresholds (f32), or 256 uint16 key patterns (u8) in 128 floats
     int sign = 1;        // -1: subtract the histogram from out
     bool scan = true;    // false: leave out as a histogram (the caller scans once at the end)
+    bool zero_out = false;  // true: the launcher zeroes out first (when it needs zeroing)
 };
 cudaError_t hard_run(const HardPlan &pl, cudaStream_t s);
 // out[b][k] = running sum over k of out[b][k], for batch rows of H bins

@@ -94,6 +94,23 @@ def test_nbins_variants(nbins):
     check(q, nbins, 0.0, 255.0)
 
 
+@pytest.mark.parametrize("shape,batch,nbins,kind", [((20, 37), 500, 100, "f32"),
+                                                     ((64, 130), 460, 256, "u8"),
+                                                     ((9, 300), 470, 4096, "f32"),
+                                                     ((3, 5), 600, 1, "f32"),
+                                                     ((1, 1), 700, 7, "u8")])
+def test_one_block_per_image_stores_the_curve_itself(shape, batch, nbins, kind):
+    """A batch larger than the blocks that fit on the device at once gives each image a single
+    block, which scans its own histogram and stores the curve (no zeroing, no atomics, no scan
+    launch); every image must still match the oracle bit for bit."""
+    f = synthetic.grf(shape, nbins + batch, batch=batch) if min(shape) > 1 else \
+        np.random.default_rng(batch).random((batch,) + shape).astype(np.float32)
+    if kind == "u8":
+        check(synthetic.quantise_u8(f), nbins, 0.0, 255.0, ndim=2)
+    else:
+        check(f, nbins, 0.0, 1.0, ndim=2)
+
+
 def test_special_values():
     f = synthetic.grf((64, 160), 8)
     g = f.copy()
