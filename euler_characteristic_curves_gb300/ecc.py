@@ -13,6 +13,7 @@ PyTorch layer ("Key designs -- differentiable ECC layer (sigmoid relaxation)" in
 from __future__ import annotations
 
 import ctypes
+import functools
 import os
 import threading
 
@@ -87,15 +88,26 @@ def _check(rc: int, where: str):
         raise ECCError(rc, where)
 
 
+@functools.lru_cache(maxsize=256)
+def _dims_tuple_array(dims):
+    return (ctypes.c_int64 * len(dims))(*dims)  # read-only for the library (const int64_t *)
+
+
 def _dims_array(dims):
-    arr = (ctypes.c_int64 * len(dims))(*[int(x) for x in dims])
-    return arr
+    return _dims_tuple_array(tuple(int(x) for x in dims))
+
+
+# The current stream's raw handle without building a Stream object (a few microseconds per call
+# on small inputs); the public call where this build of torch lacks it.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
 def _stream_handle(stream):
-    if stream is None:
-        stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None:
+        return _raw_stream(torch.cuda.current_device())
+    return torch.cuda.current_stream().cuda_stream
 
 
 def _need_cuda(t: torch.Tensor, name: str):
@@ -143,9 +155,8 @@ def ecc_hard(img: torch.Tensor, nbins: int, vmin: float, vmax: float, ndim: int 
         if out.dtype != torch.int64 or out.numel() != batch * nbins:
             raise ValueError("out must be int64 with batch * nbins elements")
     lib = load_library()
-    rc = lib.ecc_hard(ctypes.c_void_p(img.data_ptr()), dt, ndim, _dims_array(dims), batch,
-                      int(nbins), float(vmin), float(vmax), ctypes.c_void_p(out.data_ptr()),
-                      _stream_handle(stream))
+    rc = lib.ecc_hard(img.data_ptr(), dt, ndim, _dims_array(dims), batch, int(nbins),
+                      float(vmin), float(vmax), out.data_ptr(), _stream_handle(stream))
     _check(rc, "ecc_hard")
     out = out.view(batch, nbins)
     return out if batched else out[0]

@@ -200,6 +200,17 @@ def test_3d_batches_special_values():
     check(q, 9, 100.0, 140.0, ndim=3)
 
 
+def test_calls_without_a_stream_use_the_current_stream():
+    assert ecc._stream_handle(None) == torch.cuda.current_stream().cuda_stream
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        assert ecc._stream_handle(None) == s.cuda_stream != torch.cuda.default_stream().cuda_stream
+        f = synthetic.grf((70, 90), 15)
+        got = ecc.ecc_hard(torch.from_numpy(f).to(DEV), 33, 0.0, 1.0)
+    s.synchronize()
+    np.testing.assert_array_equal(got.cpu().numpy(), oracle.ecc_hard(f, 33, 0.0, 1.0))
+
+
 def test_deterministic_and_stream_independent():
     f = synthetic.grf((333, 444), 14)
     t = torch.from_numpy(f).to(DEV)
