@@ -923,23 +923,29 @@ static int num_sms()
     return n;
 }
 
-// Planes per 3-D block task: the power of two from 32 up that maximises the useful fraction of
-// the block time -- tasks shared evenly over the blocks (the busiest block sets the time) times
-// R / (R + 2) for the two prologue planes of each task.
+// Planes per 3-D block task. Cutting D planes into k chunks of R = ceil(D / k) planes gives
+// tiles * ceil(D / R) tasks; with G blocks taking tasks g, g + G, ..., the busiest block runs
+// ceil(tasks / G) of them, each R + 2 planes long (two prologue planes). R minimises that block
+// time over k = 1, 2, ... (chunks of at least 8 planes, the prologue then at most a fifth), the
+// first k winning ties; more than 64 rounds of tasks cannot gain more than a sixty-fourth.
 static int64_t pick_chunk(int64_t D, int64_t tiles, int64_t blocks)
 {
-    int64_t best = 32;
-    double best_eff = -1.0;
-    for (int64_t R = 32;; R *= 2) {
+    const int64_t rmin = D < 8 ? D : 8;
+    int64_t best = D, prev = -1;
+    double best_time = -1.0;
+    for (int64_t k = 1; k <= D; ++k) {
+        const int64_t R = (D + k - 1) / k;
+        if (R < rmin) break;
+        if (R == prev) continue;
+        prev = R;
         const int64_t tasks = tiles * ((D + R - 1) / R);
-        const double per = (double)tasks / (double)blocks;
-        const double busiest = (double)((tasks + blocks - 1) / blocks);
-        const double eff = (per / busiest) * ((double)R / (double)(R + 2));
-        if (eff > best_eff + 1e-9) {
-            best_eff = eff;
+        const int64_t rounds = (tasks + blocks - 1) / blocks;
+        const double t = (double)rounds * (double)(R + 2);
+        if (best_time < 0.0 || t < best_time - 1e-9) {
+            best_time = t;
             best = R;
         }
-        if (R >= D) break;
+        if (rounds > 64) break;
     }
     return best;
 }
