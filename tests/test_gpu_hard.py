@@ -265,3 +265,46 @@ def test_workload_1024cube_f32_inclusion_exclusion():
         slab = v[a: a + 6, 100:420, :].contiguous()
         got = ecc.ecc_hard(slab.unsqueeze(0), 256, 0.0, 1.0)[0].cpu().numpy()
         np.testing.assert_array_equal(got, oracle.ecc_hard(slab.cpu().numpy(), 256, 0.0, 1.0))
+
+
+def test_library_calls_replay_from_a_cuda_graph():
+    """Calls are asynchronous on the current stream and allocate nothing on the device, so they
+    capture into a CUDA graph; a replay after the inputs change in place must give what eager
+    calls give on the new inputs (hard 2-D with one block per image, hard 3-D, soft fwd + bwd)."""
+    img2 = torch.from_numpy(synthetic.grf((96, 200), 21, batch=3)).to(DEV)
+    vol = torch.from_numpy(synthetic.grf((20, 40, 150), 22)).to(DEV)
+    simg = torch.from_numpy(synthetic.grf((64, 64), 23, batch=2)).to(DEV)
+    tau = torch.from_numpy(synthetic.uniform_thresholds(32)).to(DEV)
+    alpha = torch.ones(1, device=DEV)
+    u = torch.from_numpy(synthetic.soft_direction(2, 24)).to(DEV)
+    g = torch.from_numpy(synthetic.upstream_grad((2, 32), 25)).to(DEV)
+    o2 = torch.empty((3, 77), dtype=torch.int64, device=DEV)
+    o3 = torch.empty((1, 64), dtype=torch.int64, device=DEV)
+    ws = torch.empty(ecc.soft_workspace_bytes((64, 64), 2, 32), dtype=torch.uint8, device=DEV)
+    s_out = torch.empty((2, 32), dtype=torch.float32, device=DEV)
+
+    def calls():
+        ecc.ecc_hard(img2, 77, 0.0, 1.0, ndim=2, out=o2)
+        ecc.ecc_hard(vol.unsqueeze(0), 64, 0.0, 1.0, out=o3)
+        ecc.ecc_soft_fwd(simg, tau, 50.0, alpha, u, ws=ws, out=s_out)
+        return ecc.ecc_soft_bwd(simg, tau, 50.0, alpha, u, g, ws)
+
+    calls()  # warm-up outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        grads = calls()
+    for seed in (26, 27):
+        img2.copy_(torch.from_numpy(synthetic.grf((96, 200), seed, batch=3)))
+        vol.copy_(torch.from_numpy(synthetic.grf((20, 40, 150), seed)))
+        simg.copy_(torch.from_numpy(synthetic.grf((64, 64), seed, batch=2)))
+        graph.replay()
+        torch.cuda.synchronize()
+        got = [o2.clone(), o3.clone(), s_out.clone()] + [grads[k].clone() for k in sorted(grads)]
+        want_g = calls()
+        torch.cuda.synchronize()
+        want = [o2, o3, s_out] + [want_g[k] for k in sorted(want_g)]
+        for a, b in zip(got, want):
+            assert torch.equal(a, b)
+        np.testing.assert_array_equal(got[0].cpu().numpy(),
+                                      oracle.ecc_hard(img2.cpu().numpy(), 77, 0.0, 1.0, ndim=2))
