@@ -729,6 +729,7 @@ def main(argv=None):
     if args.impl == "reference":
         if rank != 0:
             return 0
+        config["timing"] = "the oracle on one host core, a bounded sample of every part per step"
         vox, dt, _ = time_oracle(args.steps, args.warmup, parts)
         value = vox / dt / 1e9
         line = {"impl": "reference", "metric": METRIC, "value": round(value, 6),
