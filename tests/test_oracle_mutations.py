@@ -3,7 +3,9 @@ source (on the CPU), builds it, swaps it in, and checks that the pins that shoul
 
 Mistakes planted: a flipped sign for odd-dimensional cells, a dropped cell type, '<' for '<=' in
 the threshold comparison, a transposed offset for one axis, a reversed sigmoid argument, a wrong
-sign in the backward pass, the opposite tie rule for the cell owner, and swapped coordinate axes.
+sign in the backward pass, the opposite tie rule for the cell owner, and swapped coordinate axes;
+and, in a copy of the transform's Python bookkeeping, a direction reading another direction's
+upstream gradient or writing its u-gradient to another row.
 """
 import os
 import subprocess
@@ -167,3 +169,28 @@ def test_hard_pins_catch(tmp_path, swap_oracle, name, old, new):
 def test_soft_pins_catch(tmp_path, swap_oracle, name, old, new):
     swap_oracle(_build_mutant(tmp_path, old, new))
     assert not soft_pins_pass(), f"mutation not caught: {name}"
+
+
+def _mutant_python(monkeypatch, func_name, old, new):
+    """Plant a mistake in a copy of one of the oracle's Python functions and swap it in."""
+    import inspect
+    import textwrap
+
+    src = textwrap.dedent(inspect.getsource(getattr(oracle, func_name)))
+    assert src.count(old) == 1, f"mutation anchor not found: {old!r}"
+    ns = dict(vars(oracle))
+    exec(compile(src.replace(old, new), f"<mutant {func_name}>", "exec"), ns)
+    monkeypatch.setattr(oracle, func_name, ns[func_name])
+
+
+@pytest.mark.parametrize("old,new", [
+    ("go[..., j, :]", "go[..., (j + 1) % U.shape[0], :]"),       # another direction's upstream
+    ('res["grad_u"][j] = ', 'res["grad_u"][(j + 1) % U.shape[0]] = '),  # u-gradient row swapped
+])
+def test_transform_pin_catches_direction_bookkeeping(monkeypatch, old, new):
+    from tests import test_oracle_soft as pins
+
+    pins.test_ect_gradients_match_finite_differences((5, 6))  # the real oracle passes
+    _mutant_python(monkeypatch, "ecc_soft_ect_bwd", old, new)
+    with pytest.raises(AssertionError):
+        pins.test_ect_gradients_match_finite_differences((5, 6))

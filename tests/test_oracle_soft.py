@@ -219,3 +219,52 @@ def test_ect_of_one_direction_is_the_soft_ecc_and_batches_stack():
     assert s.shape == (3, 3, 6)
     for j in range(3):
         np.testing.assert_array_equal(s[:, j], oracle.ecc_soft_fwd(img, tau, 40.0, 1.0, U[j], ndim=2))
+
+
+@pytest.mark.parametrize("shape", [(5, 6), (3, 4, 5)])
+def test_ect_gradients_match_finite_differences(shape):
+    """The transform's backward against central differences of its own forward, with two images
+    and three directions: catches a direction's upstream slice or its u-gradient row taken from
+    the wrong place (the single-direction pins cannot)."""
+    rng = np.random.default_rng(7)
+    n = int(np.prod(shape))
+    f = np.stack([rng.permutation(n).reshape(shape) for _ in range(2)]).astype(np.float32) / n
+    K, nd, lam, alpha = 4, 3, 3.0, 1.25
+    tau = np.linspace(0.1, 0.9, K).astype(np.float32)
+    U = (0.05 * rng.standard_normal((nd, len(shape)))).astype(np.float32)
+    g = rng.standard_normal((2, nd, K))
+
+    def L(f_=f, tau_=tau, alpha_=alpha, U_=U):
+        s = oracle.ecc_soft_ect_fwd(f_, tau_, lam, alpha_, U_, ndim=len(shape))
+        assert s.shape == g.shape
+        return float(np.sum(g * s))
+
+    res = oracle.ecc_soft_ect_bwd(f, tau, lam, alpha, U, g, ndim=len(shape))
+    step = np.float32(2.0 ** -12)
+
+    def close(fd, got):
+        return abs(fd - got) <= 1e-5 * max(1.0, abs(fd))
+
+    for k in range(K):
+        tp, tm = tau.copy(), tau.copy()
+        tp[k] += step
+        tm[k] -= step
+        fd = (L(tau_=tp) - L(tau_=tm)) / (float(tp[k]) - float(tm[k]))
+        assert close(fd, res["grad_tau"][k]), (k, fd, res["grad_tau"][k])
+    ap, am = np.float32(alpha + step), np.float32(alpha - step)
+    assert close((L(alpha_=ap) - L(alpha_=am)) / (float(ap) - float(am)), res["grad_alpha"])
+    for j in range(nd):
+        for d in range(len(shape)):
+            Up, Um = U.copy(), U.copy()
+            Up[j, d] += step
+            Um[j, d] -= step
+            fd = (L(U_=Up) - L(U_=Um)) / (float(Up[j, d]) - float(Um[j, d]))
+            assert close(fd, res["grad_u"][j, d]), (j, d, fd, res["grad_u"][j, d])
+    flat = f.reshape(-1)
+    for p in rng.choice(flat.size, size=10, replace=False):
+        fp, fm = flat.copy(), flat.copy()
+        fp[p] += np.float32(2.0 ** -16)
+        fm[p] -= np.float32(2.0 ** -16)
+        fd = (L(f_=fp.reshape(f.shape)) - L(f_=fm.reshape(f.shape))) / (float(fp[p]) - float(fm[p]))
+        got = res["grad_img"].reshape(-1)[p]
+        assert close(fd, got), (p, fd, got)
