@@ -110,10 +110,12 @@ const char *ecc_status_str(int status)
 
 int ecc_version(void) { return 10000; }
 
-int ecc_hard(const void *img, int dtype, int ndim, const int64_t *dims, int64_t batch, int nbins,
-             double vmin, double vmax, int64_t *out, ecc_stream_t stream)
+// Sizes of a hard-ECC call: the checks ecc_hard makes on its shape arguments, and the plan's
+// extents on success.
+static int hard_shape_check(int dtype, int ndim, const int64_t *dims, int64_t batch, int nbins,
+                            HardPlan &pl)
 {
-    if (!img || !out || !dims) return ECC_EINVAL;
+    if (!dims) return ECC_EINVAL;
     if (dtype != ECC_U8 && dtype != ECC_F32) return ECC_EDTYPE;
     if (ndim != 2 && ndim != 3) return ECC_EDIM;
     for (int d = 0; d < ndim; ++d)
@@ -121,16 +123,17 @@ int ecc_hard(const void *img, int dtype, int ndim, const int64_t *dims, int64_t 
     if (batch < 1) return ECC_EINVAL;
     if (nbins < 1) return ECC_EINVAL;
     if (nbins > ECC_MAX_NBINS) return ECC_ERANGE;
-    if (!isfinite(vmin) || !isfinite(vmax) || !(vmin <= vmax) || !isfinite(vmax - vmin))
-        return ECC_EINVAL;
+    // the kernels index rows, columns and strips with 32-bit integers
+    for (int d = 0; d < ndim; ++d)
+        if (dims[d] > ECC_MAX_EXTENT) return ECC_ERANGE;
     const int64_t D = ndim == 3 ? dims[0] : 1;
     const int64_t Hy = dims[ndim - 2], W = dims[ndim - 1];
     int64_t plane, elems, total, outn;
     if (!mul_ok(Hy, W, plane) || !mul_ok(plane, D, elems) || !mul_ok(elems, batch, total) ||
         total > ((int64_t)1 << 50) || !mul_ok(batch, nbins, outn) || batch > 65535)
         return ECC_ERANGE;
-
-    HardPlan pl;
+    // 2-D: one warp per (128-column strip, row range); their count stays below 2^31
+    if (ndim == 2 && ((W + 127) / 128) * Hy >= ((int64_t)1 << 31)) return ECC_ERANGE;
     pl.ndim = ndim;
     pl.dtype = dtype;
     pl.D = D;
@@ -138,16 +141,46 @@ int ecc_hard(const void *img, int dtype, int ndim, const int64_t *dims, int64_t 
     pl.W = W;
     pl.batch = batch;
     pl.H = nbins;
+    return ECC_OK;
+}
+
+int ecc_hard(const void *img, int dtype, int ndim, const int64_t *dims, int64_t batch, int nbins,
+             double vmin, double vmax, int64_t *out, ecc_stream_t stream)
+{
+    if (!img || !out || !dims) return ECC_EINVAL;
+    HardPlan pl;
+    const int rc = hard_shape_check(dtype, ndim, dims, batch, nbins, pl);
+    if (rc != ECC_OK) return rc;
+    if (!isfinite(vmin) || !isfinite(vmax) || !(vmin <= vmax) || !isfinite(vmax - vmin))
+        return ECC_EINVAL;
     pl.img = img;
     pl.out = out;
     float table[ECC_MAX_NBINS + 2];
     hard_keys(dtype, nbins, vmin, vmax, pl, table);
     const size_t align = dtype == ECC_U8 ? 4 : 16;
-    pl.vec_ok = ((uintptr_t)img % align == 0) && (W % 4 == 0);
+    pl.vec_ok = ((uintptr_t)img % align == 0) && (pl.W % 4 == 0);
     pl.table = table;
     pl.zero_out = true;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (hard_run(pl, s) != cudaSuccess) return ECC_ECUDA;
+    return ECC_OK;
+}
+
+int ecc_hard_launch_info(int dtype, int ndim, const int64_t *dims, int64_t batch, int nbins,
+                         int sm_count, int64_t *info)
+{
+    if (!info) return ECC_EINVAL;
+    HardPlan pl;
+    const int rc = hard_shape_check(dtype, ndim, dims, batch, nbins, pl);
+    if (rc != ECC_OK) return rc;
+    const int sms = sm_count > 0 ? sm_count : num_sms();
+    const HardShape sh = plan_hard(pl, sms);
+    info[0] = sh.blocks_per_image;
+    info[1] = sh.tasks_per_image;
+    info[2] = sh.rows_per_task;
+    info[3] = sh.rounds;
+    info[4] = sh.direct ? 1 : 0;
+    info[5] = sms;
     return ECC_OK;
 }
 

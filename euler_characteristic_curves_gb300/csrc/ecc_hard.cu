@@ -915,7 +915,7 @@ __global__ void __launch_bounds__(kScanThreads) ecc_bin_scan_kernel(int64_t *out
 // Host-side launch (called from the C ABI after validation)
 // ----------------------------------------------------------------------------------------------
 
-static int num_sms()
+int num_sms()
 {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 148;
@@ -950,6 +950,52 @@ static int64_t pick_chunk(int64_t D, int64_t tiles, int64_t blocks)
     return best;
 }
 
+HardShape plan_hard(const HardPlan &pl, int sms)
+{
+    HardShape sh;
+    const int64_t strips = (pl.W + kStrip - 1) / kStrip;
+    const int per_sm = pl.ndim == 2 ? ECC_2D_MIN_BLOCKS : ECC_3D_MIN_BLOCKS;
+    const int64_t resident = (int64_t)sms * per_sm;  // blocks that fit at once
+    // blocks per image: the resident blocks shared out over the batch, rounded down so that the
+    // whole grid is one wave (rounding up left a few blocks to run alone in a second wave)
+    int64_t per_image = resident / pl.batch;
+    if (per_image < 1) per_image = 1;  // batches larger than a wave run in several waves
+    if (pl.ndim == 2) {
+        // R row ranges per strip, one warp per (strip, range), at least 32 rows per warp
+        const int64_t N = strips * pl.Hy;
+        const int64_t need = (N + 32 * kHardWarps - 1) / (32 * kHardWarps);
+        if (per_image > need) per_image = need;
+        if (per_image < 1) per_image = 1;
+        int64_t R = per_image * kHardWarps / strips;
+        if (R < 1) R = 1;
+        if (R > pl.Hy) R = pl.Hy;
+        per_image = (strips * R + kHardWarps - 1) / kHardWarps;  // every (strip, range) a warp
+        sh.rows_per_task = R;
+        sh.tasks_x = strips;
+        sh.tasks_y = pl.Hy;
+        sh.tasks_z = 1;
+        sh.tasks_per_image = strips * R;  // warps with a band
+    } else {
+        const int64_t tiles_y = (pl.Hy + kTileRows - 1) / kTileRows;
+        const int64_t tiles = strips * tiles_y;
+        if (per_image > tiles * pl.D) per_image = tiles * pl.D;
+        const int64_t R = pick_chunk(pl.D, tiles, per_image);
+        sh.rows_per_task = R;
+        sh.tasks_x = strips;
+        sh.tasks_y = tiles_y;
+        sh.tasks_z = (pl.D + R - 1) / R;
+        sh.tasks_per_image = sh.tasks_x * sh.tasks_y * sh.tasks_z;
+        if (per_image > sh.tasks_per_image) per_image = sh.tasks_per_image;
+    }
+    if (per_image < 1) per_image = 1;
+    sh.blocks_per_image = per_image;
+    // 3-D: block g takes tasks g, g + G, ...; 2-D: one band per warp
+    sh.rounds = pl.ndim == 2 ? 1 : (sh.tasks_per_image + per_image - 1) / per_image;
+    // 2-D, one block per image: it holds the whole histogram and stores the curve itself
+    sh.direct = pl.ndim == 2 && per_image == 1 && pl.scan && pl.sign == 1;
+    return sh;
+}
+
 template <typename T, int CAP, bool SEARCH>
 static cudaError_t launch_hard(const HardPlan &pl, cudaStream_t s)
 {
@@ -973,47 +1019,17 @@ static cudaError_t launch_hard(const HardPlan &pl, cudaStream_t s)
     for (int i = 0; i < ntab; ++i) P.table[i] = pl.table[i];
     for (int i = ntab; i < CAP + 2; ++i) P.table[i] = 0.0f;
 
-    const int sms = num_sms();
-    const int64_t strips = (pl.W + kStrip - 1) / kStrip;
-    const int per_sm = pl.ndim == 2 ? ECC_2D_MIN_BLOCKS : ECC_3D_MIN_BLOCKS;
-    const int64_t resident = (int64_t)sms * per_sm;  // blocks that fit at once
-    // blocks per image: the resident blocks shared out over the batch, rounded down so that the
-    // whole grid is one wave (rounding up left a few blocks to run alone in a second wave)
-    int64_t per_image = resident / pl.batch;
-    if (per_image < 1) per_image = 1;  // batches larger than a wave run in several waves
-    if (pl.ndim == 2) {
-        // R row ranges per strip, one warp per (strip, range), at least 32 rows per warp
-        const int64_t N = strips * pl.Hy;
-        if (N >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;  // 32-bit row arithmetic
-        const int64_t need = (N + 32 * kHardWarps - 1) / (32 * kHardWarps);
-        if (per_image > need) per_image = need;
-        if (per_image < 1) per_image = 1;
-        int64_t R = per_image * kHardWarps / strips;
-        if (R < 1) R = 1;
-        if (R > pl.Hy) R = pl.Hy;
-        per_image = (strips * R + kHardWarps - 1) / kHardWarps;  // every (strip, range) a warp
-        P.rows_per_task = (int)R;
-        P.rows_extra = 0;
-        P.tasks_x = (int)strips;
-        P.tasks_y = (int)pl.Hy;
-        P.tasks_z = 1;
-        P.tasks_per_image = N;
-    } else {
-        const int64_t tiles_y = (pl.Hy + kTileRows - 1) / kTileRows;
-        const int64_t tiles = strips * tiles_y;
-        if (per_image > tiles * pl.D) per_image = tiles * pl.D;
-        const int64_t R = pick_chunk(pl.D, tiles, per_image);
-        P.rows_per_task = (int)R;
-        P.tasks_x = (int)strips;
-        P.tasks_y = (int)tiles_y;
-        P.tasks_z = (int)((pl.D + R - 1) / R);
-        P.tasks_per_image = (int64_t)P.tasks_x * P.tasks_y * P.tasks_z;
-        if (per_image > P.tasks_per_image) per_image = P.tasks_per_image;
-    }
-    if (per_image < 1) per_image = 1;
-    P.ctas_per_image = (int)per_image;
-    // 2-D, one block per image: it holds the whole histogram and stores the curve itself
-    P.direct = (pl.ndim == 2 && per_image == 1 && pl.scan && pl.sign == 1) ? 1 : 0;
+    const HardShape sh = plan_hard(pl, num_sms());
+    if (pl.ndim == 2 && sh.tasks_x * sh.tasks_y >= ((int64_t)1 << 31))
+        return cudaErrorInvalidValue;  // 32-bit row arithmetic (the C ABI rejects such sizes)
+    P.rows_per_task = (int)sh.rows_per_task;
+    P.rows_extra = 0;
+    P.tasks_x = (int)sh.tasks_x;
+    P.tasks_y = (int)sh.tasks_y;
+    P.tasks_z = (int)sh.tasks_z;
+    P.tasks_per_image = pl.ndim == 2 ? sh.tasks_x * sh.tasks_y : sh.tasks_per_image;
+    P.ctas_per_image = (int)sh.blocks_per_image;
+    P.direct = sh.direct ? 1 : 0;
     if (!P.direct && pl.zero_out) {
         const cudaError_t m =
             cudaMemsetAsync(pl.out, 0, sizeof(int64_t) * (size_t)(pl.batch * pl.H), s);
@@ -1022,7 +1038,7 @@ static cudaError_t launch_hard(const HardPlan &pl, cudaStream_t s)
 
     const size_t smem =
         (size_t)hist_words(pl.H) * sizeof(int) + (size_t)(CAP + 2) * sizeof(float);
-    dim3 grid((unsigned)per_image, (unsigned)pl.batch);
+    dim3 grid((unsigned)sh.blocks_per_image, (unsigned)pl.batch);
     if (pl.ndim == 2) {
         ecc_hard2d_kernel<T, CAP, SEARCH><<<grid, kHardThreads, smem, s>>>(P);
     } else {

@@ -79,6 +79,19 @@ struct HardPlan {
     bool scan = true;    // false: leave out as a histogram (the caller scans once at the end)
     bool zero_out = false;  // true: the launcher zeroes out first (when it needs zeroing)
 };
+// Launch shape of a hard-ECC call on a device of `sms` SMs (shared by the launcher and
+// ecc_hard_launch_info). 2-D: one warp per (strip, row range); 3-D: tasks (tile, chunk of planes)
+// taken by the blocks of an image in rounds, block g taking tasks g, g + G, ...
+struct HardShape {
+    int64_t blocks_per_image;
+    int64_t tasks_per_image;  // 2-D: (strip, row range) bands; 3-D: (tile, chunk) tasks
+    int64_t rows_per_task;    // 2-D: row ranges per strip; 3-D: planes per chunk
+    int64_t tasks_x, tasks_y, tasks_z;
+    int64_t rounds;  // 3-D: most tasks one block takes; 2-D: 1
+    bool direct;     // 2-D: the image's only block stores the curve itself
+};
+HardShape plan_hard(const HardPlan &pl, int sms);
+int num_sms();  // of the current device (148 when the query fails)
 cudaError_t hard_run(const HardPlan &pl, cudaStream_t s);
 // out[b][k] = running sum over k of out[b][k], for batch rows of H bins
 cudaError_t hard_scan(int64_t *out, int H, int64_t batch, cudaStream_t s);

@@ -8,12 +8,11 @@
 //
 // The array is a file-scope __device__ variable of ECC_NOALLOC_SCRATCH_BYTES bytes: every GPU that
 // loads the library holds one until the process exits. Host code cannot use the array's name as
-// a device address, so the first call on each device looks the address up with
-// cudaGetSymbolAddress (with that device current) and caches it.
+// a device address (on the host it names a stand-in), so every call looks the address up with
+// cudaGetSymbolAddress for the current device. The lookup is cheap, and doing it per call keeps
+// it right after cudaDeviceReset or a new primary context, where a cached address would be stale.
 #include <cuda_runtime.h>
 #include <stdint.h>
-
-#include <mutex>
 
 #include "ecc.h"
 #include "ecc_internal.cuh"
@@ -23,23 +22,13 @@ namespace {
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[ECC_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 128;
-void *g_scratch_addr[kMaxDevices];
-std::mutex g_scratch_mutex;
-
-// Device address of this device's copy of g_noalloc_scratch (looked up once per device).
+// Device address of the current device's copy of g_noalloc_scratch.
 int scratch_address(void **addr)
 {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ECC_ECUDA;
-    std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (g_scratch_addr[dev] == nullptr) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
-            return ECC_ECUDA;
-        g_scratch_addr[dev] = p;
-    }
-    *addr = g_scratch_addr[dev];
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+        return ECC_ECUDA;
+    *addr = p;
     return ECC_OK;
 }
 
@@ -62,7 +51,8 @@ extern "C" int ecc_soft_fwd_noalloc(const float *img, int ndim, const int64_t *d
     if (!(lambda > 0.0f) || !isfinite(lambda)) return ECC_EINVAL;
     SoftLayout L;
     if (!soft_layout(ndim, dims, batch, K, 1, L)) return ECC_ERANGE;
-    if (L.total > (size_t)ECC_NOALLOC_SCRATCH_BYTES) return ECC_ERANGE;
+    // the forward pass uses the workspace up to the backward-only scalar partials
+    if (L.off_scal > (size_t)ECC_NOALLOC_SCRATCH_BYTES) return ECC_ERANGE;
     void *ws = nullptr;
     const int rc = scratch_address(&ws);
     if (rc != ECC_OK) return rc;

@@ -74,7 +74,7 @@ bool soft_layout(int ndim, const int64_t *dims, int64_t batch, int K, int ndirs,
 {
     if ((ndim != 2 && ndim != 3) || !dims || batch < 1 || K < 1 || K > ECC_MAX_K) return false;
     for (int d = 0; d < ndim; ++d)
-        if (dims[d] < 1 || dims[d] > ((int64_t)1 << 31)) return false;
+        if (dims[d] < 1 || dims[d] > ECC_MAX_EXTENT) return false;
     if (ndirs < 1 || ndirs > ECC_MAX_DIRS) return false;
     if (batch * ndirs > 65535) return false;  // (image, direction) pairs run along gridDim.y
     L.ndirs = ndirs;

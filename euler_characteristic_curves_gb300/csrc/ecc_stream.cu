@@ -23,7 +23,7 @@ static size_t slab_bytes(int dtype, const int64_t *dims, int slab_planes)
 {
     if (!dims || (dtype != ECC_U8 && dtype != ECC_F32) || slab_planes < 2) return 0;
     for (int d = 0; d < 3; ++d)
-        if (dims[d] < 1 || dims[d] > ((int64_t)1 << 31)) return 0;
+        if (dims[d] < 1 || dims[d] > ECC_MAX_EXTENT) return 0;
     const int64_t planes = slab_planes < dims[0] ? slab_planes : dims[0];
     const double bytes = (double)planes * (double)dims[1] * (double)dims[2] *
                          (dtype == ECC_U8 ? 1.0 : 4.0);

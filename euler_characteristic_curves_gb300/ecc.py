@@ -12,6 +12,7 @@ PyTorch layer ("Key designs -- differentiable ECC layer (sigmoid relaxation)" in
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import functools
 import os
@@ -46,6 +47,8 @@ def load_library():
                                ctypes.c_float, ctypes.c_size_t)
         lib.ecc_hard.argtypes = [p, i, i, p, i64, i, d, d, p, p]
         lib.ecc_hard.restype = i
+        lib.ecc_hard_launch_info.argtypes = [i, i, p, i64, i, i, p]
+        lib.ecc_hard_launch_info.restype = i
         lib.ecc_hard_stream_buffer_bytes.argtypes = [i, p, i]
         lib.ecc_hard_stream_buffer_bytes.restype = sz
         lib.ecc_hard_stream.argtypes = [p, i, p, i, d, d, i, p, sz, p, p]
@@ -110,6 +113,26 @@ def _stream_handle(stream):
     return torch.cuda.current_stream().cuda_stream
 
 
+_no_switch = contextlib.nullcontext()
+
+
+def _on_device(t: torch.Tensor):
+    """Makes t's device current for a library call: the library launches on the current device,
+    and the current stream is looked up there. No switch when it already is current."""
+    idx = t.device.index
+    if idx is None or idx == torch.cuda.current_device():
+        return _no_switch
+    return torch.cuda.device(idx)
+
+
+def _check_out(out: torch.Tensor, like: torch.Tensor, dtype, numel: int):
+    """A caller-supplied output must be a contiguous tensor of `dtype` with `numel` elements on
+    the input's device (the library writes exactly that many)."""
+    _need_cuda(out, "out")
+    if out.dtype != dtype or out.numel() != numel or out.device != like.device:
+        raise ValueError(f"out must be {dtype} with {numel} elements on {like.device}")
+
+
 def _need_cuda(t: torch.Tensor, name: str):
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor (the ECC library has no CPU path)")
@@ -151,15 +174,27 @@ def ecc_hard(img: torch.Tensor, nbins: int, vmin: float, vmax: float, ndim: int 
     if out is None:
         out = torch.empty((batch, nbins), dtype=torch.int64, device=img.device)
     else:
-        _need_cuda(out, "out")
-        if out.dtype != torch.int64 or out.numel() != batch * nbins:
-            raise ValueError("out must be int64 with batch * nbins elements")
+        _check_out(out, img, torch.int64, batch * nbins)
     lib = load_library()
-    rc = lib.ecc_hard(img.data_ptr(), dt, ndim, _dims_array(dims), batch, int(nbins),
-                      float(vmin), float(vmax), out.data_ptr(), _stream_handle(stream))
+    with _on_device(img):
+        rc = lib.ecc_hard(img.data_ptr(), dt, ndim, _dims_array(dims), batch, int(nbins),
+                          float(vmin), float(vmax), out.data_ptr(), _stream_handle(stream))
     _check(rc, "ecc_hard")
     out = out.view(batch, nbins)
     return out if batched else out[0]
+
+
+def hard_launch_info(dims, batch: int, nbins: int, dtype=torch.float32, sm_count: int = 0):
+    """The launch shape ecc_hard takes for these sizes (ecc_hard_launch_info): a dict with
+    blocks_per_image, tasks_per_image, rows_per_task, rounds, direct and sms. ``sm_count`` 0
+    plans for the current device."""
+    dt = ECC_U8 if dtype == torch.uint8 else ECC_F32
+    info = (ctypes.c_int64 * 6)()
+    _check(load_library().ecc_hard_launch_info(dt, len(dims), _dims_array(dims), int(batch),
+                                               int(nbins), int(sm_count), info),
+           "ecc_hard_launch_info")
+    keys = ("blocks_per_image", "tasks_per_image", "rows_per_task", "rounds", "direct", "sms")
+    return dict(zip(keys, (int(v) for v in info)))
 
 
 def hard_stream_buffer_bytes(dims, dtype, slab_planes: int) -> int:
@@ -197,6 +232,10 @@ def ecc_hard_stream(img: torch.Tensor, nbins: int, vmin: float, vmax: float,
         raise ValueError(f"buf must be a CUDA tensor of at least {need} bytes")
     if out is None:
         out = torch.empty(nbins, dtype=torch.int64, device=dev)
+    elif (not out.is_cuda or not out.is_contiguous() or out.dtype != torch.int64
+          or out.numel() != nbins or out.device != buf.device):
+        raise ValueError(f"out must be a contiguous int64 CUDA tensor of {nbins} elements on "
+                         f"{buf.device}")
     with torch.cuda.device(dev):
         rc = load_library().ecc_hard_stream(ctypes.c_void_p(img.data_ptr()), dt,
                                             _dims_array(dims), int(nbins), float(vmin),
@@ -247,12 +286,15 @@ def ecc_soft_fwd(img, tau, lam: float, alpha, u, ws=None, out=None, ndim=None, s
     ws = _workspace(ws, dims, batch, K, img.device)
     if out is None:
         out = torch.empty((batch, K), dtype=torch.float32, device=img.device)
+    else:
+        _check_out(out, img, torch.float32, batch * K)
     lib = load_library()
-    rc = lib.ecc_soft_fwd(ctypes.c_void_p(img.data_ptr()), ndim, _dims_array(dims), batch,
-                          ctypes.c_void_p(tau.data_ptr()), K, float(lam),
-                          ctypes.c_void_p(alpha.data_ptr()), ctypes.c_void_p(u.data_ptr()),
-                          ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(ws.data_ptr()),
-                          ws.numel(), _stream_handle(stream))
+    with _on_device(img):
+        rc = lib.ecc_soft_fwd(ctypes.c_void_p(img.data_ptr()), ndim, _dims_array(dims), batch,
+                              ctypes.c_void_p(tau.data_ptr()), K, float(lam),
+                              ctypes.c_void_p(alpha.data_ptr()), ctypes.c_void_p(u.data_ptr()),
+                              ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(ws.data_ptr()),
+                              ws.numel(), _stream_handle(stream))
     _check(rc, "ecc_soft_fwd")
     out = out.view(batch, K)
     return (out if batched else out[0]), ws
@@ -266,9 +308,11 @@ def ecc_soft_stats(img, K: int, ws, ndim=None, stream=None) -> torch.Tensor:
     _need_cuda(ws, "ws")
     ndim, batch, dims, _ = _split(img, 2 if ndim is None and img.dim() != 4 else ndim)
     stats = torch.empty(3, dtype=torch.int64, device=img.device)
-    rc = load_library().ecc_soft_stats(ndim, _dims_array(dims), batch, int(K),
-                                       ctypes.c_void_p(ws.data_ptr()), ws.numel(),
-                                       ctypes.c_void_p(stats.data_ptr()), _stream_handle(stream))
+    with _on_device(img):
+        rc = load_library().ecc_soft_stats(ndim, _dims_array(dims), batch, int(K),
+                                           ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+                                           ctypes.c_void_p(stats.data_ptr()),
+                                           _stream_handle(stream))
     _check(rc, "ecc_soft_stats")
     return stats
 
@@ -282,12 +326,15 @@ def ecc_soft_fwd_noalloc(img, tau, lam: float, alpha, u, out=None, ndim=None, st
     K = tau.numel()
     if out is None:
         out = torch.empty((batch, K), dtype=torch.float32, device=img.device)
+    else:
+        _check_out(out, img, torch.float32, batch * K)
     lib = load_library()
-    rc = lib.ecc_soft_fwd_noalloc(ctypes.c_void_p(img.data_ptr()), ndim, _dims_array(dims),
-                                  batch, ctypes.c_void_p(tau.data_ptr()), K, float(lam),
-                                  ctypes.c_void_p(alpha.data_ptr()),
-                                  ctypes.c_void_p(u.data_ptr()), ctypes.c_void_p(out.data_ptr()),
-                                  _stream_handle(stream))
+    with _on_device(img):
+        rc = lib.ecc_soft_fwd_noalloc(ctypes.c_void_p(img.data_ptr()), ndim, _dims_array(dims),
+                                      batch, ctypes.c_void_p(tau.data_ptr()), K, float(lam),
+                                      ctypes.c_void_p(alpha.data_ptr()),
+                                      ctypes.c_void_p(u.data_ptr()),
+                                      ctypes.c_void_p(out.data_ptr()), _stream_handle(stream))
     _check(rc, "ecc_soft_fwd_noalloc")
     out = out.view(batch, K)
     return out if batched else out[0]
@@ -309,13 +356,15 @@ def ecc_soft_bwd(img, tau, lam: float, alpha, u, grad_out, ws, want_img: bool = 
     gu = torch.empty(ndim, dtype=torch.float32, device=dev)
     gi = torch.empty_like(img) if want_img else None
     lib = load_library()
-    rc = lib.ecc_soft_bwd(ctypes.c_void_p(img.data_ptr()), ndim, _dims_array(dims), batch,
-                          ctypes.c_void_p(tau.data_ptr()), K, float(lam),
-                          ctypes.c_void_p(alpha.data_ptr()), ctypes.c_void_p(u.data_ptr()),
-                          ctypes.c_void_p(grad_out.data_ptr()), ctypes.c_void_p(gt.data_ptr()),
-                          ctypes.c_void_p(ga.data_ptr()), ctypes.c_void_p(gu.data_ptr()),
-                          ctypes.c_void_p(gi.data_ptr() if gi is not None else None),
-                          ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream_handle(stream))
+    with _on_device(img):
+        rc = lib.ecc_soft_bwd(ctypes.c_void_p(img.data_ptr()), ndim, _dims_array(dims), batch,
+                              ctypes.c_void_p(tau.data_ptr()), K, float(lam),
+                              ctypes.c_void_p(alpha.data_ptr()), ctypes.c_void_p(u.data_ptr()),
+                              ctypes.c_void_p(grad_out.data_ptr()),
+                              ctypes.c_void_p(gt.data_ptr()), ctypes.c_void_p(ga.data_ptr()),
+                              ctypes.c_void_p(gu.data_ptr()),
+                              ctypes.c_void_p(gi.data_ptr() if gi is not None else None),
+                              ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream_handle(stream))
     _check(rc, "ecc_soft_bwd")
     res = {"grad_tau": gt, "grad_alpha": ga, "grad_u": gu}
     if want_img:
@@ -353,12 +402,17 @@ def ecc_soft_ect_fwd(img, tau, lam: float, alpha, U, ws=None, out=None, ndim=Non
     ws = _workspace(ws, dims, batch, K, img.device, nd)
     if out is None:
         out = torch.empty((batch, nd, K), dtype=torch.float32, device=img.device)
+    else:
+        _check_out(out, img, torch.float32, batch * nd * K)
     lib = load_library()
-    rc = lib.ecc_soft_ect_fwd(ctypes.c_void_p(img.data_ptr()), ndim, _dims_array(dims), batch,
-                              ctypes.c_void_p(tau.data_ptr()), K, float(lam),
-                              ctypes.c_void_p(alpha.data_ptr()), ctypes.c_void_p(U.data_ptr()),
-                              nd, ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(ws.data_ptr()),
-                              ws.numel(), _stream_handle(stream))
+    with _on_device(img):
+        rc = lib.ecc_soft_ect_fwd(ctypes.c_void_p(img.data_ptr()), ndim, _dims_array(dims),
+                                  batch, ctypes.c_void_p(tau.data_ptr()), K, float(lam),
+                                  ctypes.c_void_p(alpha.data_ptr()),
+                                  ctypes.c_void_p(U.data_ptr()), nd,
+                                  ctypes.c_void_p(out.data_ptr()),
+                                  ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+                                  _stream_handle(stream))
     _check(rc, "ecc_soft_ect_fwd")
     out = out.view(batch, nd, K)
     return (out if batched else out[0]), ws
@@ -380,14 +434,17 @@ def ecc_soft_ect_bwd(img, tau, lam: float, alpha, U, grad_out, ws, want_img: boo
     gu = torch.empty((nd, ndim), dtype=torch.float32, device=dev)
     gi = torch.empty_like(img) if want_img else None
     lib = load_library()
-    rc = lib.ecc_soft_ect_bwd(ctypes.c_void_p(img.data_ptr()), ndim, _dims_array(dims), batch,
-                              ctypes.c_void_p(tau.data_ptr()), K, float(lam),
-                              ctypes.c_void_p(alpha.data_ptr()), ctypes.c_void_p(U.data_ptr()),
-                              nd, ctypes.c_void_p(grad_out.data_ptr()),
-                              ctypes.c_void_p(gt.data_ptr()), ctypes.c_void_p(ga.data_ptr()),
-                              ctypes.c_void_p(gu.data_ptr()),
-                              ctypes.c_void_p(gi.data_ptr() if gi is not None else None),
-                              ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream_handle(stream))
+    with _on_device(img):
+        rc = lib.ecc_soft_ect_bwd(ctypes.c_void_p(img.data_ptr()), ndim, _dims_array(dims),
+                                  batch, ctypes.c_void_p(tau.data_ptr()), K, float(lam),
+                                  ctypes.c_void_p(alpha.data_ptr()),
+                                  ctypes.c_void_p(U.data_ptr()), nd,
+                                  ctypes.c_void_p(grad_out.data_ptr()),
+                                  ctypes.c_void_p(gt.data_ptr()), ctypes.c_void_p(ga.data_ptr()),
+                                  ctypes.c_void_p(gu.data_ptr()),
+                                  ctypes.c_void_p(gi.data_ptr() if gi is not None else None),
+                                  ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+                                  _stream_handle(stream))
     _check(rc, "ecc_soft_ect_bwd")
     res = {"grad_tau": gt, "grad_alpha": ga, "grad_u": gu}
     if want_img:
@@ -401,10 +458,11 @@ def ecc_soft_ect_stats(img, K: int, ndirs: int, ws, ndim=None, stream=None) -> t
     _need_cuda(ws, "ws")
     ndim, batch, dims, _ = _split(img, 2 if ndim is None and img.dim() != 4 else ndim)
     stats = torch.empty(3, dtype=torch.int64, device=img.device)
-    rc = load_library().ecc_soft_ect_stats(ndim, _dims_array(dims), batch, int(K), int(ndirs),
-                                           ctypes.c_void_p(ws.data_ptr()), ws.numel(),
-                                           ctypes.c_void_p(stats.data_ptr()),
-                                           _stream_handle(stream))
+    with _on_device(img):
+        rc = load_library().ecc_soft_ect_stats(ndim, _dims_array(dims), batch, int(K),
+                                               int(ndirs), ctypes.c_void_p(ws.data_ptr()),
+                                               ws.numel(), ctypes.c_void_p(stats.data_ptr()),
+                                               _stream_handle(stream))
     _check(rc, "ecc_soft_ect_stats")
     return stats
 

@@ -56,6 +56,7 @@ enum ecc_status {
 };
 
 #define ECC_MAX_NBINS 4096 /* largest nbins accepted by ecc_hard */
+#define ECC_MAX_EXTENT (1 << 30) /* largest extent of any one axis (ECC_ERANGE above) */
 #define ECC_MAX_K 8192     /* largest number of soft thresholds */
 #define ECC_MAX_DIRS 4096  /* largest number of directions of the soft transform */
 
@@ -76,8 +77,9 @@ enum ecc_status {
  *         values above vmax never enter; values below vmin enter at t_0.
  * dtype   ECC_U8 or ECC_F32.
  * ndim    2 ([H][W] per image) or 3 ([D][H][W] per image).
- * dims    host array of ndim extents, each >= 1, slowest first.
- * batch   number of independent images (>= 1); no cell joins two images.
+ * dims    host array of ndim extents, each >= 1, slowest first; an extent above ECC_MAX_EXTENT
+ *         returns ECC_ERANGE (the kernels index rows and columns with 32-bit integers).
+ * batch   number of independent images (>= 1, at most 65535); no cell joins two images.
  * nbins   number of thresholds, 1 <= nbins <= ECC_MAX_NBINS.
  * vmin, vmax  finite, vmin <= vmax.
  * out     device pointer to batch * nbins int64; fully overwritten.
@@ -85,6 +87,25 @@ enum ecc_status {
  */
 int ecc_hard(const void *img, int dtype, int ndim, const int64_t *dims, int64_t batch, int nbins,
              double vmin, double vmax, int64_t *out, ecc_stream_t stream);
+
+/*
+ * Launch shape that ecc_hard takes for these sizes -- a diagnostic with no counterpart in the paper
+ * notes, for tests and tuning. It validates the shape arguments as ecc_hard does (same status
+ * codes) and launches nothing.
+ *
+ * sm_count  SMs of the device to plan for; <= 0 means the current device's.
+ * info      host array of 6 int64, written on success:
+ *   info[0] blocks per image
+ *   info[1] work items per image: 2-D, (128-column strip, row range) bands, one per warp;
+ *           3-D, (tile of 128 x 32 columns x rows, chunk of planes) tasks
+ *   info[2] 2-D: row ranges per strip; 3-D: planes per chunk
+ *   info[3] 3-D: rounds, the most tasks one block walks (block g takes tasks g, g + G, ...);
+ *           2-D: 1
+ *   info[4] 1 when a 2-D image's only block stores the running sum itself, else 0
+ *   info[5] the SM count planned for
+ */
+int ecc_hard_launch_info(int dtype, int ndim, const int64_t *dims, int64_t batch, int nbins,
+                         int sm_count, int64_t *info);
 
 /*
  * Hard ECC of one 3-D volume read in slabs of planes from memory the device need not hold
@@ -151,8 +172,9 @@ int ecc_soft_fwd(const float *img, int ndim, const int64_t *dims, int64_t batch,
 /*
  * Soft ECC, backward: analytic gradients of L = sum_{b,k} grad_out[b,k] * out[b,k].
  *
- * Section "Key designs -- differentiable ECC layer (sigmoid relaxation)" ("a custom CUDA backward
- * kernel computes analytic gradients") of the ECC paper notes. With s = sigma(lambda (tau_k - X))
+ * Section "Key designs -- differentiable ECC layer (sigmoid relaxation)" of the ECC paper notes:
+ * the gradients below are evaluated in closed form by the library's own kernels. With
+ * s = sigma(lambda (tau_k - X))
  * evaluated at each cell's argmax vertex o (ties: the larger linear index owns the cell):
  *   grad_tau[k]   = sum_{b, cells} grad_out[b,k] (-1)^dim lambda s (1 - s)
  *   dX[b, o]      = - sum_{k, cells owned by o} grad_out[b,k] (-1)^dim lambda s (1 - s)
@@ -236,12 +258,15 @@ int ecc_soft_stats(int ndim, const int64_t *dims, int64_t batch, int K, const vo
  * ECC_NOALLOC_SCRATCH_BYTES bytes, which every GPU that loads the library holds until the process
  * exits. The call allocates nothing (no cudaMalloc / cudaFree, no allocating library routine).
  *
- * Sizes whose workspace (ecc_soft_workspace_bytes) exceeds ECC_NOALLOC_SCRATCH_BYTES are rejected
- * with ECC_ERANGE before anything runs. The first call on each device looks up that device's
- * array address (cudaGetSymbolAddress) with the device current; make that first call before any
+ * The array serves as the forward pass's workspace: the part of ecc_soft_workspace_bytes() that
+ * the forward pass uses (all of it except the backward-only scalar partials) must fit in
+ * ECC_NOALLOC_SCRATCH_BYTES; larger sizes are rejected with ECC_ERANGE before anything runs. At
+ * K = 128, up to 15 images of 256 x 256 fit (16 need about 16.5 MiB). Each call looks up the
+ * current device's array address (cudaGetSymbolAddress) with that device current; the first call
+ * on a device may also load the library's device code there, so make that first call before any
  * stream capture. All calls on a device share one array, which keeps the last call's contents
- * (each call overwrites whatever it reads): calls whose executions overlap on the GPU race and
- * must be serialised by the caller, e.g. by issuing them on one stream.
+ * (each call overwrites whatever it reads before reading it): calls whose executions overlap on
+ * the GPU race and must be serialised by the caller, e.g. by issuing them on one stream.
  */
 #define ECC_NOALLOC_SCRATCH_BYTES (16u << 20)
 int ecc_soft_fwd_noalloc(const float *img, int ndim, const int64_t *dims, int64_t batch,

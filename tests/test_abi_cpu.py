@@ -69,6 +69,38 @@ def test_hard_validation(lib):
     assert h(FAKE, 1, 2, dims(1 << 40, 1 << 30), 1, 4, 0.0, 1.0, FAKE, None) == ERANGE
 
 
+MAX_EXTENT = 1 << 30  # ECC_MAX_EXTENT
+
+
+def test_extents_the_kernels_cannot_index_are_rejected(lib):
+    """Every axis is limited to ECC_MAX_EXTENT: the kernels index rows, columns and strips with
+    32-bit integers, so a longer axis returns ECC_ERANGE before any launch instead of wrapping.
+    The pointers are fakes that are never dereferenced."""
+    h = lib.ecc_hard
+    for dt in (0, 1):
+        assert h(FAKE, dt, 2, dims(1, 3 * 10**9), 1, 4, 0.0, 1.0, FAKE, None) == ERANGE
+        assert h(FAKE, dt, 2, dims(3 * 10**9, 1), 1, 4, 0.0, 1.0, FAKE, None) == ERANGE
+        assert h(FAKE, dt, 2, dims(1, MAX_EXTENT + 1), 1, 4, 0.0, 1.0, FAKE, None) == ERANGE
+        assert h(FAKE, dt, 3, dims(1, 1, 3 * 10**9), 1, 4, 0.0, 1.0, FAKE, None) == ERANGE
+        assert h(FAKE, dt, 3, dims(3 * 10**9, 1, 1), 1, 4, 0.0, 1.0, FAKE, None) == ERANGE
+        assert h(FAKE, dt, 3, dims(1, MAX_EXTENT + 1, 1), 1, 4, 0.0, 1.0, FAKE, None) == ERANGE
+        # 2-D: one warp per (128-column strip, row range), at most 2^31 of them
+        assert h(FAKE, dt, 2, dims(MAX_EXTENT, 300), 1, 4, 0.0, 1.0, FAKE, None) == ERANGE
+    bb = lib.ecc_hard_stream_buffer_bytes
+    assert bb(1, dims(4, 1, 3 * 10**9), 2) == 0
+    assert bb(1, dims(4, MAX_EXTENT + 1, 1), 2) == 0
+    st = lib.ecc_hard_stream
+    buf = ctypes.c_void_p(0x100000)
+    assert st(FAKE, 1, dims(4, 1, 3 * 10**9), 8, 0.0, 1.0, 2, buf, 1 << 40, FAKE, None) == ERANGE
+    w = lib.ecc_soft_workspace_bytes
+    assert w(2, dims(1, MAX_EXTENT + 1), 1, 4) == 0
+    assert w(3, dims(MAX_EXTENT + 1, 1, 1), 1, 4) == 0
+    f = lib.ecc_soft_fwd
+    ws = ctypes.c_void_p(0x100000)
+    assert f(FAKE, 2, dims(1, 3 * 10**9), 1, FAKE, 8, 50.0, FAKE, FAKE, FAKE, ws, 1 << 40,
+             None) == ERANGE
+
+
 def test_soft_workspace_size(lib):
     w = lib.ecc_soft_workspace_bytes
     assert w(2, dims(256, 256), 64, 128) > 64 * 256 * 256 * 16

@@ -5,9 +5,9 @@ Covers small shapes spanning several tiles with ragged tails, every special case
 (NaN, infinities, out-of-range values, ties, constant and checkerboard images, degenerate
 threshold ranges, misaligned buffers, nbins from 1 to the maximum), 2-D and 3-D, uint8 and
 float32, batches, and each benchmark workload at full size in the benchmark's launch
-configuration (the library derives the launch from the sizes). The 1024^3 volume is too large
-for the oracle; it is checked through inclusion-exclusion over slabs, a property of the Euler
-characteristic that holds at any size, with oracle-checked slabs.
+configuration (the library derives the launch from the sizes), 3-D launches whose blocks walk
+several tasks in turn included. The oracle computes the largest volumes on every host core
+(tests/_oracle_pool.py).
 """
 import numpy as np
 import pytest
@@ -15,6 +15,7 @@ import torch
 
 import oracle
 from euler_characteristic_curves_gb300 import ecc, synthetic
+from tests import _oracle_pool
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -247,24 +248,45 @@ def test_workload_512cube_u8():
     np.testing.assert_array_equal(got, want)
 
 
-def test_workload_1024cube_f32_inclusion_exclusion():
-    """chi(V) = sum chi(slab_i) - sum chi(plane shared by slab_i and slab_{i+1}); the full
-    volume runs in the benchmark's launch, the slabs and planes in their own launches, and two
-    slabs are also checked against the oracle."""
+def test_workload_1024cube_f32():
+    """The 1024^3 volume in the benchmark's launch -- 4096 tasks on the resident blocks, so every
+    block walks several tasks in turn -- against the oracle, bit for bit. The oracle curve comes
+    from slabs that share one plane, one oracle process per host core."""
     v = synthetic.grf((1024, 1024, 1024), seed=4, device=DEV)
-    full = ecc.ecc_hard(v.unsqueeze(0), 256, 0.0, 1.0)[0].cpu().numpy()
-    cuts = [0, 200, 511, 777, 1023]
-    total = np.zeros(256, np.int64)
-    for a, b in zip(cuts[:-1], cuts[1:]):
-        total += ecc.ecc_hard(v[a: b + 1].unsqueeze(0), 256, 0.0, 1.0)[0].cpu().numpy()
-    for c in cuts[1:-1]:
-        total -= ecc.ecc_hard(v[c], 256, 0.0, 1.0).cpu().numpy()
-    np.testing.assert_array_equal(full, total)
-    assert full[-1] == 1
-    for a in (0, 600):
-        slab = v[a: a + 6, 100:420, :].contiguous()
-        got = ecc.ecc_hard(slab.unsqueeze(0), 256, 0.0, 1.0)[0].cpu().numpy()
-        np.testing.assert_array_equal(got, oracle.ecc_hard(slab.cpu().numpy(), 256, 0.0, 1.0))
+    plan = ecc.hard_launch_info(tuple(v.shape), 1, 256)
+    assert plan["rounds"] > 1 and plan["tasks_per_image"] > plan["blocks_per_image"]
+    got = ecc.ecc_hard(v.unsqueeze(0), 256, 0.0, 1.0)[0].cpu().numpy()
+    want = _oracle_pool.hard_volume(v.cpu().numpy(), 256, 0.0, 1.0)
+    np.testing.assert_array_equal(got, want)
+    assert got[-1] == 1
+
+
+@pytest.mark.parametrize("depth,kind", [(64, "f32"), (32, "u8")])
+def test_3d_blocks_walking_several_tasks(depth, kind):
+    """depth x 1024^2 volumes give more (tile, chunk) tasks than resident blocks (64 x 1024^2:
+    three rounds on 152 SMs, 32 x 1024^2: two), so each block reuses its key ring, carried rows
+    and histogram from one task to the next; the curve must still match the oracle bit for bit."""
+    v = synthetic.grf((depth, 1024, 1024), seed=30 + depth, device=DEV)
+    if kind == "u8":
+        v, nbins, vmax = synthetic.quantise_u8(v), 256, 255.0
+    else:
+        nbins, vmax = 256, 1.0
+    plan = ecc.hard_launch_info(tuple(v.shape), 1, nbins, dtype=v.dtype)
+    assert plan["rounds"] > 1
+    got = ecc.ecc_hard(v.unsqueeze(0), nbins, 0.0, vmax)[0].cpu().numpy()
+    want = _oracle_pool.hard_volume(v.cpu().numpy(), nbins, 0.0, vmax)
+    np.testing.assert_array_equal(got, want)
+
+
+def test_3d_rounds_on_a_small_device_plan():
+    """The multi-round path on small volumes: a batch of volumes shares the resident blocks, so
+    each image gets few blocks and many tasks (checked with the planner), ragged tiles included."""
+    v = synthetic.grf((30, 40, 260), seed=33, batch=40)
+    plan = ecc.hard_launch_info(v.shape[1:], 40, 77)
+    assert plan["rounds"] > 1
+    check(v, 77, 0.0, 1.0, ndim=3)
+    q = synthetic.quantise_u8(v)
+    check(q, 256, 0.0, 255.0, ndim=3)
 
 
 def test_library_calls_replay_from_a_cuda_graph():

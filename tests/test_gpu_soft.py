@@ -13,6 +13,7 @@ import torch
 
 import oracle
 from euler_characteristic_curves_gb300 import ecc, synthetic
+from tests import _oracle_pool
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -33,6 +34,7 @@ def assert_close(got, want, what, extra=None):
     bad = err > tol
     assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} outside tolerance; worst "
                            f"err/tol = {np.max(err / tol):.3g}")
+    return float(np.max(err / tol))
 
 
 def run_both(img, tau, lam, alpha, u, g, want_img=True, sample=None):
@@ -151,25 +153,31 @@ def test_autograd_layer_matches_direct_calls():
 
 def test_workload_64x256sq_soft():
     """The benchmark workload at full size: 64 GRF images 256^2, K = 128 thresholds on [0, 1],
-    lambda = 50, alpha = 1, u ~ N(0, 0.1^2). The oracle checks S on sampled images; for the
-    backward pass the upstream gradient is non-zero on the sampled images only, so the oracle
-    reproduces every gradient from those images while the kernels run the full launch."""
+    lambda = 50, alpha = 1, u ~ N(0, 0.1^2), upstream dL/dS ~ N(0, 1) on every image. The oracle
+    runs on all 64 images (one process per host core) and every output is compared element by
+    element: S, grad_tau, grad_alpha, grad_u and grad_img. For grad_img the test also reports how
+    far inside its documented bound the kernels land (worst err/tol with and without the
+    cancellation term)."""
     img = synthetic.grf((256, 256), seed=6, batch=64)
     tau = synthetic.uniform_thresholds(128)
     u = synthetic.soft_direction(2, seed=7)
-    g_full = synthetic.upstream_grad((64, 128), seed=8)
-    sample = np.asarray([0, 17, 42, 63])
-    g = np.zeros_like(g_full)
-    g[sample] = g_full[sample]
-    s, res, ref_s, ref = run_both(img, tau, 50.0, 1.0, u, g, want_img=True, sample=sample)
-    assert_close(s[sample], ref_s, "S")
+    g = synthetic.upstream_grad((64, 128), seed=8)
+    a = np.asarray([1.0], np.float32)
+    s, ws = ecc.ecc_soft_fwd(dev(img), dev(tau), 50.0, dev(a), dev(u))
+    res = ecc.ecc_soft_bwd(dev(img), dev(tau), 50.0, dev(a), dev(u), dev(g), ws, want_img=True)
+    s = s.cpu().numpy()
+    res = {k: v.cpu().numpy() for k, v in res.items()}
+    ref_s, ref = _oracle_pool.soft_batch(img, tau, 50.0, 1.0, u, g, ndim=2, want_img=True)
+    assert_close(s, ref_s, "S")
     assert_close(res["grad_tau"], ref["grad_tau"], "grad_tau")
     assert_close(res["grad_alpha"][0], ref["grad_alpha"], "grad_alpha")
     assert_close(res["grad_u"], ref["grad_u"], "grad_u")
-    assert_close(res["grad_img"][sample], ref["grad_img"], "grad_img",
-                 extra=4e-6 * ref["grad_img_absterms"])
-    others = np.setdiff1d(np.arange(64), sample)
-    assert not np.any(res["grad_img"][others])
+    extra = 4e-6 * ref["grad_img_absterms"]
+    worst = assert_close(res["grad_img"], ref["grad_img"], "grad_img", extra=extra)
+    err = np.abs(res["grad_img"].astype(np.float64) - ref["grad_img"])
+    plain = np.max(err / (ATOL + RTOL * np.abs(ref["grad_img"])))
+    print(f"grad_img 64x256^2: worst err/tol {worst:.3g} (bound with the cancellation term), "
+          f"{plain:.3g} against 1e-6 + 1e-4 |ref| alone")
 
 
 # ---------------------------------------------------------------------------------------------

@@ -263,3 +263,17 @@ def test_nan_and_out_of_range_values():
     lo2[5, 5] = -5.0
     np.testing.assert_array_equal(oracle.ecc_hard(lo, 32, 0.0, 1.0),
                                   oracle.ecc_hard(lo2, 32, 0.0, 1.0))
+
+
+def test_pool_of_slabs_equals_the_whole_volume():
+    """The helper that spreads the oracle over the host's cores (slabs sharing one plane, one
+    process each) must give the whole volume's curve exactly, for several slab lengths."""
+    from tests import _oracle_pool
+
+    f = _rand_field((23, 9, 14), 40)
+    want = oracle.ecc_hard(f, 30, 0.0, 1.0)
+    for slab in (2, 3, 7, 30):
+        np.testing.assert_array_equal(_oracle_pool.hard_volume(f, 30, 0.0, 1.0, slab), want)
+    q = (f * 255).astype(np.uint8)
+    np.testing.assert_array_equal(_oracle_pool.hard_volume(q, 256, 0.0, 255.0),
+                                  oracle.ecc_hard(q, 256, 0.0, 255.0))

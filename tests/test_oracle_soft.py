@@ -268,3 +268,20 @@ def test_ect_gradients_match_finite_differences(shape):
         fd = (L(f_=fp.reshape(f.shape)) - L(f_=fm.reshape(f.shape))) / (float(fp[p]) - float(fm[p]))
         got = res["grad_img"].reshape(-1)[p]
         assert close(fd, got), (p, fd, got)
+
+
+def test_pool_of_images_equals_the_batch():
+    """The per-image pool helper gives the batch oracle's S and gradients."""
+    from tests import _oracle_pool
+
+    f = synthetic.grf((11, 15), 41, batch=3)
+    tau = np.linspace(0, 1, 9).astype(np.float32)
+    g = synthetic.upstream_grad((3, 9), 42)
+    u = np.asarray([0.1, -0.2], np.float32)
+    s, r = _oracle_pool.soft_batch(f, tau, 20.0, 1.0, u, g, ndim=2)
+    np.testing.assert_array_equal(s, oracle.ecc_soft_fwd(f, tau, 20.0, 1.0, u, ndim=2))
+    ref = oracle.ecc_soft_bwd(f, tau, 20.0, 1.0, u, g, ndim=2)
+    np.testing.assert_allclose(r["grad_tau"], ref["grad_tau"], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(r["grad_alpha"], ref["grad_alpha"], rtol=1e-12)
+    np.testing.assert_allclose(r["grad_u"], ref["grad_u"], rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(r["grad_img"], ref["grad_img"])
