@@ -104,11 +104,22 @@ const char *ecc_status_str(int status)
     case ECC_EWS: return "ECC_EWS: workspace missing or too small";
     case ECC_ECUDA: return "ECC_ECUDA: CUDA error";
     case ECC_ERANGE: return "ECC_ERANGE: size above the library maximum";
+    case ECC_ETIMEOUT: return "ECC_ETIMEOUT: a kernel gave up waiting for its own staged copy";
     default: return "ECC: unknown status";
     }
 }
 
-int ecc_version(void) { return 10000; }
+int ecc_version(void) { return 10100; }
+
+int ecc_device_status(int clear)
+{
+    int *word = nullptr;
+    if (wait_error_word(&word) != cudaSuccess) return ECC_ECUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, word, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return ECC_ECUDA;
+    if (clear && v != 0 && cudaMemset(word, 0, sizeof v) != cudaSuccess) return ECC_ECUDA;
+    return v != 0 ? ECC_ETIMEOUT : ECC_OK;
+}
 
 // Sizes of a hard-ECC call: the checks ecc_hard makes on its shape arguments, and the plan's
 // extents on success.
@@ -174,6 +185,9 @@ int ecc_hard_launch_info(int dtype, int ndim, const int64_t *dims, int64_t batch
     const int rc = hard_shape_check(dtype, ndim, dims, batch, nbins, pl);
     if (rc != ECC_OK) return rc;
     const int sms = sm_count > 0 ? sm_count : num_sms();
+    // float32: the thresholds of an ordinary range are estimated (a degenerate range searches)
+    pl.key_mode = dtype == ECC_U8 ? kKeyLut : kKeyEstimate;
+    pl.tma = tma3d_shape_ok(pl);
     const HardShape sh = plan_hard(pl, sms);
     info[0] = sh.blocks_per_image;
     info[1] = sh.tasks_per_image;

@@ -29,6 +29,7 @@
 // shared keys of planes z and z + 1 once per plane and reuses them down its rows, so the row
 // building, the max rows and the first-row flags are paid once per eight rows. The raw values of
 // the next plane are loaded into registers one plane ahead.
+#include <cuda.h>  // CUtensorMap and its enums (the encoder is fetched through the runtime)
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -870,6 +871,462 @@ __global__ void __launch_bounds__(k3Threads, ECC_3D_MIN_BLOCKS) ecc_hard3d_kerne
 }
 
 // ----------------------------------------------------------------------------------------------
+// 3-D kernel with TMA-staged planes (float32 volumes whose rows hold a multiple of 4 values on a
+// 16-byte-aligned base; tables of at most 256 bins; estimated keys)
+// ----------------------------------------------------------------------------------------------
+//
+// Same tiles, tasks, slice fold and shared key ring as ecc_hard3d_kernel, with three changes.
+//
+// * Staging. One thread copies each plane's tile plus its one-voxel halo (136 x 34 floats,
+//   columns x0 - 4 .. x0 + 131, rows y0 - 1 .. y0 + 32) into shared memory with one
+//   cp.async.bulk.tensor copy that completes on an mbarrier. The copy fills every position outside
+//   the volume (columns, rows and planes) with NaN, whose key is "never", so no thread computes a
+//   grid bound and no raw value waits in registers: four blocks fit per SM where
+//   ecc_hard3d_kernel fits three.
+// * Coded keys. A voxel's key k is carried as the fp16 value 1024 + 4k + (x & 1) + 2 (y & 1).
+//   Ordering voxels by (k, x & 1, y & 1, z) still refines the threshold order, and two vertices of
+//   one cell differ in x & 1 or y & 1 unless they are vertical neighbours, so every in-plane
+//   comparison is strict, [a earlier than p] = sat(p - a), with no p + 1 term; vertical
+//   neighbours break ties by z as before. The bin is (pattern - 0x6400) >> 2. "Never" is
+//   1024 + 4H + code, above every valid key (for H = 256 it rounds to 2048 or more, an even
+//   integer, so differences with it stay integers and the flags stay 0 or 1).
+// * Carried fold. up = [k_{z+1} < k_z] decides which of the two voxels of a pixel takes the
+//   vertical cells above it: voxel z takes up c2(M_z), voxel z + 1 takes (1 - up) c2(M_z). Each
+//   plane computes up once per voxel and carries q = -(1 - up) c2(M_z) to the next plane instead
+//   of the keys and M contributions of the plane below:
+//       1280 + c(p) = (1280 + c2(S_z; p)) - up c2(M_z) + q_{z-1}.
+//
+// Every mbarrier wait gives up after kWaitNs; the block then records the failure in the device
+// error word, waits (bounded again) for its copy in flight and leaves without flushing.
+// ecc_device_status() reports and clears the word.
+
+constexpr int kT3Blocks = 4;            // resident blocks per SM the TMA kernel is built for
+constexpr int kRawPitch = kKeyPitch;    // floats per staged row (columns x0 - 4 .. x0 + 131)
+constexpr int kRawRows = kKeyRowsHalo;  // rows y0 - 1 .. y0 + 32
+constexpr int kRawBytes = kRawPitch * kRawRows * 4;
+constexpr int kKeyRingBytes = 3 * kKeyPlane * 2;
+constexpr int kCodedMaxBins = 256;  // 1024 + 4 (H - 1) + 3 < 2048
+constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per mbarrier wait
+static_assert(kRawBytes % 16 == 0 && kKeyRingBytes % 16 == 0, "shared layout");
+static_assert(kStrip + 8 == kRawPitch, "a staged row starts 4 columns left of the tile");
+
+__device__ int g_wait_error;  // set by a block whose staged copy did not arrive in time
+
+struct Hard3TmaParams {
+    CUtensorMap map;  // [batch][D][Hy][W] float32; box 136 x 34 x 1 x 1; NaN outside
+    int64_t *out;
+    int64_t tasks_per_image;
+    int D, H, sign;
+    int rows_per_task, tasks_x, tasks_y, ctas_per_image;
+    float key_a, key_b, key_clo, key_chi;
+    float table[kCodedMaxBins + 2];
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits for the completion of the phase of parity `parity`; false if it has not come in kWaitNs.
+__device__ __noinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() - t0 > kWaitNs) return false;
+    return true;
+}
+
+// One thread: plane z of image b's tile at (x0, y0) into the staging buffer.
+__device__ __forceinline__ void stage_plane(const Hard3TmaParams &P, uint32_t raw_s, uint32_t bar,
+                                            int x0, int y0, int z, int b)
+{
+    // the block's earlier reads of the buffer (generic proxy) before the copy's writes
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                 "r"((uint32_t)kRawBytes)
+                 : "memory");
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(raw_s),
+        "l"(reinterpret_cast<uint64_t>(&P.map)), "r"(x0 - 4), "r"(y0 - 1), "r"(z), "r"(b),
+        "r"(bar)
+        : "memory");
+}
+
+// Packed fp32 pairs (sm_100-family f32x2 instructions; each element rounds as the scalar op does).
+__device__ __forceinline__ uint64_t pk(float a, float b)
+{
+    return (uint64_t)__float_as_uint(a) | ((uint64_t)__float_as_uint(b) << 32);
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add_rp(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rp.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t h2_fma(uint32_t a, uint32_t b, uint32_t c)
+{
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t h2_neg(uint32_t a)
+{
+    uint32_t d;
+    asm("neg.f16x2 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+
+// Estimated key patterns of two values (low halves 0x6400 + ceil(t - E), as key_fast); ORs into
+// `amb` a non-zero value when either estimate is ambiguous. The normalisation saturates value by
+// value; the rest runs on packed pairs.
+struct KeyPairConsts {
+    uint64_t nH, clo, chi, magic;
+};
+__device__ __forceinline__ void key_fast2(float v0, float v1, const KeyConsts &K,
+                                          const KeyPairConsts &K2, uint32_t &k0, uint32_t &k1,
+                                          uint32_t &amb)
+{
+    const uint64_t u = pk(__saturatef(fmaf(v0, K.a, K.b)), __saturatef(fmaf(v1, K.a, K.b)));
+    const uint64_t lo = f2_add_rp(f2_fma(u, K2.nH, K2.clo), K2.magic);
+    const uint64_t hi = f2_add_rp(f2_fma(u, K2.nH, K2.chi), K2.magic);
+    k0 = (uint32_t)lo;
+    k1 = (uint32_t)(lo >> 32);
+    amb |= (k0 ^ (uint32_t)hi) | (k1 ^ (uint32_t)(hi >> 32));
+}
+
+// Coding of a key pair: patterns 0x6400 + k -> 0x6400 + 4k + code, in each half at once. As a
+// 32-bit integer, 4 * pair + C with C = c0 + (c1 << 16) - 3 * 0x64006400 (mod 2^32) gives
+// (0x6400 + 4 k0 + c0) + (0x6400 + 4 k1 + c1) << 16: each half stays below 2^16 (at most 0x6803
+// for k = 256), so no carry crosses into the other half.
+__device__ __forceinline__ uint32_t code_pair_const(int yodd)
+{
+    // codes (x & 1) + 2 (y & 1) of the pair's two columns (the first column is even)
+    const uint32_t c0 = 2u * (uint32_t)yodd, c1 = c0 + 1u;
+    return c0 + (c1 << 16) - 3u * 0x64006400u;
+}
+__device__ __forceinline__ uint32_t code_pair(uint32_t pair, uint32_t C) { return 4u * pair + C; }
+
+// A halo item of the staged plane: its index (the same in the raw and the key buffers) and its
+// code. Items: rows y0 - 1 and y0 + 32 over columns x0 - 1 .. x0 + 128, then columns x0 - 1 and
+// x0 + 128 over the tile's rows.
+__device__ __forceinline__ void halo_item_coded(int i, int &off, uint32_t &code)
+{
+    int row, c;
+    if (i < 2 * kHaloRowItems) {
+        const int below = i >= kHaloRowItems;
+        c = i - below * kHaloRowItems - 1;  // -1 .. 128
+        row = below ? kKeyRowsHalo - 1 : 0;
+    } else {
+        const int j = i - 2 * kHaloRowItems;
+        const int right = j >= kTileRows;
+        row = 1 + j - right * kTileRows;
+        c = right ? kStrip : -1;
+    }
+    off = row * kKeyPitch + 4 + c;
+    // x0 and y0 are even: x & 1 = c & 1, and buffer row `row` is y = y0 - 1 + row
+    code = (uint32_t)(c & 1) + 2u * (uint32_t)((row + 1) & 1);
+}
+
+// Keys of the staged plane into the key buffer `dst` (coded patterns). Each thread takes its
+// warp's eight rows (four columns each) and its halo items; the rare exact fix-up revisits a
+// group of two rows (the halo items join the first).
+__device__ __forceinline__ void plane_keys_coded(const float *raw, uint16_t *dst,
+                                                 const KeyConsts &K, const KeyPairConsts &K2,
+                                                 const float *__restrict__ T, int r0, int lane,
+                                                 const int *h_off, const uint32_t *h_code)
+{
+    constexpr int kFixRows = 2, kGroups = k3Rows / kFixRows;
+    uint32_t amb[kGroups];
+#pragma unroll
+    for (int q = 0; q < kGroups; ++q) amb[q] = 0;
+    const int base = (1 + r0) * kKeyPitch + 4 + 4 * lane;
+#pragma unroll
+    for (int i = 0; i < k3Rows; ++i) {
+        const float4 v = *reinterpret_cast<const float4 *>(raw + base + i * kKeyPitch);
+        uint32_t k0, k1, k2, k3;
+        key_fast2(v.x, v.y, K, K2, k0, k1, amb[i / kFixRows]);
+        key_fast2(v.z, v.w, K, K2, k2, k3, amb[i / kFixRows]);
+        const uint32_t cc = code_pair_const(i & 1);
+        *reinterpret_cast<uint2 *>(dst + base + i * kKeyPitch) =
+            make_uint2(code_pair(prmt(k0, k1, 0x5410), cc), code_pair(prmt(k2, k3, 0x5410), cc));
+    }
+    uint32_t hk[kHaloSlots];
+#pragma unroll
+    for (int s = 0; s < kHaloSlots; ++s) {
+        hk[s] = 0;
+        if (s + 1 < kHaloSlots || h_off[s] >= 0) hk[s] = key_fast(raw[h_off[s]], K, amb[0]);
+    }
+    uint32_t any = 0;
+#pragma unroll
+    for (int q = 0; q < kGroups; ++q) any |= amb[q];
+    if (__any_sync(kFull, any != 0)) {  // rare: a value within E of a threshold
+#pragma unroll
+        for (int q = 0; q < kGroups; ++q) {
+            if (amb[q] != 0) {
+#pragma unroll
+                for (int i = q * kFixRows; i < (q + 1) * kFixRows; ++i) {
+                    const float4 v =
+                        *reinterpret_cast<const float4 *>(raw + base + i * kKeyPitch);
+                    uint32_t scratch = 0;
+                    const uint32_t k0 = key_fix(v.x, key_fast(v.x, K, scratch), K.H, T);
+                    const uint32_t k1 = key_fix(v.y, key_fast(v.y, K, scratch), K.H, T);
+                    const uint32_t k2 = key_fix(v.z, key_fast(v.z, K, scratch), K.H, T);
+                    const uint32_t k3 = key_fix(v.w, key_fast(v.w, K, scratch), K.H, T);
+                    const uint32_t cc = code_pair_const(i & 1);
+                    *reinterpret_cast<uint2 *>(dst + base + i * kKeyPitch) =
+                        make_uint2(code_pair(prmt(k0, k1, 0x5410), cc),
+                                   code_pair(prmt(k2, k3, 0x5410), cc));
+                }
+                if (q == 0) {
+#pragma unroll
+                    for (int s = 0; s < kHaloSlots; ++s)
+                        if (s + 1 < kHaloSlots || h_off[s] >= 0)
+                            hk[s] = key_fix(raw[h_off[s]], hk[s], K.H, T);
+                }
+            }
+        }
+    }
+    // a halo key: pattern 0x6400 + k -> 0x6400 + 4k + code (k = 256: 0x6800 + code, >= 2048)
+#pragma unroll
+    for (int s = 0; s < kHaloSlots; ++s)
+        if (s + 1 < kHaloSlots || h_off[s] >= 0)
+            dst[h_off[s]] = (uint16_t)(4u * (hk[s] & 0xffffu) - 3u * kKeyBase + h_code[s]);
+}
+
+// The local Euler contribution of a pixel pair on coded keys (every flag strict:
+// [a earlier than p] = sat(p - a)). NEG: return -c2 (plain); otherwise 1280 + c2.
+template <bool NEG>
+__device__ __forceinline__ uint32_t c2_pair_coded(uint32_t p, uint32_t L, uint32_t R, uint32_t aL,
+                                                  uint32_t aR, uint32_t d, uint32_t dL,
+                                                  uint32_t dR, uint32_t Sp, uint32_t &S_out)
+{
+    const uint32_t W = h2_sub_sat(p, L), E = h2_sub_sat(p, R), S = h2_sub_sat(p, d);
+    const uint32_t NW = h2_sub_sat(p, aL), NE = h2_sub_sat(p, aR);
+    const uint32_t SW = h2_sub_sat(p, dL), SE = h2_sub_sat(p, dR);
+    const uint32_t A = lop_or_and(Sp, E, NE);
+    const uint32_t B = E & ~(S & SE);
+    const uint32_t C = S & ~(W & SW);
+    const uint32_t D = W & (Sp | ~NW);
+    S_out = S;
+    if (NEG) return h2_sub(h2_add(C, D), h2_sub(A, B));
+    return h2_sub(h2_sub(h2_add(kBias, A), B), h2_add(C, D));
+}
+
+template <bool NEG>
+__device__ __forceinline__ void c2_quad_coded(const KeyRow &a, const KeyRow &b, const KeyRow &d,
+                                              uint32_t &Sp0, uint32_t &Sp1, uint32_t &c0,
+                                              uint32_t &c1)
+{
+    uint32_t S0, S1;
+    c0 = c2_pair_coded<NEG>(b.own0, b.L0, b.R0, a.L0, a.R0, d.own0, d.L0, d.R0, Sp0, S0);
+    c1 = c2_pair_coded<NEG>(b.own1, b.R0, b.R1, a.R0, a.R1, d.own1, d.R0, d.R1, Sp1, S1);
+    Sp0 = S0;
+    Sp1 = S1;
+}
+
+// Histogram update for a pair of coded keys: bin (pattern - 0x6400) >> 2, i.e. the byte offset
+// (pattern & 0xfffc) from hist_c = (shared address of the histogram) - 0x6400.
+__device__ __forceinline__ void hist_pair_coded(uint32_t keys, uint32_t cv, uint32_t hist_c)
+{
+    red_shared_add(hist_c + (keys & 0xfffcu), sext_byte0(cv));
+    red_shared_add(hist_c + ((keys >> 16) & 0xfffcu), sext_byte2(cv));
+}
+
+// One vertical fold step of a pair: returns 1280 + c and updates the carry q for the plane above.
+// cs_b = 1280 + c2(S_z), ncn = -c2(M_z), k / k_up: the keys of planes z and z + 1.
+__device__ __forceinline__ uint32_t fold_carry(uint32_t cs_b, uint32_t ncn, uint32_t k,
+                                               uint32_t k_up, uint32_t &q)
+{
+    const uint32_t up = h2_sub_sat(k, k_up);  // [k_{z+1} < k_z]
+    const uint32_t cv = h2_add(cs_b, h2_fma(up, ncn, q));
+    q = h2_fma(h2_neg(up), ncn, ncn);  // -(1 - up) c2(M_z)
+    return cv;
+}
+
+__global__ void __launch_bounds__(k3Threads, kT3Blocks)
+    ecc_hard3d_tma_kernel(const __grid_constant__ Hard3TmaParams P)
+{
+    extern __shared__ __align__(128) unsigned char smem_t3[];
+    // the staging buffer starts on a 128-byte boundary (the launch adds 128 bytes of slack)
+    unsigned char *base = smem_t3 + ((128u - (smem_u32(smem_t3) & 127u)) & 127u);
+    float *raw = reinterpret_cast<float *>(base);
+    uint16_t *kb = reinterpret_cast<uint16_t *>(base + kRawBytes);
+    int *hist = reinterpret_cast<int *>(base + kRawBytes + kKeyRingBytes);
+    float *table = reinterpret_cast<float *>(hist + hist_words(P.H));
+    __shared__ __align__(8) unsigned long long mbar;
+
+    const int tid = threadIdx.x, lane = tid & (kWarp - 1), warp = tid >> 5;
+    for (int i = tid; i <= P.H; i += k3Threads) hist[i] = 0;
+    for (int i = tid; i < P.H + 2; i += k3Threads) table[i] = P.table[i];
+    const uint32_t bar = smem_u32(&mbar), raw_s = smem_u32(raw);
+    if (tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    int h_off[kHaloSlots];
+    uint32_t h_code[kHaloSlots];
+#pragma unroll
+    for (int s = 0; s < kHaloSlots; ++s) {
+        const int i = tid + s * k3Threads;
+        h_off[s] = -1;
+        h_code[s] = 0;
+        if (i < kHaloItems) halo_item_coded(i, h_off[s], h_code[s]);
+    }
+    KeyConsts K;
+    K.a = P.key_a;
+    K.b = P.key_b;
+    K.nH = -(float)P.H;
+    K.clo = P.key_clo;
+    K.chi = P.key_chi;
+    K.H = P.H;
+    KeyPairConsts K2;
+    K2.nH = pk(K.nH, K.nH);
+    K2.clo = pk(K.clo, K.clo);
+    K2.chi = pk(K.chi, K.chi);
+    K2.magic = pk(kMagicKey, kMagicKey);
+    const int r0 = warp * k3Rows;  // buffer row of the row above the warp's first row
+    const int b = blockIdx.y;
+    const uint32_t hist_c = smem_u32(hist) - kKeyBase;
+    const int64_t Tn = P.tasks_per_image, G = P.ctas_per_image;
+    uint32_t phase = 0;  // parity of the next copy's completion
+    bool failed = false;
+
+    for (int64_t t = blockIdx.x; t < Tn && !failed; t += G) {
+        const int tx = (int)(t % P.tasks_x);
+        const int64_t rest = t / P.tasks_x;
+        const int ty = (int)(rest % P.tasks_y);
+        const int z0 = (int)(rest / P.tasks_y) * P.rows_per_task;
+        const int z1 = min(z0 + P.rows_per_task, P.D);
+        const int x0 = tx * kStrip, y0 = ty * kTileRows;
+
+        // prologue: keys of planes z0 - 1 (buffer 0) and z0 (buffer 1); plane z0 + 1 in flight
+        __syncthreads();  // the previous task's readers are done with every buffer
+        for (int j = 0; j < 2; ++j) {
+            if (tid == 0) stage_plane(P, raw_s, bar, x0, y0, z0 - 1 + j, b);
+            const bool late = !mbar_wait_bounded(bar, phase);
+            phase ^= 1;
+            plane_keys_coded(raw, kb + j * kKeyPlane, K, K2, table, r0, lane, h_off, h_code);
+            if (__syncthreads_or(late)) {  // block-uniform
+                failed = true;
+                break;
+            }
+        }
+        if (failed) break;
+        if (tid == 0) stage_plane(P, raw_s, bar, x0, y0, z0 + 1, b);
+
+        // q: -(1 - up) c2(M_{z0-1}) at the warp's pixels, up = [k_{z0} < k_{z0-1}]
+        uint32_t q[k3Rows][2];
+        {
+            const uint16_t *bp = kb, *bq = kb + kKeyPlane;
+            KeyRow pb = smem_key_row(bp, r0 + 1, lane), cb = smem_key_row(bq, r0 + 1, lane);
+            KeyRow Ma = max_rows(smem_key_row(bp, r0, lane), smem_key_row(bq, r0, lane));
+            KeyRow Mb = max_rows(pb, cb);
+            uint32_t s0, s1;
+            sp_init<true>(Ma, Mb, s0, s1);
+#pragma unroll
+            for (int i = 0; i < k3Rows; ++i) {
+                const KeyRow pd = smem_key_row(bp, r0 + i + 2, lane);
+                const KeyRow cd = smem_key_row(bq, r0 + i + 2, lane);
+                const KeyRow Md = max_rows(pd, cd);
+                uint32_t n0, n1;
+                c2_quad_coded<true>(Ma, Mb, Md, s0, s1, n0, n1);
+                q[i][0] = h2_fma(h2_neg(h2_sub_sat(pb.own0, cb.own0)), n0, n0);
+                q[i][1] = h2_fma(h2_neg(h2_sub_sat(pb.own1, cb.own1)), n1, n1);
+                pb = pd;
+                cb = cd;
+                Ma = Mb;
+                Mb = Md;
+            }
+        }
+
+        // Three key buffers in a ring: at step z plane z + 1 goes to the buffer of plane z - 1,
+        // read last at step z - 1, before that step's barrier.
+        const uint16_t *bc = kb + kKeyPlane;
+        uint16_t *bn = kb + 2 * kKeyPlane, *bo = kb;
+        for (int z = z0; z < z1; ++z) {
+            const bool late = !mbar_wait_bounded(bar, phase);
+            phase ^= 1;
+            plane_keys_coded(raw, bn, K, K2, table, r0, lane, h_off, h_code);
+            if (__syncthreads_or(late)) {  // block-uniform
+                failed = true;
+                break;
+            }
+            if (tid == 0 && z + 2 <= z1) stage_plane(P, raw_s, bar, x0, y0, z + 2, b);
+            KeyRow c0 = smem_key_row(bc, r0, lane), c1 = smem_key_row(bc, r0 + 1, lane);
+            KeyRow n1 = smem_key_row(bn, r0 + 1, lane);
+            KeyRow Ma = max_rows(c0, smem_key_row(bn, r0, lane)), Mb = max_rows(c1, n1);
+            uint32_t ss0, ss1, sm0, sm1;
+            sp_init<true>(c0, c1, ss0, ss1);
+            sp_init<true>(Ma, Mb, sm0, sm1);
+#pragma unroll
+            for (int i = 0; i < k3Rows; ++i) {
+                const KeyRow c2 = smem_key_row(bc, r0 + i + 2, lane);
+                const KeyRow n2 = smem_key_row(bn, r0 + i + 2, lane);
+                uint32_t cs0, cs1, nc0, nc1;
+                c2_quad_coded<false>(c0, c1, c2, ss0, ss1, cs0, cs1);
+                const KeyRow Md = max_rows(c2, n2);
+                c2_quad_coded<true>(Ma, Mb, Md, sm0, sm1, nc0, nc1);
+                hist_pair_coded(c1.own0, fold_carry(cs0, nc0, c1.own0, n1.own0, q[i][0]),
+                                hist_c);
+                hist_pair_coded(c1.own1, fold_carry(cs1, nc1, c1.own1, n1.own1, q[i][1]),
+                                hist_c);
+                c0 = c1;
+                c1 = c2;
+                n1 = n2;
+                Ma = Mb;
+                Mb = Md;
+            }
+            const uint16_t *tmp = bc;
+            bc = bn;
+            bn = bo;
+            bo = const_cast<uint16_t *>(tmp);
+        }
+    }
+    if (failed) {  // block-uniform: a copy did not arrive in time
+        if (tid == 0) {
+            mbar_wait_bounded(bar, phase ^ 1u);  // the copy that timed out, if it still lands
+            atomicOr(&g_wait_error, 1);
+        }
+        return;
+    }
+    __syncthreads();
+    unsigned long long *dst = reinterpret_cast<unsigned long long *>(P.out + b * (int64_t)P.H);
+    for (int i = tid; i < P.H; i += k3Threads) {
+        const int v = hist[i];
+        if (v != 0) atomicAdd(dst + i, (unsigned long long)(long long)(P.sign * v));
+    }
+}
+
+// ----------------------------------------------------------------------------------------------
 // Running sum over bins: out[b][k] = sum_{j <= k} hist[b][j]  (one block per image)
 // ----------------------------------------------------------------------------------------------
 constexpr int kScanThreads = 1024;
@@ -954,7 +1411,7 @@ HardShape plan_hard(const HardPlan &pl, int sms)
 {
     HardShape sh;
     const int64_t strips = (pl.W + kStrip - 1) / kStrip;
-    const int per_sm = pl.ndim == 2 ? ECC_2D_MIN_BLOCKS : ECC_3D_MIN_BLOCKS;
+    const int per_sm = pl.ndim == 2 ? ECC_2D_MIN_BLOCKS : (pl.tma ? kT3Blocks : ECC_3D_MIN_BLOCKS);
     const int64_t resident = (int64_t)sms * per_sm;  // blocks that fit at once
     // blocks per image: the resident blocks shared out over the batch, rounded down so that the
     // whole grid is one wave (rounding up left a few blocks to run alone in a second wave)
@@ -1056,6 +1513,93 @@ static cudaError_t launch_hard(const HardPlan &pl, cudaStream_t s)
     return hard_scan(pl.out, pl.H, pl.batch, s);
 }
 
+// The tensor-map encoder of the driver, fetched through the runtime (no link against libcuda).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_tiled()
+{
+    static const EncodeTiledFn fn = []() -> EncodeTiledFn {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+bool tma3d_shape_ok(const HardPlan &pl)
+{
+    // float32 volumes with rows of a multiple of 4 values (16-byte row strides), estimated keys,
+    // at most 256 bins; every tensor-map stride below 2^40 bytes
+    return pl.ndim == 3 && pl.dtype == ECC_F32 && pl.key_mode == kKeyEstimate &&
+           pl.H <= kCodedMaxBins && pl.W % 4 == 0 &&
+           (double)pl.D * (double)pl.Hy * (double)pl.W * 4.0 < (double)((int64_t)1 << 40);
+}
+
+// 3-D hard ECC through ecc_hard3d_tma_kernel; cudaErrorNotSupported when the tensor map cannot be
+// built (the caller then takes ecc_hard3d_kernel).
+static cudaError_t launch_hard3d_tma(const HardPlan &pl, cudaStream_t s)
+{
+    const EncodeTiledFn encode = encode_tiled();
+    if (!encode) return cudaErrorNotSupported;
+    Hard3TmaParams P;
+    const cuuint64_t gdim[4] = {(cuuint64_t)pl.W, (cuuint64_t)pl.Hy, (cuuint64_t)pl.D,
+                                (cuuint64_t)pl.batch};
+    const cuuint64_t gstride[3] = {(cuuint64_t)pl.W * 4, (cuuint64_t)(pl.Hy * pl.W) * 4,
+                                   (cuuint64_t)(pl.D * pl.Hy * pl.W) * 4};
+    const cuuint32_t box[4] = {(cuuint32_t)kRawPitch, (cuuint32_t)kRawRows, 1, 1};
+    const cuuint32_t estride[4] = {1, 1, 1, 1};
+    if (encode(&P.map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void *>(pl.img), gdim,
+               gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NAN_REQUEST_ZERO_FMA) != CUDA_SUCCESS)
+        return cudaErrorNotSupported;
+    HardPlan tp = pl;
+    tp.tma = true;
+    const HardShape sh = plan_hard(tp, num_sms());
+    P.out = pl.out;
+    P.tasks_per_image = sh.tasks_per_image;
+    P.D = (int)pl.D;
+    P.H = pl.H;
+    P.sign = pl.sign;
+    P.rows_per_task = (int)sh.rows_per_task;
+    P.tasks_x = (int)sh.tasks_x;
+    P.tasks_y = (int)sh.tasks_y;
+    P.ctas_per_image = (int)sh.blocks_per_image;
+    P.key_a = pl.key_a;
+    P.key_b = pl.key_b;
+    P.key_clo = pl.key_clo;
+    P.key_chi = pl.key_chi;
+    for (int i = 0; i < pl.H + 2; ++i) P.table[i] = pl.table[i];
+    for (int i = pl.H + 2; i < kCodedMaxBins + 2; ++i) P.table[i] = 0.0f;
+    if (pl.zero_out) {
+        const cudaError_t m =
+            cudaMemsetAsync(pl.out, 0, sizeof(int64_t) * (size_t)(pl.batch * pl.H), s);
+        if (m != cudaSuccess) return m;
+    }
+    const size_t smem = 128 + (size_t)kRawBytes + kKeyRingBytes +
+                        (size_t)hist_words(pl.H) * 4 + (size_t)(pl.H + 2) * 4;
+    const cudaError_t a = cudaFuncSetAttribute(
+        ecc_hard3d_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (a != cudaSuccess) return a;
+    const dim3 grid((unsigned)sh.blocks_per_image, (unsigned)pl.batch);
+    ecc_hard3d_tma_kernel<<<grid, k3Threads, smem, s>>>(P);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || !pl.scan) return e;
+    return hard_scan(pl.out, pl.H, pl.batch, s);
+}
+
+cudaError_t wait_error_word(int **p)
+{
+    return cudaGetSymbolAddress(reinterpret_cast<void **>(p), g_wait_error);
+}
+
 cudaError_t hard_scan(int64_t *out, int H, int64_t batch, cudaStream_t s)
 {
     ecc_bin_scan_kernel<<<(unsigned)batch, kScanThreads, 0, s>>>(out, H);
@@ -1070,6 +1614,10 @@ cudaError_t hard_run(const HardPlan &pl, cudaStream_t s)
         return launch_hard<uint8_t, ECC_MAX_NBINS, false>(pl, s);
     }
     if (pl.key_mode == kKeySearch) return launch_hard<float, ECC_MAX_NBINS, true>(pl, s);
+    if (pl.vec_ok && tma3d_shape_ok(pl)) {  // 16-byte-aligned rows: the TMA-staged kernel
+        const cudaError_t e = launch_hard3d_tma(pl, s);
+        if (e != cudaErrorNotSupported) return e;
+    }
     if (pl.H <= 256) return launch_hard<float, 256, false>(pl, s);
     if (pl.H <= 1024) return launch_hard<float, 1024, false>(pl, s);
     return launch_hard<float, ECC_MAX_NBINS, false>(pl, s);

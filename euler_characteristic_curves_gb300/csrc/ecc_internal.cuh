@@ -78,6 +78,7 @@ struct HardPlan {
     int sign = 1;        // -1: subtract the histogram from out
     bool scan = true;    // false: leave out as a histogram (the caller scans once at the end)
     bool zero_out = false;  // true: the launcher zeroes out first (when it needs zeroing)
+    bool tma = false;       // planned for the TMA-staged 3-D kernel (four blocks per SM)
 };
 // Launch shape of a hard-ECC call on a device of `sms` SMs (shared by the launcher and
 // ecc_hard_launch_info). 2-D: one warp per (strip, row range); 3-D: tasks (tile, chunk of planes)
@@ -92,6 +93,11 @@ struct HardShape {
 };
 HardShape plan_hard(const HardPlan &pl, int sms);
 int num_sms();  // of the current device (148 when the query fails)
+// Whether a 3-D call of these sizes and keys takes the TMA-staged kernel when its volume is
+// 16-byte aligned.
+bool tma3d_shape_ok(const HardPlan &pl);
+// Device address of the word a kernel sets when a bounded wait on its own copy gave up.
+cudaError_t wait_error_word(int **p);
 cudaError_t hard_run(const HardPlan &pl, cudaStream_t s);
 // out[b][k] = running sum over k of out[b][k], for batch rows of H bins
 cudaError_t hard_scan(int64_t *out, int H, int64_t batch, cudaStream_t s);

@@ -52,7 +52,8 @@ enum ecc_status {
     ECC_EDIM = -3,    /* ndim outside the supported set, or an extent < 1 */
     ECC_EWS = -4,     /* workspace NULL or smaller than ecc_soft_workspace_bytes() */
     ECC_ECUDA = -5,   /* a CUDA call failed (no device, launch failure...) */
-    ECC_ERANGE = -6   /* nbins or K above the library maximum, or a size that overflows */
+    ECC_ERANGE = -6,  /* nbins or K above the library maximum, or a size that overflows */
+    ECC_ETIMEOUT = -7 /* a kernel gave up waiting for its own staged copy (ecc_device_status) */
 };
 
 #define ECC_MAX_NBINS 4096 /* largest nbins accepted by ecc_hard */
@@ -272,6 +273,16 @@ int ecc_soft_stats(int ndim, const int64_t *dims, int64_t batch, int K, const vo
 int ecc_soft_fwd_noalloc(const float *img, int ndim, const int64_t *dims, int64_t batch,
                          const float *tau, int K, float lambda, const float *alpha,
                          const float *u, float *out, ecc_stream_t stream);
+
+/*
+ * Status of the current device's kernels -- a safety net with no counterpart in the paper notes.
+ * A kernel that stages data with asynchronous copies waits for each copy with a time limit
+ * (2 s); if the limit passes, the kernel sets a device error word, leaves its result incomplete
+ * and returns instead of hanging. This call synchronises with the device, reads that word, clears
+ * it when `clear` is non-zero, and returns ECC_ETIMEOUT if it was set, else ECC_OK (ECC_ECUDA
+ * when the device cannot be read).
+ */
+int ecc_device_status(int clear);
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *ecc_status_str(int status);

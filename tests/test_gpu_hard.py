@@ -261,31 +261,35 @@ def test_workload_1024cube_f32():
     assert got[-1] == 1
 
 
-@pytest.mark.parametrize("depth,kind", [(64, "f32"), (32, "u8")])
-def test_3d_blocks_walking_several_tasks(depth, kind):
-    """depth x 1024^2 volumes give more (tile, chunk) tasks than resident blocks (64 x 1024^2:
-    three rounds on 152 SMs, 32 x 1024^2: two), so each block reuses its key ring, carried rows
-    and histogram from one task to the next; the curve must still match the oracle bit for bit."""
-    v = synthetic.grf((depth, 1024, 1024), seed=30 + depth, device=DEV)
+@pytest.mark.parametrize("shape,kind,nbins", [((16, 2048, 2048), "f32", 256),
+                                              ((64, 1024, 1024), "f32", 1000),
+                                              ((32, 1024, 1024), "u8", 256)])
+def test_3d_blocks_walking_several_tasks(shape, kind, nbins):
+    """Volumes with more (tile, chunk) tasks than resident blocks, so each block reuses its key
+    ring, carried rows and histogram from one task to the next: float32 with 256 bins (the
+    TMA-staged kernel, 608 blocks on 152 SMs: two rounds for 16 x 2048^2), float32 with 1000
+    bins and uint8 (the register-prefetch kernel, 456 blocks: three and two rounds). The planner
+    says how many rounds the launch takes; the curve must match the oracle bit for bit."""
+    v = synthetic.grf(shape, seed=30 + shape[0], device=DEV)
+    vmax = 1.0
     if kind == "u8":
-        v, nbins, vmax = synthetic.quantise_u8(v), 256, 255.0
-    else:
-        nbins, vmax = 256, 1.0
+        v, vmax = synthetic.quantise_u8(v), 255.0
     plan = ecc.hard_launch_info(tuple(v.shape), 1, nbins, dtype=v.dtype)
-    assert plan["rounds"] > 1
+    assert plan["rounds"] > 1, plan
     got = ecc.ecc_hard(v.unsqueeze(0), nbins, 0.0, vmax)[0].cpu().numpy()
     want = _oracle_pool.hard_volume(v.cpu().numpy(), nbins, 0.0, vmax)
     np.testing.assert_array_equal(got, want)
 
 
 def test_3d_rounds_on_a_small_device_plan():
-    """The multi-round path on small volumes: a batch of volumes shares the resident blocks, so
-    each image gets few blocks and many tasks (checked with the planner), ragged tiles included."""
-    v = synthetic.grf((30, 40, 260), seed=33, batch=40)
-    plan = ecc.hard_launch_info(v.shape[1:], 40, 77)
-    assert plan["rounds"] > 1
+    """The multi-round path on small volumes: a batch of 100 volumes shares the resident blocks,
+    so each image gets a few blocks and more tiles than blocks (checked with the planner), ragged
+    tiles included; float32 (TMA-staged kernel) and uint8 (register-prefetch kernel)."""
+    v = synthetic.grf((8, 70, 300), seed=33, batch=100)
+    assert ecc.hard_launch_info(v.shape[1:], 100, 77)["rounds"] > 1
     check(v, 77, 0.0, 1.0, ndim=3)
     q = synthetic.quantise_u8(v)
+    assert ecc.hard_launch_info(v.shape[1:], 100, 256, dtype=torch.uint8)["rounds"] > 1
     check(q, 256, 0.0, 255.0, ndim=3)
 
 

@@ -90,6 +90,97 @@ def test_3d_fold_matches_oracle(seed):
                                   oracle.ecc_hard(f, 256, 0, 1))
 
 
+# ---------------------------------------------------------------------------------------------
+# Coded keys (the TMA-staged 3-D kernel): 1024 + 4k + (x & 1) + 2 (y & 1) as fp16 patterns,
+# strict in-plane flags, and the vertical fold carried from plane to plane
+# ---------------------------------------------------------------------------------------------
+
+def coded_values(K, H, yx0=(0, 0)):
+    """fp16 values of the kernel's coded key patterns 0x6400 + 4k + code (k = H, "never", gives
+    0x6800 + code for H = 256: the values 2048 .. 2054)."""
+    yy, xx = np.indices(K.shape[-2:])
+    code = ((xx + yx0[1]) & 1) + 2 * ((yy + yx0[0]) & 1)
+    pat = (0x6400 + 4 * K + code).astype(np.uint16)
+    return pat.view(np.float16).astype(np.float64), pat
+
+
+def c2_coded(P):
+    """c2 of one plane of coded values P (padded by one with coded "never" values)."""
+    Hh, Ww = P.shape[0] - 2, P.shape[1] - 2
+
+    def nb(dy, dx):
+        return P[1 + dy:1 + dy + Hh, 1 + dx:1 + dx + Ww]
+
+    p = nb(0, 0)
+    sat = lambda d: np.clip(d, 0.0, 1.0)  # the kernel's sub.sat of exact fp16 differences
+    # every difference of these fp16 integers is exact, so each flag is exactly 0 or 1
+    f = {k: sat(p - nb(*o)) > 0 for k, o in
+         dict(W=(0, -1), E=(0, 1), S=(1, 0), NW=(-1, -1), NE=(-1, 1), SW=(1, -1),
+              SE=(1, 1)).items()}
+    Sp = sat(nb(-1, 0) - p) > 0
+    W, E, S, NW, NE, SW, SE = (f[k] for k in ("W", "E", "S", "NW", "NE", "SW", "SE"))
+    return ((Sp | (E & NE)).astype(int) - (E & ~(S & SE)) - (S & ~(W & SW)) - (W & (Sp | ~NW)))
+
+
+def curve_3d_coded(K, H):
+    """The TMA kernel's algebra: coded keys, strict flags, carried fold, bin = (pattern -
+    0x6400) >> 2 (bin H collects the discarded "never" voxels)."""
+    D, Hy, Wx = K.shape
+    Kp = np.full((D + 2, Hy + 2, Wx + 2), H, np.int64)  # outside: NaN, i.e. key H
+    Kp[1:-1, 1:-1, 1:-1] = K
+    V, PAT = coded_values(Kp, H, yx0=(1, 1))  # padded index i is grid index i - 1
+    h = np.zeros(H + 1, np.int64)
+    up = lambda z: V[z + 1, 1:-1, 1:-1] < V[z, 1:-1, 1:-1]  # [k_{z+1} < k_z] (padded z)
+    c2M = lambda z: c2_coded(np.maximum(V[z], V[z + 1]))
+    q = -(1 - up(0)) * c2M(0)  # the plane below the volume (all never)
+    for z in range(1, D + 1):
+        u = up(z)
+        cm = c2M(z)
+        c = c2_coded(V[z]) - u * cm + q
+        q = -(1 - u) * cm
+        assert c.min() >= -8 and c.max() <= 7
+        bins = ((PAT[z, 1:-1, 1:-1].astype(np.int64) - 0x6400) >> 2)
+        np.add.at(h, np.minimum(bins, H).ravel(), c.ravel())
+    return np.cumsum(h[:H])
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_coded_keys_and_carried_fold_match_oracle(seed):
+    """Ties, NaN and every table size up to 256 (where "never" rounds above 2048)."""
+    rng = np.random.default_rng(300 + seed)
+    for _ in range(25):
+        shp = tuple(rng.integers(1, 7, size=3))
+        H = int(rng.choice([1, 2, 3, 7, 11, 255, 256]))
+        img = rng.integers(0, 6, size=shp).astype(np.float32) / 5
+        img[rng.random(shp) < 0.08] = np.nan
+        K = keys_of(img, H, 0.0, 0.8)
+        np.testing.assert_array_equal(curve_3d_coded(K, H), oracle.ecc_hard(img, H, 0.0, 0.8))
+    f = synthetic.grf((12, 20, 26), 30 + seed)
+    np.testing.assert_array_equal(curve_3d_coded(keys_of(f, 256, 0, 1), 256),
+                                  oracle.ecc_hard(f, 256, 0, 1))
+
+
+def test_coded_key_patterns():
+    """Coded keys are finite fp16 integers ordered like (k, code); "never" (k = H <= 256) lies
+    above every valid coded key, is an even integer when it exceeds 2048, and falls in bin H; the
+    integer coding of a key pair carries nothing across halves."""
+    for H in (1, 5, 200, 255, 256):
+        k = np.arange(H + 1)
+        for code in range(4):
+            pat = 0x6400 + 4 * k + code
+            val = pat.astype(np.uint16).view(np.float16).astype(np.float64)
+            assert np.all(np.diff(val[:H]) > 0) and val[H] > (1024 + 4 * (H - 1) + 3)
+            assert np.all(((pat - 0x6400) >> 2) == k)
+            if val[H] >= 2048:
+                assert val[H] % 2 == 0
+    # pair coding: 4 * pair + C (mod 2^32), C = c0 + (c1 << 16) - 3 * 0x64006400
+    for k0, k1, c0, c1 in [(0, 0, 0, 1), (255, 256, 2, 3), (256, 0, 0, 1), (256, 256, 2, 3)]:
+        pair = (0x6400 + k0) | ((0x6400 + k1) << 16)
+        C = (c0 + (c1 << 16) - 3 * 0x64006400) % 2 ** 32
+        got = (4 * pair + C) % 2 ** 32
+        assert got == (0x6400 + 4 * k0 + c0) | ((0x6400 + 4 * k1 + c1) << 16)
+
+
 def test_key_patterns_and_contribution_encoding():
     # 0x6400 + k is a strictly increasing fp16 pattern for k <= 6143, below +inf (absent)
     k = np.arange(0, 6144)
