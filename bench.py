@@ -57,6 +57,9 @@ WORKLOADS = {
     # the 1024^3 volume streamed from page-locked host memory in 64-plane slabs (a hard part
     # with a ninth field, the slab length): the out-of-core path, bound by the host link
     "3d1024stream": [("hard", (1024, 1024, 1024), 1, "f32", 256, 0.0, 1.0, 4, 64)],
+    # the 1024^3 volume sharded over the ranks in slabs that share one plane: each rank adds its
+    # slab's partial histogram, one all-reduce of 256 int64, one running sum (strong scaling)
+    "3d1024shard": [("shard", (1024, 1024, 1024), 1, "f32", 256, 0.0, 1.0, 4)],
 }
 WORKLOADS["headline"] = WORKLOADS["2d8192"] + WORKLOADS["3d1024"] + WORKLOADS["soft"]
 
@@ -77,11 +80,44 @@ def part_dirs(p):
 
 
 def part_name(p):
+    if p[0] == "shard":
+        return f"hard_3d_sharded_{'x'.join(str(s) for s in p[1])}_{p[3]}_H{p[4]}"
     if p[0] == "hard":
         dims = "x".join(str(s) for s in p[1])
         return f"hard_{len(p[1])}d_{p[2]}x{dims}_{p[3]}_H{p[4]}"
     name = f"soft_fwd_bwd_{p[2]}x{'x'.join(str(x) for x in p[1])}_K{p[3]}"
     return name if part_dirs(p) == 1 else name.replace("soft_", "soft_ect_") + f"_D{part_dirs(p)}"
+
+
+def hard_kernel_name(p):
+    """The library's kernel for a hard part: the TMA-staged 3-D kernel for float32 volumes with
+    rows of a multiple of 4 values and at most 256 bins, else the register-prefetch 3-D kernel or
+    the 2-D kernel."""
+    if len(p[1]) == 2:
+        return "ecc_hard2d_kernel"
+    if p[3] == "f32" and p[4] <= 256 and p[1][-1] % 4 == 0:
+        return "ecc_hard3d_tma_kernel"
+    return "ecc_hard3d_kernel"
+
+
+def time_inputs_planes(p, rank, world):
+    """Planes this rank processes of a sharded part (None for other parts)."""
+    if p[0] != "shard":
+        return None
+    from euler_characteristic_curves_gb300 import shard
+
+    a, b = shard.slab_plan(p[1][0], world)[rank]
+    return b - a + 1
+
+
+def part_alg_bytes(p, planes=None):
+    """Algorithmic bytes of a hard part per call on this rank: every voxel read once, one int64
+    per (image, bin) written. A sharded part counts this rank's slab."""
+    elem = 1 if p[3].startswith("u8") else 4
+    vox = part_voxels(p)
+    if planes is not None:
+        vox = vox // p[1][0] * planes
+    return vox * elem + 8 * p[2] * p[4]
 
 
 def part_voxels(p):
@@ -127,6 +163,91 @@ def recorded_traffic(kernel_key):
     if not ent or ent.get("source_hash") != kernel_source_hash():
         return None
     return ent.get("bytes_per_launch")
+
+
+class NvmlClockSampler:
+    """Reads SM clocks, power and clock-event reasons through NVML (read-only queries, loaded
+    with ctypes) every 2 ms while the timed region runs; a short timed region still gets many
+    samples. Raises OSError when NVML cannot be loaded (the nvidia-smi sampler is used then)."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device_index: int, period_s: float = 0.002):
+        import ctypes
+
+        import torch
+
+        self.ct = ctypes
+        self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.nvml.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        props = torch.cuda.get_device_properties(device_index)
+        bus = getattr(props, "pci_bus_id", None)
+        dom = getattr(props, "pci_domain_id", 0)
+        dev = getattr(props, "pci_device_id", 0)
+        self.handle = ctypes.c_void_p()
+        ok = False
+        if bus is not None:
+            pci = f"{dom:08x}:{bus:02x}:{dev:02x}.0".encode()
+            ok = self.nvml.nvmlDeviceGetHandleByPciBusId_v2(pci, ctypes.byref(self.handle)) == 0
+        if not ok and self.nvml.nvmlDeviceGetHandleByIndex_v2(
+                ctypes.c_uint(device_index), ctypes.byref(self.handle)) != 0:
+            raise OSError("no NVML handle for the device")
+        self.reasons_fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.period = period_s
+        self.samples = []
+        self.stop_flag = False
+        self.thread = None
+
+    def _one(self):
+        ct = self.ct
+        sm, smax, mw, rs = ct.c_uint(), ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ct.byref(sm)) != 0:  # SM clock
+            return None
+        self.nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, ct.byref(smax))
+        self.nvml.nvmlDeviceGetPowerUsage(self.handle, ct.byref(mw))
+        self.reasons_fn(self.handle, ct.byref(rs))
+        return sm.value, smax.value, mw.value / 1000.0, rs.value
+
+    def start(self):
+        import threading
+        import time
+
+        def run():
+            while not self.stop_flag:
+                s = self._one()
+                if s is not None:
+                    self.samples.append(s)
+                time.sleep(self.period)
+
+        self.thread = threading.Thread(target=run, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        self.stop_flag = True
+        if self.thread:
+            self.thread.join(timeout=5)
+        s = self._one()  # at least one sample, taken at the end of the timed region
+        if s is not None:
+            self.samples.append(s)
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        reasons = sorted({name for *_, r in self.samples for bit, name in self.REASONS.items()
+                          if r & bit})
+        return {"sm_mhz": statistics.median(x[0] for x in self.samples),
+                "sm_max_mhz": max(x[1] for x in self.samples), "samples": len(self.samples),
+                "power_w_max": max(x[2] for x in self.samples), "reasons": reasons,
+                "sampler": "NVML every 2 ms"}
+
+
+def clock_sampler(device_index: int):
+    """NVML sampler when NVML loads, else the nvidia-smi one."""
+    try:
+        return NvmlClockSampler(device_index)
+    except (OSError, AttributeError):
+        return ClockSampler(device_index)
 
 
 class ClockSampler:
@@ -232,7 +353,19 @@ def make_inputs(parts, device):
     from euler_characteristic_curves_gb300 import synthetic
 
     inputs = []
+    rank, world, _ = dist_env()
     for p in parts:
+        if p[0] == "shard":  # this rank's slab of the volume (the whole volume at N = 1)
+            from euler_characteristic_curves_gb300 import shard
+
+            _, shape, batch, kind, nbins, vmin, vmax, seed = p[:8]
+            vol = synthetic.grf(shape, seed, device=device)
+            a, b = shard.slab_plan(shape[0], world)[rank]
+            slab = vol[a:b + 1].clone()
+            del vol
+            torch.cuda.empty_cache()
+            inputs.append({"img": slab, "ndim": 3, "rank": rank, "planes": (a, b)})
+            continue
         if p[0] == "hard":
             _, shape, batch, kind, nbins, vmin, vmax, seed = p[:8]
             if part_slab(p):
@@ -303,7 +436,9 @@ class OurStep:
         self.parts, self.inputs = parts, inputs
         self.outs = []
         for p, x in zip(parts, inputs):
-            if p[0] == "hard" and part_slab(p):
+            if p[0] == "shard":
+                self.outs.append(torch.empty(p[4], dtype=torch.int64, device=device))
+            elif p[0] == "hard" and part_slab(p):
                 nbytes = ecc.hard_stream_buffer_bytes(p[1], torch.float32, part_slab(p))
                 self.outs.append({"out": torch.empty(p[4], dtype=torch.int64, device=device),
                                   "buf": torch.empty(nbytes, dtype=torch.uint8, device=device)})
@@ -320,12 +455,20 @@ class OurStep:
                                 device=device)
                 self.outs.append({"ws": ws, "s": s})
         sms = torch.cuda.get_device_properties(device).multi_processor_count
-        self.launches_per_step = sum(hard_launches(p, sms) if p[0] == "hard" else 6
-                                     for p in parts)
+        self.launches_per_step = sum(
+            hard_launches(p, sms) if p[0] == "hard" else
+            (2 + (x["rank"] > 0)) if p[0] == "shard" else 6 for p, x in zip(parts, inputs))
 
     def run_part(self, i):
         p, x, o = self.parts[i], self.inputs[i], self.outs[i]
-        if p[0] == "hard" and part_slab(p):
+        if p[0] == "shard":
+            from euler_characteristic_curves_gb300 import shard
+
+            o.zero_()
+            shard.volume_partial(x["img"], p[4], p[5], p[6], x["rank"], o)
+            shard._default_allreduce(None)(o)
+            self.ecc.hist_to_curve(o)
+        elif p[0] == "hard" and part_slab(p):
             self.ecc.ecc_hard_stream(x["host"], p[4], p[5], p[6], slab_planes=part_slab(p),
                                      buf=o["buf"], out=o["out"])
         elif p[0] == "hard":
@@ -376,6 +519,8 @@ class OurStep:
 
     def results_of(self, i):
         p, o = self.parts[i], self.outs[i]
+        if p[0] == "shard":
+            return [o]
         if p[0] == "hard":
             return [o["out"] if part_slab(p) else o]
         return [o["s"], *o["grads"].values()]
@@ -429,7 +574,7 @@ def time_ours(args, parts, rank, world, device):
             step.run_part(i)
     torch.cuda.synchronize()
     barrier(world)
-    sampler = ClockSampler(torch.cuda.current_device())
+    sampler = clock_sampler(torch.cuda.current_device())
     sampler.start()
     run = step.run_part
     if args.graph:
@@ -524,14 +669,15 @@ def time_e2e(args, parts, inputs, step, device, world):
     per_step = [marks[i].elapsed_time(marks[i + 1]) for i in range(steps)]
     ms = max_over_ranks(marks[0].elapsed_time(marks[-1]) / steps, world)
     med = max_over_ranks(statistics.median(per_step), world)
-    hard_vox = sum(part_voxels(p) for p in parts if p[0] == "hard") or \
+    hard_vox = sum(part_voxels(p) for p in parts if p[0] in ("hard", "shard")) or \
         sum(part_voxels(p) for p in parts)
-    return {"value": round(hard_vox * world / (ms * 1e-3) / 1e9, 3), "unit": "Gvoxels/s",
+    ranks = 1 if any(p[0] == "shard" for p in parts) else world  # a sharded volume: one problem
+    return {"value": round(hard_vox * ranks / (ms * 1e-3) / 1e9, 3), "unit": "Gvoxels/s",
             "ms_per_step": round(ms, 3), "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": steps,
             "link_gbs": link, "link_floor_ms": round(h2d / (link * 1e9) * 1e3, 3),
             "ms_per_step_median": round(med, 3),
-            "value_median": round(hard_vox * world / (med * 1e-3) / 1e9, 3),
+            "value_median": round(hard_vox * ranks / (med * 1e-3) / 1e9, 3),
             "ms_steps": [round(x, 2) for x in per_step],
             "path": ("3-D volumes through ecc_hard_stream from pinned host memory in "
                      f"{E2E_SLAB}-plane slabs; other parts copied and run on a second stream"
@@ -584,7 +730,7 @@ def oracle_sample_step(parts, cache):
     for p in parts:
         key = part_name(p)
         if key not in cache:
-            if p[0] == "hard":
+            if p[0] in ("hard", "shard"):
                 _, shape, batch, kind, nbins, vmin, vmax, seed = p[:8]
                 if len(shape) == 2:
                     sh = (min(shape[0], SAMPLE_2D), min(shape[1], SAMPLE_2D))
@@ -610,7 +756,7 @@ def oracle_sample_step(parts, cache):
                 cache[key] = (synthetic.grf(sh, s_img), synthetic.uniform_thresholds(K), U,
                               synthetic.upstream_grad((1, nd, K), s_g))
         x = cache[key]
-        if p[0] == "hard":
+        if p[0] in ("hard", "shard"):
             oracle.ecc_hard(x, p[4], p[5], p[6])
             vox += x.size
         else:
@@ -716,13 +862,16 @@ def main(argv=None):
         ap.error("--warmup must be at least 3")
     rank, world, local = dist_env()
     parts = WORKLOADS[args.workload]
-    hard_vox = sum(part_voxels(p) for p in parts if p[0] == "hard")
+    hard_vox = sum(part_voxels(p) for p in parts if p[0] in ("hard", "shard"))
     unit_vox = hard_vox if hard_vox else sum(part_voxels(p) for p in parts)
+    # a sharded volume is one problem split over the ranks (total work fixed as N grows)
+    strong = any(p[0] == "shard" for p in parts)
     config = {"workload": DESCRIPTION.get(args.workload, args.workload),
               "parts": [part_name(p) for p in parts],
               "l2": "inputs larger than L2 (the 268 MB image and the 4 GiB volume evict L2 "
                     "between passes)" if args.workload == "headline" else "not flushed",
-              "parallelism": f"independent replicas x{world}",
+              "parallelism": (f"one volume in {world} slabs sharing a plane, one all-reduce"
+                              if strong else f"independent replicas x{world}"),
               "timing": ("one CUDA graph per part (its library calls captured once), replayed "
                          "every step" if args.graph else "eager library calls")}
 
@@ -735,7 +884,8 @@ def main(argv=None):
         line = {"impl": "reference", "metric": METRIC, "value": round(value, 6),
                 "unit": "Gvoxels/s", "n_gpus": args.gpus, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "higher_is_better": True, "scaling": "strong" if strong else "weak",
+                "vs_baseline": None,
                 "dtype": "f64 oracle on f32/u8 inputs", "data": "synthetic (seeded GRF)",
                 "config": config,
                 "cpu_baseline": {"value": round(value, 6), "unit": "Gvoxels/s", "cores": 1,
@@ -756,7 +906,7 @@ def main(argv=None):
     total_ms, part_ms, clocks, launches, e2e, soft_stats = time_ours(args, parts, rank, world,
                                                                      device)
     ms_step = total_ms / args.steps
-    value = unit_vox * world / (ms_step * 1e-3) / 1e9
+    value = unit_vox * (1 if strong else world) / (ms_step * 1e-3) / 1e9
 
     peak, peak_kind = load_peaks()
     # dominant kernel: the part with the largest device time
@@ -765,9 +915,8 @@ def main(argv=None):
     for i, p in enumerate(parts):
         ms = part_ms[i]
         ent = {"ms": round(ms, 4), "gvoxels_s": round(part_voxels(p) / (ms * 1e-3) / 1e9, 3)}
-        if p[0] == "hard":
-            elem = 1 if p[3].startswith("u8") else 4
-            alg = part_voxels(p) * elem + 8 * p[2] * p[4]
+        if p[0] in ("hard", "shard"):
+            alg = part_alg_bytes(p, time_inputs_planes(p, rank, world))
             ent["hbm_gbs"] = round(alg / (ms * 1e-3) / 1e9, 1)
             if part_slab(p):  # streamed: every voxel crosses the host link once per step
                 ent["link_gbs"] = ent["hbm_gbs"]
@@ -781,11 +930,10 @@ def main(argv=None):
         breakdown[part_name(p)] = ent
     roofline = None
     pd = parts[dom]
-    if pd[0] == "hard":
-        elem = 1 if pd[3].startswith("u8") else 4
-        alg = part_voxels(pd) * elem + 8 * pd[2] * pd[4]
+    if pd[0] in ("hard", "shard"):
+        alg = part_alg_bytes(pd, time_inputs_planes(pd, rank, world))
         achieved = alg / (part_ms[dom] * 1e-3) / 1e9
-        key = "ecc_hard3d_kernel" if len(pd[1]) == 3 else "ecc_hard2d_kernel"
+        key = hard_kernel_name(pd)
         roofline = {"bound": "hbm", "kernel": key, "achieved": round(achieved, 1),
                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
@@ -806,7 +954,8 @@ def main(argv=None):
     soft_ms = [part_ms[i] for i, p in enumerate(parts) if p[0] == "soft"]
     line = {"metric": METRIC, "value": round(value, 3), "unit": "Gvoxels/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "higher_is_better": True, "scaling": "strong" if strong else "weak",
+            "vs_baseline": None,
             "dtype": "f32 compare / int32+int64 histogram (hard); f32 + fp64 reductions (soft)",
             "data": "synthetic (seeded Gaussian random fields, k^-3 spectrum)",
             "config": config, "parts": breakdown,

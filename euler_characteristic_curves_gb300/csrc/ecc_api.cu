@@ -177,6 +177,41 @@ int ecc_hard(const void *img, int dtype, int ndim, const int64_t *dims, int64_t 
     return ECC_OK;
 }
 
+int ecc_hard_partial(const void *img, int dtype, int ndim, const int64_t *dims, int64_t batch,
+                     int nbins, double vmin, double vmax, int sign, int64_t *hist,
+                     ecc_stream_t stream)
+{
+    if (!img || !hist || !dims) return ECC_EINVAL;
+    if (sign != 1 && sign != -1) return ECC_EINVAL;
+    HardPlan pl;
+    const int rc = hard_shape_check(dtype, ndim, dims, batch, nbins, pl);
+    if (rc != ECC_OK) return rc;
+    if (!isfinite(vmin) || !isfinite(vmax) || !(vmin <= vmax) || !isfinite(vmax - vmin))
+        return ECC_EINVAL;
+    pl.img = img;
+    pl.out = hist;
+    float table[ECC_MAX_NBINS + 2];
+    hard_keys(dtype, nbins, vmin, vmax, pl, table);
+    const size_t align = dtype == ECC_U8 ? 4 : 16;
+    pl.vec_ok = ((uintptr_t)img % align == 0) && (pl.W % 4 == 0);
+    pl.table = table;
+    pl.sign = sign;
+    pl.scan = false;     // a histogram: the caller adds partials, then takes one running sum
+    pl.zero_out = false; // added to what hist holds
+    if (hard_run(pl, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return ECC_ECUDA;
+    return ECC_OK;
+}
+
+int ecc_hist_to_curve(int64_t *hist, int nbins, int64_t batch, ecc_stream_t stream)
+{
+    if (!hist) return ECC_EINVAL;
+    if (nbins < 1 || batch < 1) return ECC_EINVAL;
+    if (nbins > ECC_MAX_NBINS || batch > 65535) return ECC_ERANGE;
+    if (hard_scan(hist, nbins, batch, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return ECC_ECUDA;
+    return ECC_OK;
+}
+
 int ecc_hard_launch_info(int dtype, int ndim, const int64_t *dims, int64_t batch, int nbins,
                          int sm_count, int64_t *info)
 {

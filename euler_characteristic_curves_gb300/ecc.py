@@ -4,7 +4,8 @@ Every computation runs in the CUDA library libecc_gb300.so; this module checks s
 device pointers, sizes and the current CUDA stream, and turns negative status codes into
 exceptions. There is no CPU path: CPU tensors are rejected, and a missing library raises.
 
-Names follow the C entry points: ``ecc_hard``, ``ecc_hard_stream``, ``ecc_soft_fwd``, ``ecc_soft_bwd``,
+Names follow the C entry points: ``ecc_hard``, ``ecc_hard_partial``, ``hist_to_curve``,
+``hard_launch_info``, ``device_status``, ``ecc_hard_stream``, ``ecc_soft_fwd``, ``ecc_soft_bwd``,
 ``ecc_soft_stats``, ``ecc_soft_fwd_noalloc``, ``ecc_soft_ect_fwd``, ``ecc_soft_ect_bwd``,
 ``ecc_soft_ect_stats``, ``soft_workspace_bytes``; ``SoftECT`` / ``soft_ect`` wrap the transform; ``SoftECC`` / ``soft_ecc`` wrap the soft pair as a differentiable
 PyTorch layer ("Key designs -- differentiable ECC layer (sigmoid relaxation)" in the paper notes
@@ -47,6 +48,12 @@ def load_library():
                                ctypes.c_float, ctypes.c_size_t)
         lib.ecc_hard.argtypes = [p, i, i, p, i64, i, d, d, p, p]
         lib.ecc_hard.restype = i
+        lib.ecc_hard_partial.argtypes = [p, i, i, p, i64, i, d, d, i, p, p]
+        lib.ecc_hard_partial.restype = i
+        lib.ecc_hist_to_curve.argtypes = [p, i, i64, p]
+        lib.ecc_hist_to_curve.restype = i
+        lib.ecc_device_status.argtypes = [i]
+        lib.ecc_device_status.restype = i
         lib.ecc_hard_launch_info.argtypes = [i, i, p, i64, i, i, p]
         lib.ecc_hard_launch_info.restype = i
         lib.ecc_hard_stream_buffer_bytes.argtypes = [i, p, i]
@@ -182,6 +189,51 @@ def ecc_hard(img: torch.Tensor, nbins: int, vmin: float, vmax: float, ndim: int 
     _check(rc, "ecc_hard")
     out = out.view(batch, nbins)
     return out if batched else out[0]
+
+
+def ecc_hard_partial(img: torch.Tensor, nbins: int, vmin: float, vmax: float, hist: torch.Tensor,
+                     sign: int = 1, ndim: int | None = None, stream=None) -> torch.Tensor:
+    """Adds sign * (the unscanned per-bin cell counts of img) into hist (int64 [batch, nbins] on
+    img's device, not zeroed): the partial that sharded calls sum before one running sum
+    (``hist_to_curve``). img as for ``ecc_hard``."""
+    _need_cuda(img, "img")
+    if img.dtype == torch.uint8:
+        dt = ECC_U8
+    elif img.dtype == torch.float32:
+        dt = ECC_F32
+    else:
+        raise TypeError(f"img dtype {img.dtype}: uint8 or float32 expected")
+    ndim, batch, dims, _ = _split(img, ndim)
+    _check_out(hist, img, torch.int64, batch * nbins)
+    with _on_device(img):
+        rc = load_library().ecc_hard_partial(img.data_ptr(), dt, ndim, _dims_array(dims), batch,
+                                             int(nbins), float(vmin), float(vmax), int(sign),
+                                             hist.data_ptr(), _stream_handle(stream))
+    _check(rc, "ecc_hard_partial")
+    return hist
+
+
+def hist_to_curve(hist: torch.Tensor, stream=None) -> torch.Tensor:
+    """In place: hist[..., k] becomes the running sum over bins 0..k (int64 CUDA tensor, last axis
+    the bins). Returns hist."""
+    _need_cuda(hist, "hist")
+    if hist.dtype != torch.int64 or hist.dim() < 1:
+        raise ValueError("hist must be an int64 tensor with the bins on its last axis")
+    nbins = hist.shape[-1]
+    with _on_device(hist):
+        rc = load_library().ecc_hist_to_curve(hist.data_ptr(), int(nbins),
+                                              hist.numel() // max(1, nbins),
+                                              _stream_handle(stream))
+    _check(rc, "ecc_hist_to_curve")
+    return hist
+
+
+def device_status(clear: bool = True, device=None) -> int:
+    """ecc_device_status on ``device`` (default: the current one): 0, or the ECC_ETIMEOUT status
+    when a kernel gave up waiting for its own staged copy since the last clear."""
+    ctx = torch.cuda.device(device) if device is not None else _no_switch
+    with ctx:
+        return int(load_library().ecc_device_status(1 if clear else 0))
 
 
 def hard_launch_info(dims, batch: int, nbins: int, dtype=torch.float32, sm_count: int = 0):

@@ -90,6 +90,34 @@ int ecc_hard(const void *img, int dtype, int ndim, const int64_t *dims, int64_t 
              double vmin, double vmax, int64_t *out, ecc_stream_t stream);
 
 /*
+ * Sharded hard ECC: the partial histogram of one piece of a grid, and the running sum that turns
+ * summed partials into the curve.
+ *
+ * Section "Limitations" of the ECC paper notes: the method runs on one device, without batching
+ * or multi-GPU execution. The ECC is a sum over cells, and each cell enters at the bin of its
+ * largest vertex, so per-bin counts add over pieces that share no cells:
+ *   - a batch splits by images (no cell joins two images);
+ *   - one volume splits into slabs of planes in which consecutive slabs share one plane. Every
+ *     cell lies in some slab, and two consecutive slabs share exactly the cells of their common
+ *     plane, so hist(volume) = sum_i hist_3D(slab i) - sum_{i > 0} hist_2D(first plane of slab i).
+ * Each rank (or device) adds the partials of its pieces into one int64 [batch][nbins] histogram,
+ * the ranks sum their histograms (one all-reduce of batch * nbins int64), and ecc_hist_to_curve
+ * turns the sum into the curve ecc_hard would return.
+ *
+ * ecc_hard_partial: arguments as for ecc_hard, plus
+ *   sign  +1 or -1: hist[b * nbins + k] += sign * (sum over the cells of image b whose largest
+ *         vertex value first enters at t_k of (-1)^dim). Cells that never enter add nothing.
+ *   hist  device int64 [batch][nbins], accumulated into (not zeroed): the caller zeroes it once.
+ * ecc_hist_to_curve: hist[b][k] = sum_{j <= k} hist[b][j], in place, for batch rows of nbins.
+ * Both are asynchronous on `stream`; calls on one stream accumulate in order. Returns ECC_OK or a
+ * negative status (ECC_EINVAL for a sign other than +1 / -1).
+ */
+int ecc_hard_partial(const void *img, int dtype, int ndim, const int64_t *dims, int64_t batch,
+                     int nbins, double vmin, double vmax, int sign, int64_t *hist,
+                     ecc_stream_t stream);
+int ecc_hist_to_curve(int64_t *hist, int nbins, int64_t batch, ecc_stream_t stream);
+
+/*
  * Launch shape that ecc_hard takes for these sizes -- a diagnostic with no counterpart in the paper
  * notes, for tests and tuning. It validates the shape arguments as ecc_hard does (same status
  * codes) and launches nothing.

@@ -101,6 +101,37 @@ def test_extents_the_kernels_cannot_index_are_rejected(lib):
              None) == ERANGE
 
 
+def test_partial_and_curve_validation(lib):
+    p = lib.ecc_hard_partial
+    d2 = dims(8, 8)
+    assert p(None, 1, 2, d2, 1, 4, 0.0, 1.0, 1, FAKE, None) == EINVAL
+    assert p(FAKE, 1, 2, d2, 1, 4, 0.0, 1.0, 1, None, None) == EINVAL
+    assert p(FAKE, 1, 2, d2, 1, 4, 0.0, 1.0, 0, FAKE, None) == EINVAL  # sign must be +1 / -1
+    assert p(FAKE, 1, 2, d2, 1, 4, 0.0, 1.0, 2, FAKE, None) == EINVAL
+    assert p(FAKE, 9, 2, d2, 1, 4, 0.0, 1.0, 1, FAKE, None) == EDTYPE
+    assert p(FAKE, 1, 5, d2, 1, 4, 0.0, 1.0, -1, FAKE, None) == EDIM
+    assert p(FAKE, 1, 2, d2, 1, 4097, 0.0, 1.0, 1, FAKE, None) == ERANGE
+    assert p(FAKE, 1, 2, d2, 1, 4, 1.0, 0.0, 1, FAKE, None) == EINVAL
+    assert p(FAKE, 1, 2, dims(1, 3 * 10**9), 1, 4, 0.0, 1.0, 1, FAKE, None) == ERANGE
+    c = lib.ecc_hist_to_curve
+    assert c(None, 4, 1, None) == EINVAL
+    assert c(FAKE, 0, 1, None) == EINVAL and c(FAKE, 4, 0, None) == EINVAL
+    assert c(FAKE, 4097, 1, None) == ERANGE and c(FAKE, 4, 65536, None) == ERANGE
+
+
+def test_launch_info(lib):
+    info = (ctypes.c_int64 * 6)()
+    li = lib.ecc_hard_launch_info
+    assert li(1, 3, dims(1024, 1024, 1024), 1, 256, 152, info) == OK
+    blocks, tasks, rows, rounds, direct, sms = list(info)
+    assert sms == 152 and blocks <= 152 * 4 and rounds == -(-tasks // blocks) and rounds > 1
+    assert tasks % (8 * 32) == 0  # 8 x 32 tiles of 128 x 32 per chunk of planes
+    assert li(1, 2, dims(128, 128), 1, 256, 152, info) == OK and info[4] == 1  # one block
+    assert li(1, 2, dims(8192, 8192), 1, 1024, 152, info) == OK and info[4] == 0
+    assert li(1, 3, dims(8, 8, 8), 1, 4097, 152, info) == ERANGE
+    assert li(1, 3, dims(8, 8, 8), 1, 16, 152, None) == EINVAL
+
+
 def test_soft_workspace_size(lib):
     w = lib.ecc_soft_workspace_bytes
     assert w(2, dims(256, 256), 64, 128) > 64 * 256 * 256 * 16

@@ -55,3 +55,20 @@ def test_hard_launch_count_per_part():
     # a batch larger than the resident blocks gives every image its own single block
     big_batch = ("hard", (1024, 1024), 1000, "f32", 256, 0.0, 1.0, 2)
     assert bench.hard_launches(big_batch, 152) == 1
+
+
+def test_sharded_workload_reference_line_and_plan():
+    """The sharded-volume workload: its reference line reports strong scaling, and its
+    per-rank algorithmic bytes follow the slab plan (every plane once, the shared ones twice)."""
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        assert bench.main(["--impl", "reference", "--workload", "3d1024shard", "--steps", "1",
+                           "--warmup", "3"]) == 0
+    d = json.loads(buf.getvalue().strip().splitlines()[-1])
+    assert d["scaling"] == "strong" and d["value"] > 0
+    p = bench.WORKLOADS["3d1024shard"][0]
+    assert bench.hard_kernel_name(p) == "ecc_hard3d_tma_kernel"
+    for world in (1, 2, 4, 8):
+        planes = [bench.time_inputs_planes(p, r, world) for r in range(world)]
+        assert sum(planes) == 1024 + world - 1
+        assert bench.part_alg_bytes(p, planes[0]) == planes[0] * 1024 * 1024 * 4 + 8 * 256
