@@ -403,9 +403,9 @@ def make_inputs(parts, device):
 
 
 def hard_launches(p, sms):
-    """Kernels one hard-ECC call launches: the pass and the scan, or the pass alone when a 2-D
-    image gets a single block (which stores its curve itself). Mirrors the library's grid
-    choice: 2-D blocks of 8 warps, 128-column strips, 3 blocks per SM."""
+    """Kernels one hard-ECC call launches: a 3-D call the pass and the scan; a 2-D call the pass
+    alone (an image's only block stores its curve, several blocks add the running sums of their
+    histograms)."""
     if part_slab(p):  # slabs sharing one plane: a 3-D pass each, a plane pass from the second
         D, S, n, a = p[1][0], part_slab(p), 0, 0  # slab on, and one scan at the end
         while True:
@@ -416,12 +416,7 @@ def hard_launches(p, sms):
             a = b
     if len(p[1]) != 2:
         return 2
-    Hy, W = p[1]
-    strips = -(-W // 128)
-    per_image = max(1, sms * 3 // p[2])
-    per_image = min(per_image, max(1, -(-strips * Hy // (32 * 8))))
-    R = min(max(1, per_image * 8 // strips), Hy)
-    return 1 if -(-strips * R // 8) == 1 else 2
+    return 1  # a 2-D image's blocks add the running sums of their histograms: no scan launch
 
 
 class OurStep:

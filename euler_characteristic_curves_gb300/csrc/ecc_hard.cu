@@ -102,13 +102,51 @@ __device__ __forceinline__ void block_store_curve(const int *hist, int H, int64_
     }
 }
 
-// DIRECT_OK: the kernel may run with P.direct (the 2-D kernel; the 3-D kernel always flushes).
+// The block adds the running sum of its histogram into the curve dst (zeroed before the launch):
+// the running sum is linear, so the blocks' running sums add up to the running sum of the
+// image's histogram, and no scan launch follows. Warp w takes the contiguous bins
+// [w per, (w + 1) per) as in block_store_curve; bins whose running sum is 0 add nothing.
+__device__ __forceinline__ void block_add_curve(const int *hist, int H, int64_t *dst)
+{
+    __shared__ long long warp_total[32];
+    const int lane = threadIdx.x & (kWarp - 1), warp = threadIdx.x >> 5;
+    const int nw = blockDim.x >> 5;
+    const int per = (H + nw - 1) / nw;
+    const int lo = min(H, warp * per), hi = min(H, lo + per);
+    long long t = 0;
+    for (int i = lo + lane; i < hi; i += kWarp) t += hist[i];
+#pragma unroll
+    for (int o = kWarp / 2; o > 0; o >>= 1) t += __shfl_xor_sync(kFull, t, o);
+    if (lane == 0) warp_total[warp] = t;
+    __syncthreads();
+    long long carry = 0;
+    for (int w = 0; w < warp; ++w) carry += warp_total[w];
+    unsigned long long *d = reinterpret_cast<unsigned long long *>(dst);
+    for (int c = lo; c < hi; c += kWarp) {  // warp-uniform bounds
+        const int i = c + lane;
+        long long v = i < hi ? (long long)hist[i] : 0;
+#pragma unroll
+        for (int o = 1; o < kWarp; o <<= 1) {
+            const long long n = __shfl_up_sync(kFull, v, o);
+            if (lane >= o) v += n;
+        }
+        if (i < hi && carry + v != 0) atomicAdd(d + i, (unsigned long long)(carry + v));
+        carry += __shfl_sync(kFull, v, kWarp - 1);
+    }
+}
+
+// DIRECT_OK: the kernel may run with P.direct or P.prefix (the 2-D kernels; the 3-D kernel
+// always flushes its histogram).
 template <bool DIRECT_OK, int CAP>
 __device__ __forceinline__ void block_flush(const HardParams<CAP> &P, const int *hist, int64_t b)
 {
     __syncthreads();
     if (DIRECT_OK && P.direct) {  // grid-uniform
         block_store_curve(hist, P.H, P.out + b * (int64_t)P.H);
+        return;
+    }
+    if (DIRECT_OK && P.prefix) {  // grid-uniform
+        block_add_curve(hist, P.H, P.out + b * (int64_t)P.H);
         return;
     }
     unsigned long long *dst = reinterpret_cast<unsigned long long *>(P.out + b * (int64_t)P.H);
@@ -128,6 +166,7 @@ __device__ __forceinline__ KeyConsts key_consts(const HardParams<CAP> &P)
     K.clo = P.key_clo;
     K.chi = P.key_chi;
     K.H = P.H;
+    key_pairs(K);
     return K;
 }
 
@@ -978,54 +1017,6 @@ __device__ __forceinline__ void stage_plane(const Hard3TmaParams &P, uint32_t ra
         : "memory");
 }
 
-// Packed fp32 pairs (sm_100-family f32x2 instructions; each element rounds as the scalar op does).
-__device__ __forceinline__ uint64_t pk(float a, float b)
-{
-    return (uint64_t)__float_as_uint(a) | ((uint64_t)__float_as_uint(b) << 32);
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c)
-{
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-__device__ __forceinline__ uint64_t f2_add_rp(uint64_t a, uint64_t b)
-{
-    uint64_t d;
-    asm("add.rp.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ uint32_t h2_fma(uint32_t a, uint32_t b, uint32_t c)
-{
-    uint32_t d;
-    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-__device__ __forceinline__ uint32_t h2_neg(uint32_t a)
-{
-    uint32_t d;
-    asm("neg.f16x2 %0, %1;" : "=r"(d) : "r"(a));
-    return d;
-}
-
-// Estimated key patterns of two values (low halves 0x6400 + ceil(t - E), as key_fast); ORs into
-// `amb` a non-zero value when either estimate is ambiguous. The normalisation saturates value by
-// value; the rest runs on packed pairs.
-struct KeyPairConsts {
-    uint64_t nH, clo, chi, magic;
-};
-__device__ __forceinline__ void key_fast2(float v0, float v1, const KeyConsts &K,
-                                          const KeyPairConsts &K2, uint32_t &k0, uint32_t &k1,
-                                          uint32_t &amb)
-{
-    const uint64_t u = pk(__saturatef(fmaf(v0, K.a, K.b)), __saturatef(fmaf(v1, K.a, K.b)));
-    const uint64_t lo = f2_add_rp(f2_fma(u, K2.nH, K2.clo), K2.magic);
-    const uint64_t hi = f2_add_rp(f2_fma(u, K2.nH, K2.chi), K2.magic);
-    k0 = (uint32_t)lo;
-    k1 = (uint32_t)(lo >> 32);
-    amb |= (k0 ^ (uint32_t)hi) | (k1 ^ (uint32_t)(hi >> 32));
-}
-
 // Coding of a key pair: patterns 0x6400 + k -> 0x6400 + 4k + code, in each half at once. As a
 // 32-bit integer, 4 * pair + C with C = c0 + (c1 << 16) - 3 * 0x64006400 (mod 2^32) gives
 // (0x6400 + 4 k0 + c0) + (0x6400 + 4 k1 + c1) << 16: each half stays below 2^16 (at most 0x6803
@@ -1063,9 +1054,9 @@ __device__ __forceinline__ void halo_item_coded(int i, int &off, uint32_t &code)
 // warp's eight rows (four columns each) and its halo items; the rare exact fix-up revisits a
 // group of two rows (the halo items join the first).
 __device__ __forceinline__ void plane_keys_coded(const float *raw, uint16_t *dst,
-                                                 const KeyConsts &K, const KeyPairConsts &K2,
-                                                 const float *__restrict__ T, int r0, int lane,
-                                                 const int *h_off, const uint32_t *h_code)
+                                                 const KeyConsts &K, const float *__restrict__ T,
+                                                 int r0, int lane, const int *h_off,
+                                                 const uint32_t *h_code)
 {
     constexpr int kFixRows = 2, kGroups = k3Rows / kFixRows;
     uint32_t amb[kGroups];
@@ -1076,8 +1067,8 @@ __device__ __forceinline__ void plane_keys_coded(const float *raw, uint16_t *dst
     for (int i = 0; i < k3Rows; ++i) {
         const float4 v = *reinterpret_cast<const float4 *>(raw + base + i * kKeyPitch);
         uint32_t k0, k1, k2, k3;
-        key_fast2(v.x, v.y, K, K2, k0, k1, amb[i / kFixRows]);
-        key_fast2(v.z, v.w, K, K2, k2, k3, amb[i / kFixRows]);
+        key_fast2(v.x, v.y, K, k0, k1, amb[i / kFixRows]);
+        key_fast2(v.z, v.w, K, k2, k3, amb[i / kFixRows]);
         const uint32_t cc = code_pair_const(i & 1);
         *reinterpret_cast<uint2 *>(dst + base + i * kKeyPitch) =
             make_uint2(code_pair(prmt(k0, k1, 0x5410), cc), code_pair(prmt(k2, k3, 0x5410), cc));
@@ -1216,11 +1207,7 @@ __global__ void __launch_bounds__(k3Threads, kT3Blocks)
     K.clo = P.key_clo;
     K.chi = P.key_chi;
     K.H = P.H;
-    KeyPairConsts K2;
-    K2.nH = pk(K.nH, K.nH);
-    K2.clo = pk(K.clo, K.clo);
-    K2.chi = pk(K.chi, K.chi);
-    K2.magic = pk(kMagicKey, kMagicKey);
+    key_pairs(K);
     const int r0 = warp * k3Rows;  // buffer row of the row above the warp's first row
     const int b = blockIdx.y;
     const uint32_t hist_c = smem_u32(hist) - kKeyBase;
@@ -1242,7 +1229,7 @@ __global__ void __launch_bounds__(k3Threads, kT3Blocks)
             if (tid == 0) stage_plane(P, raw_s, bar, x0, y0, z0 - 1 + j, b);
             const bool late = !mbar_wait_bounded(bar, phase);
             phase ^= 1;
-            plane_keys_coded(raw, kb + j * kKeyPlane, K, K2, table, r0, lane, h_off, h_code);
+            plane_keys_coded(raw, kb + j * kKeyPlane, K, table, r0, lane, h_off, h_code);
             if (__syncthreads_or(late)) {  // block-uniform
                 failed = true;
                 break;
@@ -1283,7 +1270,7 @@ __global__ void __launch_bounds__(k3Threads, kT3Blocks)
         for (int z = z0; z < z1; ++z) {
             const bool late = !mbar_wait_bounded(bar, phase);
             phase ^= 1;
-            plane_keys_coded(raw, bn, K, K2, table, r0, lane, h_off, h_code);
+            plane_keys_coded(raw, bn, K, table, r0, lane, h_off, h_code);
             if (__syncthreads_or(late)) {  // block-uniform
                 failed = true;
                 break;
@@ -1495,6 +1482,9 @@ static cudaError_t launch_hard(const HardPlan &pl, cudaStream_t s)
     P.tasks_per_image = pl.ndim == 2 ? sh.tasks_x * sh.tasks_y : sh.tasks_per_image;
     P.ctas_per_image = (int)sh.blocks_per_image;
     P.direct = sh.direct ? 1 : 0;
+    // 2-D images of several blocks: each block adds the running sum of its histogram, so the
+    // call needs no scan launch
+    P.prefix = (pl.ndim == 2 && !P.direct && pl.scan && pl.sign == 1) ? 1 : 0;
     if (!P.direct && pl.zero_out) {
         const cudaError_t m =
             cudaMemsetAsync(pl.out, 0, sizeof(int64_t) * (size_t)(pl.batch * pl.H), s);
@@ -1517,7 +1507,7 @@ static cudaError_t launch_hard(const HardPlan &pl, cudaStream_t s)
         ecc_hard3d_kernel<T, CAP, SEARCH><<<grid, k3Threads, smem, s>>>(P);
     }
     cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess || !pl.scan || P.direct) return e;
+    if (e != cudaSuccess || !pl.scan || P.direct || P.prefix) return e;
     return hard_scan(pl.out, pl.H, pl.batch, s);
 }
 

@@ -57,6 +57,7 @@ struct HardParams {
     int64_t tasks_per_image;
     int ctas_per_image;
     int direct;  // 1: one block per image, which stores the running sum itself (no memset, scan)
+    int prefix;  // 1: each block adds the running sum of its histogram (no scan launch)
     float table[CAP + 2];  // f32: T_0..T_{H-1}, +inf, +inf;  u8: uint16 key pattern per byte
 };
 

@@ -40,6 +40,7 @@ struct KeyConsts {
     float nH;        // -H
     float clo, chi;  // H - 1/2 - E, H - 1/2 + E
     int H;
+    uint64_t nH2, clo2, chi2, magic2;  // nH, clo, chi and kMagicKey in both halves of a pair
 };
 
 // Fast key of one value: returns bits whose low half is the fp16 pattern of ceil(t - E), and ORs
@@ -51,6 +52,59 @@ __device__ __forceinline__ uint32_t key_fast(float v, const KeyConsts &K, uint32
     const float hi = __fadd_ru(fmaf(u, K.nH, K.chi), kMagicKey);
     amb |= __float_as_uint(lo) ^ __float_as_uint(hi);
     return __float_as_uint(lo);
+}
+
+// Packed fp32 pairs (sm_100-family f32x2 instructions; each element rounds as the scalar op does).
+__device__ __forceinline__ uint64_t pk(float a, float b)
+{
+    return (uint64_t)__float_as_uint(a) | ((uint64_t)__float_as_uint(b) << 32);
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add_rp(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rp.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t h2_fma(uint32_t a, uint32_t b, uint32_t c)
+{
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t h2_neg(uint32_t a)
+{
+    uint32_t d;
+    asm("neg.f16x2 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+
+// Fills the packed copies of the estimator constants.
+__device__ __forceinline__ void key_pairs(KeyConsts &K)
+{
+    K.nH2 = pk(K.nH, K.nH);
+    K.clo2 = pk(K.clo, K.clo);
+    K.chi2 = pk(K.chi, K.chi);
+    K.magic2 = pk(kMagicKey, kMagicKey);
+}
+
+// Estimated key patterns of two values (low halves 0x6400 + ceil(t - E), as key_fast); ORs into
+// `amb` a non-zero value when either estimate is ambiguous. The normalisation saturates value by
+// value; the rest runs on packed pairs.
+__device__ __forceinline__ void key_fast2(float v0, float v1, const KeyConsts &K, uint32_t &k0,
+                                          uint32_t &k1, uint32_t &amb)
+{
+    const uint64_t u = pk(__saturatef(fmaf(v0, K.a, K.b)), __saturatef(fmaf(v1, K.a, K.b)));
+    const uint64_t lo = f2_add_rp(f2_fma(u, K.nH2, K.clo2), K.magic2);
+    const uint64_t hi = f2_add_rp(f2_fma(u, K.nH2, K.chi2), K.magic2);
+    k0 = (uint32_t)lo;
+    k1 = (uint32_t)(lo >> 32);
+    amb |= (k0 ^ (uint32_t)hi) | (k1 ^ (uint32_t)(hi >> 32));
 }
 
 // Exact key given the fast estimate `lo_bits` (any value whose estimate window holds the key):
