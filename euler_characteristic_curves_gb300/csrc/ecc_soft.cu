@@ -57,8 +57,7 @@ static_assert(SoftTile<2>::X * SoftTile<2>::Y == kTileCap, "2-D tile size");
 static_assert(SoftTile<3>::X * SoftTile<3>::Y * SoftTile<3>::Z == kTileCap, "3-D tile size");
 constexpr int kPrepThreads = 256;
 constexpr int64_t kPrepBlocks = 4096;      // prep grid size aimed at when directions are grouped
-constexpr int kSoftThreads = 64;           // each thread owns two thresholds per pass
-constexpr int kKPerPass = 2 * kSoftThreads;
+constexpr int kSoftThreads = 64;           // two warps per block
 constexpr int kChunk = 256;                // entries staged in shared memory at a time
 // The backward kernel stages half as many, so that its shared memory (and registers) let a
 // full wave of blocks be resident on a 64-image batch of 256^2 images.
@@ -608,81 +607,144 @@ __device__ __forceinline__ void kahan_fma2(f32x2 &s, f32x2 &nc, f32x2 a, f32x2 b
     s = t;
 }
 
-// Forward inner loop over staged entries for the thread's two thresholds, direct form (tiles
-// whose exponents leave the factorised range). The integer parts w0, w1 are sums of small
-// integers (|w| <= 8 kTileCap < 2^24), exact in fp32.
-__device__ __forceinline__ void fwd_loop_direct(const float4 *sh, int m_ent, const KState &s0,
-                                                const KState &s1, float l2, float &w0, float &w1,
-                                                float &a0, float &c0, float &a1, float &c1)
+// Threshold passes of the forward and backward kernels: lane l of a warp owns thresholds
+// k = kb + l + 32 j, j = 0 .. 3 (two packed pairs: j = 0, 1 and j = 2, 3), so one warp covers
+// a pass of kWarpK thresholds and reads each staged entry once for four of them; the block's
+// warps share the entries of a tile out between them.
+constexpr int kLaneK = 4;
+constexpr int kWarpK = kLaneK * kWarp;  // 128
+constexpr int kSoftWarps = kSoftThreads / kWarp;
+
+struct Lane4 {
+    KState s[kLaneK];
+    bool ok;  // all four in the factorised range
+};
+__device__ __forceinline__ Lane4 lane_thresholds(const float *__restrict__ tau, int kb, int lane,
+                                                 int K, float l2, float m)
 {
-#pragma unroll 4
-    for (int i = 0; i < m_ent; ++i) {
+    Lane4 t;
+    t.ok = true;
+#pragma unroll
+    for (int j = 0; j < kLaneK; ++j) {
+        t.s[j] = k_state(tau, kb + lane + kWarp * j, K, l2, m);
+        t.ok = t.ok && t.s[j].ok;
+    }
+    return t;
+}
+
+// Sums of the forward for a lane's four thresholds: integer parts w, Kahan sums a (compensation
+// carried negated in nc) of the small parts; pairs (j = 0, 1) and (j = 2, 3).
+struct FwdAcc {
+    f32x2 w[2], a[2], nc[2];
+};
+
+// Forward over the staged entries i = first, first + step, ... < m_ent, factorised form (the same
+// per-term arithmetic as the scalar form: e = E F_k, r = min(e, 1) / (1 + e), w += [e <= 1] c,
+// Kahan over -+c r).
+// The below-threshold flag enters as a float b (1.0 / 0.0, one set instruction on the ALU pipe)
+// through packed fused multiply-adds on the FMA pipe, w += b c and the small part's coefficient
+// c (1 - 2 b) = fma(b, -2 c, c), instead of a compare and two selects on the ALU pipe, which
+// this loop saturates. Each value is exact (c, 2c and their sums are small integers), so the
+// sums are the same bits as the select form.
+__device__ __forceinline__ void fwd_loop4_packed(const float4 *sh, int first, int step,
+                                                 int m_ent, const f32x2 *F, FwdAcc &acc)
+{
+#pragma unroll 2
+    for (int i = first; i < m_ent; i += step) {
         const float4 en = sh[i];
         const float cf = entry_cf(en);
-        bool b0, b1;
-        const float r0 = small_sigma_direct(en, s0.tau, l2, b0);
-        const float r1 = small_sigma_direct(en, s1.tau, l2, b1);
-        w0 += b0 ? cf : 0.0f;
-        w1 += b1 ? cf : 0.0f;
-        kahan_fma(a0, c0, b0 ? -cf : cf, r0);
-        kahan_fma(a1, c1, b1 ? -cf : cf, r1);
+        const f32x2 c2 = pk2(cf, cf), m2c2 = pk2(-2.0f * cf, -2.0f * cf);
+        const f32x2 E = pk2(en.x, en.x);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float e0, e1, d0, d1;
+            const f32x2 e = mul2(E, F[h]);
+            upk2(e, e0, e1);
+            upk2(add2(e, pk2(1.0f, 1.0f)), d0, d1);
+            const f32x2 b = pk2(e0 <= 1.0f ? 1.0f : 0.0f, e1 <= 1.0f ? 1.0f : 0.0f);
+            const f32x2 r =
+                mul2(pk2(fminf(e0, 1.0f), fminf(e1, 1.0f)), pk2(rcp_approx(d0), rcp_approx(d1)));
+            acc.w[h] = fma2(b, c2, acc.w[h]);
+            kahan_fma2(acc.a[h], acc.nc[h], fma2(b, m2c2, c2), r);
+        }
     }
 }
 
-// The factorised forward loop with both thresholds in packed pairs (the same bits as the scalar
-// form: e = E F_k, r = min(e, 1) / (1 + e), w += [e <= 1] c, Kahan over -+c r).
-__device__ __forceinline__ void fwd_loop_packed(const float4 *sh, int m_ent, const KState &s0,
-                                                const KState &s1, float &w0, float &w1,
-                                                float &a0, float &c0, float &a1, float &c1)
+// The same, direct form (tiles whose exponents leave the factorised range).
+__device__ __forceinline__ void fwd_loop4_direct(const float4 *sh, int first, int step,
+                                                 int m_ent, const Lane4 &t, float l2,
+                                                 float *w, float *a, float *c)
 {
-    const f32x2 F = pk2(s0.F, s1.F);
-    f32x2 w = pk2(w0, w1), a = pk2(a0, a1), nc = pk2(-c0, -c1);
-#pragma unroll 4
-    for (int i = 0; i < m_ent; ++i) {
+#pragma unroll 2
+    for (int i = first; i < m_ent; i += step) {
         const float4 en = sh[i];
         const float cf = entry_cf(en);
-        bool b0, b1;
-        const f32x2 r = small_sigma_fact2(en.x, F, b0, b1);
-        w = add2(w, pk2(b0 ? cf : 0.0f, b1 ? cf : 0.0f));
-        kahan_fma2(a, nc, pk2(b0 ? -cf : cf, b1 ? -cf : cf), r);
+#pragma unroll
+        for (int j = 0; j < kLaneK; ++j) {
+            bool bj;
+            const float r = small_sigma_direct(en, t.s[j].tau, l2, bj);
+            w[j] += bj ? cf : 0.0f;
+            kahan_fma(a[j], c[j], bj ? -cf : cf, r);
+        }
     }
-    float n0, n1;
-    upk2(w, w0, w1);
-    upk2(a, a0, a1);
-    upk2(nc, n0, n1);
-    c0 = -n0;
-    c1 = -n1;
 }
 
-// Forward: one block per (tile, image); thread t owns thresholds k = kb + t and kb + t + 64.
+// Forward: one block per unit (tile, image x direction). Each warp runs a pass of kWarpK
+// thresholds over every other staged entry (warp w: entries w, w + kSoftWarps, ...); the warps'
+// sums meet in shared memory, in a fixed order, as fp64 partials per (unit, threshold).
 __global__ void __launch_bounds__(kSoftThreads) soft_fwd_kernel(
     const float *__restrict__ tau, int K, float l2, const int *__restrict__ counts,
     const float4 *__restrict__ entries, double *__restrict__ part, int64_t tiles)
 {
     __shared__ float4 sh[kChunk];
+    __shared__ double wsum[kSoftWarps][kWarpK];
     const int64_t unit = blockIdx.y * tiles + blockIdx.x;
     const int cnt = counts[unit];
     const int n = cnt & (kTileFlagDirect - 1);
     const float4 *__restrict__ list = entries + unit * (int64_t)kTileCap;
     const float m = tau_midpoint(tau, K);
-    for (int kb = 0; kb < K; kb += kKPerPass) {
-        const int k0 = kb + threadIdx.x, k1 = k0 + kSoftThreads;
-        const KState s0 = k_state(tau, k0, K, l2, m), s1 = k_state(tau, k1, K, l2, m);
-        const bool fact = __syncthreads_and(s0.ok && s1.ok && !(cnt & kTileFlagDirect));
-        float w0 = 0.f, w1 = 0.f;
-        float a0 = 0.f, c0 = 0.f, a1 = 0.f, c1 = 0.f;
+    const int lane = threadIdx.x & (kWarp - 1), warp = threadIdx.x >> 5;
+    for (int kb = 0; kb < K; kb += kWarpK) {
+        const Lane4 t = lane_thresholds(tau, kb, lane, K, l2, m);
+        const bool fact = __syncthreads_and(t.ok && !(cnt & kTileFlagDirect));
+        float w[kLaneK] = {0.f, 0.f, 0.f, 0.f}, a[kLaneK] = {0.f, 0.f, 0.f, 0.f};
+        float c[kLaneK] = {0.f, 0.f, 0.f, 0.f};
+        FwdAcc acc;
+        const f32x2 F[2] = {pk2(t.s[0].F, t.s[1].F), pk2(t.s[2].F, t.s[3].F)};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) acc.w[h] = acc.a[h] = acc.nc[h] = 0ull;
         for (int e0 = 0; e0 < n; e0 += kChunk) {
             const int m_ent = min(kChunk, n - e0);
             __syncthreads();
             for (int i = threadIdx.x; i < m_ent; i += kSoftThreads) sh[i] = list[e0 + i];
             __syncthreads();
             if (fact)
-                fwd_loop_packed(sh, m_ent, s0, s1, w0, w1, a0, c0, a1, c1);
+                fwd_loop4_packed(sh, warp, kSoftWarps, m_ent, F, acc);
             else
-                fwd_loop_direct(sh, m_ent, s0, s1, l2, w0, w1, a0, c0, a1, c1);
+                fwd_loop4_direct(sh, warp, kSoftWarps, m_ent, t, l2, w, a, c);
         }
-        if (k0 < K) part[unit * K + k0] = (double)w0 + ((double)a0 - (double)c0);
-        if (k1 < K) part[unit * K + k1] = (double)w1 + ((double)a1 - (double)c1);
+        if (fact) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                float n0, n1;
+                upk2(acc.w[h], w[2 * h], w[2 * h + 1]);
+                upk2(acc.a[h], a[2 * h], a[2 * h + 1]);
+                upk2(acc.nc[h], n0, n1);
+                c[2 * h] = -n0;
+                c[2 * h + 1] = -n1;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kLaneK; ++j)
+            wsum[warp][lane + kWarp * j] = (double)w[j] + ((double)a[j] - (double)c[j]);
+        __syncthreads();
+        for (int k = threadIdx.x; k < kWarpK; k += kSoftThreads) {
+            double v = 0.0;
+#pragma unroll
+            for (int ww = 0; ww < kSoftWarps; ++ww) v += wsum[ww][k];
+            if (kb + k < K) part[unit * K + kb + k] = v;
+        }
+        __syncthreads();  // wsum is read before the next pass writes it
     }
 }
 
@@ -725,64 +787,66 @@ __global__ void __launch_bounds__(kFwdRedMaxWarps * kWarp) soft_fwd_reduce_kerne
     }
 }
 
-// Backward group of eight staged entries for the thread's two thresholds (direct form):
-//   dtau partial[k] += c_p w_pk,   w = s (1 - s) = r (1 - r)      (times lambda g_k at the end)
-//   row sum (per entry, over the warp's thresholds) of g_k w_pk   (for dX_p)
-// Each lane writes its eight values to a shared 8 x 32 block; lane l sums eight entries of row
-// l / 4, and two xor shuffles combine the four lanes of the row.
-__device__ __forceinline__ void bwd_group_direct(const float4 *en8, const KState &s0,
-                                                 const KState &s1, float g0, float g1, float l2,
-                                                 float &a0, float &c0, float &a1, float &c1,
-                                                 float (*qw)[kWarp], int lane, float &row_sum)
+// Backward over one group of kGroup staged entries for a lane's four thresholds: w = r - r^2
+// per term, the dtau Kahan sums over c w, and the entry's sum over the warp's thresholds of
+// g_k w (qw: this warp's [kGroup][32] transpose buffer). Returns, in lanes 4e .. 4e + 3, the sum
+// over all kWarpK thresholds of the pass for entry e of the group.
+__device__ __forceinline__ float group_row_sum(float (*qw)[kWarp], int lane)
 {
-#pragma unroll
-    for (int j = 0; j < kGroup; ++j) {
-        const float4 en = en8[j];
-        const float cf = entry_cf(en);
-        bool b0, b1;
-        const float r0 = small_sigma_direct(en, s0.tau, l2, b0);
-        const float r1 = small_sigma_direct(en, s1.tau, l2, b1);
-        const float w0 = fmaf(-r0, r0, r0), w1 = fmaf(-r1, r1, r1);
-        kahan_fma(a0, c0, cf, w0);
-        kahan_fma(a1, c1, cf, w1);
-        qw[j][lane] = fmaf(g0, w0, g1 * w1);
-    }
     __syncwarp();
     const float4 *rowp = reinterpret_cast<const float4 *>(&qw[lane >> 2][(lane & 3) * 8]);
     const float4 x = rowp[0], y = rowp[1];
     float s = ((x.x + x.y) + (x.z + x.w)) + ((y.x + y.y) + (y.z + y.w));
     s += __shfl_xor_sync(kFull, s, 1);
     s += __shfl_xor_sync(kFull, s, 2);
-    row_sum = s;  // the warp's partial of sum_k g_k w for entry lane / 4 of the group
     __syncwarp();
+    return s;
 }
 
-// The factorised backward group with both thresholds in packed pairs (the same bits as the
-// scalar form); the dtau sums stay packed in (a, nc) across groups.
-__device__ __forceinline__ void bwd_group_packed(const float4 *en8, f32x2 F, float g0, float g1,
-                                                 f32x2 &a, f32x2 &nc, float (*qw)[kWarp],
-                                                 int lane, float &row_sum)
+__device__ __forceinline__ float bwd_group4_packed(const float4 *en8, const f32x2 *F,
+                                                   const f32x2 *g, f32x2 *a, f32x2 *nc,
+                                                   float (*qw)[kWarp], int lane)
 {
 #pragma unroll
     for (int j = 0; j < kGroup; ++j) {
         const float4 en = en8[j];
         const float cf = entry_cf(en);
-        bool b0, b1;
-        const f32x2 r = small_sigma_fact2(en.x, F, b0, b1);
-        const f32x2 w = fma2(sub2(0ull, r), r, r);  // r - r^2, one rounding as fmaf(-r, r, r)
-        kahan_fma2(a, nc, pk2(cf, cf), w);
-        float w0, w1;
-        upk2(w, w0, w1);
-        qw[j][lane] = fmaf(g0, w0, g1 * w1);
+        f32x2 gw = 0ull;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            bool b0, b1;
+            const f32x2 r = small_sigma_fact2(en.x, F[h], b0, b1);
+            const f32x2 w = fma2(sub2(0ull, r), r, r);  // r - r^2, one rounding as fmaf(-r, r, r)
+            kahan_fma2(a[h], nc[h], pk2(cf, cf), w);
+            gw = fma2(g[h], w, gw);
+        }
+        float q0, q1;
+        upk2(gw, q0, q1);
+        qw[j][lane] = q0 + q1;
     }
-    __syncwarp();
-    const float4 *rowp = reinterpret_cast<const float4 *>(&qw[lane >> 2][(lane & 3) * 8]);
-    const float4 x = rowp[0], y = rowp[1];
-    float s = ((x.x + x.y) + (x.z + x.w)) + ((y.x + y.y) + (y.z + y.w));
-    s += __shfl_xor_sync(kFull, s, 1);
-    s += __shfl_xor_sync(kFull, s, 2);
-    row_sum = s;
-    __syncwarp();
+    return group_row_sum(qw, lane);
+}
+
+__device__ __forceinline__ float bwd_group4_direct(const float4 *en8, const Lane4 &t,
+                                                   const float *g, float l2, float *a, float *c,
+                                                   float (*qw)[kWarp], int lane)
+{
+#pragma unroll
+    for (int j = 0; j < kGroup; ++j) {
+        const float4 en = en8[j];
+        const float cf = entry_cf(en);
+        float q = 0.0f;
+#pragma unroll
+        for (int k = 0; k < kLaneK; ++k) {
+            bool bk;
+            const float r = small_sigma_direct(en, t.s[k].tau, l2, bk);
+            const float w = fmaf(-r, r, r);
+            kahan_fma(a[k], c[k], cf, w);
+            q = fmaf(g[k], w, q);
+        }
+        qw[j][lane] = q;
+    }
+    return group_row_sum(qw, lane);
 }
 
 // Backward: one block per (tile, image, direction), or, when the image gradient is wanted, one
@@ -801,7 +865,7 @@ __global__ void __launch_bounds__(kSoftThreads) soft_bwd_kernel(
     constexpr int NW = kSoftThreads / kWarp;
     __shared__ __align__(16) float4 sh[kBwdChunk];
     __shared__ __align__(16) float qbuf[NW][kGroup][kWarp];
-    __shared__ float red[NW][kBwdChunk];
+    __shared__ double tsum[NW][kWarpK];
     __shared__ float dxs[kTileCap];
     extern __shared__ float gacc[];  // kTileCap floats, present only when grad_img is wanted
     __shared__ double scal_red[NW][kScal];
@@ -838,15 +902,21 @@ __global__ void __launch_bounds__(kSoftThreads) soft_bwd_kernel(
         __syncthreads();  // the previous direction is done with dxs
         for (int i = threadIdx.x; i < n; i += kSoftThreads) dxs[i] = 0.0f;
 
-        for (int kb = 0; kb < K; kb += kKPerPass) {
-            const int k0 = kb + threadIdx.x, k1 = k0 + kSoftThreads;
-            const KState s0 = k_state(tau, k0, K, l2, m), s1 = k_state(tau, k1, K, l2, m);
-            const float g0 = (k0 < K) ? __ldg(grad_out + bj * K + k0) : 0.0f;
-            const float g1 = (k1 < K) ? __ldg(grad_out + bj * K + k1) : 0.0f;
-            const bool fact = __syncthreads_and(s0.ok && s1.ok && !(cnt & kTileFlagDirect));
-            float a0 = 0.f, c0 = 0.f, a1 = 0.f, c1 = 0.f;
-            const f32x2 F = pk2(s0.F, s1.F);
-            f32x2 ap = 0ull, ncp = 0ull;  // packed dtau sums (+0.0f pairs) of the factorised form
+        for (int kb = 0; kb < K; kb += kWarpK) {
+            // lane l: thresholds kb + l + 32 j; warp w: groups w, w + NW, ... of each chunk, so
+            // every entry's sum over the pass's thresholds is one warp's (no cross-warp sum)
+            const Lane4 t = lane_thresholds(tau, kb, lane, K, l2, m);
+            float g[kLaneK];
+#pragma unroll
+            for (int k = 0; k < kLaneK; ++k) {
+                const int kk = kb + lane + kWarp * k;
+                g[k] = kk < K ? __ldg(grad_out + bj * K + kk) : 0.0f;
+            }
+            const bool fact = __syncthreads_and(t.ok && !(cnt & kTileFlagDirect));
+            float a[kLaneK] = {0.f, 0.f, 0.f, 0.f}, c[kLaneK] = {0.f, 0.f, 0.f, 0.f};
+            const f32x2 F[2] = {pk2(t.s[0].F, t.s[1].F), pk2(t.s[2].F, t.s[3].F)};
+            const f32x2 gp[2] = {pk2(g[0], g[1]), pk2(g[2], g[3])};
+            f32x2 ap[2] = {0ull, 0ull}, ncp[2] = {0ull, 0ull};  // packed dtau sums (factorised)
             for (int e0 = 0; e0 < n; e0 += kBwdChunk) {
                 const int m_ent = min(kBwdChunk, n - e0);
                 __syncthreads();
@@ -855,35 +925,38 @@ __global__ void __launch_bounds__(kSoftThreads) soft_bwd_kernel(
                     sh[i] = (i < m_ent) ? list[e0 + i]
                                         : make_float4(0.f, 0.f, 0.f, __int_as_float(kPadWord));
                 __syncthreads();
-                for (int gi = 0; gi * kGroup < m_ent; ++gi) {
-                    float rs;
-                    if (fact)
-                        bwd_group_packed(sh + gi * kGroup, F, g0, g1, ap, ncp, qbuf[warp], lane,
-                                         rs);
-                    else
-                        bwd_group_direct(sh + gi * kGroup, s0, s1, g0, g1, l2, a0, c0, a1, c1,
-                                         qbuf[warp], lane, rs);
-                    if ((lane & 3) == 0) red[warp][gi * kGroup + (lane >> 2)] = rs;
-                }
-                __syncthreads();
-                for (int i = threadIdx.x; i < m_ent; i += kSoftThreads) {
-                    float q = 0.0f;
-#pragma unroll
-                    for (int w2 = 0; w2 < NW; ++w2) q += red[w2][i];
-                    dxs[e0 + i] += q;
+                for (int gi = warp; gi * kGroup < m_ent; gi += NW) {
+                    const float rs =
+                        fact ? bwd_group4_packed(sh + gi * kGroup, F, gp, ap, ncp, qbuf[warp], lane)
+                             : bwd_group4_direct(sh + gi * kGroup, t, g, l2, a, c, qbuf[warp],
+                                                 lane);
+                    // padding entries (index n and above) add 0 to unused slots
+                    if ((lane & 3) == 0) dxs[e0 + gi * kGroup + (lane >> 2)] += rs;
                 }
             }
             if (fact) {
-                float n0, n1;
-                upk2(ap, a0, a1);
-                upk2(ncp, n0, n1);
-                c0 = -n0;
-                c1 = -n1;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    float n0, n1;
+                    upk2(ap[h], a[2 * h], a[2 * h + 1]);
+                    upk2(ncp[h], n0, n1);
+                    c[2 * h] = -n0;
+                    c[2 * h + 1] = -n1;
+                }
             }
-            if (k0 < K)
-                part[k0 * units + unit] = (double)lambda * (double)g0 * ((double)a0 - (double)c0);
-            if (k1 < K)
-                part[k1 * units + unit] = (double)lambda * (double)g1 * ((double)a1 - (double)c1);
+#pragma unroll
+            for (int k = 0; k < kLaneK; ++k)
+                tsum[warp][lane + kWarp * k] = (double)a[k] - (double)c[k];
+            __syncthreads();
+            for (int k = threadIdx.x; k < kWarpK; k += kSoftThreads) {
+                if (kb + k >= K) continue;
+                double v = 0.0;
+#pragma unroll
+                for (int ww = 0; ww < NW; ++ww) v += tsum[ww][k];
+                const double gk = (double)__ldg(grad_out + bj * K + kb + k);
+                part[(kb + k) * units + unit] = (double)lambda * gk * v;
+            }
+            __syncthreads();  // tsum and dxs are read before the next pass writes them
         }
         __syncthreads();
 
