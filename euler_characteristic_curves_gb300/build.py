@@ -18,6 +18,10 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libecc_gb300.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
+# The debug variant: the same sources with ECC_DEBUG_BOUNDS=1 (bounds checks that record a bit
+# in the device error word and skip the access), loaded by the binding when ECC_DEBUG=1.
+DEBUG_DIR = os.path.join(HERE, "_build_debug")
+DEBUG_LIB_PATH = os.path.join(DEBUG_DIR, "libecc_gb300_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
@@ -42,23 +46,27 @@ def _deps():
     return deps
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def up_to_date(path: str = LIB_PATH) -> bool:
+    if not os.path.exists(path):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile and link the library; returns its path. Skips work when nothing changed."""
-    if not force and up_to_date():
-        return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug: bool = False) -> str:
+    """Compile and link the library (``debug``: the bounds-checked variant); returns its path.
+    Skips work when nothing changed."""
+    build_dir, lib_path = (DEBUG_DIR, DEBUG_LIB_PATH) if debug else (BUILD_DIR, LIB_PATH)
+    if debug:
+        extra_flags = (*extra_flags, "-DECC_DEBUG_BOUNDS=1")
+    if not force and up_to_date(lib_path):
+        return lib_path
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
     objs = []
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra_flags, "-I", INCLUDE, "-I", CSRC, "-c", src,
                "-o", obj]
         res = subprocess.run(cmd, capture_output=True, text=True)
@@ -70,17 +78,18 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=min(8, len(sources()))) as ex:
         objs = list(ex.map(compile_one, sources()))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", *objs, "-o", tmp]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{res.stdout}\n{res.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
     import sys
 
     print(build(force="--force" in sys.argv, verbose=True,
-                extra_flags=["-Xptxas", "-v"] if "--ptxas-v" in sys.argv else []))
+                extra_flags=["-Xptxas", "-v"] if "--ptxas-v" in sys.argv else [],
+                debug="--debug" in sys.argv))

@@ -105,21 +105,44 @@ const char *ecc_status_str(int status)
     case ECC_ECUDA: return "ECC_ECUDA: CUDA error";
     case ECC_ERANGE: return "ECC_ERANGE: size above the library maximum";
     case ECC_ETIMEOUT: return "ECC_ETIMEOUT: a kernel gave up waiting for its own staged copy";
+    case ECC_EBOUNDS: return "ECC_EBOUNDS: a debug-build bounds check failed (access skipped)";
     default: return "ECC: unknown status";
     }
 }
 
 int ecc_version(void) { return 10100; }
 
+// The OR of the hard and soft device error words (read, and cleared when asked); -1 on failure.
+static int64_t device_error_bits(int clear)
+{
+    unsigned *words[2] = {nullptr, nullptr};
+    if (hard_error_word(&words[0]) != cudaSuccess || soft_error_word(&words[1]) != cudaSuccess)
+        return -1;
+    unsigned bits = 0;
+    for (unsigned *w : words) {
+        unsigned v = 0;
+        if (cudaMemcpy(&v, w, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return -1;
+        if (clear && v != 0 && cudaMemset(w, 0, sizeof v) != cudaSuccess) return -1;
+        bits |= v;
+    }
+    return bits;
+}
+
 int ecc_device_status(int clear)
 {
-    int *word = nullptr;
-    if (wait_error_word(&word) != cudaSuccess) return ECC_ECUDA;
-    int v = 0;
-    if (cudaMemcpy(&v, word, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return ECC_ECUDA;
-    if (clear && v != 0 && cudaMemset(word, 0, sizeof v) != cudaSuccess) return ECC_ECUDA;
-    return v != 0 ? ECC_ETIMEOUT : ECC_OK;
+    const int64_t bits = device_error_bits(clear);
+    if (bits < 0) return ECC_ECUDA;
+    if (bits & kErrWaitTimeout) return ECC_ETIMEOUT;
+    return bits != 0 ? ECC_EBOUNDS : ECC_OK;
 }
+
+int64_t ecc_device_error_bits(int clear)
+{
+    const int64_t bits = device_error_bits(clear);
+    return bits < 0 ? ECC_ECUDA : bits;
+}
+
+int ecc_debug_build(void) { return ECC_DEBUG_BOUNDS ? 1 : 0; }
 
 // Sizes of a hard-ECC call: the checks ecc_hard makes on its shape arguments, and the plan's
 // extents on success.

@@ -39,6 +39,17 @@
 
 namespace ecc {
 
+__device__ unsigned g_hard_error;  // device error word of the hard kernels (DeviceErrorBit)
+
+// A pair of key patterns (0x6400 + k each) and its contributions into the block histogram; the
+// debug build first checks both bins against [0, H].
+__device__ __forceinline__ void hist_pair_h(uint32_t keys, uint32_t cv, uint32_t hist_s, int H)
+{
+    const int lo = (int)(keys & 0xffffu) - (int)kKeyBase, hi = (int)(keys >> 16) - (int)kKeyBase;
+    if (bounds_ok(&g_hard_error, lo >= 0 && lo <= H && hi >= 0 && hi <= H, kErrHardBin))
+        hist_pair(keys, cv, hist_s);
+}
+
 constexpr int kHardThreads = 256;
 constexpr int kHardWarps = kHardThreads / kWarp;
 constexpr int kStrip = 128;  // columns per warp strip / block tile
@@ -326,7 +337,8 @@ template <bool FULL>
 __device__ __forceinline__ Raw<float> next_row(RowCursor<float> &rc, const Cols &c)
 {
     Raw<float> out;
-    if ((unsigned)rc.r < (unsigned)rc.rlim) {  // warp-uniform
+    if ((unsigned)rc.r < (unsigned)rc.rlim &&  // warp-uniform
+        bounds_ok(&g_hard_error, !FULL || c.x + 4 <= rc.W, kErrHardRow)) {
         if (FULL) {
             const float4 q = __ldg(reinterpret_cast<const float4 *>(rc.own));
             out.v[0] = q.x;
@@ -354,7 +366,8 @@ template <bool FULL>
 __device__ __forceinline__ Raw<uint8_t> next_row(RowCursor<uint8_t> &rc, const Cols &c)
 {
     Raw<uint8_t> out;
-    if ((unsigned)rc.r < (unsigned)rc.rlim) {  // warp-uniform
+    if ((unsigned)rc.r < (unsigned)rc.rlim &&  // warp-uniform
+        bounds_ok(&g_hard_error, !FULL || c.x + 4 <= rc.W, kErrHardRow)) {
         if (FULL) {
             out.bytes = __ldg(reinterpret_cast<const unsigned int *>(rc.own));
         } else {
@@ -402,8 +415,8 @@ __device__ __forceinline__ void band2d(const T *__restrict__ img, int Hy, int W,
         QS = next_row<FULL>(rc, c);                                                         \
         uint32_t c0, c1;                                                                    \
         c2_quad<SAT>(ka, kb, kd, kBias, Sp0, Sp1, c0, c1);                                  \
-        hist_pair(kb.own0, c0, hist_s);                                            \
-        hist_pair(kb.own1, c1, hist_s);                                            \
+        hist_pair_h(kb.own0, c0, hist_s, K.H);                                     \
+        hist_pair_h(kb.own1, c1, hist_s, K.H);                                     \
         ka = kb;                                                                            \
         kb = kd;                                                                            \
         ++y;                                                                                \
@@ -886,10 +899,12 @@ __global__ void __launch_bounds__(k3Threads, ECC_3D_MIN_BLOCKS) ecc_hard3d_kerne
                 c2_quad<SAT, !SAT>(c0, c1, c2, kBias, ss0, ss1, cs0, cs1);
                 const KeyRow Md = max_rows(c2, n2);
                 c2_quad<SAT, false>(Ma, Mb, Md, kPlain, sm0, sm1, cn0, cn1);
-                hist_pair(c1.own0, fold3<SAT>(cs0, cn0, cm[i][0], n1.own0, below[i][0], c1.own0),
-                          hist_s);
-                hist_pair(c1.own1, fold3<SAT>(cs1, cn1, cm[i][1], n1.own1, below[i][1], c1.own1),
-                          hist_s);
+                hist_pair_h(c1.own0,
+                            fold3<SAT>(cs0, cn0, cm[i][0], n1.own0, below[i][0], c1.own0),
+                            hist_s, K.H);
+                hist_pair_h(c1.own1,
+                            fold3<SAT>(cs1, cn1, cm[i][1], n1.own1, below[i][1], c1.own1),
+                            hist_s, K.H);
                 cm[i][0] = cn0;
                 cm[i][1] = cn1;
                 below[i][0] = c1.own0;
@@ -951,13 +966,12 @@ constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per mbarrier wait
 static_assert(kRawBytes % 16 == 0 && kKeyRingBytes % 16 == 0, "shared layout");
 static_assert(kStrip + 8 == kRawPitch, "a staged row starts 4 columns left of the tile");
 
-__device__ int g_wait_error;  // set by a block whose staged copy did not arrive in time
 
 struct Hard3TmaParams {
     CUtensorMap map;  // [batch][D][Hy][W] float32; box 136 x 34 x 1 x 1; NaN outside
     int64_t *out;
     int64_t tasks_per_image;
-    int D, H, sign;
+    int D, Hy, W, H, sign;
     int rows_per_task, tasks_x, tasks_y, ctas_per_image;
     float key_a, key_b, key_clo, key_chi;
     float table[kCodedMaxBins + 2];
@@ -1004,6 +1018,8 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
 __device__ __forceinline__ void stage_plane(const Hard3TmaParams &P, uint32_t raw_s, uint32_t bar,
                                             int x0, int y0, int z, int b)
 {
+    // (debug build) the tile starts inside the volume; planes -1 and D are the fill planes
+    bounds_ok(&g_hard_error, x0 < P.W && y0 < P.Hy && z >= -1 && z <= P.D, kErrTmaTile);
     // the block's earlier reads of the buffer (generic proxy) before the copy's writes
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
@@ -1152,8 +1168,12 @@ __device__ __forceinline__ void c2_quad_coded(const KeyRow &a, const KeyRow &b, 
 
 // Histogram update for a pair of coded keys: bin (pattern - 0x6400) >> 2, i.e. the byte offset
 // (pattern & 0xfffc) from hist_c = (shared address of the histogram) - 0x6400.
-__device__ __forceinline__ void hist_pair_coded(uint32_t keys, uint32_t cv, uint32_t hist_c)
+__device__ __forceinline__ void hist_pair_coded(uint32_t keys, uint32_t cv, uint32_t hist_c,
+                                                int H)
 {
+    const int lo = ((int)(keys & 0xffffu) - (int)kKeyBase) >> 2;
+    const int hi = ((int)(keys >> 16) - (int)kKeyBase) >> 2;
+    if (!bounds_ok(&g_hard_error, lo >= 0 && lo <= H && hi >= 0 && hi <= H, kErrHardBin)) return;
     red_shared_add(hist_c + (keys & 0xfffcu), sext_byte0(cv));
     red_shared_add(hist_c + ((keys >> 16) & 0xfffcu), sext_byte2(cv));
 }
@@ -1291,9 +1311,9 @@ __global__ void __launch_bounds__(k3Threads, kT3Blocks)
                 const KeyRow Md = max_rows(c2, n2);
                 c2_quad_coded<true>(Ma, Mb, Md, sm0, sm1, nc0, nc1);
                 hist_pair_coded(c1.own0, fold_carry(cs0, nc0, c1.own0, n1.own0, q[i][0]),
-                                hist_c);
+                                hist_c, P.H);
                 hist_pair_coded(c1.own1, fold_carry(cs1, nc1, c1.own1, n1.own1, q[i][1]),
-                                hist_c);
+                                hist_c, P.H);
                 c0 = c1;
                 c1 = c2;
                 n1 = n2;
@@ -1309,7 +1329,7 @@ __global__ void __launch_bounds__(k3Threads, kT3Blocks)
     if (failed) {  // block-uniform: a copy did not arrive in time
         if (tid == 0) {
             mbar_wait_bounded(bar, phase ^ 1u);  // the copy that timed out, if it still lands
-            atomicOr(&g_wait_error, 1);
+            atomicOr(&g_hard_error, kErrWaitTimeout);
         }
         return;
     }
@@ -1564,6 +1584,8 @@ static cudaError_t launch_hard3d_tma(const HardPlan &pl, cudaStream_t s)
     P.out = pl.out;
     P.tasks_per_image = sh.tasks_per_image;
     P.D = (int)pl.D;
+    P.Hy = (int)pl.Hy;
+    P.W = (int)pl.W;
     P.H = pl.H;
     P.sign = pl.sign;
     P.rows_per_task = (int)sh.rows_per_task;
@@ -1593,9 +1615,9 @@ static cudaError_t launch_hard3d_tma(const HardPlan &pl, cudaStream_t s)
     return hard_scan(pl.out, pl.H, pl.batch, s);
 }
 
-cudaError_t wait_error_word(int **p)
+cudaError_t hard_error_word(unsigned **p)
 {
-    return cudaGetSymbolAddress(reinterpret_cast<void **>(p), g_wait_error);
+    return cudaGetSymbolAddress(reinterpret_cast<void **>(p), g_hard_error);
 }
 
 cudaError_t hard_scan(int64_t *out, int H, int64_t batch, cudaStream_t s)

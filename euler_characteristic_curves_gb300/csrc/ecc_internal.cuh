@@ -25,6 +25,35 @@ namespace ecc {
 constexpr int kWarp = 32;
 constexpr unsigned kFull = 0xffffffffu;
 
+// Device error word bits. Bit 0: a kernel gave up waiting for its own staged copy (every build).
+// The others are set only by the debug build (ECC_DEBUG_BOUNDS = 1, the library's debug variant),
+// which checks data-dependent indices before it uses them and skips the access when a check
+// fails (no trap): a histogram bin outside [0, H], a global row or column outside the grid, a
+// staged plane's tile outside the volume, a soft-list slot or location outside its tile, a soft
+// global index outside the image. Each translation unit keeps its own word; ecc_device_status()
+// reads them all.
+#ifndef ECC_DEBUG_BOUNDS
+#define ECC_DEBUG_BOUNDS 0
+#endif
+enum DeviceErrorBit : unsigned {
+    kErrWaitTimeout = 1u << 0,
+    kErrHardBin = 1u << 1,
+    kErrHardRow = 1u << 2,
+    kErrTmaTile = 1u << 3,
+    kErrSoftSlot = 1u << 8,
+    kErrSoftLoc = 1u << 9,
+    kErrSoftIndex = 1u << 10,
+};
+// In the debug build: records `bit` in *word when `ok` is false and returns ok; otherwise true.
+__device__ __forceinline__ bool bounds_ok(unsigned *word, bool ok, unsigned bit)
+{
+    if (ECC_DEBUG_BOUNDS && !ok) {
+        atomicOr(word, bit);
+        return false;
+    }
+    return true;
+}
+
 __device__ __forceinline__ float qnan() { return __int_as_float(0x7fffffff); }
 
 // ------------------------------------------------------------------------------------------
@@ -97,8 +126,9 @@ int num_sms();  // of the current device (148 when the query fails)
 // Whether a 3-D call of these sizes and keys takes the TMA-staged kernel when its volume is
 // 16-byte aligned.
 bool tma3d_shape_ok(const HardPlan &pl);
-// Device address of the word a kernel sets when a bounded wait on its own copy gave up.
-cudaError_t wait_error_word(int **p);
+// Device addresses of the error words of the hard and soft kernels (bits above).
+cudaError_t hard_error_word(unsigned **p);
+cudaError_t soft_error_word(unsigned **p);
 cudaError_t hard_run(const HardPlan &pl, cudaStream_t s);
 // out[b][k] = running sum over k of out[b][k], for batch rows of H bins
 cudaError_t hard_scan(int64_t *out, int H, int64_t batch, cudaStream_t s);

@@ -40,6 +40,13 @@
 
 namespace ecc {
 
+__device__ unsigned g_soft_error;  // device error word of the soft kernels (DeviceErrorBit)
+
+cudaError_t soft_error_word(unsigned **p)
+{
+    return cudaGetSymbolAddress(reinterpret_cast<void **>(p), g_soft_error);
+}
+
 // ---------------------------------------------------------------------------------------------
 // Workspace layout
 // ---------------------------------------------------------------------------------------------
@@ -492,7 +499,8 @@ __global__ void __launch_bounds__(kPrepThreads) soft_prep_kernel(
                 const float E = pow2_scaled(l2, s, e + p.y, ex);
                 direct |= !(fabsf(ex) <= kExpLimit);
                 const int packed = (i << 4) | (cr[r] + 8);
-                out[slot] = make_float4(E, p.x, p.y, __int_as_float(packed));
+                if (bounds_ok(&g_soft_error, slot >= 0 && slot < kTileCap, kErrSoftSlot))
+                    out[slot] = make_float4(E, p.x, p.y, __int_as_float(packed));
             }
         }
         direct = __syncthreads_or(direct);
@@ -965,8 +973,11 @@ __global__ void __launch_bounds__(kSoftThreads) soft_bwd_kernel(
         for (int i = threadIdx.x; i < n; i += kSoftThreads) {
             const float4 en = list[i];
             const int loc = entry_loc(en);
+            if (!bounds_ok(&g_soft_error, loc >= 0 && loc < kTileCap, kErrSoftLoc)) continue;
             const int64_t gx = x0 + loc % T::X, gy = y0 + (loc / T::X) % T::Y,
                           gz = z0 + loc / (T::X * T::Y);
+            if (!bounds_ok(&g_soft_error, gx < g.W && gy < g.Hy && gz < g.D, kErrSoftIndex))
+                continue;
             const int64_t idx = (gz * g.Hy + gy) * g.W + gx;
             const float dX = -lambda * entry_cf(en) * dxs[i];
             if (grad_img) gacc[loc] += alpha * dX;  // one entry per voxel and direction

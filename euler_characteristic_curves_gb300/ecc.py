@@ -28,21 +28,29 @@ _lock = threading.Lock()
 _lib = None
 
 
+def debug_requested() -> bool:
+    """ECC_DEBUG=1 selects the bounds-checked debug build of the library."""
+    return os.environ.get("ECC_DEBUG", "") == "1"
+
+
 def library_path() -> str:
-    return _build.LIB_PATH
+    return _build.DEBUG_LIB_PATH if debug_requested() else _build.LIB_PATH
 
 
 def load_library():
-    """Load libecc_gb300.so (built in-tree by ``build.build()``); raises if it is missing."""
+    """Load libecc_gb300.so (built in-tree by ``build.build()``), or its bounds-checked debug
+    variant when ECC_DEBUG=1 (``build.build(debug=True)``); raises if it is missing."""
     global _lib
     with _lock:
         if _lib is not None:
             return _lib
-        path = _build.LIB_PATH
+        path = library_path()
         if not os.path.exists(path):
+            flag = " --debug" if debug_requested() else ""
             raise RuntimeError(
                 f"ECC CUDA library not found at {path}; build it first with "
-                "`python -m euler_characteristic_curves_gb300.build` (there is no CPU fallback)")
+                f"`python -m euler_characteristic_curves_gb300.build{flag}` (there is no CPU "
+                "fallback)")
         lib = ctypes.CDLL(path)
         p, i, i64, d, f, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double,
                                ctypes.c_float, ctypes.c_size_t)
@@ -54,6 +62,10 @@ def load_library():
         lib.ecc_hist_to_curve.restype = i
         lib.ecc_device_status.argtypes = [i]
         lib.ecc_device_status.restype = i
+        lib.ecc_device_error_bits.argtypes = [i]
+        lib.ecc_device_error_bits.restype = i64
+        lib.ecc_debug_build.argtypes = []
+        lib.ecc_debug_build.restype = i
         lib.ecc_hard_launch_info.argtypes = [i, i, p, i64, i, i, p]
         lib.ecc_hard_launch_info.restype = i
         lib.ecc_hard_stream_buffer_bytes.argtypes = [i, p, i]
@@ -226,6 +238,14 @@ def hist_to_curve(hist: torch.Tensor, stream=None) -> torch.Tensor:
                                               _stream_handle(stream))
     _check(rc, "ecc_hist_to_curve")
     return hist
+
+
+def device_error_bits(clear: bool = True, device=None) -> int:
+    """ecc_device_error_bits on ``device`` (default: the current one): the raw error-word bits
+    (bit 0 a wait gave up; the others debug-build bounds checks, see include/ecc.h)."""
+    ctx = torch.cuda.device(device) if device is not None else _no_switch
+    with ctx:
+        return int(load_library().ecc_device_error_bits(1 if clear else 0))
 
 
 def device_status(clear: bool = True, device=None) -> int:

@@ -53,7 +53,8 @@ enum ecc_status {
     ECC_EWS = -4,     /* workspace NULL or smaller than ecc_soft_workspace_bytes() */
     ECC_ECUDA = -5,   /* a CUDA call failed (no device, launch failure...) */
     ECC_ERANGE = -6,  /* nbins or K above the library maximum, or a size that overflows */
-    ECC_ETIMEOUT = -7 /* a kernel gave up waiting for its own staged copy (ecc_device_status) */
+    ECC_ETIMEOUT = -7, /* a kernel gave up waiting for its own staged copy (ecc_device_status) */
+    ECC_EBOUNDS = -8   /* debug build: a bounds check failed and its access was skipped */
 };
 
 #define ECC_MAX_NBINS 4096 /* largest nbins accepted by ecc_hard */
@@ -304,13 +305,25 @@ int ecc_soft_fwd_noalloc(const float *img, int ndim, const int64_t *dims, int64_
 
 /*
  * Status of the current device's kernels -- a safety net with no counterpart in the paper notes.
+ *
  * A kernel that stages data with asynchronous copies waits for each copy with a time limit
  * (2 s); if the limit passes, the kernel sets a device error word, leaves its result incomplete
- * and returns instead of hanging. This call synchronises with the device, reads that word, clears
- * it when `clear` is non-zero, and returns ECC_ETIMEOUT if it was set, else ECC_OK (ECC_ECUDA
- * when the device cannot be read).
+ * and returns instead of hanging. The debug build of the library (built with ECC_DEBUG_BOUNDS=1
+ * and loaded by the Python binding when the environment variable ECC_DEBUG is 1) also checks
+ * data-dependent indices before using them -- histogram bins, global rows and columns, staged
+ * tiles, soft-list slots and locations -- and on a failed check sets a bit of the same word and
+ * skips the access (no trap).
+ *
+ * ecc_device_status synchronises with the device, reads the word (clearing it when `clear` is
+ * non-zero) and returns ECC_ETIMEOUT if a wait gave up, ECC_EBOUNDS if a bounds check failed,
+ * else ECC_OK (ECC_ECUDA when the device cannot be read). ecc_device_error_bits returns the raw
+ * bits (>= 0: bit 0 wait timeout; bit 1 histogram bin, bit 2 global row or column, bit 3 staged
+ * tile, bit 8 soft-list slot, bit 9 soft-list location, bit 10 soft global index) or ECC_ECUDA.
+ * ecc_debug_build returns 1 for the debug build, 0 otherwise.
  */
 int ecc_device_status(int clear);
+int64_t ecc_device_error_bits(int clear);
+int ecc_debug_build(void);
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *ecc_status_str(int status);

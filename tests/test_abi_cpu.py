@@ -246,3 +246,17 @@ def test_binding_rejects_cpu_tensors():
         ecc.ecc_hard(torch.zeros(4, 4), 4, 0.0, 1.0)
     with pytest.raises(TypeError):
         ecc.ecc_soft_fwd(torch.zeros(4, 4), torch.zeros(3), 1.0, torch.ones(1), torch.zeros(2))
+
+
+def test_debug_build_exports_every_declared_symbol():
+    """The bounds-checked variant builds from the same sources, exports the same C ABI and says
+    which build it is (no GPU needed for either)."""
+    path = libbuild.build(debug=True)
+    dbg = ctypes.CDLL(path)
+    for n in declared_functions():
+        assert hasattr(dbg, n), n
+    dbg.ecc_debug_build.restype = ctypes.c_int
+    assert dbg.ecc_debug_build() == 1
+    rel = ecc.load_library()
+    assert rel.ecc_debug_build() == 0
+    assert rel.ecc_status_str(-8).startswith(b"ECC_EBOUNDS")
