@@ -421,13 +421,23 @@ __global__ void __launch_bounds__(kPrepThreads) soft_prep_kernel(
         }
         ctile[i] = cv;
     }
-    for (int i = threadIdx.x; i < HZ * HP; i += kPrepThreads) {
+    // all of a thread's loads are issued before any of them is stored, so their latencies overlap
+    // (one load per iteration, stored before the next, waited on each in turn)
+    constexpr int kLoads = (HZ * HP + kPrepThreads - 1) / kPrepThreads;
+    float fl[kLoads];
+#pragma unroll
+    for (int r = 0; r < kLoads; ++r) {
+        const int i = threadIdx.x + r * kPrepThreads;
         const int iz = i / HP, iy = (i / HX) % HY, ix = i % HX;
         const int64_t gz = z0 - ZO + iz, gy = y0 - 1 + iy, gx = x0 - 1 + ix;
-        float fv = qnan();
-        if (gz >= 0 && gz < g.D && gy >= 0 && gy < g.Hy && gx >= 0 && gx < g.W)
-            fv = __ldg(f + (gz * g.Hy + gy) * g.W + gx);
-        Fv[i] = fv;
+        fl[r] = qnan();
+        if (i < HZ * HP && gz >= 0 && gz < g.D && gy >= 0 && gy < g.Hy && gx >= 0 && gx < g.W)
+            fl[r] = __ldg(f + (gz * g.Hy + gy) * g.W + gx);
+    }
+#pragma unroll
+    for (int r = 0; r < kLoads; ++r) {
+        const int i = threadIdx.x + r * kPrepThreads;
+        if (i < HZ * HP) Fv[i] = fl[r];
     }
 
     for (int j = jbeg; j < jend; ++j) {
