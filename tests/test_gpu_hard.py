@@ -96,6 +96,8 @@ def test_nbins_variants(nbins):
 
 
 @pytest.mark.parametrize("shape,batch,nbins,kind", [((20, 37), 500, 100, "f32"),
+                                                     ((20, 36), 500, 100, "f32"),
+                                                     ((70, 260), 470, 1024, "f32"),
                                                      ((64, 130), 460, 256, "u8"),
                                                      ((9, 300), 470, 4096, "f32"),
                                                      ((3, 5), 600, 1, "f32"),
@@ -134,6 +136,37 @@ def test_special_values():
     check(cb, 2, 0.0, 1.0)
     check(cb.astype(np.uint8), 2, 0.0, 1.0)
     check(1.0 - cb, 3, 0.0, 1.0)
+
+
+def test_2d_vector_rows_special_cases():
+    """2-D float32 images with rows of a multiple of 4 values (each lane reads its four values
+    with one load) on the cases that decide the flags and keys: ties broken by position
+    (checkerboards, quantised values, constants), values on and one ulp around every threshold
+    (the exact fix-up of ambiguous estimates), NaN and infinities, strips and row ranges with
+    ragged ends, and the largest table of the saturating flags."""
+    cb = (np.indices((41, 68)).sum(0) % 2).astype(np.float32)
+    check(cb, 2, 0.0, 1.0)
+    check(1.0 - cb, 3, 0.0, 1.0)
+    check(np.full((33, 44), np.nan, np.float32), 10, 0.0, 1.0)
+    check(np.full((33, 44), 0.5, np.float32), 11, 0.0, 1.0)
+    check(rand_field((65, 132), 3, "ties"), 6, 0.0, 1.0)
+    H = 64
+    t = oracle.thresholds(H, 0.0, 1.0)
+    vals = []
+    for x in t:
+        x32 = np.float32(x)
+        vals += [np.nextafter(x32, np.float32(-1)), x32, np.nextafter(x32, np.float32(2))]
+    rng = np.random.default_rng(19)
+    check(rng.choice(np.asarray(vals, np.float32), size=(50, 76)).astype(np.float32), H, 0.0, 1.0)
+    check(rng.choice(np.arange(1024, dtype=np.float32), size=(90, 260)), 1024, 0.0, 1023.0)
+    g = synthetic.grf((97, 388), 20)
+    g[0, :] = np.nan
+    g[:, 127:129] = np.inf
+    g[31:33, :] = -np.inf
+    g[96, 387] = np.nan
+    check(g, 1024, 0.0, 1.0)
+    check(g, 1, 0.0, 1.0)
+    check(synthetic.grf((300, 516), 22, batch=3), 100, 0.0, 1.0, ndim=2)
 
 
 def test_threshold_edges_exact():
