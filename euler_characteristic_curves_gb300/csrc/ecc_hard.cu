@@ -932,11 +932,11 @@ __global__ void __launch_bounds__(k3Threads, ECC_3D_MIN_BLOCKS) ecc_hard3d_kerne
 // Same tiles, tasks, slice fold and shared key ring as ecc_hard3d_kernel, with three changes.
 //
 // * Staging. One thread copies each plane's tile plus its one-voxel halo (136 x 34 floats,
-//   columns x0 - 4 .. x0 + 131, rows y0 - 1 .. y0 + 32) into shared memory with one
-//   cp.async.bulk.tensor copy that completes on an mbarrier. The copy fills every position outside
-//   the volume (columns, rows and planes) with NaN, whose key is "never", so no thread computes a
-//   grid bound and no raw value waits in registers: four blocks fit per SM where
-//   ecc_hard3d_kernel fits three.
+//   columns x0 - 4 .. x0 + 131, rows y0 - 1 .. y0 + 32) into one of two shared staging buffers
+//   with one cp.async.bulk.tensor copy that completes on the buffer's mbarrier, two planes ahead
+//   of its use. The copy fills every position outside the volume (columns, rows and planes) with
+//   NaN, whose key is "never", so no thread computes a grid bound and no raw value waits in
+//   registers.
 // * Coded keys. A voxel's key k is carried as the fp16 value 1024 + 4k + (x & 1) + 2 (y & 1).
 //   Ordering voxels by (k, x & 1, y & 1, z) still refines the threshold order, and two vertices of
 //   one cell differ in x & 1 or y & 1 unless they are vertical neighbours, so every in-plane
@@ -956,10 +956,18 @@ __global__ void __launch_bounds__(k3Threads, ECC_3D_MIN_BLOCKS) ecc_hard3d_kerne
 
 // Three blocks per SM: with four, the 128-register cap made the compiler spill and serialise
 // (1.355 against 1.338 ms on 1024^3).
-constexpr int kT3Blocks = 3;            // resident blocks per SM the TMA kernel is built for
+#ifndef ECC_3D_TMA_BLOCKS
+#define ECC_3D_TMA_BLOCKS 3
+#endif
+constexpr int kT3Blocks = ECC_3D_TMA_BLOCKS;  // resident blocks per SM the TMA kernel is built for
 constexpr int kRawPitch = kKeyPitch;    // floats per staged row (columns x0 - 4 .. x0 + 131)
 constexpr int kRawRows = kKeyRowsHalo;  // rows y0 - 1 .. y0 + 32
 constexpr int kRawBytes = kRawPitch * kRawRows * 4;
+constexpr int kRawStride = (kRawBytes + 127) & ~127;  // staging buffers on 128-byte boundaries
+#ifndef ECC_3D_TMA_STAGES
+#define ECC_3D_TMA_STAGES 2
+#endif
+constexpr int kT3Stages = ECC_3D_TMA_STAGES;  // staging buffers: copies run this many planes ahead
 constexpr int kKeyRingBytes = 3 * kKeyPlane * 2;
 constexpr int kCodedMaxBins = 256;  // 1024 + 4 (H - 1) + 3 < 2048
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per mbarrier wait
@@ -1193,20 +1201,20 @@ __global__ void __launch_bounds__(k3Threads, kT3Blocks)
     ecc_hard3d_tma_kernel(const __grid_constant__ Hard3TmaParams P)
 {
     extern __shared__ __align__(128) unsigned char smem_t3[];
-    // the staging buffer starts on a 128-byte boundary (the launch adds 128 bytes of slack)
+    // the staging buffers start on 128-byte boundaries (the launch adds 128 bytes of slack)
     unsigned char *base = smem_t3 + ((128u - (smem_u32(smem_t3) & 127u)) & 127u);
-    float *raw = reinterpret_cast<float *>(base);
-    uint16_t *kb = reinterpret_cast<uint16_t *>(base + kRawBytes);
-    int *hist = reinterpret_cast<int *>(base + kRawBytes + kKeyRingBytes);
+    uint16_t *kb = reinterpret_cast<uint16_t *>(base + kT3Stages * kRawStride);
+    int *hist = reinterpret_cast<int *>(base + kT3Stages * kRawStride + kKeyRingBytes);
     float *table = reinterpret_cast<float *>(hist + hist_words(P.H));
-    __shared__ __align__(8) unsigned long long mbar;
+    __shared__ __align__(8) unsigned long long mbar[kT3Stages];
 
     const int tid = threadIdx.x, lane = tid & (kWarp - 1), warp = tid >> 5;
     for (int i = tid; i <= P.H; i += k3Threads) hist[i] = 0;
     for (int i = tid; i < P.H + 2; i += k3Threads) table[i] = P.table[i];
-    const uint32_t bar = smem_u32(&mbar), raw_s = smem_u32(raw);
+    const uint32_t bar0 = smem_u32(&mbar[0]), raw0 = smem_u32(base);
     if (tid == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+        for (int s = 0; s < kT3Stages; ++s)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0 + 8u * s) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -1232,7 +1240,10 @@ __global__ void __launch_bounds__(k3Threads, kT3Blocks)
     const int b = blockIdx.y;
     const uint32_t hist_c = smem_u32(hist) - kKeyBase;
     const int64_t Tn = P.tasks_per_image, G = P.ctas_per_image;
-    uint32_t phase = 0;  // parity of the next copy's completion
+    // The block's plane copies in issue order: copy n goes to staging buffer n % kT3Stages and
+    // completes phase (n / kT3Stages) & 1 of that buffer's mbarrier; copies are waited for in
+    // the same order. nq: copies issued, nw: copies waited for.
+    uint32_t nq = 0, nw = 0;
     bool failed = false;
 
     for (int64_t t = blockIdx.x; t < Tn && !failed; t += G) {
@@ -1243,20 +1254,38 @@ __global__ void __launch_bounds__(k3Threads, kT3Blocks)
         const int z1 = min(z0 + P.rows_per_task, P.D);
         const int x0 = tx * kStrip, y0 = ty * kTileRows;
 
-        // prologue: keys of planes z0 - 1 (buffer 0) and z0 (buffer 1); plane z0 + 1 in flight
+        // The task reads planes z0 - 1 .. z1 (n_planes of them; planes -1 and D are filled with
+        // NaN by the copies). Plane j of the task (z = z0 - 1 + j) is copied kT3Stages planes
+        // ahead: its copy is issued once the keys of plane j - kT3Stages are in the key ring,
+        // into the staging buffer that plane has just left.
+        const int n_planes = z1 - z0 + 2;
+        auto issue = [&](int j) {
+            if (tid == 0)
+                stage_plane(P, raw0 + (uint32_t)((nq % kT3Stages) * kRawStride),
+                            bar0 + 8u * (nq % kT3Stages), x0, y0, z0 - 1 + j, b);
+            ++nq;
+        };
+        auto wait = [&](bool &late) {
+            const uint32_t s = nw % kT3Stages;
+            late = !mbar_wait_bounded(bar0 + 8u * s, (nw / kT3Stages) & 1u);
+            ++nw;
+            return reinterpret_cast<const float *>(base + s * kRawStride);
+        };
+
+        // prologue: keys of planes z0 - 1 (key buffer 0) and z0 (key buffer 1)
         __syncthreads();  // the previous task's readers are done with every buffer
+        for (int j = 0; j < kT3Stages && j < n_planes; ++j) issue(j);
         for (int j = 0; j < 2; ++j) {
-            if (tid == 0) stage_plane(P, raw_s, bar, x0, y0, z0 - 1 + j, b);
-            const bool late = !mbar_wait_bounded(bar, phase);
-            phase ^= 1;
+            bool late;
+            const float *raw = wait(late);
             plane_keys_coded(raw, kb + j * kKeyPlane, K, table, r0, lane, h_off, h_code);
             if (__syncthreads_or(late)) {  // block-uniform
                 failed = true;
                 break;
             }
+            if (j + kT3Stages < n_planes) issue(j + kT3Stages);
         }
         if (failed) break;
-        if (tid == 0) stage_plane(P, raw_s, bar, x0, y0, z0 + 1, b);
 
         // q: -(1 - up) c2(M_{z0-1}) at the warp's pixels, up = [k_{z0} < k_{z0-1}]
         uint32_t q[k3Rows][2];
@@ -1288,14 +1317,15 @@ __global__ void __launch_bounds__(k3Threads, kT3Blocks)
         const uint16_t *bc = kb + kKeyPlane;
         uint16_t *bn = kb + 2 * kKeyPlane, *bo = kb;
         for (int z = z0; z < z1; ++z) {
-            const bool late = !mbar_wait_bounded(bar, phase);
-            phase ^= 1;
+            const int j = z - z0 + 2;  // the task's plane z + 1
+            bool late;
+            const float *raw = wait(late);
             plane_keys_coded(raw, bn, K, table, r0, lane, h_off, h_code);
             if (__syncthreads_or(late)) {  // block-uniform
                 failed = true;
                 break;
             }
-            if (tid == 0 && z + 2 <= z1) stage_plane(P, raw_s, bar, x0, y0, z + 2, b);
+            if (j + kT3Stages < n_planes) issue(j + kT3Stages);
             KeyRow c0 = smem_key_row(bc, r0, lane), c1 = smem_key_row(bc, r0 + 1, lane);
             KeyRow n1 = smem_key_row(bn, r0 + 1, lane);
             KeyRow Ma = max_rows(c0, smem_key_row(bn, r0, lane)), Mb = max_rows(c1, n1);
@@ -1328,7 +1358,9 @@ __global__ void __launch_bounds__(k3Threads, kT3Blocks)
     }
     if (failed) {  // block-uniform: a copy did not arrive in time
         if (tid == 0) {
-            mbar_wait_bounded(bar, phase ^ 1u);  // the copy that timed out, if it still lands
+            // the copy that timed out and those issued after it, if they still land
+            for (uint32_t n = nw - 1; n < nq; ++n)
+                mbar_wait_bounded(bar0 + 8u * (n % kT3Stages), (n / kT3Stages) & 1u);
             atomicOr(&g_hard_error, kErrWaitTimeout);
         }
         return;
@@ -1603,7 +1635,7 @@ static cudaError_t launch_hard3d_tma(const HardPlan &pl, cudaStream_t s)
             cudaMemsetAsync(pl.out, 0, sizeof(int64_t) * (size_t)(pl.batch * pl.H), s);
         if (m != cudaSuccess) return m;
     }
-    const size_t smem = 128 + (size_t)kRawBytes + kKeyRingBytes +
+    const size_t smem = 128 + (size_t)kT3Stages * kRawStride + kKeyRingBytes +
                         (size_t)hist_words(pl.H) * 4 + (size_t)(pl.H + 2) * 4;
     const cudaError_t a = cudaFuncSetAttribute(
         ecc_hard3d_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
