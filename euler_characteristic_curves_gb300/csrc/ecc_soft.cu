@@ -65,6 +65,7 @@ static_assert(SoftTile<3>::X * SoftTile<3>::Y * SoftTile<3>::Z == kTileCap, "3-D
 constexpr int kPrepThreads = 256;
 constexpr int64_t kPrepBlocks = 4096;      // prep grid size aimed at when directions are grouped
 constexpr int kSoftThreads = 64;           // two warps per block
+constexpr int kTailBatch = 4;              // backward per-voxel loop: entries in flight per thread
 constexpr int kChunk = 256;                // entries staged in shared memory at a time
 // The backward kernel stages half as many, so that its shared memory (and registers) let a
 // full wave of blocks be resident on a 64-image batch of 256^2 images.
@@ -979,26 +980,51 @@ __global__ void __launch_bounds__(kSoftThreads) soft_bwd_kernel(
         __syncthreads();
 
         // per-voxel gradient: dX = -lambda c sum_k g w; grad_img += alpha dX; dalpha, du partials
+        // A thread takes its entries i = tid, tid + 64, ... in that order, kTailBatch at a time:
+        // the batch's loads (entry, then image value and coordinates) are all issued before any
+        // is used, so their latencies overlap; the sums see the entries in the same order.
         float sum[kScal] = {0.f, 0.f, 0.f, 0.f}, comp[kScal] = {0.f, 0.f, 0.f, 0.f};
-        for (int i = threadIdx.x; i < n; i += kSoftThreads) {
-            const float4 en = list[i];
-            const int loc = entry_loc(en);
-            if (!bounds_ok(&g_soft_error, loc >= 0 && loc < kTileCap, kErrSoftLoc)) continue;
-            const int64_t gx = x0 + loc % T::X, gy = y0 + (loc / T::X) % T::Y,
-                          gz = z0 + loc / (T::X * T::Y);
-            if (!bounds_ok(&g_soft_error, gx < g.W && gy < g.Hy && gz < g.D, kErrSoftIndex))
-                continue;
-            const int64_t idx = (gz * g.Hy + gy) * g.W + gx;
-            const float dX = -lambda * entry_cf(en) * dxs[i];
-            if (grad_img) gacc[loc] += alpha * dX;  // one entry per voxel and direction
-            const float2 xy = __ldg(cy + gy), xx = __ldg(cx + gx);
-            kahan_add(sum[0], comp[0], dX * __ldg(f + idx));
-            if (NDIM == 3) {
-                const float2 xz = __ldg(cz + gz);
-                kahan_add(sum[1], comp[1], dX * (xz.x + xz.y));
+        for (int i0 = threadIdx.x; i0 < n; i0 += kTailBatch * kSoftThreads) {
+            float4 en[kTailBatch];
+            bool ok[kTailBatch];
+#pragma unroll
+            for (int u = 0; u < kTailBatch; ++u) {
+                const int i = i0 + u * kSoftThreads;
+                ok[u] = i < n;
+                en[u] = ok[u] ? list[i] : make_float4(0.f, 0.f, 0.f, 0.f);
             }
-            kahan_add(sum[NDIM - 1], comp[NDIM - 1], dX * (xy.x + xy.y));
-            kahan_add(sum[NDIM], comp[NDIM], dX * (xx.x + xx.y));
+            int loc[kTailBatch];
+            float fv[kTailBatch];
+            float2 xy[kTailBatch], xx[kTailBatch], xz[kTailBatch];
+#pragma unroll
+            for (int u = 0; u < kTailBatch; ++u) {
+                loc[u] = entry_loc(en[u]);
+                ok[u] = ok[u] && bounds_ok(&g_soft_error, loc[u] >= 0 && loc[u] < kTileCap,
+                                           kErrSoftLoc);
+                const int l = ok[u] ? loc[u] : 0;
+                const int64_t gx = x0 + l % T::X, gy = y0 + (l / T::X) % T::Y,
+                              gz = z0 + l / (T::X * T::Y);
+                ok[u] = ok[u] && bounds_ok(&g_soft_error, gx < g.W && gy < g.Hy && gz < g.D,
+                                           kErrSoftIndex);
+                fv[u] = 0.f;
+                xy[u] = xx[u] = xz[u] = make_float2(0.f, 0.f);
+                if (ok[u]) {
+                    fv[u] = __ldg(f + (gz * g.Hy + gy) * g.W + gx);
+                    xy[u] = __ldg(cy + gy);
+                    xx[u] = __ldg(cx + gx);
+                    if (NDIM == 3) xz[u] = __ldg(cz + gz);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kTailBatch; ++u) {
+                if (!ok[u]) continue;
+                const float dX = -lambda * entry_cf(en[u]) * dxs[i0 + u * kSoftThreads];
+                if (grad_img) gacc[loc[u]] += alpha * dX;  // one entry per voxel and direction
+                kahan_add(sum[0], comp[0], dX * fv[u]);
+                if (NDIM == 3) kahan_add(sum[1], comp[1], dX * (xz[u].x + xz[u].y));
+                kahan_add(sum[NDIM - 1], comp[NDIM - 1], dX * (xy[u].x + xy[u].y));
+                kahan_add(sum[NDIM], comp[NDIM], dX * (xx[u].x + xx[u].y));
+            }
         }
         double v[kScal];
 #pragma unroll
