@@ -144,6 +144,15 @@ int64_t ecc_device_error_bits(int clear)
 
 int ecc_debug_build(void) { return ECC_DEBUG_BOUNDS ? 1 : 0; }
 
+int ecc_wait_probe(int64_t limit_ns, ecc_stream_t stream)
+{
+    if (limit_ns <= 0) return ECC_EINVAL;
+    if (limit_ns > ECC_WAIT_LIMIT_NS) return ECC_ERANGE;
+    return wait_probe((unsigned long long)limit_ns, (cudaStream_t)stream) == cudaSuccess
+               ? ECC_OK
+               : ECC_ECUDA;
+}
+
 // Sizes of a hard-ECC call: the checks ecc_hard makes on its shape arguments, and the plan's
 // extents on success.
 static int hard_shape_check(int dtype, int ndim, const int64_t *dims, int64_t batch, int nbins,

@@ -970,7 +970,7 @@ constexpr int kRawStride = (kRawBytes + 127) & ~127;  // staging buffers on 128-
 constexpr int kT3Stages = ECC_3D_TMA_STAGES;  // staging buffers: copies run this many planes ahead
 constexpr int kKeyRingBytes = 3 * kKeyPlane * 2;
 constexpr int kCodedMaxBins = 256;  // 1024 + 4 (H - 1) + 3 < 2048
-constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per mbarrier wait
+constexpr unsigned long long kWaitNs = ECC_WAIT_LIMIT_NS;  // 2 s per mbarrier wait
 static_assert(kRawBytes % 16 == 0 && kKeyRingBytes % 16 == 0, "shared layout");
 static_assert(kStrip + 8 == kRawPitch, "a staged row starts 4 columns left of the tile");
 
@@ -1009,12 +1009,14 @@ __device__ __forceinline__ unsigned long long global_ns()
     return t;
 }
 
-// Waits for the completion of the phase of parity `parity`; false if it has not come in kWaitNs.
-__device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity)
+// Waits for the completion of the phase of parity `parity`; false if it has not come in
+// limit_ns (kWaitNs in the kernels).
+__device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
+                                               unsigned long long limit_ns = kWaitNs)
 {
     const unsigned long long t0 = global_ns();
     while (!mbar_try_wait(bar, parity))
-        if (global_ns() - t0 > kWaitNs) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     return true;
 }
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
@@ -1371,6 +1373,28 @@ __global__ void __launch_bounds__(k3Threads, kT3Blocks)
         const int v = hist[i];
         if (v != 0) atomicAdd(dst + i, (unsigned long long)(long long)(P.sign * v));
     }
+}
+
+// ----------------------------------------------------------------------------------------------
+// Probe of the wait-timeout path: one thread waits, with the kernels' bounded wait cut to
+// limit_ns, for a phase of an mbarrier that nothing arrives at, then records the timeout in the
+// device error word as the TMA kernel does. No copy is in flight, so the block may leave.
+// ----------------------------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(1) ecc_wait_probe_kernel(unsigned long long limit_ns)
+{
+    __shared__ __align__(8) unsigned long long mbar;
+    const uint32_t bar = smem_u32(&mbar);
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (!(mbar_try_wait(bar, 0) || mbar_wait_slow(bar, 0, limit_ns)))
+        atomicOr(&g_hard_error, kErrWaitTimeout);
+}
+
+cudaError_t wait_probe(unsigned long long limit_ns, cudaStream_t s)
+{
+    ecc_wait_probe_kernel<<<1, 1, 0, s>>>(limit_ns);
+    return cudaGetLastError();
 }
 
 // ----------------------------------------------------------------------------------------------

@@ -126,6 +126,8 @@ int num_sms();  // of the current device (148 when the query fails)
 // Whether a 3-D call of these sizes and keys takes the TMA-staged kernel when its volume is
 // 16-byte aligned.
 bool tma3d_shape_ok(const HardPlan &pl);
+// Launches the probe of the wait-timeout path (ecc_wait_probe).
+cudaError_t wait_probe(unsigned long long limit_ns, cudaStream_t s);
 // Device addresses of the error words of the hard and soft kernels (bits above).
 cudaError_t hard_error_word(unsigned **p);
 cudaError_t soft_error_word(unsigned **p);

@@ -5,7 +5,7 @@ device pointers, sizes and the current CUDA stream, and turns negative status co
 exceptions. There is no CPU path: CPU tensors are rejected, and a missing library raises.
 
 Names follow the C entry points: ``ecc_hard``, ``ecc_hard_partial``, ``hist_to_curve``,
-``hard_launch_info``, ``device_status``, ``ecc_hard_stream``, ``ecc_soft_fwd``, ``ecc_soft_bwd``,
+``hard_launch_info``, ``device_status``, ``wait_probe``, ``ecc_hard_stream``, ``ecc_soft_fwd``, ``ecc_soft_bwd``,
 ``ecc_soft_stats``, ``ecc_soft_fwd_noalloc``, ``ecc_soft_ect_fwd``, ``ecc_soft_ect_bwd``,
 ``ecc_soft_ect_stats``, ``soft_workspace_bytes``; ``SoftECT`` / ``soft_ect`` wrap the transform; ``SoftECC`` / ``soft_ecc`` wrap the soft pair as a differentiable
 PyTorch layer ("Key designs -- differentiable ECC layer (sigmoid relaxation)" in the paper notes
@@ -66,6 +66,8 @@ def load_library():
         lib.ecc_device_error_bits.restype = i64
         lib.ecc_debug_build.argtypes = []
         lib.ecc_debug_build.restype = i
+        lib.ecc_wait_probe.argtypes = [i64, p]
+        lib.ecc_wait_probe.restype = i
         lib.ecc_hard_launch_info.argtypes = [i, i, p, i64, i, i, p]
         lib.ecc_hard_launch_info.restype = i
         lib.ecc_hard_stream_buffer_bytes.argtypes = [i, p, i]
@@ -254,6 +256,16 @@ def device_status(clear: bool = True, device=None) -> int:
     ctx = torch.cuda.device(device) if device is not None else _no_switch
     with ctx:
         return int(load_library().ecc_device_status(1 if clear else 0))
+
+
+def wait_probe(limit_ns: int, device=None, stream=None) -> None:
+    """ecc_wait_probe on ``device`` (default: the current one): a kernel that waits, with the
+    kernels' bounded wait cut to ``limit_ns``, for an mbarrier nothing completes, then records a
+    wait timeout in the device error word (read it with ``device_status``)."""
+    ctx = torch.cuda.device(device) if device is not None else _no_switch
+    with ctx:
+        _check(load_library().ecc_wait_probe(int(limit_ns), _stream_handle(stream)),
+               "ecc_wait_probe")
 
 
 def hard_launch_info(dims, batch: int, nbins: int, dtype=torch.float32, sm_count: int = 0):

@@ -325,6 +325,20 @@ int ecc_device_status(int clear);
 int64_t ecc_device_error_bits(int clear);
 int ecc_debug_build(void);
 
+/*
+ * Probe of the wait-timeout path -- a test hook with no counterpart in the paper notes.
+ *
+ * Launches, on `stream`, one kernel whose single thread waits for an mbarrier phase that nothing
+ * completes, with the kernels' bounded wait cut to limit_ns nanoseconds (the kernels' own
+ * limit is ECC_WAIT_LIMIT_NS); when the limit passes it records the timeout in the device error
+ * word exactly as a kernel whose staged copy is late does, and returns. No copy is in flight and
+ * the context stays usable, so afterwards ecc_device_status() returns ECC_ETIMEOUT (and clears
+ * the word when asked). Returns ECC_EINVAL for limit_ns <= 0, ECC_ERANGE above
+ * ECC_WAIT_LIMIT_NS, ECC_ECUDA if the launch fails, else ECC_OK.
+ */
+#define ECC_WAIT_LIMIT_NS 2000000000LL
+int ecc_wait_probe(int64_t limit_ns, ecc_stream_t stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *ecc_status_str(int status);
 

@@ -34,6 +34,14 @@ def test_exports_every_declared_symbol(lib):
         assert hasattr(lib, n), n
 
 
+def test_wait_probe_validation(lib):
+    """The wait-timeout probe rejects limits outside (0, 2 s] before it touches a device."""
+    lib.ecc_wait_probe.argtypes = [ctypes.c_int64, ctypes.c_void_p]
+    assert lib.ecc_wait_probe(0, None) == EINVAL
+    assert lib.ecc_wait_probe(-5, None) == EINVAL
+    assert lib.ecc_wait_probe(2_000_000_001, None) == ERANGE
+
+
 def test_status_strings_and_version(lib):
     for code in (OK, EINVAL, EDTYPE, EDIM, EWS, ECUDA, ERANGE, 12345):
         s = lib.ecc_status_str(code)
