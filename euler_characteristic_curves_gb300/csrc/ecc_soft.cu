@@ -537,7 +537,7 @@ __device__ __forceinline__ KState k_state(const float *__restrict__ tau, int k, 
 }
 
 // r = sigma(-lambda |tau - X|) and below = [X <= tau] by the direct form (the factorised form,
-// for both thresholds at once, is small_sigma_fact2).
+// for both thresholds at once, is written out in the packed loops below).
 __device__ __forceinline__ float small_sigma_direct(const float4 &en, float t, float l2,
                                                     bool &below)
 {
@@ -600,20 +600,6 @@ __device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c)
     f32x2 r;
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
     return r;
-}
-
-// The factorised r for both thresholds: e = E F_k = exp(lambda (X - tau_k)),
-// r = min(e, 1) / (1 + e), below_k = [e <= 1]. e may overflow to +inf (r = 1 * 0 = 0) or
-// underflow to 0 (r = 0).
-__device__ __forceinline__ f32x2 small_sigma_fact2(float E, f32x2 F, bool &b0, bool &b1)
-{
-    float e0, e1, d0, d1;
-    const f32x2 e = mul2(pk2(E, E), F);
-    upk2(e, e0, e1);
-    upk2(add2(e, pk2(1.0f, 1.0f)), d0, d1);
-    b0 = e0 <= 1.0f;
-    b1 = e1 <= 1.0f;
-    return mul2(pk2(fminf(e0, 1.0f), fminf(e1, 1.0f)), pk2(rcp_approx(d0), rcp_approx(d1)));
 }
 
 // Kahan step for both thresholds with the compensation carried negated (nc = -comp), which
@@ -822,22 +808,40 @@ __device__ __forceinline__ float group_row_sum(float (*qw)[kWarp], int lane)
     return s;
 }
 
+// The factorised small part for both thresholds, negated: e = E F_k = exp(lambda (X - tau_k)),
+// -r = max(-e, -1) / (1 + e) = -min(e, 1) / (1 + e); e may overflow to +inf (-r = -1 * 0) or
+// underflow to 0. The backward's terms carry -r and -w: -w = r^2 - r = fma(-r, -r, -r) is one
+// packed FMA, where w = fma(-r, r, r) needed a negation first. With -c and -g as the other
+// factors every product, and so every sum, keeps its bits.
+__device__ __forceinline__ f32x2 neg_small_sigma_fact2(float E, f32x2 F)
+{
+    float e0, e1, d0, d1;
+    const f32x2 e = mul2(pk2(E, E), F);
+    upk2(e, e0, e1);
+    upk2(add2(e, pk2(1.0f, 1.0f)), d0, d1);
+    return mul2(pk2(fmaxf(-e0, -1.0f), fmaxf(-e1, -1.0f)), pk2(rcp_approx(d0), rcp_approx(d1)));
+}
+__device__ __forceinline__ float entry_neg_cf(const float4 &en)
+{
+    return 8388616.0f - __int_as_float(0x4B000000 | (__float_as_int(en.w) & 15));
+}
+
+// ng: the lane's upstream gradients negated, as pairs.
 __device__ __forceinline__ float bwd_group4_packed(const float4 *en8, const f32x2 *F,
-                                                   const f32x2 *g, f32x2 *a, f32x2 *nc,
+                                                   const f32x2 *ng, f32x2 *a, f32x2 *nc,
                                                    float (*qw)[kWarp], int lane)
 {
 #pragma unroll
     for (int j = 0; j < kGroup; ++j) {
         const float4 en = en8[j];
-        const float cf = entry_cf(en);
+        const float ncf = entry_neg_cf(en);
         f32x2 gw = 0ull;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            bool b0, b1;
-            const f32x2 r = small_sigma_fact2(en.x, F[h], b0, b1);
-            const f32x2 w = fma2(sub2(0ull, r), r, r);  // r - r^2, one rounding as fmaf(-r, r, r)
-            kahan_fma2(a[h], nc[h], pk2(cf, cf), w);
-            gw = fma2(g[h], w, gw);
+            const f32x2 rn = neg_small_sigma_fact2(en.x, F[h]);  // -r
+            const f32x2 wn = fma2(rn, rn, rn);                   // -w = r^2 - r
+            kahan_fma2(a[h], nc[h], pk2(ncf, ncf), wn);          // (-c)(-w) = c w
+            gw = fma2(ng[h], wn, gw);                            // (-g)(-w) = g w
         }
         float q0, q1;
         upk2(gw, q0, q1);
@@ -934,7 +938,7 @@ __global__ void __launch_bounds__(kSoftThreads) soft_bwd_kernel(
             const bool fact = __syncthreads_and(t.ok && !(cnt & kTileFlagDirect));
             float a[kLaneK] = {0.f, 0.f, 0.f, 0.f}, c[kLaneK] = {0.f, 0.f, 0.f, 0.f};
             const f32x2 F[2] = {pk2(t.s[0].F, t.s[1].F), pk2(t.s[2].F, t.s[3].F)};
-            const f32x2 gp[2] = {pk2(g[0], g[1]), pk2(g[2], g[3])};
+            const f32x2 ngp[2] = {pk2(-g[0], -g[1]), pk2(-g[2], -g[3])};
             f32x2 ap[2] = {0ull, 0ull}, ncp[2] = {0ull, 0ull};  // packed dtau sums (factorised)
             for (int e0 = 0; e0 < n; e0 += kBwdChunk) {
                 const int m_ent = min(kBwdChunk, n - e0);
@@ -946,7 +950,8 @@ __global__ void __launch_bounds__(kSoftThreads) soft_bwd_kernel(
                 __syncthreads();
                 for (int gi = warp; gi * kGroup < m_ent; gi += NW) {
                     const float rs =
-                        fact ? bwd_group4_packed(sh + gi * kGroup, F, gp, ap, ncp, qbuf[warp], lane)
+                        fact ? bwd_group4_packed(sh + gi * kGroup, F, ngp, ap, ncp, qbuf[warp],
+                                                 lane)
                              : bwd_group4_direct(sh + gi * kGroup, t, g, l2, a, c, qbuf[warp],
                                                  lane);
                     // padding entries (index n and above) add 0 to unused slots
