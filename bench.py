@@ -21,6 +21,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -142,13 +143,21 @@ def load_peaks():
 HARD_SOURCES = ("ecc_hard.cu", "ecc_internal.cuh", "ecc_keys.cuh")
 
 
+def _code_only(text: str) -> str:
+    """The source without comments and blank lines (a comment edit leaves the kernels as they
+    were, so it does not void their recorded counters)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(ln.rstrip() for ln in text.splitlines() if ln.strip())
+
+
 def kernel_source_hash(files=HARD_SOURCES):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "euler_characteristic_curves_gb300", "csrc")
     for f in sorted(files):
-        with open(os.path.join(csrc, f), "rb") as fh:
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
             h.update(f.encode())
-            h.update(fh.read())
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -108,7 +108,7 @@ struct HardPlan {
     int sign = 1;        // -1: subtract the histogram from out
     bool scan = true;    // false: leave out as a histogram (the caller scans once at the end)
     bool zero_out = false;  // true: the launcher zeroes out first (when it needs zeroing)
-    bool tma = false;       // planned for the TMA-staged 3-D kernel (four blocks per SM)
+    bool tma = false;       // planned for the TMA-staged 3-D kernel (three blocks per SM)
 };
 // Launch shape of a hard-ECC call on a device of `sms` SMs (shared by the launcher and
 // ecc_hard_launch_info). 2-D: one warp per (strip, row range); 3-D: tasks (tile, chunk of planes)
