@@ -53,7 +53,7 @@ def _load():
             lib.oracle_thresholds.argtypes = [i, d, d, p]
             lib.oracle_ecc_hard.argtypes = [p, i, i, p, i64, i, d, d, p]
             lib.oracle_ecc_soft_fwd.argtypes = [p, i, p, i64, p, i, d, d, p, p]
-            lib.oracle_ecc_soft_bwd.argtypes = [p, i, p, i64, p, i, d, d, p, p, p, p, p, p, p]
+            lib.oracle_ecc_soft_bwd.argtypes = [p, i, p, i64, p, i, d, d, p, p, p, p, p, p, p, p]
             for fn in (lib.oracle_thresholds, lib.oracle_ecc_hard, lib.oracle_ecc_soft_fwd,
                        lib.oracle_ecc_soft_bwd):
                 fn.restype = i
@@ -138,8 +138,9 @@ def ecc_soft_fwd(img, tau, lam, alpha, u, ndim=None):
 
 def ecc_soft_bwd(img, tau, lam, alpha, u, grad_out, ndim=None, want_img=True):
     """Analytic gradients of sum(grad_out * S). Returns a dict of fp64 arrays:
-    grad_tau [K], grad_alpha (scalar), grad_u [ndim], and when want_img: grad_img (img's shape)
-    and grad_img_absterms (same shape; the sum of |terms| that make up each grad_img entry)."""
+    grad_tau [K], grad_tau_absterms [K] (the sum of |terms| that make up each grad_tau entry),
+    grad_alpha (scalar), grad_u [ndim], and when want_img: grad_img (img's shape) and
+    grad_img_absterms (same shape; the sum of |terms| that make up each grad_img entry)."""
     img, tau, u, ndim, batch, dims = _soft_args(img, tau, u, ndim)
     K = tau.shape[0]
     go = np.ascontiguousarray(np.asarray(grad_out, np.float64).reshape(batch, K))
@@ -148,12 +149,13 @@ def ecc_soft_bwd(img, tau, lam, alpha, u, grad_out, ndim=None, want_img=True):
     gu = np.empty(ndim, np.float64)
     gi = np.empty(img.shape, np.float64) if want_img else None
     gabs = np.empty(img.shape, np.float64) if want_img else None
+    gtabs = np.empty(K, np.float64)
     lam64 = float(np.float32(lam))
     alpha64 = float(np.float32(alpha))
     _check(_load().oracle_ecc_soft_bwd(_ptr(img), ndim, _ptr(dims), batch, _ptr(tau), K, lam64,
                                        alpha64, _ptr(u), _ptr(go), _ptr(gt), _ptr(ga), _ptr(gu),
-                                       _ptr(gi), _ptr(gabs)), "ecc_soft_bwd")
-    res = {"grad_tau": gt, "grad_alpha": float(ga[0]), "grad_u": gu}
+                                       _ptr(gi), _ptr(gabs), _ptr(gtabs)), "ecc_soft_bwd")
+    res = {"grad_tau": gt, "grad_alpha": float(ga[0]), "grad_u": gu, "grad_tau_absterms": gtabs}
     if want_img:
         res["grad_img"] = gi
         res["grad_img_absterms"] = gabs

@@ -310,12 +310,15 @@ int oracle_ecc_soft_fwd(const float *img, int ndim, const int64_t *dims, int64_t
  *   grad_u[d]     = sum_{b,p} dX[b,p] x_{p,d}
  *   grad_img[b,p] = alpha dX[b,p]                      (only when grad_img is not NULL)
  * with s = sigma(lambda (t_k - max X over the cell)). grad_img_absterms (nullable) receives
- * alpha * (sum over the contributing terms of |term|), the scale of the cancellation in grad_img.
+ * alpha * (sum over the contributing terms of |term|), the scale of the cancellation in grad_img;
+ * grad_tau_absterms (nullable) receives sum_b sum_cells |term| for each k, the same scale for
+ * grad_tau.
  */
 int oracle_ecc_soft_bwd(const float *img, int ndim, const int64_t *dims, int64_t batch,
                         const float *tau, int K, double lambda, double alpha, const double *u,
                         const double *grad_out, double *grad_tau, double *grad_alpha,
-                        double *grad_u, double *grad_img, double *grad_img_absterms)
+                        double *grad_u, double *grad_img, double *grad_img_absterms,
+                        double *grad_tau_absterms)
 {
     grid_t g;
     if (!img || !tau || !u || !grad_out || !grad_tau || !grad_alpha || !grad_u || K < 1 ||
@@ -335,6 +338,8 @@ int oracle_ecc_soft_bwd(const float *img, int ndim, const int64_t *dims, int64_t
     int64_t voff[8];
     for (int T = 0; T < ncell_types; ++T) voff[T] = vertex_offset(&g, T);
     for (int k = 0; k < K; ++k) grad_tau[k] = 0.0;
+    if (grad_tau_absterms)
+        for (int k = 0; k < K; ++k) grad_tau_absterms[k] = 0.0;
     *grad_alpha = 0.0;
     for (int d = 0; d < ndim; ++d) grad_u[d] = 0.0;
 
@@ -354,6 +359,7 @@ int oracle_ecc_soft_bwd(const float *img, int ndim, const int64_t *dims, int64_t
                     double s = sigmoid(lambda * ((double)tau[k] - X[owner]));
                     double term = go[k] * sign * lambda * s * (1.0 - s);
                     grad_tau[k] += term;
+                    if (grad_tau_absterms) grad_tau_absterms[k] += fabs(term);
                     dX[owner] -= term;
                     dXabs[owner] += fabs(term);
                 }

@@ -114,6 +114,21 @@ def test_one_block_per_image_stores_the_curve_itself(shape, batch, nbins, kind):
         check(f, nbins, 0.0, 1.0, ndim=2)
 
 
+@pytest.mark.parametrize("shape,kind", [((3, 5), "f32"), ((4, 8), "f32"), ((2, 7), "u8"),
+                                        ((2, 3, 4), "f32"), ((2, 2, 8), "u8")])
+def test_hard_at_the_largest_batch(shape, kind):
+    """65535 images or volumes (the grid's y extent), each its own block: every curve must match
+    the oracle bit for bit. Rows of 8 values take the vector loads (2-D) and the TMA-staged
+    kernel (3-D float32)."""
+    rng = np.random.default_rng(sum(shape))
+    f = rng.random((65535,) + shape).astype(np.float32)
+    nd = len(shape)
+    if kind == "u8":
+        check(synthetic.quantise_u8(f), 256, 0.0, 255.0, ndim=nd)
+    else:
+        check(f, 17, 0.0, 1.0, ndim=nd)
+
+
 def test_special_values():
     f = synthetic.grf((64, 160), 8)
     g = f.copy()

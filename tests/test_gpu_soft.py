@@ -312,3 +312,40 @@ def test_dense_critical_lists(ndim):
     st = ecc.ecc_soft_stats(dev(img), K, ws, ndim=ndim).cpu().numpy()
     assert st[0] > 0.4 * img.size  # dense lists: most voxels contribute
     compare(img, tau, 50.0, 1.0, u, g)
+
+
+def test_soft_at_the_largest_K():
+    """K = 8192 (ECC_MAX_K): 64 threshold passes per tile in the forward and backward, spread
+    over a range wider than the data, so thresholds sit on both sides of every value.
+
+    S, grad_alpha, grad_u and grad_img are held to the bounds of the other tests. Among 8192
+    grad_tau entries some are sums whose terms cancel to a thousandth of their size; those are
+    held, like grad_img, to the plain bound plus 4e-6 times the sum of |terms| (the oracle's
+    grad_tau_absterms), and every other entry to the plain bound."""
+    img = synthetic.grf((9, 21), 51, batch=2)
+    tau = np.linspace(-0.25, 1.25, 8192).astype(np.float32)
+    g = synthetic.upstream_grad((2, 8192), seed=52)
+    u = np.asarray([0.03, -0.02], np.float32)
+    s, res, ref_s, ref = run_both(img, tau, 50.0, 1.0, u, g)
+    assert_close(s, ref_s, "S")
+    assert_close(res["grad_alpha"][0], ref["grad_alpha"], "grad_alpha")
+    assert_close(res["grad_u"], ref["grad_u"], "grad_u")
+    assert_close(res["grad_img"], ref["grad_img"], "grad_img",
+                 extra=4e-6 * ref["grad_img_absterms"])
+    gt, rt, ab = res["grad_tau"], ref["grad_tau"], ref["grad_tau_absterms"]
+    worst = assert_close(gt, rt, "grad_tau", extra=4e-6 * ab)
+    plain = np.abs(gt - rt) > ATOL + RTOL * np.abs(rt)
+    cancelled = np.abs(rt) < 1e-2 * ab  # sums cancelled to under a hundredth of their terms
+    print(f"grad_tau: worst err/tol {worst:.3g} of the cancellation-aware bound; "
+          f"{plain.sum()} of {plain.size} outside the plain bound")
+    assert not (plain & ~cancelled).any()
+
+
+def test_soft_at_the_largest_batch():
+    """65535 images (the grid's y extent holds one (image, direction) pair each), 2 x 3 pixels,
+    every image different; forward and backward against the oracle over the whole batch."""
+    rng = np.random.default_rng(53)
+    img = rng.random((65535, 2, 3)).astype(np.float32)
+    tau = synthetic.uniform_thresholds(5)
+    g = rng.standard_normal((65535, 5)).astype(np.float32)
+    compare(img, tau, 20.0, 1.0, np.asarray([0.1, 0.05], np.float32), g, want_img=False)

@@ -285,3 +285,31 @@ def test_pool_of_images_equals_the_batch():
     np.testing.assert_allclose(r["grad_alpha"], ref["grad_alpha"], rtol=1e-12)
     np.testing.assert_allclose(r["grad_u"], ref["grad_u"], rtol=1e-12, atol=1e-12)
     np.testing.assert_array_equal(r["grad_img"], ref["grad_img"])
+
+
+def test_grad_tau_absterms_bounds_and_single_vertex_closed_form():
+    """grad_tau_absterms (the scale of the cancellation in grad_tau) against what fixes it: for a
+    1 x 1 image the only cell is its vertex (sign +1), so every term of grad_tau[k] is
+    g_k lambda s (1 - s) with s = sigma(lambda (t_k - alpha f)) and the sum of |terms| is the
+    same closed form with |g_k|; for any image it bounds |grad_tau| (triangle inequality) and
+    equals it where every term has one sign (g >= 0 on a 1 x 1 image)."""
+    lam, alpha, f = 30.0, 1.0, 0.4
+    tau = np.linspace(0.0, 1.0, 9).astype(np.float32)
+    g = np.asarray([[0.5, -1.0, 2.0, -0.25, 1.0, -3.0, 0.75, 0.1, -0.6]])
+    img = np.full((1, 1, 1), f, np.float32)
+    r = oracle.ecc_soft_bwd(img, tau, lam, alpha, np.zeros(2, np.float32), g, ndim=2,
+                            want_img=False)
+    s = 1.0 / (1.0 + np.exp(-lam * (tau.astype(np.float64) - np.float32(f))))
+    w = lam * s * (1.0 - s)
+    np.testing.assert_allclose(r["grad_tau"], g[0] * w, rtol=1e-12, atol=0)
+    np.testing.assert_allclose(r["grad_tau_absterms"], np.abs(g[0]) * w, rtol=1e-12, atol=0)
+    rp = oracle.ecc_soft_bwd(img, tau, lam, alpha, np.zeros(2, np.float32), np.abs(g), ndim=2,
+                             want_img=False)
+    np.testing.assert_array_equal(rp["grad_tau_absterms"], rp["grad_tau"])
+    img = synthetic.grf((7, 9), 61, batch=2)
+    tau = synthetic.uniform_thresholds(20)
+    g = synthetic.upstream_grad((2, 20), seed=62)
+    r = oracle.ecc_soft_bwd(img, tau, 40.0, 1.0, np.asarray([0.1, -0.05], np.float32), g,
+                            ndim=2, want_img=False)
+    assert np.all(np.abs(r["grad_tau"]) <= r["grad_tau_absterms"] * (1 + 1e-12))
+    assert np.all(r["grad_tau_absterms"] > 0)
