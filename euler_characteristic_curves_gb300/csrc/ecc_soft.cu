@@ -362,6 +362,28 @@ __device__ __forceinline__ int local_c3(const float2 *c, const int8_t *c2tab)
     return v;
 }
 
+// Position (iz, iy, ix) of element i of a halo box with rows of HX, planes of HP = HX HY
+// elements, advanced by kPrepThreads elements at a time (one carry at most per axis).
+template <int HX, int HY, int HP>
+struct HaloPos {
+    static constexpr int dX = kPrepThreads % HX, dY = (kPrepThreads / HX) % HY,
+                         dZ = kPrepThreads / HP;
+    int ix, iy, iz;
+    __device__ __forceinline__ explicit HaloPos(int i) : ix(i % HX), iy((i / HX) % HY), iz(i / HP)
+    {
+    }
+    __device__ __forceinline__ void advance()
+    {
+        ix += dX;
+        const int cx = ix >= HX;
+        ix -= cx ? HX : 0;
+        iy += dY + cx;
+        const int cy = iy >= HY;
+        iy -= cy ? HY : 0;
+        iz += dZ + cy;
+    }
+};
+
 // One block per (tile, image). Reads f on the tile plus a one-voxel halo once, then for each
 // direction u_j computes X_j = alpha f + u_j . x there, c_X per voxel, and writes the contributing
 // voxels of the tile, in the tile's own raster order, to the slot of unit (image, direction,
@@ -423,17 +445,25 @@ __global__ void __launch_bounds__(kPrepThreads) soft_prep_kernel(
         ctile[i] = cv;
     }
     // all of a thread's loads are issued before any of them is stored, so their latencies overlap
-    // (one load per iteration, stored before the next, waited on each in turn)
+    // (one load per iteration, stored before the next, waited on each in turn). The element
+    // i = thread + r kPrepThreads of the halo box advances by kPrepThreads each round, its
+    // position (iz, iy, ix) by carries instead of divisions; grid coordinates fit in 32 bits
+    // (extents are at most 2^30) and one unsigned compare tests both ends of an axis.
     constexpr int kLoads = (HZ * HP + kPrepThreads - 1) / kPrepThreads;
+    const int tx0 = (int)x0 - 1, ty0 = (int)y0 - 1, tz0 = (int)z0 - ZO;
+    const unsigned uW = (unsigned)g.W, uH = (unsigned)g.Hy, uD = (unsigned)g.D;
     float fl[kLoads];
+    {
+        HaloPos<HX, HY, HP> hp(threadIdx.x);
 #pragma unroll
-    for (int r = 0; r < kLoads; ++r) {
-        const int i = threadIdx.x + r * kPrepThreads;
-        const int iz = i / HP, iy = (i / HX) % HY, ix = i % HX;
-        const int64_t gz = z0 - ZO + iz, gy = y0 - 1 + iy, gx = x0 - 1 + ix;
-        fl[r] = qnan();
-        if (i < HZ * HP && gz >= 0 && gz < g.D && gy >= 0 && gy < g.Hy && gx >= 0 && gx < g.W)
-            fl[r] = __ldg(f + (gz * g.Hy + gy) * g.W + gx);
+        for (int r = 0; r < kLoads; ++r) {
+            const int i = threadIdx.x + r * kPrepThreads;
+            const int gz = tz0 + hp.iz, gy = ty0 + hp.iy, gx = tx0 + hp.ix;
+            fl[r] = qnan();
+            if (i < HZ * HP && (unsigned)gz < uD && (unsigned)gy < uH && (unsigned)gx < uW)
+                fl[r] = __ldg(f + ((int64_t)gz * g.Hy + gy) * g.W + gx);
+            hp.advance();
+        }
     }
 #pragma unroll
     for (int r = 0; r < kLoads; ++r) {
@@ -445,8 +475,9 @@ __global__ void __launch_bounds__(kPrepThreads) soft_prep_kernel(
         const float *u = u_p + j * NDIM;
         const float u0 = __ldg(u), u1 = __ldg(u + 1), u2 = NDIM == 3 ? __ldg(u + 2) : 0.0f;
         __syncthreads();  // Fv is complete; the previous direction is done with X and running
-        for (int i = threadIdx.x; i < HZ * HP; i += kPrepThreads) {
-            const int iz = i / HP, iy = (i / HX) % HY, ix = i % HX;
+        HaloPos<HX, HY, HP> hp(threadIdx.x);
+        for (int i = threadIdx.x; i < HZ * HP; i += kPrepThreads, hp.advance()) {
+            const int iz = hp.iz, iy = hp.iy, ix = hp.ix;
             const float fv = Fv[i];
             float2 v = make_float2(inf, 0.0f);  // outside the grid: never earlier
             if (fv == fv) {  // inside the grid (NaN marks outside; inputs are finite)
@@ -474,7 +505,7 @@ __global__ void __launch_bounds__(kPrepThreads) soft_prep_kernel(
             const int lx = i % T::X, ly = (i / T::X) % T::Y, lz = i / (T::X * T::Y);
             const float2 *cp = &X[(lz + ZO) * HP + (ly + 1) * HX + lx + 1];
             int c = 0;
-            if (z0 + lz < g.D && y0 + ly < g.Hy && x0 + lx < g.W)
+            if (tz0 + ZO + lz < (int)uD && ty0 + 1 + ly < (int)uH && tx0 + 1 + lx < (int)uW)
                 c = NDIM == 3 ? local_c3<HX, HP>(cp, c2tab) : local_c2<HX>(cp);
             cr[r] = c;
             bal[r] = __ballot_sync(kFull, c != 0);
