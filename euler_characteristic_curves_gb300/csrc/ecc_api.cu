@@ -139,7 +139,7 @@ int ecc_device_status(int clear)
 int64_t ecc_device_error_bits(int clear)
 {
     const int64_t bits = device_error_bits(clear);
-    return bits < 0 ? ECC_ECUDA : bits;
+    return bits < 0 ? (int64_t)ECC_ECUDA : bits;
 }
 
 int ecc_debug_build(void) { return ECC_DEBUG_BOUNDS ? 1 : 0; }
