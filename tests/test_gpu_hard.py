@@ -228,6 +228,25 @@ def test_misaligned_buffers(offset):
     np.testing.assert_array_equal(got, oracle.ecc_hard(q, 256, 0.0, 255.0))
 
 
+@pytest.mark.parametrize("offset", [1, 2, 3])
+def test_misaligned_volumes(offset):
+    """3-D float32 volumes whose rows hold a multiple of 4 values but whose base is not 16-byte
+    aligned: the TMA-staged kernel's tensor map needs the aligned base, so these take the
+    register-prefetch kernel, and must match the oracle like the aligned ones (uint8 too)."""
+    v = synthetic.grf((6, 40, 132), 70 + offset)
+    base = torch.zeros(v.size + 8, dtype=torch.float32, device=DEV)
+    view = base[offset: offset + v.size].view(v.shape)
+    view.copy_(torch.from_numpy(v).to(DEV))
+    got = ecc.ecc_hard(view, 64, 0.0, 1.0, ndim=3).cpu().numpy()
+    np.testing.assert_array_equal(got, oracle.ecc_hard(v, 64, 0.0, 1.0))
+    q = synthetic.quantise_u8(v)
+    b8 = torch.zeros(q.size + 8, dtype=torch.uint8, device=DEV)
+    v8 = b8[offset: offset + q.size].view(q.shape)
+    v8.copy_(torch.from_numpy(q).to(DEV))
+    got = ecc.ecc_hard(v8, 256, 0.0, 255.0, ndim=3).cpu().numpy()
+    np.testing.assert_array_equal(got, oracle.ecc_hard(q, 256, 0.0, 255.0))
+
+
 @pytest.mark.parametrize("shape", [(1, 1, 1), (2, 2, 2), (3, 1, 7), (1, 9, 9), (5, 6, 7),
                                    (9, 17, 33), (4, 8, 128), (3, 9, 129), (17, 20, 131),
                                    (2, 67, 260), (40, 12, 5)])
