@@ -676,7 +676,7 @@ struct FwdAcc {
 
 // Forward over the staged entries i = first, first + step, ... < m_ent, factorised form (the same
 // per-term arithmetic as the scalar form: e = E F_k, r = min(e, 1) / (1 + e), w += [e <= 1] c,
-// Kahan over -+c r).
+// Kahan over -+c r). The entries are staged as the pairs (E, E), (c, c).
 // The below-threshold flag enters as a float b (1.0 / 0.0, one set instruction on the ALU pipe)
 // through packed fused multiply-adds on the FMA pipe, w += b c and the small part's coefficient
 // c (1 - 2 b) = fma(b, -2 c, c), instead of a compare and two selects on the ALU pipe, which
@@ -685,12 +685,11 @@ struct FwdAcc {
 __device__ __forceinline__ void fwd_loop4_packed(const float4 *sh, int first, int step,
                                                  int m_ent, const f32x2 *F, FwdAcc &acc)
 {
+    const f32x2 minus2 = pk2(-2.0f, -2.0f);
 #pragma unroll 2
     for (int i = first; i < m_ent; i += step) {
-        const float4 en = sh[i];
-        const float cf = entry_cf(en);
-        const f32x2 c2 = pk2(cf, cf), m2c2 = pk2(-2.0f * cf, -2.0f * cf);
-        const f32x2 E = pk2(en.x, en.x);
+        const ulonglong2 en = *reinterpret_cast<const ulonglong2 *>(sh + i);  // (E, E), (c, c)
+        const f32x2 E = en.x, c2 = en.y, m2c2 = mul2(c2, minus2);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             float e0, e1, d0, d1;
@@ -752,7 +751,11 @@ __global__ void __launch_bounds__(kSoftThreads) soft_fwd_kernel(
         for (int e0 = 0; e0 < n; e0 += kChunk) {
             const int m_ent = min(kChunk, n - e0);
             __syncthreads();
-            for (int i = threadIdx.x; i < m_ent; i += kSoftThreads) sh[i] = list[e0 + i];
+            // factorised form: each entry staged as the pairs (E, E), (c, c) the packed loop uses
+            for (int i = threadIdx.x; i < m_ent; i += kSoftThreads) {
+                const float4 en = list[e0 + i];
+                sh[i] = fact ? make_float4(en.x, en.x, entry_cf(en), entry_cf(en)) : en;
+            }
             __syncthreads();
             if (fact)
                 fwd_loop4_packed(sh, warp, kSoftWarps, m_ent, F, acc);
@@ -844,10 +847,10 @@ __device__ __forceinline__ float group_row_sum(float (*qw)[kWarp], int lane)
 // underflow to 0. The backward's terms carry -r and -w: -w = r^2 - r = fma(-r, -r, -r) is one
 // packed FMA, where w = fma(-r, r, r) needed a negation first. With -c and -g as the other
 // factors every product, and so every sum, keeps its bits.
-__device__ __forceinline__ f32x2 neg_small_sigma_fact2(float E, f32x2 F)
+__device__ __forceinline__ f32x2 neg_small_sigma_fact2(f32x2 E2, f32x2 F)
 {
     float e0, e1, d0, d1;
-    const f32x2 e = mul2(pk2(E, E), F);
+    const f32x2 e = mul2(E2, F);
     upk2(e, e0, e1);
     upk2(add2(e, pk2(1.0f, 1.0f)), d0, d1);
     return mul2(pk2(fmaxf(-e0, -1.0f), fmaxf(-e1, -1.0f)), pk2(rcp_approx(d0), rcp_approx(d1)));
@@ -857,21 +860,20 @@ __device__ __forceinline__ float entry_neg_cf(const float4 &en)
     return 8388616.0f - __int_as_float(0x4B000000 | (__float_as_int(en.w) & 15));
 }
 
-// ng: the lane's upstream gradients negated, as pairs.
+// ng: the lane's upstream gradients negated, as pairs; en8: entries staged as (E, E), (-c, -c).
 __device__ __forceinline__ float bwd_group4_packed(const float4 *en8, const f32x2 *F,
                                                    const f32x2 *ng, f32x2 *a, f32x2 *nc,
                                                    float (*qw)[kWarp], int lane)
 {
 #pragma unroll
     for (int j = 0; j < kGroup; ++j) {
-        const float4 en = en8[j];
-        const float ncf = entry_neg_cf(en);
+        const ulonglong2 en = *reinterpret_cast<const ulonglong2 *>(en8 + j);  // (E, E), (-c, -c)
         f32x2 gw = 0ull;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const f32x2 rn = neg_small_sigma_fact2(en.x, F[h]);  // -r
             const f32x2 wn = fma2(rn, rn, rn);                   // -w = r^2 - r
-            kahan_fma2(a[h], nc[h], pk2(ncf, ncf), wn);          // (-c)(-w) = c w
+            kahan_fma2(a[h], nc[h], en.y, wn);                   // (-c)(-w) = c w
             gw = fma2(ng[h], wn, gw);                            // (-g)(-w) = g w
         }
         float q0, q1;
@@ -975,9 +977,14 @@ __global__ void __launch_bounds__(kSoftThreads) soft_bwd_kernel(
                 const int m_ent = min(kBwdChunk, n - e0);
                 __syncthreads();
                 // stage the chunk; pad the last group with c = 0 entries
-                for (int i = threadIdx.x; i < kBwdChunk; i += kSoftThreads)
-                    sh[i] = (i < m_ent) ? list[e0 + i]
-                                        : make_float4(0.f, 0.f, 0.f, __int_as_float(kPadWord));
+                // factorised form: each entry staged as the pairs (E, E), (-c, -c)
+                for (int i = threadIdx.x; i < kBwdChunk; i += kSoftThreads) {
+                    const float4 en = (i < m_ent)
+                                          ? list[e0 + i]
+                                          : make_float4(0.f, 0.f, 0.f, __int_as_float(kPadWord));
+                    sh[i] = fact ? make_float4(en.x, en.x, entry_neg_cf(en), entry_neg_cf(en))
+                                 : en;
+                }
                 __syncthreads();
                 for (int gi = warp; gi * kGroup < m_ent; gi += NW) {
                     const float rs =
