@@ -686,7 +686,7 @@ __device__ __forceinline__ void fwd_loop4_packed(const float4 *sh, int first, in
                                                  int m_ent, const f32x2 *F, FwdAcc &acc)
 {
     const f32x2 minus2 = pk2(-2.0f, -2.0f);
-#pragma unroll 2
+#pragma unroll 3
     for (int i = first; i < m_ent; i += step) {
         const ulonglong2 en = *reinterpret_cast<const ulonglong2 *>(sh + i);  // (E, E), (c, c)
         const f32x2 E = en.x, c2 = en.y, m2c2 = mul2(c2, minus2);
