@@ -975,6 +975,16 @@ static_assert(kRawBytes % 16 == 0 && kKeyRingBytes % 16 == 0, "shared layout");
 static_assert(kStrip + 8 == kRawPitch, "a staged row starts 4 columns left of the tile");
 
 
+// Block g's segment [a, b) of the W tile-planes of an image shared out over G blocks: lengths
+// W / G, the first W % G blocks one more.
+__host__ __device__ __forceinline__ void tma3d_segment(int64_t W, int64_t G, int64_t g,
+                                                       int64_t &a, int64_t &b)
+{
+    const int64_t q = W / G, r = W % G;
+    a = g * q + (g < r ? g : r);
+    b = a + q + (g < r ? 1 : 0);
+}
+
 struct Hard3TmaParams {
     CUtensorMap map;  // [batch][D][Hy][W] float32; box 136 x 34 x 1 x 1; NaN outside
     int64_t *out;
@@ -1241,19 +1251,23 @@ __global__ void __launch_bounds__(k3Threads, kT3Blocks)
     const int r0 = warp * k3Rows;  // buffer row of the row above the warp's first row
     const int b = blockIdx.y;
     const uint32_t hist_c = smem_u32(hist) - kKeyBase;
-    const int64_t Tn = P.tasks_per_image, G = P.ctas_per_image;
+    const int64_t G = P.ctas_per_image;
     // The block's plane copies in issue order: copy n goes to staging buffer n % kT3Stages and
     // completes phase (n / kT3Stages) & 1 of that buffer's mbarrier; copies are waited for in
     // the same order. nq: copies issued, nw: copies waited for.
     uint32_t nq = 0, nw = 0;
     bool failed = false;
 
-    for (int64_t t = blockIdx.x; t < Tn && !failed; t += G) {
-        const int tx = (int)(t % P.tasks_x);
-        const int64_t rest = t / P.tasks_x;
-        const int ty = (int)(rest % P.tasks_y);
-        const int z0 = (int)(rest / P.tasks_y) * P.rows_per_task;
-        const int z1 = min(z0 + P.rows_per_task, P.D);
+    // The block's segment of the image's tiles x planes (tile-major), in pieces that end where
+    // a tile does: each piece is one task, planes z0 .. z1 - 1 of one tile.
+    int64_t s0, s1;
+    tma3d_segment((int64_t)P.tasks_x * P.tasks_y * P.D, G, blockIdx.x, s0, s1);
+    while (s0 < s1 && !failed) {
+        const int64_t tile = s0 / P.D;
+        const int z0 = (int)(s0 % P.D);
+        const int z1 = (int)min((int64_t)P.D, (int64_t)z0 + (s1 - s0));
+        s0 += z1 - z0;
+        const int tx = (int)(tile % P.tasks_x), ty = (int)(tile / P.tasks_x);
         const int x0 = tx * kStrip, y0 = ty * kTileRows;
 
         // The task reads planes z0 - 1 .. z1 (n_planes of them; planes -1 and D are filled with
@@ -1503,6 +1517,30 @@ HardShape plan_hard(const HardPlan &pl, int sms)
         sh.tasks_y = pl.Hy;
         sh.tasks_z = 1;
         sh.tasks_per_image = strips * R;  // warps with a band
+    } else if (pl.tma) {
+        // segments: block g takes a contiguous share of the image's tiles x planes, numbered
+        // tile-major (a tile's planes in order), cut into pieces where a tile ends
+        const int64_t tiles_y = (pl.Hy + kTileRows - 1) / kTileRows;
+        const int64_t tiles = strips * tiles_y, Wt = tiles * pl.D;
+        if (per_image > Wt) per_image = Wt;
+        if (per_image < 1) per_image = 1;
+        int64_t pieces = 0, most = 0;
+        for (int64_t g = 0; g < per_image; ++g) {
+            int64_t a, b;
+            tma3d_segment(Wt, per_image, g, a, b);
+            const int64_t n = (b - 1) / pl.D - a / pl.D + 1;
+            pieces += n;
+            if (n > most) most = n;
+        }
+        sh.tasks_x = strips;
+        sh.tasks_y = tiles_y;
+        sh.tasks_z = 1;
+        sh.rows_per_task = (Wt + per_image - 1) / per_image;  // tile-planes per block, at most
+        sh.tasks_per_image = pieces;
+        sh.blocks_per_image = per_image;
+        sh.rounds = most;
+        sh.direct = false;
+        return sh;
     } else {
         const int64_t tiles_y = (pl.Hy + kTileRows - 1) / kTileRows;
         const int64_t tiles = strips * tiles_y;

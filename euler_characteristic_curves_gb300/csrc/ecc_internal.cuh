@@ -111,14 +111,17 @@ struct HardPlan {
     bool tma = false;       // planned for the TMA-staged 3-D kernel (three blocks per SM)
 };
 // Launch shape of a hard-ECC call on a device of `sms` SMs (shared by the launcher and
-// ecc_hard_launch_info). 2-D: one warp per (strip, row range); 3-D: tasks (tile, chunk of planes)
-// taken by the blocks of an image in rounds, block g taking tasks g, g + G, ...
+// ecc_hard_launch_info). 2-D: one warp per (strip, row range); TMA-staged 3-D: block g takes a
+// contiguous segment of the image's tiles x planes (tile-major), in pieces cut where a tile
+// ends; register 3-D: tasks (tile, chunk of planes) taken by the blocks of an image in rounds,
+// block g taking tasks g, g + G, ...
 struct HardShape {
     int64_t blocks_per_image;
-    int64_t tasks_per_image;  // 2-D: (strip, row range) bands; 3-D: (tile, chunk) tasks
-    int64_t rows_per_task;    // 2-D: row ranges per strip; 3-D: planes per chunk
+    int64_t tasks_per_image;  // 2-D: (strip, row range) bands; staged 3-D: pieces; 3-D: tasks
+    int64_t rows_per_task;    // 2-D: row ranges per strip; staged 3-D: tile-planes per block;
+                              // 3-D: planes per chunk
     int64_t tasks_x, tasks_y, tasks_z;
-    int64_t rounds;  // 3-D: most tasks one block takes; 2-D: 1
+    int64_t rounds;  // staged 3-D: most pieces of a block; 3-D: most tasks of a block; 2-D: 1
     bool direct;     // 2-D: the image's only block stores the curve itself
 };
 HardShape plan_hard(const HardPlan &pl, int sms);

@@ -127,10 +127,14 @@ int ecc_hist_to_curve(int64_t *hist, int nbins, int64_t batch, ecc_stream_t stre
  * info      host array of 6 int64, written on success:
  *   info[0] blocks per image
  *   info[1] work items per image: 2-D, (128-column strip, row range) bands, one per warp;
- *           3-D, (tile of 128 x 32 columns x rows, chunk of planes) tasks
- *   info[2] 2-D: row ranges per strip; 3-D: planes per chunk
- *   info[3] 3-D: rounds, the most tasks one block walks (block g takes tasks g, g + G, ...);
- *           2-D: 1
+ *           3-D float32 with W % 4 == 0 and nbins <= 256 (the TMA-staged kernel), pieces:
+ *           block g takes a contiguous share of the image's (tile of 128 x 32 columns x rows)
+ *           x planes, numbered tile by tile, cut into pieces where a tile ends; other 3-D
+ *           calls, (tile, chunk of planes) tasks
+ *   info[2] 2-D: row ranges per strip; staged 3-D: tile-planes per block (at most); other 3-D:
+ *           planes per chunk
+ *   info[3] staged 3-D: the most pieces one block walks; other 3-D: rounds, the most tasks
+ *           one block walks (block g takes tasks g, g + G, ...); 2-D: 1
  *   info[4] 1 when a 2-D image's only block stores the running sum itself, else 0
  *   info[5] the SM count planned for
  */

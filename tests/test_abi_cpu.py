@@ -132,8 +132,13 @@ def test_launch_info(lib):
     li = lib.ecc_hard_launch_info
     assert li(1, 3, dims(1024, 1024, 1024), 1, 256, 152, info) == OK
     blocks, tasks, rows, rounds, direct, sms = list(info)
-    assert sms == 152 and blocks <= 152 * 4 and rounds == -(-tasks // blocks) and rounds > 1
-    assert tasks % (8 * 32) == 0  # 8 x 32 tiles of 128 x 32 per chunk of planes
+    # float32, rows of 4k values, <= 256 bins: the TMA-staged kernel's segments, each block a
+    # contiguous share of the 8 x 32 tiles x 1024 planes, cut where a tile ends
+    assert sms == 152 and blocks == 152 * 3 and rows == -(-(8 * 32 * 1024) // blocks)
+    assert rounds == 2 and blocks < tasks < 2 * blocks
+    assert li(0, 3, dims(1024, 1024, 1024), 1, 256, 152, info) == OK  # uint8: task rounds
+    blocks, tasks, rows, rounds, direct, sms = list(info)
+    assert rounds == -(-tasks // blocks) > 1 and tasks % (8 * 32) == 0
     assert li(1, 2, dims(128, 128), 1, 256, 152, info) == OK and info[4] == 1  # one block
     assert li(1, 2, dims(8192, 8192), 1, 1024, 152, info) == OK and info[4] == 0
     assert li(1, 3, dims(8, 8, 8), 1, 4097, 152, info) == ERANGE

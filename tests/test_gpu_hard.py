@@ -316,9 +316,10 @@ def test_workload_512cube_u8():
 
 
 def test_workload_1024cube_f32():
-    """The 1024^3 volume in the benchmark's launch -- 4096 tasks on the resident blocks, so every
-    block walks several tasks in turn -- against the oracle, bit for bit. The oracle curve comes
-    from slabs that share one plane, one oracle process per host core."""
+    """The 1024^3 volume in the benchmark's launch -- 456 blocks, each a contiguous segment of
+    the tiles x planes in up to two pieces (tasks), so blocks carry their key buffers and
+    histogram from one piece to the next -- against the oracle, bit for bit. The oracle curve
+    comes from slabs that share one plane, one oracle process per host core."""
     v = synthetic.grf((1024, 1024, 1024), seed=4, device=DEV)
     plan = ecc.hard_launch_info(tuple(v.shape), 1, 256)
     assert plan["rounds"] > 1 and plan["tasks_per_image"] > plan["blocks_per_image"]
@@ -332,11 +333,11 @@ def test_workload_1024cube_f32():
                                               ((64, 1024, 1024), "f32", 1000),
                                               ((32, 1024, 1024), "u8", 256)])
 def test_3d_blocks_walking_several_tasks(shape, kind, nbins):
-    """Volumes with more (tile, chunk) tasks than resident blocks, so each block reuses its key
-    ring, carried rows and histogram from one task to the next: float32 with 256 bins (the
-    TMA-staged kernel, 608 blocks on 152 SMs: two rounds for 16 x 2048^2), float32 with 1000
-    bins and uint8 (the register-prefetch kernel, 456 blocks: three and two rounds). The planner
-    says how many rounds the launch takes; the curve must match the oracle bit for bit."""
+    """Volumes where each block walks several tasks, reusing its key ring, carried rows and
+    histogram from one to the next: float32 with 256 bins (the TMA-staged kernel: 456 segments
+    of 16 x 2048^2's tiles x planes, up to four pieces each), float32 with 1000 bins and uint8
+    (the register-prefetch kernel, 456 blocks taking (tile, chunk) tasks in rounds). The planner
+    says how many tasks a block walks; the curve must match the oracle bit for bit."""
     v = synthetic.grf(shape, seed=30 + shape[0], device=DEV)
     vmax = 1.0
     if kind == "u8":
@@ -349,9 +350,10 @@ def test_3d_blocks_walking_several_tasks(shape, kind, nbins):
 
 
 def test_3d_rounds_on_a_small_device_plan():
-    """The multi-round path on small volumes: a batch of 100 volumes shares the resident blocks,
-    so each image gets a few blocks and more tiles than blocks (checked with the planner), ragged
-    tiles included; float32 (TMA-staged kernel) and uint8 (register-prefetch kernel)."""
+    """Blocks walking several tasks on small volumes: a batch of 100 volumes shares the resident
+    blocks, so each image gets a few blocks and more tiles than blocks (checked with the
+    planner), ragged tiles included; float32 (TMA-staged kernel: segments in several pieces)
+    and uint8 (register-prefetch kernel: tasks in rounds)."""
     v = synthetic.grf((8, 70, 300), seed=33, batch=100)
     assert ecc.hard_launch_info(v.shape[1:], 100, 77)["rounds"] > 1
     check(v, 77, 0.0, 1.0, ndim=3)
