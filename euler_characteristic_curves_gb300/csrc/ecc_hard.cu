@@ -991,6 +991,7 @@ struct Hard3TmaParams {
     int64_t tasks_per_image;
     int D, Hy, W, H, sign;
     int rows_per_task, tasks_x, tasks_y, ctas_per_image;
+    int group;  // blocks per group: tasks_x (a row of tiles side by side) or 1
     float key_a, key_b, key_clo, key_chi;
     float table[kCodedMaxBins + 2];
 };
@@ -1258,15 +1259,23 @@ __global__ void __launch_bounds__(k3Threads, kT3Blocks)
     uint32_t nq = 0, nw = 0;
     bool failed = false;
 
-    // The block's segment of the image's tiles x planes (tile-major), in pieces that end where
-    // a tile does: each piece is one task, planes z0 .. z1 - 1 of one tile.
+    // Blocks work in groups of P.group blocks: a whole row of tiles (one block per strip) when
+    // the image has blocks enough, else single tiles. Group h takes a contiguous segment of the
+    // image's (row of tiles or tile) x planes, numbered row by row, and its blocks walk the same
+    // rows and planes side by side, so the halo columns that neighbouring tiles share are read
+    // once into L2 for both. The segment is cut into pieces where a row ends: each piece is one
+    // task, planes z0 .. z1 - 1 of this block's tile of the row.
+    const int gsz = P.group;
+    const int64_t groups = G / gsz, h = blockIdx.x / gsz;
+    const int64_t rows = (int64_t)P.tasks_x * P.tasks_y / gsz;
     int64_t s0, s1;
-    tma3d_segment((int64_t)P.tasks_x * P.tasks_y * P.D, G, blockIdx.x, s0, s1);
+    tma3d_segment(rows * P.D, groups, h, s0, s1);
     while (s0 < s1 && !failed) {
-        const int64_t tile = s0 / P.D;
+        const int64_t row = s0 / P.D;
         const int z0 = (int)(s0 % P.D);
         const int z1 = (int)min((int64_t)P.D, (int64_t)z0 + (s1 - s0));
         s0 += z1 - z0;
+        const int64_t tile = row * gsz + blockIdx.x % gsz;
         const int tx = (int)(tile % P.tasks_x), ty = (int)(tile / P.tasks_x);
         const int x0 = tx * kStrip, y0 = ty * kTileRows;
 
@@ -1518,26 +1527,29 @@ HardShape plan_hard(const HardPlan &pl, int sms)
         sh.tasks_z = 1;
         sh.tasks_per_image = strips * R;  // warps with a band
     } else if (pl.tma) {
-        // segments: block g takes a contiguous share of the image's tiles x planes, numbered
-        // tile-major (a tile's planes in order), cut into pieces where a tile ends
+        // segments: groups of blocks (a row of tiles side by side when there are blocks enough,
+        // else single tiles) take contiguous shares of the image's (row or tile) x planes,
+        // numbered row by row, cut into pieces where a row ends
         const int64_t tiles_y = (pl.Hy + kTileRows - 1) / kTileRows;
-        const int64_t tiles = strips * tiles_y, Wt = tiles * pl.D;
-        if (per_image > Wt) per_image = Wt;
-        if (per_image < 1) per_image = 1;
+        const int64_t group = per_image >= strips ? strips : 1;
+        const int64_t units = strips * tiles_y / group * pl.D;
+        int64_t groups = per_image / group;
+        if (groups > units) groups = units;
+        if (groups < 1) groups = 1;
         int64_t pieces = 0, most = 0;
-        for (int64_t g = 0; g < per_image; ++g) {
+        for (int64_t h = 0; h < groups; ++h) {
             int64_t a, b;
-            tma3d_segment(Wt, per_image, g, a, b);
+            tma3d_segment(units, groups, h, a, b);
             const int64_t n = (b - 1) / pl.D - a / pl.D + 1;
-            pieces += n;
+            pieces += n * group;
             if (n > most) most = n;
         }
         sh.tasks_x = strips;
         sh.tasks_y = tiles_y;
-        sh.tasks_z = 1;
-        sh.rows_per_task = (Wt + per_image - 1) / per_image;  // tile-planes per block, at most
+        sh.tasks_z = group;  // blocks per group
+        sh.rows_per_task = (units + groups - 1) / groups;  // (row or tile)-planes per group
         sh.tasks_per_image = pieces;
-        sh.blocks_per_image = per_image;
+        sh.blocks_per_image = groups * group;
         sh.rounds = most;
         sh.direct = false;
         return sh;
@@ -1686,6 +1698,7 @@ static cudaError_t launch_hard3d_tma(const HardPlan &pl, cudaStream_t s)
     P.tasks_x = (int)sh.tasks_x;
     P.tasks_y = (int)sh.tasks_y;
     P.ctas_per_image = (int)sh.blocks_per_image;
+    P.group = (int)sh.tasks_z;
     P.key_a = pl.key_a;
     P.key_b = pl.key_b;
     P.key_clo = pl.key_clo;
