@@ -316,10 +316,11 @@ def test_workload_512cube_u8():
 
 
 def test_workload_1024cube_f32():
-    """The 1024^3 volume in the benchmark's launch -- 456 blocks, each a contiguous segment of
-    the tiles x planes in up to two pieces (tasks), so blocks carry their key buffers and
-    histogram from one piece to the next -- against the oracle, bit for bit. The oracle curve
-    comes from slabs that share one plane, one oracle process per host core."""
+    """The 1024^3 volume in the benchmark's launch -- 57 groups of 8 side-by-side blocks, each
+    group a contiguous segment of the 32 rows of tiles x 1024 planes in up to two pieces (tasks),
+    so blocks carry their key buffers and histogram from one piece to the next -- against the
+    oracle, bit for bit. The oracle curve comes from slabs that share one plane, one oracle
+    process per host core."""
     v = synthetic.grf((1024, 1024, 1024), seed=4, device=DEV)
     plan = ecc.hard_launch_info(tuple(v.shape), 1, 256)
     assert plan["rounds"] > 1 and plan["tasks_per_image"] > plan["blocks_per_image"]
@@ -334,8 +335,9 @@ def test_workload_1024cube_f32():
                                               ((32, 1024, 1024), "u8", 256)])
 def test_3d_blocks_walking_several_tasks(shape, kind, nbins):
     """Volumes where each block walks several tasks, reusing its key ring, carried rows and
-    histogram from one to the next: float32 with 256 bins (the TMA-staged kernel: 456 segments
-    of 16 x 2048^2's tiles x planes, up to four pieces each), float32 with 1000 bins and uint8
+    histogram from one to the next: float32 with 256 bins (the TMA-staged kernel: 28 groups of 16
+    side-by-side blocks, each a segment of the 64 rows of tiles x 16 planes in up to four
+    pieces), float32 with 1000 bins and uint8
     (the register-prefetch kernel, 456 blocks taking (tile, chunk) tasks in rounds). The planner
     says how many tasks a block walks; the curve must match the oracle bit for bit."""
     v = synthetic.grf(shape, seed=30 + shape[0], device=DEV)
